@@ -1,0 +1,431 @@
+"""Benchmark: valid-token jagged attention TFLOP/s, forward + backward, on GB300.
+
+One step = the whole hot path over one synthetic batch: plan (tile lists +
+schedule, uploaded), forward, backward.  Inputs are resident in HBM when the
+timed region starts; L2 is flushed (a 256 MiB write) between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ID] [--impl ours|reference]
+
+With torchrun (N > 1) every rank runs the full batch on its own GPU (weak
+scaling, no collective on the data path); the reported time is the max over
+ranks and the value counts the work of all ranks.  --impl reference times the
+fp64 CPU oracle instead (rank 0 only), on a bounded sample of the same batch.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from jagged_attention_recommendation_gb300 import workloads as W  # noqa: E402
+
+METRIC = "valid-token attention TFLOPs fwd+bwd (bf16), % of GB300 dense-BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_config(w: W.Workload, act: int, Bn: int, flush: bool) -> dict:
+    return {"workload": "%s (B=%d, H=%d, D=%d, %s%s%s)" % (
+        w.name, Bn, w.H, w.D, W.ACT_NAMES[act], ", rel-pos bias %d buckets" % w.bias_buckets if w.bias_buckets
+        else "", ", block %d" % w.block if w.block else ""),
+        "B": Bn, "H": w.H, "D": w.D, "act": W.ACT_NAMES[act], "block": w.block, "bias_buckets": w.bias_buckets,
+        "input_dtype": w.dtype, "l2": "flushed between timed steps (256 MiB write)" if flush else "not flushed",
+        "parallelism": "one batch per GPU (data-parallel replicas)"}
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled while the timed region runs
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = np.array([num(r[1]) for r in rows])
+        mx = np.array([num(r[2]) for r in rows])
+        pw = np.array([num(r[3]) for r in rows])
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        load = sm[pw >= np.nanmedian(pw)] if np.isfinite(pw).any() else sm
+        return {"sm_mhz": float(np.nanmedian(load)), "sm_max_mhz": float(np.nanmax(mx)), "reasons": reasons,
+                "samples": len(rows), "power_w_max": float(np.nanmax(pw))}
+
+
+# ---------------------------------------------------------------------------
+# oracle timing (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def sample_sequences(q_off, kv_off, frac: float, seed: int = 0):
+    """Seeded subset of sequences holding about `frac` of the batch's valid pairs."""
+    lq = np.diff(q_off.astype(np.int64))
+    lk = np.diff(kv_off.astype(np.int64))
+    pairs = lq * lk
+    order = np.random.default_rng(seed).permutation(len(lq))
+    target = frac * pairs.sum()
+    picked, acc = [], 0
+    for b in order:
+        picked.append(int(b))
+        acc += pairs[b]
+        if acc >= target:
+            break
+    return sorted(picked)
+
+
+def time_oracle(batch: W.Batch, frac: float, seed: int = 0):
+    from oracle import oracle
+    w = batch.w
+    seqs = sample_sequences(batch.q_off, batch.kv_off, frac, seed)
+    qo, ko, (q, dout), (k, v), _, _ = oracle.sub_batch(batch.q_off, batch.kv_off, seqs, batch.q, batch.dout,
+                                                       tensors_kv=(batch.k, batch.v))
+    nthreads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.forward(qo, ko, q, k, v, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
+                   nthreads=nthreads)
+    oracle.backward(qo, ko, q, k, v, dout, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
+                    nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    f, b = W.flops(qo, ko, w.H, w.D, w.block)
+    desc = "%d of %d sequences (seeded), %.1f%% of the valid pairs" % (
+        len(seqs), batch.B, 100.0 * W.valid_pairs(qo, ko, w.block) / max(W.valid_pairs(batch.q_off, batch.kv_off,
+                                                                                          w.block), 1))
+    return (f + b) / dt / 1e12, dt, nthreads, desc
+
+
+def run_reference(args, w, batch):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        time_oracle(batch, args.ref_frac, seed=1)
+    vals, times = [], []
+    for s in range(args.steps):
+        v, dt, cores, desc = time_oracle(batch, args.ref_frac, seed=2 + s)
+        vals.append(v)
+        times.append(dt)
+    value = float(np.mean(vals))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, batch.act, batch.B, False),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "per step: " + desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+KERNELS_FULL = ["fwd", "bwd_delta", "bwd_dq", "bwd_dkdv"]
+KERNELS_BLOCK = ["fwd", "bwd_block"]
+
+
+def kernel_work(w, batch, name, pk):
+    """Algorithmic (flops, bytes) of one launch of `name` over the batch."""
+    H, D = w.H, w.D
+    p = W.valid_pairs(batch.q_off, batch.kv_off, w.block)
+    Tq, Tk = batch.Tq, batch.Tk
+    e = H * D * 2
+    if name == "fwd":
+        return 4.0 * D * H * p, W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)[0]
+    if name == "bwd_block":
+        return 10.0 * D * H * p, W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)[1]
+    if name == "bwd_delta":
+        return 0.0, 2.0 * Tq * e + 4.0 * H * Tq
+    if name == "bwd_dq":  # dQ GEMM; its S and dP recompute is not counted
+        lse = 8.0 * H * Tq if batch.act == W.SOFTMAX else 0.0
+        return 2.0 * D * H * p, 2.0 * Tq * e + 2.0 * Tk * e + Tq * e + lse
+    if name == "bwd_dkdv":  # S, dP, dV, dK
+        lse = 8.0 * H * Tq if batch.act == W.SOFTMAX else 0.0
+        return 8.0 * D * H * p, 2.0 * Tq * e + 2.0 * Tk * e + 2.0 * Tk * e + lse
+    raise KeyError(name)
+
+
+def run_ours(args, w, batch):
+    import torch.distributed as dist
+
+    import jagged_attention_recommendation_gb300 as J
+    ws, rank, local = dist_env()
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    H, D = w.H, w.D
+    f32 = w.dtype == "fp32"
+    tdt = torch.float32 if f32 else torch.bfloat16
+
+    # resident inputs and outputs
+    q, k, v, dout = (t.to(dev) for t in (batch.q, batch.k, batch.v, batch.dout))
+    bias = batch.bias.to(dev) if batch.bias is not None else None
+    plan = J.Plan(batch.q_off, batch.kv_off, H, D, act=batch.act, block=w.block, bias_buckets=w.bias_buckets,
+                  dtype="fp32" if f32 else "bf16", device=local)
+    out = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
+    lse = torch.empty(H, batch.Tq, dtype=torch.float32, device=dev) if batch.act == W.SOFTMAX else None
+    dq = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
+    dk = torch.empty(batch.Tk, H, D, dtype=tdt, device=dev)
+    dv = torch.empty(batch.Tk, H, D, dtype=tdt, device=dev)
+    fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(plan.bwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        plan.update(batch.q_off, batch.kv_off, stream)
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = plan.check_status()
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + J.status_str(st))
+
+    names = KERNELS_BLOCK if w.block else [n for n in KERNELS_FULL if n != "bwd_delta" or batch.act == W.SOFTMAX]
+    n_fwd, n_bwd = 1, len(names) - 1
+    if f32 or D == 32:
+        raise SystemExit("bench: staged (fp32 / D=32) workloads are parity cases, not bench lines")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    phys = int(visible[local]) if local < len(visible) and visible[local].strip().isdigit() else local
+    sampler = ClockSampler(phys)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = plan.launch_count
+    sampler.start()
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        starts[s].record(stream)
+        plan.update(batch.q_off, batch.kv_off, stream)
+        plan.set_events(kev[s][0:n_fwd + 1])
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
+        plan.set_events(kev[s][n_fwd:])
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
+        ends[s].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    plan.set_events(None)
+    launches = plan.launch_count - launches0
+    st = plan.check_status()
+    if st != 0:
+        raise RuntimeError("device status after timed region: " + J.status_str(st))
+
+    step_ms = np.array([starts[s].elapsed_time(ends[s]) for s in range(args.steps)])
+    ms = float(step_ms.mean())
+    per_kernel = {n: float(np.mean([kev[s][i].elapsed_time(kev[s][i + 1]) for s in range(args.steps)]))
+                  for i, n in enumerate(names)}
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block)
+    value = ws * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
+    pk, pk_kind = peaks()
+
+    # roofline of the dominant kernel (largest share of the step's kernel time)
+    dom = max(per_kernel, key=per_kernel.get)
+    fl, by = kernel_work(w, batch, dom, pk)
+    t_dom = per_kernel[dom] * 1e-3
+    bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
+    intensity = (f_fwd + f_bwd) / (bf + bb)
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if fl > 0 and fl / by >= ridge * 0.5:
+        roof = {"bound": "tensor", "achieved": fl / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = dom
+    roof["peak_source"] = pk_kind + " (burst)"
+    roof["algorithmic_flops_per_launch"] = fl
+    roof["algorithmic_bytes_per_launch"] = by
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, w, batch, plan, dev, stream) if not args.no_e2e else None
+    if ws > 1 and e2e is not None:
+        t = torch.tensor([e2e["ms_per_step"]], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(t.item())
+        e2e["value"] = ws * (f_fwd + f_bwd) / (e2e["ms_per_step"] * 1e-3) / 1e12
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(w, batch.act, batch.B, True),
+            "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
+            "pct_of_bf16_peak_sustained": 100.0 * value / ws / pk["bf16_tflops_sustained"],
+            "per_kernel_ms": per_kernel, "gpu_launches": int(launches),
+            "roofline": roof, "clocks": clocks,
+            "workload_intensity_flop_per_byte": intensity,
+            "timed_wall_s": t_wall}
+    if e2e is not None:
+        line["e2e"] = {k2: e2e[k2] for k2 in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
+        line["e2e"]["ms_per_step"] = e2e["ms_per_step"]
+    if rank == 0 and ws == 1 and not args.no_cpu:
+        v_cpu, dt, cores, desc = time_oracle(batch, args.cpu_frac, seed=0)
+        line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, w, batch, plan, dev, stream):
+    """Same step through the C ABI with HOST inputs and outputs: pinned host -> device
+    copies of q, k, v, dO, bias and the offsets (re-planned from host arrays), the
+    kernels, and device -> host copies of O, dQ, dK, dV, all inside the timed region."""
+    H, D = w.H, w.D
+    tdt = batch.q.dtype
+    hq, hk, hv, hdo = (t.pin_memory() for t in (batch.q, batch.k, batch.v, batch.dout))
+    hbias = batch.bias.pin_memory() if batch.bias is not None else None
+    q = torch.empty_like(hq, device=dev)
+    k = torch.empty_like(hk, device=dev)
+    v = torch.empty_like(hv, device=dev)
+    dout = torch.empty_like(hdo, device=dev)
+    bias = torch.empty_like(hbias, device=dev) if hbias is not None else None
+    out = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
+    lse = torch.empty(H, batch.Tq, dtype=torch.float32, device=dev) if batch.act == W.SOFTMAX else None
+    dq = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
+    dk = torch.empty(batch.Tk, H, D, dtype=tdt, device=dev)
+    dv = torch.empty(batch.Tk, H, D, dtype=tdt, device=dev)
+    ho, hdq, hdk, hdv = (torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, dq, dk, dv))
+    fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(plan.bwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo) + ((hbias,) if hbias is not None else ()))
+    h2d += 4 * (len(batch.q_off) + len(batch.kv_off))  # offsets (the plan's tile upload is counted too)
+    tiles_q, cta_q = plan.tiles(0)
+    tiles_k, cta_k = plan.tiles(1)
+    h2d += 24 * (len(tiles_q) + len(tiles_k)) + 4 * (len(cta_q) + len(cta_k))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
+
+    def step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        dout.copy_(hdo, non_blocking=True)
+        if bias is not None:
+            bias.copy_(hbias, non_blocking=True)
+        plan.update(batch.q_off, batch.kv_off, stream)
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
+        ho.copy_(out, non_blocking=True)
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 10))
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block)
+    return {"value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: jagged self-attention + bias)")
+    ap.add_argument("--act", choices=["softmax", "silu", "gelu_tanh"], default=None)
+    ap.add_argument("--cpu-frac", type=float, default=0.25, help="share of the batch's pairs the CPU baseline runs")
+    ap.add_argument("--ref-frac", type=float, default=1.0 / 32, help="share of the batch per reference-arm step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    act = None if args.act is None else {"softmax": 0, "silu": 1, "gelu_tanh": 2}[args.act]
+    batch = W.make_batch(args.workload, act=act)
+    if args.impl == "reference":
+        run_reference(args, batch.w, batch)
+    else:
+        run_ours(args, batch.w, batch)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,180 @@
+/*
+ * jattn.h -- C ABI of the GB300 (sm_103a) jagged attention library.
+ *
+ * The operation ("Training GEM at LLM scale", section "Jagged Sequence Flash
+ * Attention"): FlashAttention computed directly on variable-length jagged
+ * tensors, with asymmetric query / key-value lengths, custom attention biases
+ * and a backward pass; section "Generalized Dot-Product Attention (GDPA)": the
+ * softmax replaced by a pointwise GELU or SiLU with no normalisation; section
+ * "BlockAttention": each 64-token query block attends only to its own 64-token
+ * key/value block.
+ *
+ * For sequence b with local query rows i < Lq_b and keys j < Lk_b, head h:
+ *   s_ij = scale * <q_i, k_j> + T[h, min(|i - j|, NB - 1)]     (bias optional, not scaled)
+ *   softmax: O_i = sum_j softmax_j(s_ij) v_j,  lse_i = ln sum_j exp(s_ij)
+ *   SiLU / tanh-GELU: O_i = sum_j act(s_ij) v_j
+ *   BlockAttention: j restricted to floor(j/64) == floor(i/64)
+ *
+ * Tensor layout (every device tensor, caller-owned):
+ *   q, out, dout, dq : [Tq, H, D] row-major (token, head, feature), row stride H*D
+ *   k, v, dk, dv     : [Tk, H, D]
+ *   offsets          : int32 exclusive prefix sums, length B+1, offsets[0] = 0,
+ *                      non-decreasing; Tq = q_offsets[B], Tk = kv_offsets[B]
+ *   bias table       : float32 [H, NB] (NB = mode.bias_buckets), or NULL
+ *   lse              : float32 [H, Tq] (softmax only)
+ *   element type     : bfloat16 (JATTN_BF16) or float32 (JATTN_FP32) for q, k, v,
+ *                      out, dout, dq, dk, dv alike; all arithmetic runs in bf16
+ *                      tensor-core products with fp32 accumulation.
+ * Device pointers must be 16-byte aligned.  D is 32, 64 or 128.  Positions i, j
+ * are local to the sequence (also in cross-attention).  A sequence with Lk = 0
+ * yields O_i = 0 and lse_i = -inf; a sequence with Lq = 0 yields dk = dv = 0.
+ *
+ * Errors: argument errors are returned before anything is launched; a failed
+ * launch returns JATTN_ERR_CUDA; errors found on the device while a kernel runs
+ * (a bounded wait that ran out, a tile record that fails its checks) are
+ * written to the plan's device status word and reported, and cleared, by
+ * jattn_check_device_status.  Nothing in the library aborts the process or
+ * traps on the device.
+ *
+ * Calls that take a stream are stream-ordered and do not block the host,
+ * except jattn_check_device_status (synchronises the stream).  A plan must not
+ * be used on two streams at once.
+ */
+#ifndef JATTN_H_
+#define JATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    JATTN_OK = 0,
+    JATTN_ERR_INVALID_ARG = 1,    /* bad offsets, sizes, NULL pointers, mode fields */
+    JATTN_ERR_UNSUPPORTED = 2,    /* valid but not implemented (e.g. D = 96) */
+    JATTN_ERR_ALIGNMENT = 3,      /* a device pointer is not 16-byte aligned */
+    JATTN_ERR_WORKSPACE = 4,      /* workspace NULL or smaller than required */
+    JATTN_ERR_CUDA = 5,           /* a CUDA runtime call or launch failed */
+    JATTN_ERR_DEVICE_TIMEOUT = 6, /* a kernel's bounded wait ran out (device status) */
+    JATTN_ERR_DEVICE_CHECK = 7,   /* a kernel rejected a tile record (device status) */
+    JATTN_ERR_NO_DEVICE = 8       /* the plan was made host-only (device = -1) */
+} jattn_status;
+
+typedef enum { JATTN_SOFTMAX = 0, JATTN_SILU = 1, JATTN_GELU_TANH = 2 } jattn_act;
+typedef enum { JATTN_BF16 = 0, JATTN_FP32 = 1 } jattn_dtype;
+
+/* Which operation a plan serves. */
+typedef struct {
+    int32_t act;          /* jattn_act */
+    int32_t block;        /* 0 = full attention, 64 = BlockAttention (needs q_offsets == kv_offsets) */
+    float scale;          /* score scale; 0 selects 1/sqrt(D) */
+    int32_t bias_buckets; /* 0 = no bias, else NB >= 1 with H * NB <= 256 */
+    int32_t dtype;        /* jattn_dtype */
+} jattn_mode;
+
+/* One unit of work: rows [q_start, q_start+q_len) of Q against rows
+ * [kv_start, kv_start+kv_len) of K/V for sequence b and head h.  24 bytes. */
+typedef struct {
+    int32_t b, h, q_start, q_len, kv_start, kv_len;
+} jattn_tile;
+
+typedef enum {
+    JATTN_TILES_Q = 0,  /* query-major tiles: forward and the dQ pass (128 query rows each) */
+    JATTN_TILES_KV = 1  /* key-major tiles: the dK/dV pass (128 key rows each) */
+} jattn_tile_list;
+
+typedef struct jattn_plan jattn_plan; /* opaque */
+
+/*
+ * Build the tile lists and the persistent-grid schedule for one jagged batch
+ * ("Training GEM at LLM scale", section "Generalized Dot-Product Attention
+ * (GDPA)": valid tiles are precomputed on the CPU, empty tiles skipped, and the
+ * tiles spread over the SMs to remove workload skew).
+ *   q_offsets, kv_offsets : HOST int32 arrays of length B+1 (copied; caller keeps ownership)
+ *   B >= 1, H >= 1, D in {32, 64, 128}
+ *   mode                  : HOST pointer, copied
+ *   device                : CUDA device ordinal, or -1 for a host-only plan (tile
+ *                           lists only; jattn_fwd / jattn_bwd then return JATTN_ERR_NO_DEVICE)
+ *   out                   : receives the plan; free it with jattn_plan_destroy
+ * With a device the plan allocates its tile arrays and a status word on that
+ * device and uploads the tiles with one host-to-device copy on the default
+ * stream (synchronised before return).
+ */
+jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B, int32_t H, int32_t D,
+                               const jattn_mode *mode, int32_t device, jattn_plan **out);
+
+/*
+ * Re-plan the same plan (same H, D and mode) for a new batch: rebuilds the tile
+ * lists on the host and uploads them with an asynchronous copy on `stream`
+ * (a cudaStream_t; NULL = default stream) from pinned memory the plan owns.
+ * Device buffers grow (stream-synchronising) only when the new batch has more
+ * tiles or sequences than any before.  Stream order makes the new tiles visible
+ * to every later call on `stream` and keeps earlier calls on the old tiles.
+ */
+jattn_status jattn_plan_update(jattn_plan *plan, const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B,
+                               void *stream);
+
+/*
+ * Host view of a scheduled tile list, for inspection and tests.  The records are
+ * grouped by CTA: CTA c runs tiles[cta_begin[c] .. cta_begin[c+1]) in order.
+ * The pointers stay valid until the next jattn_plan_update or jattn_plan_destroy.
+ */
+jattn_status jattn_plan_tiles(const jattn_plan *plan, int32_t which, const jattn_tile **tiles, int64_t *n_tiles,
+                              const int32_t **cta_begin, int32_t *n_ctas);
+
+/* Device scratch the caller must pass to jattn_fwd / jattn_bwd (bytes; 0 = none needed). */
+size_t jattn_fwd_workspace_bytes(const jattn_plan *plan);
+size_t jattn_bwd_workspace_bytes(const jattn_plan *plan);
+
+/* Frees the plan's host and device memory (synchronises its device). NULL is a no-op. */
+void jattn_plan_destroy(jattn_plan *plan);
+
+/*
+ * Forward.  q, k, v: DEVICE inputs; out: DEVICE output [Tq, H, D];
+ * bias: DEVICE [H, NB] float32 iff mode.bias_buckets > 0 (else must be NULL);
+ * lse: DEVICE float32 [H, Tq], written when non-NULL in softmax mode (required
+ * later by jattn_bwd in full softmax mode), must be NULL otherwise.
+ * workspace: DEVICE scratch of jattn_fwd_workspace_bytes (may be NULL when 0).
+ * stream: cudaStream_t.
+ */
+jattn_status jattn_fwd(const jattn_plan *plan, const void *q, const void *k, const void *v, const float *bias,
+                       void *out, float *lse, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward.  dout, q, k, v, out: DEVICE inputs (out = the forward output);
+ * lse: the forward's lse (required in full softmax mode, ignored otherwise);
+ * dq, dk, dv: DEVICE outputs, fully overwritten (no accumulation, no atomics);
+ * dbias: DEVICE float32 [H, NB] gradient of the bias table, written when non-NULL
+ * (needs a bias); workspace: DEVICE scratch of jattn_bwd_workspace_bytes.
+ * dq and dk include the score scale; dbias is the plain sum of dS per bucket.
+ */
+jattn_status jattn_bwd(const jattn_plan *plan, const void *dout, const void *q, const void *k, const void *v,
+                       const float *bias, const void *out, const float *lse, void *dq, void *dk, void *dv,
+                       float *dbias, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Profiling hook (optional).  After this call every jattn_fwd / jattn_bwd on
+ * the plan records events[0] on its stream before its first kernel and
+ * events[i] right after its i-th kernel (i < n_events), so elapsed times
+ * between consecutive events are per-kernel device durations.  `events` is a
+ * HOST array of cudaEvent_t handles owned by the caller (copied; the handles
+ * must stay valid while set); NULL or n_events = 0 turns the hook off.
+ */
+jattn_status jattn_plan_set_events(jattn_plan *plan, void *const *events, int32_t n_events);
+
+/* Number of kernels launched through this plan since it was created (host counter). */
+int64_t jattn_plan_launch_count(const jattn_plan *plan);
+
+/* Synchronises `stream`, then returns and clears the plan's device status word. */
+jattn_status jattn_check_device_status(const jattn_plan *plan, void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *jattn_status_str(jattn_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JATTN_H_ */

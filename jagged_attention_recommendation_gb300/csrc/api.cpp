@@ -1,0 +1,589 @@
+// api.cpp -- the C ABI (include/jattn.h): argument checks, the jagged batch
+// planner (tile lists + persistent-grid schedule), tensor-map construction and
+// kernel dispatch.  Host code only; every step of the computation runs in the
+// CUDA kernels.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <queue>
+#include <vector>
+
+#include "common.h"
+#include "jattn.h"
+#include "kernels.h"
+
+using namespace jattn;
+
+static_assert(sizeof(jattn_tile) == sizeof(Tile), "tile record layout");
+static_assert(sizeof(jattn_tile) == 24, "tile record is 24 bytes");
+
+namespace {
+
+constexpr int kTileRows = 128;       // rows per query-major and key-major tile
+constexpr int kDefaultSms = 152;     // schedule width of a host-only plan
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct jattn_plan {
+    int32_t B = 0, H = 0, D = 0, Dp = 0;
+    jattn_mode mode{};
+    float scale = 0.0f;
+    int32_t device = -1;
+    int32_t num_sms = kDefaultSms;
+    bool staged = false;  // inputs are copied to bf16 [T, H, Dp] first (fp32 data or D = 32)
+    int64_t Tq = 0, Tk = 0;
+    std::vector<int32_t> q_off, kv_off;
+    std::vector<jattn_tile> tiles[2];
+    std::vector<int32_t> cta[2];
+    // device copies: one buffer holding both tile lists, both schedules and the offsets
+    uint8_t *d_buf = nullptr;
+    size_t d_cap = 0;
+    size_t off_tiles[2] = {0, 0}, off_cta[2] = {0, 0}, off_qoff = 0, off_kvoff = 0;
+    int *d_status = nullptr;
+    // pinned staging for the asynchronous upload, double-buffered
+    void *h_pin[2] = {nullptr, nullptr};
+    size_t h_cap[2] = {0, 0};
+    cudaEvent_t ev[2] = {nullptr, nullptr};
+    bool ev_used[2] = {false, false};
+    int pin_next = 0;
+    // profiling hook and launch counter (mutable: updated by const calls)
+    mutable std::vector<cudaEvent_t> prof_events;
+    mutable int prof_next = 0;
+    mutable int64_t launches = 0;
+};
+
+namespace {
+
+// Restores the caller's current device on scope exit.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = true;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        if (prev != dev) ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+jattn_status check_offsets(const int32_t *qo, const int32_t *ko, int32_t B, bool block) {
+    if (qo == nullptr || ko == nullptr || B < 1) return JATTN_ERR_INVALID_ARG;
+    if (qo[0] != 0 || ko[0] != 0) return JATTN_ERR_INVALID_ARG;
+    for (int32_t b = 0; b < B; ++b) {
+        if (qo[b + 1] < qo[b] || ko[b + 1] < ko[b]) return JATTN_ERR_INVALID_ARG;
+        if (block && (qo[b + 1] - qo[b]) != (ko[b + 1] - ko[b])) return JATTN_ERR_INVALID_ARG;
+    }
+    return JATTN_OK;
+}
+
+int cost_rows(int n) { return (n + 15) / 16; }
+
+// Longest-processing-time-first assignment of tiles to n_ctas persistent CTAs:
+// tiles in decreasing cost order, each to the currently least-loaded CTA (ties
+// to the lower CTA id), then regrouped so CTA c runs list[cta[c] .. cta[c+1]).
+void schedule(std::vector<jattn_tile> &list, std::vector<int32_t> &cta, int num_sms, bool kv_major, bool block) {
+    const size_t n = list.size();
+    const int n_ctas = static_cast<int>(std::min<size_t>(n, static_cast<size_t>(std::max(num_sms, 1))));
+    cta.assign(static_cast<size_t>(n_ctas) + 1, 0);
+    if (n == 0) return;
+    std::vector<int64_t> cost(n);
+    for (size_t i = 0; i < n; ++i) {
+        const jattn_tile &t = list[i];
+        const int span = block ? t.q_len : (kv_major ? t.q_len : t.kv_len);
+        cost[i] = 8 + cost_rows(span);  // fixed per-tile work + 16-column MMA groups
+    }
+    std::vector<int32_t> order(n);
+    for (size_t i = 0; i < n; ++i) order[i] = static_cast<int32_t>(i);
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+    using Slot = std::pair<int64_t, int32_t>;  // (load, cta)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t c = 0; c < n_ctas; ++c) heap.push({0, c});
+    std::vector<int32_t> owner(n);
+    std::vector<int32_t> count(static_cast<size_t>(n_ctas), 0);
+    for (int32_t idx : order) {
+        Slot s = heap.top();
+        heap.pop();
+        owner[idx] = s.second;
+        ++count[s.second];
+        heap.push({s.first + cost[idx], s.second});
+    }
+    for (int32_t c = 0; c < n_ctas; ++c) cta[c + 1] = cta[c] + count[c];
+    std::vector<jattn_tile> out(n);
+    std::vector<int32_t> fill(cta.begin(), cta.end() - 1);
+    for (int32_t idx : order) out[fill[owner[idx]]++] = list[idx];
+    list.swap(out);
+}
+
+void build_lists(jattn_plan *p) {
+    const bool block = p->mode.block != 0;
+    std::vector<jattn_tile> &tq = p->tiles[JATTN_TILES_Q];
+    std::vector<jattn_tile> &tk = p->tiles[JATTN_TILES_KV];
+    tq.clear();
+    tk.clear();
+    for (int32_t b = 0; b < p->B; ++b) {
+        const int32_t q0 = p->q_off[b], Lq = p->q_off[b + 1] - q0;
+        const int32_t k0 = p->kv_off[b], Lk = p->kv_off[b + 1] - k0;
+        for (int32_t s = 0; s < Lq; s += kTileRows) {
+            const int32_t ql = std::min(kTileRows, Lq - s);
+            for (int32_t h = 0; h < p->H; ++h) {
+                if (block)
+                    tq.push_back({b, h, q0 + s, ql, k0 + s, ql});
+                else
+                    tq.push_back({b, h, q0 + s, ql, k0, Lk});
+            }
+        }
+    }
+    if (!block) {
+        for (int32_t b = 0; b < p->B; ++b) {
+            const int32_t q0 = p->q_off[b], Lq = p->q_off[b + 1] - q0;
+            const int32_t k0 = p->kv_off[b], Lk = p->kv_off[b + 1] - k0;
+            for (int32_t s = 0; s < Lk; s += kTileRows) {
+                const int32_t kl = std::min(kTileRows, Lk - s);
+                for (int32_t h = 0; h < p->H; ++h) tk.push_back({b, h, q0, Lq, k0 + s, kl});
+            }
+        }
+    }
+    schedule(tq, p->cta[JATTN_TILES_Q], p->num_sms, false, block);
+    schedule(tk, p->cta[JATTN_TILES_KV], p->num_sms, true, block);
+}
+
+jattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? JATTN_OK : JATTN_ERR_CUDA; }
+
+// Lay out and upload tiles, schedules and offsets (asynchronously on `stream`).
+jattn_status upload(jattn_plan *p, cudaStream_t stream) {
+    size_t off = 0;
+    for (int w = 0; w < 2; ++w) {
+        p->off_tiles[w] = off;
+        off = align_up(off + p->tiles[w].size() * sizeof(jattn_tile), 16);
+    }
+    for (int w = 0; w < 2; ++w) {
+        p->off_cta[w] = off;
+        off = align_up(off + p->cta[w].size() * sizeof(int32_t), 16);
+    }
+    p->off_qoff = off;
+    off = align_up(off + p->q_off.size() * sizeof(int32_t), 16);
+    p->off_kvoff = off;
+    off = align_up(off + p->kv_off.size() * sizeof(int32_t), 16);
+    const size_t bytes = off;
+
+    if (bytes > p->d_cap) {
+        cudaError_t e = cudaStreamSynchronize(stream);  // earlier launches may still read the old buffer
+        if (e != cudaSuccess) return JATTN_ERR_CUDA;
+        if (p->d_buf) cudaFree(p->d_buf);
+        p->d_buf = nullptr;
+        p->d_cap = 0;
+        const size_t cap = std::max(bytes + bytes / 2, static_cast<size_t>(4096));
+        if (cudaMalloc(&p->d_buf, cap) != cudaSuccess) return JATTN_ERR_CUDA;
+        p->d_cap = cap;
+    }
+    const int k = p->pin_next;
+    p->pin_next ^= 1;
+    if (p->ev_used[k]) {
+        if (cudaEventSynchronize(p->ev[k]) != cudaSuccess) return JATTN_ERR_CUDA;
+    }
+    if (bytes > p->h_cap[k]) {
+        if (p->h_pin[k]) cudaFreeHost(p->h_pin[k]);
+        p->h_pin[k] = nullptr;
+        p->h_cap[k] = 0;
+        const size_t cap = std::max(bytes + bytes / 2, static_cast<size_t>(4096));
+        if (cudaMallocHost(&p->h_pin[k], cap) != cudaSuccess) return JATTN_ERR_CUDA;
+        p->h_cap[k] = cap;
+    }
+    uint8_t *h = static_cast<uint8_t *>(p->h_pin[k]);
+    for (int w = 0; w < 2; ++w) {
+        if (!p->tiles[w].empty())
+            std::memcpy(h + p->off_tiles[w], p->tiles[w].data(), p->tiles[w].size() * sizeof(jattn_tile));
+        std::memcpy(h + p->off_cta[w], p->cta[w].data(), p->cta[w].size() * sizeof(int32_t));
+    }
+    std::memcpy(h + p->off_qoff, p->q_off.data(), p->q_off.size() * sizeof(int32_t));
+    std::memcpy(h + p->off_kvoff, p->kv_off.data(), p->kv_off.size() * sizeof(int32_t));
+    if (cudaMemcpyAsync(p->d_buf, h, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return JATTN_ERR_CUDA;
+    if (cudaEventRecord(p->ev[k], stream) != cudaSuccess) return JATTN_ERR_CUDA;
+    p->ev_used[k] = true;
+    return JATTN_OK;
+}
+
+jattn_status set_batch(jattn_plan *p, const int32_t *qo, const int32_t *ko, int32_t B) {
+    jattn_status st = check_offsets(qo, ko, B, p->mode.block != 0);
+    if (st != JATTN_OK) return st;
+    p->B = B;
+    p->q_off.assign(qo, qo + B + 1);
+    p->kv_off.assign(ko, ko + B + 1);
+    p->Tq = qo[B];
+    p->Tk = ko[B];
+    build_lists(p);
+    return JATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    });
+    return fn;
+}
+
+// bf16 view [T, H*Dp] of a token-major tensor; boxes of 64 columns x box_rows rows,
+// 128-byte swizzle (the layout the MMA descriptors expect).
+bool make_tmap(CUtensorMap *m, const void *ptr, int64_t T, int H, int Dp, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H) * Dp, static_cast<cuuint64_t>(std::max<int64_t>(T, 1))};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H) * Dp * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t stage_bytes(const jattn_plan *p, int64_t rows) {
+    return align_up(static_cast<size_t>(rows) * p->H * p->Dp * 2, kAlign);
+}
+
+bool softmax_full(const jattn_plan *p) { return p->mode.act == JATTN_SOFTMAX && p->mode.block == 0; }
+
+Geom make_geom(const jattn_plan *p, int which) {
+    Geom g{};
+    g.tiles = reinterpret_cast<const Tile *>(p->d_buf + p->off_tiles[which]);
+    g.cta_begin = reinterpret_cast<const int32_t *>(p->d_buf + p->off_cta[which]);
+    g.q_off = reinterpret_cast<const int32_t *>(p->d_buf + p->off_qoff);
+    g.kv_off = reinterpret_cast<const int32_t *>(p->d_buf + p->off_kvoff);
+    g.n_tiles = static_cast<int32_t>(p->tiles[which].size());
+    g.B = p->B;
+    g.H = p->H;
+    g.max_q_len = which == JATTN_TILES_Q ? kTileRows : INT_MAX;
+    g.max_kv_len = which == JATTN_TILES_KV ? kTileRows : INT_MAX;
+    g.Tq = static_cast<int32_t>(p->Tq);
+    g.Tk = static_cast<int32_t>(p->Tk);
+    g.act = p->mode.act;
+    g.block = p->mode.block;
+    g.nb = p->mode.bias_buckets;
+    g.scale = p->scale;
+    g.bias = nullptr;
+    g.status = p->d_status;
+    return g;
+}
+
+OutDesc out_desc(const jattn_plan *p, void *ptr) {
+    OutDesc o;
+    o.ptr = ptr;
+    o.f32 = p->mode.dtype == JATTN_FP32 ? 1 : 0;
+    o.cols = p->D;
+    o.ld = static_cast<int64_t>(p->H) * p->D;
+    return o;
+}
+
+int n_ctas(const jattn_plan *p, int which) { return static_cast<int>(p->cta[which].size()) - 1; }
+
+// Per-call launch bookkeeping: records the profiling events (if any) and counts kernels.
+struct LaunchLog {
+    const jattn_plan *p;
+    cudaStream_t st;
+    LaunchLog(const jattn_plan *plan, cudaStream_t stream) : p(plan), st(stream) {
+        p->prof_next = 0;
+        mark();
+    }
+    void mark() {
+        if (p->prof_next < static_cast<int>(p->prof_events.size()))
+            cudaEventRecord(p->prof_events[p->prof_next++], st);
+    }
+    // one kernel was launched (launch functions that skip an empty grid still count as one)
+    cudaError_t done(cudaError_t e) {
+        if (e == cudaSuccess) {
+            ++p->launches;
+            mark();
+        }
+        return e;
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B, int32_t H, int32_t D,
+                               const jattn_mode *mode, int32_t device, jattn_plan **out) {
+    if (out == nullptr || mode == nullptr) return JATTN_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (H < 1 || B < 1) return JATTN_ERR_INVALID_ARG;
+    if (D != 32 && D != 64 && D != 128) return (D > 0) ? JATTN_ERR_UNSUPPORTED : JATTN_ERR_INVALID_ARG;
+    if (mode->act < JATTN_SOFTMAX || mode->act > JATTN_GELU_TANH) return JATTN_ERR_INVALID_ARG;
+    if (mode->block != 0 && mode->block != 64) return JATTN_ERR_UNSUPPORTED;
+    if (mode->dtype != JATTN_BF16 && mode->dtype != JATTN_FP32) return JATTN_ERR_INVALID_ARG;
+    if (mode->bias_buckets < 0) return JATTN_ERR_INVALID_ARG;
+    if (mode->bias_buckets > 0 && H * mode->bias_buckets > kMaxBiasFloats) return JATTN_ERR_UNSUPPORTED;
+    if (!(mode->scale >= 0.0f) || std::isinf(mode->scale)) return JATTN_ERR_INVALID_ARG;
+    if (device < -1) return JATTN_ERR_INVALID_ARG;
+
+    jattn_plan *p = new (std::nothrow) jattn_plan();
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    p->H = H;
+    p->D = D;
+    p->Dp = D < 64 ? 64 : D;
+    p->mode = *mode;
+    p->scale = mode->scale > 0.0f ? mode->scale : 1.0f / std::sqrt(static_cast<float>(D));
+    p->staged = mode->dtype == JATTN_FP32 || D == 32;
+    p->device = device;
+    if (device >= 0) {
+        DeviceGuard g(device);
+        int sms = 0;
+        if (!g.ok || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+            delete p;
+            return JATTN_ERR_CUDA;
+        }
+        p->num_sms = sms;
+    }
+    jattn_status st = set_batch(p, q_offsets, kv_offsets, B);
+    if (st != JATTN_OK) {
+        delete p;
+        return st;
+    }
+    if (device >= 0) {
+        DeviceGuard g(device);
+        bool ok = cudaMalloc(&p->d_status, 16) == cudaSuccess && cudaMemset(p->d_status, 0, 16) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&p->ev[0], cudaEventDisableTiming) == cudaSuccess &&
+                  cudaEventCreateWithFlags(&p->ev[1], cudaEventDisableTiming) == cudaSuccess;
+        if (ok) ok = upload(p, nullptr) == JATTN_OK && cudaStreamSynchronize(nullptr) == cudaSuccess;
+        if (!ok) {
+            jattn_plan_destroy(p);
+            return JATTN_ERR_CUDA;
+        }
+    }
+    *out = p;
+    return JATTN_OK;
+}
+
+jattn_status jattn_plan_update(jattn_plan *plan, const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B,
+                               void *stream) {
+    if (plan == nullptr) return JATTN_ERR_INVALID_ARG;
+    jattn_status st = check_offsets(q_offsets, kv_offsets, B, plan->mode.block != 0);
+    if (st != JATTN_OK) return st;
+    set_batch(plan, q_offsets, kv_offsets, B);
+    if (plan->device < 0) return JATTN_OK;
+    DeviceGuard g(plan->device);
+    if (!g.ok) return JATTN_ERR_CUDA;
+    return upload(plan, static_cast<cudaStream_t>(stream));
+}
+
+jattn_status jattn_plan_tiles(const jattn_plan *plan, int32_t which, const jattn_tile **tiles, int64_t *n_tiles,
+                              const int32_t **cta_begin, int32_t *n_ctas_out) {
+    if (plan == nullptr || (which != JATTN_TILES_Q && which != JATTN_TILES_KV)) return JATTN_ERR_INVALID_ARG;
+    if (tiles) *tiles = plan->tiles[which].data();
+    if (n_tiles) *n_tiles = static_cast<int64_t>(plan->tiles[which].size());
+    if (cta_begin) *cta_begin = plan->cta[which].data();
+    if (n_ctas_out) *n_ctas_out = n_ctas(plan, which);
+    return JATTN_OK;
+}
+
+size_t jattn_fwd_workspace_bytes(const jattn_plan *p) {
+    if (p == nullptr || !p->staged) return 0;
+    return stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
+}
+
+size_t jattn_bwd_workspace_bytes(const jattn_plan *p) {
+    if (p == nullptr) return 0;
+    size_t n = softmax_full(p) ? align_up(static_cast<size_t>(p->H) * p->Tq * 4, kAlign) : 0;
+    if (p->staged) n += 2 * stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
+    return n;
+}
+
+void jattn_plan_destroy(jattn_plan *p) {
+    if (p == nullptr) return;
+    if (p->device >= 0) {
+        DeviceGuard g(p->device);
+        cudaDeviceSynchronize();
+        if (p->d_buf) cudaFree(p->d_buf);
+        if (p->d_status) cudaFree(p->d_status);
+        for (int k = 0; k < 2; ++k) {
+            if (p->h_pin[k]) cudaFreeHost(p->h_pin[k]);
+            if (p->ev[k]) cudaEventDestroy(p->ev[k]);
+        }
+    }
+    delete p;
+}
+
+jattn_status jattn_fwd(const jattn_plan *p, const void *q, const void *k, const void *v, const float *bias, void *out,
+                       float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    if (!q || !k || !v || !out) return JATTN_ERR_INVALID_ARG;
+    if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;
+    if (lse != nullptr && p->mode.act != JATTN_SOFTMAX) return JATTN_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(bias))
+        return JATTN_ERR_ALIGNMENT;
+    const size_t need = jattn_fwd_workspace_bytes(p);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return JATTN_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return JATTN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int f32 = p->mode.dtype == JATTN_FP32;
+    const void *qq = q, *kk = k, *vv = v;
+    LaunchLog log(p, st);
+    if (p->staged) {
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        void *qs = ws, *ks = ws + stage_bytes(p, p->Tq), *vs = ws + stage_bytes(p, p->Tq) + stage_bytes(p, p->Tk);
+        if (log.done(launch_stage(q, f32, p->Tq * p->H, p->D, p->Dp, qs, st)) != cudaSuccess) return JATTN_ERR_CUDA;
+        if (log.done(launch_stage(k, f32, p->Tk * p->H, p->D, p->Dp, ks, st)) != cudaSuccess) return JATTN_ERR_CUDA;
+        if (log.done(launch_stage(v, f32, p->Tk * p->H, p->D, p->Dp, vs, st)) != cudaSuccess) return JATTN_ERR_CUDA;
+        qq = qs;
+        kk = ks;
+        vv = vs;
+    }
+    TmapSet tm;
+    if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
+        !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
+        return JATTN_ERR_CUDA;
+    tm.dout = tm.q;
+    FwdArgs a;
+    a.g = make_geom(p, JATTN_TILES_Q);
+    a.g.bias = bias;
+    a.out = out_desc(p, out);
+    a.lse = lse;
+    return cuda_status(log.done(launch_fwd(p->Dp, p->mode.act != JATTN_SOFTMAX, tm, a, n_ctas(p, JATTN_TILES_Q), st)));
+}
+
+jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, const void *k, const void *v,
+                       const float *bias, const void *out, const float *lse, void *dq, void *dk, void *dv,
+                       float *dbias, void *workspace, size_t workspace_bytes, void *stream) {
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    if (!dout || !q || !k || !v || !out || !dq || !dk || !dv) return JATTN_ERR_INVALID_ARG;
+    if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;
+    if (softmax_full(p) && lse == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (dbias != nullptr) return bias == nullptr ? JATTN_ERR_INVALID_ARG : JATTN_ERR_UNSUPPORTED;
+    if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv) || !aligned16(bias) || !aligned16(lse))
+        return JATTN_ERR_ALIGNMENT;
+    const size_t need = jattn_bwd_workspace_bytes(p);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return JATTN_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return JATTN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int f32 = p->mode.dtype == JATTN_FP32;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *delta = nullptr;
+    if (softmax_full(p)) {
+        delta = reinterpret_cast<float *>(ws);
+        ws += align_up(static_cast<size_t>(p->H) * p->Tq * 4, kAlign);
+    }
+    const void *qq = q, *kk = k, *vv = v, *dd = dout;
+    LaunchLog log(p, st);
+    if (p->staged) {
+        void *qs = ws;
+        void *ds = ws + stage_bytes(p, p->Tq);
+        void *ks = ws + 2 * stage_bytes(p, p->Tq);
+        void *vs = ws + 2 * stage_bytes(p, p->Tq) + stage_bytes(p, p->Tk);
+        if (log.done(launch_stage(q, f32, p->Tq * p->H, p->D, p->Dp, qs, st)) != cudaSuccess ||
+            log.done(launch_stage(dout, f32, p->Tq * p->H, p->D, p->Dp, ds, st)) != cudaSuccess ||
+            log.done(launch_stage(k, f32, p->Tk * p->H, p->D, p->Dp, ks, st)) != cudaSuccess ||
+            log.done(launch_stage(v, f32, p->Tk * p->H, p->D, p->Dp, vs, st)) != cudaSuccess)
+            return JATTN_ERR_CUDA;
+        qq = qs;
+        dd = ds;
+        kk = ks;
+        vv = vs;
+    }
+    BwdArgs a;
+    a.lse = lse;
+    a.delta = delta;
+    a.dq = out_desc(p, dq);
+    a.dk = out_desc(p, dk);
+    a.dv = out_desc(p, dv);
+    TmapSet tm;
+    if (p->mode.block != 0) {
+        if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
+            !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128))
+            return JATTN_ERR_CUDA;
+        a.g = make_geom(p, JATTN_TILES_Q);
+        a.g.bias = bias;
+        return cuda_status(log.done(launch_bwd_block(p->Dp, tm, a, n_ctas(p, JATTN_TILES_Q), st)));
+    }
+    if (delta != nullptr) {
+        if (log.done(launch_delta(out, dout, f32, p->Tq, p->H, p->D, delta, st)) != cudaSuccess)
+            return JATTN_ERR_CUDA;
+    }
+    const bool act = p->mode.act != JATTN_SOFTMAX;
+    // pass 1: dQ over query-major tiles (128 query rows, keys in blocks of 64)
+    if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128) ||
+        !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 64) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 64))
+        return JATTN_ERR_CUDA;
+    a.g = make_geom(p, JATTN_TILES_Q);
+    a.g.bias = bias;
+    if (log.done(launch_bwd_dq(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)) != cudaSuccess)
+        return JATTN_ERR_CUDA;
+    // pass 2: dK, dV over key-major tiles (128 key rows, queries in blocks of 64)
+    if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 64) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 64) ||
+        !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
+        return JATTN_ERR_CUDA;
+    a.g = make_geom(p, JATTN_TILES_KV);
+    a.g.bias = bias;
+    return cuda_status(log.done(launch_bwd_dkdv(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_KV), st)));
+}
+
+jattn_status jattn_plan_set_events(jattn_plan *p, void *const *events, int32_t n_events) {
+    if (p == nullptr || n_events < 0 || (n_events > 0 && events == nullptr)) return JATTN_ERR_INVALID_ARG;
+    p->prof_events.clear();
+    for (int32_t i = 0; i < n_events; ++i) p->prof_events.push_back(static_cast<cudaEvent_t>(events[i]));
+    return JATTN_OK;
+}
+
+int64_t jattn_plan_launch_count(const jattn_plan *p) { return p == nullptr ? 0 : p->launches; }
+
+jattn_status jattn_check_device_status(const jattn_plan *p, void *stream) {
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return JATTN_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return JATTN_ERR_CUDA;
+    int code = 0;
+    if (cudaMemcpy(&code, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return JATTN_ERR_CUDA;
+    if (code != 0 && cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) return JATTN_ERR_CUDA;
+    return static_cast<jattn_status>(code);
+}
+
+const char *jattn_status_str(jattn_status s) {
+    switch (s) {
+        case JATTN_OK: return "ok";
+        case JATTN_ERR_INVALID_ARG: return "invalid argument";
+        case JATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+        case JATTN_ERR_ALIGNMENT: return "device pointer not 16-byte aligned";
+        case JATTN_ERR_WORKSPACE: return "workspace missing or too small";
+        case JATTN_ERR_CUDA: return "CUDA runtime error";
+        case JATTN_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case JATTN_ERR_DEVICE_CHECK: return "device rejected a tile record";
+        case JATTN_ERR_NO_DEVICE: return "plan has no device";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,367 @@
+// bwd_block.cu -- BlockAttention backward for sm_103a.
+//
+// "Training GEM at LLM scale", section "BlockAttention": with fixed 64-token
+// blocks every query block attends only to its own key/value block, so the
+// problem splits into independent 64x64 attentions and a dedicated kernel
+// needs no online-softmax correction, no logsumexp traffic and no separate
+// Delta pre-processing.  Here one CTA pass handles a 128-row chunk (two
+// blocks) of one head:
+//   S = Q K^T and dP = dO V^T (128x128, block-diagonal part used),
+//   P = softmax over the row's own 64-block (recomputed, exact within the tile),
+//   Delta_i = sum_j P_ij dP_ij (= <dO_i, O_i>), dS = P (dP - Delta)
+//   (activation mode: P = act(S), dS = act'(S) dP),
+//   dV = P^T dO, dK = dS^T Q, dQ = dS K   (all in TMEM; dQ reuses the S columns).
+// P and dS are written once to shared memory as 128x128 bf16 tiles (zeros off
+// the diagonal blocks) and read by the tensor cores both as K-major and as
+// MN-major operands, so no transpose is ever materialised.  In activation mode
+// dS is unnormalised and also gets its bf16 remainder plane (hi + lo).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn.cuh"
+#include "kernels.h"
+
+namespace jattn {
+using namespace dev;
+
+template <int D>
+struct BlkCfg {
+    static constexpr int BM = 128;
+    static constexpr int NKB = D / 64;
+    static constexpr int NBUF = (D == 64) ? 2 : 1;
+    static constexpr uint32_t SUB = BM * 128;          // 16 KB sub-tile
+    static constexpr uint32_t T_BYTES = BM * D * 2;    // one [128, D] operand
+    static constexpr uint32_t IN_BYTES = 4 * T_BYTES;  // Q, K, V, dO
+    static constexpr uint32_t M_BYTES = BM * BM * 2;   // P or dS (two 16 KB sub-tiles)
+    static constexpr uint32_t OFF_IN = 0;
+    static constexpr uint32_t OFF_P = NBUF * IN_BYTES;
+    static constexpr uint32_t OFF_DS = OFF_P + M_BYTES;
+    static constexpr uint32_t OFF_DSLO = OFF_DS + M_BYTES;  // bf16 remainder of dS (activation mode)
+    static constexpr uint32_t OFF_BAR = OFF_DSLO + M_BYTES;
+    // in_full[NBUF], in_empty[NBUF], s_full, pd_full, acc_full, acc_empty, drain
+    static constexpr int NBAR = 2 * NBUF + 5;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
+    static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
+    static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = 0;  // S, later dQ
+    static constexpr uint32_t COL_DP = 128;
+    static constexpr uint32_t COL_DK = 256;
+    static constexpr uint32_t COL_DV = 256 + D;
+    // operand offsets inside one input buffer
+    static constexpr uint32_t IQ = 0, IK = T_BYTES, IV = 2 * T_BYTES, IDO = 3 * T_BYTES;
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    bwd_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const BwdArgs a) {
+    using C = BlkCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const Geom &g = a.g;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *in_full = bars;
+    uint64_t *in_empty = bars + C::NBUF;
+    uint64_t *s_full = bars + 2 * C::NBUF;
+    uint64_t *pd_full = s_full + 1;
+    uint64_t *acc_full = pd_full + 1;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *drain = acc_empty + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
+    const uint32_t sIn = smem_u32(smem + C::OFF_IN);
+    const uint32_t sP = smem_u32(smem + C::OFF_P);
+    const uint32_t sDS = smem_u32(smem + C::OFF_DS);
+    const uint32_t sDSlo = smem_u32(smem + C::OFF_DSLO);
+    const bool ACT = g.act != kSoftmax;
+
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < C::NBUF; ++b) {
+            mbar_init(&in_full[b], 1);
+            mbar_init(&in_empty[b], 1);
+        }
+        mbar_init(s_full, 1);
+        mbar_init(pd_full, 4);
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmDO);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const ErrCtx err{g.status, abort_flag};
+    const int tbeg = g.cta_begin[blockIdx.x];
+    const int tend = g.cta_begin[blockIdx.x + 1];
+
+    if (warp == 0) {
+        if (lane == 0) {
+            uint32_t t_local = 0;
+            bool ok = true;
+            for (int ti = tbeg; ti < tend && ok; ++ti) {
+                Tile t;
+                if (!load_tile(g, ti, t, err, true)) continue;
+                const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
+                if (!(ok = mbar_wait(&in_empty[buf], (use & 1) ^ 1, err))) break;
+                ++t_local;
+                mbar_arrive_expect_tx(&in_full[buf], C::IN_BYTES);
+                uint8_t *base = smem + C::OFF_IN + buf * C::IN_BYTES;
+                for (int kb = 0; kb < C::NKB; ++kb) {
+                    const int x = t.h * D + kb * 64;
+                    tma_load_2d(base + C::IQ + kb * C::SUB, &tmQ, &in_full[buf], x, t.q_start);
+                    tma_load_2d(base + C::IK + kb * C::SUB, &tmK, &in_full[buf], x, t.kv_start);
+                    tma_load_2d(base + C::IV + kb * C::SUB, &tmV, &in_full[buf], x, t.kv_start);
+                    tma_load_2d(base + C::IDO + kb * C::SUB, &tmDO, &in_full[buf], x, t.q_start);
+                }
+            }
+            if (!ok) {
+                for (uint32_t b = 0; b < C::NBUF && b < t_local; ++b) {
+                    const uint32_t last = t_local - 1 - ((t_local - 1 - b) % C::NBUF);
+                    mbar_drain(&in_full[last % C::NBUF], (last / C::NBUF) & 1);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            uint32_t t_local = 0;
+            const uint32_t idesc_mn = idesc_bf16(128, D, true, true);   // dV, dK
+            const uint32_t idesc_kmn = idesc_bf16(128, D, false, true); // dQ
+            bool ok = true;
+            for (int ti = tbeg; ti < tend && ok; ++ti) {
+                Tile t;
+                if (!load_tile(g, ti, t, err, false)) continue;
+                const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
+                if (!(ok = mbar_wait(&in_full[buf], use & 1, err))) break;
+                if (!(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
+                tc_fence_after();
+                const uint32_t base = sIn + buf * C::IN_BYTES;
+                const int n16 = round_up16(t.q_len);
+                const uint32_t idesc_s = idesc_bf16(128, n16, false, false);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t o = (ks >> 2) * C::SUB + (ks & 3) * 32;
+                    mma_bf16_ss(tmem + C::COL_S, sdesc_sw128(base + C::IQ + o, 16, 1024),
+                                sdesc_sw128(base + C::IK + o, 16, 1024), idesc_s, ks > 0);
+                    mma_bf16_ss(tmem + C::COL_DP, sdesc_sw128(base + C::IDO + o, 16, 1024),
+                                sdesc_sw128(base + C::IV + o, 16, 1024), idesc_s, ks > 0);
+                }
+                mma_commit(s_full);
+                if (!(ok = mbar_wait(pd_full, t_local & 1, err))) break;
+                tc_fence_after();
+                const int ksteps = n16 / 16;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    // dV += P^T dO and dK += dS^T Q: reduction over query rows ks*16..+15
+                    const uint32_t acc = ks > 0 ? 1u : 0u;
+                    mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sP + ks * 2048, C::SUB, 1024),
+                                sdesc_sw128(base + C::IDO + ks * 2048, C::SUB, 1024), idesc_mn, acc);
+                    mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDS + ks * 2048, C::SUB, 1024),
+                                sdesc_sw128(base + C::IQ + ks * 2048, C::SUB, 1024), idesc_mn, acc);
+                    // dQ += dS K: reduction over key rows ks*16..+15
+                    mma_bf16_ss(tmem + C::COL_S, sdesc_sw128(sDS + (ks >> 2) * C::SUB + (ks & 3) * 32, 16, 1024),
+                                sdesc_sw128(base + C::IK + ks * 2048, C::SUB, 1024), idesc_kmn, acc);
+                    if (ACT) {  // unnormalised dS: add its bf16 remainder to dK and dQ
+                        mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDSlo + ks * 2048, C::SUB, 1024),
+                                    sdesc_sw128(base + C::IQ + ks * 2048, C::SUB, 1024), idesc_mn, 1u);
+                        mma_bf16_ss(tmem + C::COL_S,
+                                    sdesc_sw128(sDSlo + (ks >> 2) * C::SUB + (ks & 3) * 32, 16, 1024),
+                                    sdesc_sw128(base + C::IK + ks * 2048, C::SUB, 1024), idesc_kmn, 1u);
+                    }
+                }
+                mma_commit(&in_empty[buf]);
+                mma_commit(acc_full);
+                ++t_local;
+            }
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        }
+    } else {
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int half = row >> 6;  // which 64-block of the chunk this row belongs to
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const float sc = ACT ? g.scale : g.scale * kLog2e;
+        uint32_t t_local = 0;
+        bool ok = true;
+        for (int ti = tbeg; ti < tend && ok; ++ti) {
+            Tile t;
+            if (!load_tile(g, ti, t, err, false)) continue;
+            const float *bt = sbias + t.h * g.nb;
+            const int len = t.q_len;
+            const int q_loc = t.q_start - g.q_off[t.b] + row;
+            const int kv_loc0 = t.kv_start - g.kv_off[t.b] + half * 64;  // first key of this row's block
+            const int nvalid = min(64, max(0, len - half * 64));          // valid keys in the block
+            // Query rows past the sequence end must contribute nothing to dK / dV.
+            const bool row_valid = row < len;
+            if (!(ok = mbar_wait_warp(s_full, t_local & 1, err))) break;
+            tc_fence_after();
+            float s[64], dp[64];
+            bool live[2];
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                live[c] = c * 32 < nvalid;  // uniform across the warp (one warp lies in one block)
+                if (live[c]) {
+                    tmem_ld32(tmem + lane_base + C::COL_S + half * 64 + c * 32, sub32(s, c));
+                    tmem_ld32(tmem + lane_base + C::COL_DP + half * 64 + c * 32, sub32(dp, c));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                if (!live[c]) continue;
+                float bv[32];
+                if (g.nb > 0) {
+                    bias32(bt, g.nb, q_loc, kv_loc0 + c * 32, bv);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) bv[i] = 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const int cc = c * 32 + i;
+                    s[cc] = (row_valid && cc < nvalid) ? fmaf(s[cc], sc, bv[i]) : (ACT ? 0.0f : -INFINITY);
+                }
+            }
+            if (!ACT) {
+                float m = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    if (live[c]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) m = fmaxf(m, s[c * 32 + i]);
+                    }
+                if (m == -INFINITY) m = 0.0f;
+                float l = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    if (live[c]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float p = ex2_approx(s[c * 32 + i] - m);
+                            s[c * 32 + i] = p;
+                            l += p;
+                        }
+                    }
+                const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+                float delta = 0.0f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    if (live[c]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            s[c * 32 + i] *= inv;
+                            delta = fmaf(s[c * 32 + i], dp[c * 32 + i], delta);
+                        }
+                    }
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    if (live[c]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) dp[c * 32 + i] = s[c * 32 + i] * (dp[c * 32 + i] - delta);
+                    }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 2; ++c)
+                    if (live[c]) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const int cc = c * 32 + i;
+                            float av;
+                            const float dv = act_bwd(g.act, s[cc], av) * dp[cc];
+                            const bool in = row_valid && cc < nvalid;
+                            s[cc] = in ? av : 0.0f;
+                            dp[cc] = in ? dv : 0.0f;
+                        }
+                    }
+            }
+            // P and dS rows: this row's block gets values, the other block zeros
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const uint32_t col = half * 64 + c * 32;
+                if (live[c] && row_valid) {
+                    st_row32_bf16(sP, C::SUB, row, col, sub32(s, c));
+                    if (ACT)
+                        st_row32_bf16_hilo(sDS, sDSlo, C::SUB, row, col, sub32(dp, c));
+                    else
+                        st_row32_bf16(sDS, C::SUB, row, col, sub32(dp, c));
+                } else {
+                    st_row32_zero(sP, C::SUB, row, col);
+                    st_row32_zero(sDS, C::SUB, row, col);
+                    if (ACT) st_row32_zero(sDSlo, C::SUB, row, col);
+                }
+                const uint32_t ocol = (1 - half) * 64 + c * 32;
+                st_row32_zero(sP, C::SUB, row, ocol);
+                st_row32_zero(sDS, C::SUB, row, ocol);
+                if (ACT) st_row32_zero(sDSlo, C::SUB, row, ocol);
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(pd_full);
+
+            if (!(ok = mbar_wait_warp(acc_full, t_local & 1, err))) break;
+            tc_fence_after();
+            const bool row_ok = row < len;
+            const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
+            const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float o[32];
+                tmem_ld32(tmem + lane_base + C::COL_S + c * 32, o);
+                if (row_ok) store_out32(a.dq, qrow, t.h, c * 32, o, g.scale);
+                tmem_ld32(tmem + lane_base + C::COL_DK + c * 32, o);
+                if (row_ok) store_out32(a.dk, krow, t.h, c * 32, o, g.scale);
+                tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
+                if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty);
+            ++t_local;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+static cudaError_t launch_block_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    using C = BlkCfg<D>;
+    static bool done[64] = {};
+    cudaError_t e = ensure_smem(bwd_block_kernel<D>, C::SMEM_ALLOC, done);
+    if (e != cudaSuccess || n_ctas <= 0) return e;
+    bwd_block_kernel<D><<<n_ctas, 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    if (D == 128) return launch_block_t<128>(tm, a, n_ctas, st);
+    if (D == 64) return launch_block_t<64>(tm, a, n_ctas, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace jattn

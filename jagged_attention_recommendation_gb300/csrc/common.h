@@ -1,0 +1,74 @@
+// common.h -- constants and kernel parameter blocks shared by the host glue
+// (api.cpp) and the CUDA kernels.  Plain C++ types only.
+#pragma once
+
+#include <stdint.h>
+
+namespace jattn {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// status codes written to the device status word (same values as jattn_status)
+constexpr int kStatusDeviceTimeout = 6;
+constexpr int kStatusDeviceCheck = 7;
+
+// a bounded wait gives up after this much wall time
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+// largest bias table (H * NB floats) the kernels stage in shared memory
+constexpr int kMaxBiasFloats = 256;
+
+// online-softmax rescale threshold (log2 units): the running max is only moved,
+// and O rescaled, when a row's max grows by more than this, so unnormalised
+// probabilities stay below 2^8.
+constexpr float kRescaleThreshold = 8.0f;
+
+struct Tile {
+    int32_t b, h, q_start, q_len, kv_start, kv_len;
+};
+
+enum Act : int32_t { kSoftmax = 0, kSilu = 1, kGeluTanh = 2 };
+
+// Geometry and mode shared by every attention kernel.
+struct Geom {
+    const Tile *tiles;        // scheduled tile list (device)
+    const int32_t *cta_begin; // [n_ctas + 1] (device)
+    const int32_t *q_off;     // [B + 1] (device)
+    const int32_t *kv_off;    // [B + 1] (device)
+    int32_t n_tiles;
+    int32_t B;
+    int32_t H;
+    int32_t max_q_len;        // tile validation: largest q_len a record may carry
+    int32_t max_kv_len;       // ... and kv_len
+    int32_t Tq, Tk;
+    int32_t act;
+    int32_t block;            // 0 or 64
+    int32_t nb;               // bias buckets, 0 = none
+    float scale;              // score scale
+    const float *bias;        // [H, nb] or nullptr
+    int *status;              // device status word
+};
+
+// Where a [T, H, D] result goes: element (t, h, c) at ptr[t*ld + h*cols + c] for c < cols.
+struct OutDesc {
+    void *ptr;
+    int32_t f32;   // 1: float32, 0: bfloat16
+    int32_t cols;  // real D (<= padded D)
+    int64_t ld;    // row stride in elements (H * cols)
+};
+
+struct FwdArgs {
+    Geom g;
+    OutDesc out;
+    float *lse;    // [H, Tq] or nullptr
+};
+
+struct BwdArgs {
+    Geom g;
+    const float *lse;    // [H, Tq] (full softmax)
+    const float *delta;  // [H, Tq] (full softmax)
+    OutDesc dq, dk, dv;
+};
+
+}  // namespace jattn

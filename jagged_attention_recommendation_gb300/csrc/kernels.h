@@ -1,0 +1,45 @@
+// kernels.h -- host-side entry points of the CUDA kernels (one per .cu file).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.h"
+
+namespace jattn {
+
+// Opt a kernel into `bytes` of dynamic shared memory, once per device.
+template <typename K>
+inline cudaError_t ensure_smem(K kern, uint32_t bytes, bool (&done)[64]) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable && done[dev]) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && cacheable) done[dev] = true;
+    return e;
+}
+
+// TMA descriptors of the bf16 [T, H*D] operand views a kernel reads.
+struct TmapSet {
+    CUtensorMap q, k, v, dout;
+};
+
+// forward: D in {64, 128}; act selects the GDPA activation path
+cudaError_t launch_fwd(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream);
+
+// backward, full attention: dQ pass (query-major tiles) and dK/dV pass (key-major tiles)
+cudaError_t launch_bwd_dq(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
+cudaError_t launch_bwd_dkdv(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
+
+// backward, BlockAttention: one fused pass over query-major tiles
+cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
+
+// Delta_i = <dO_i, O_i> (fp32) for every row and head: delta[h * Tq + t]
+cudaError_t launch_delta(const void *out, const void *dout, int f32, int64_t Tq, int H, int D, float *delta,
+                         cudaStream_t stream);
+
+// src [rows, D] (bf16 or fp32) -> dst [rows, Dp] bf16, zero-padded columns D..Dp-1
+cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, void *dst, cudaStream_t stream);
+
+}  // namespace jattn

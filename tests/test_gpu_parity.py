@@ -1,0 +1,113 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+seeded inputs, element by element, within the stated tolerances."""
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+import jagged_attention_recommendation_gb300 as J
+from jagged_attention_recommendation_gb300 import workloads as W
+from oracle import oracle
+from tests import parity as PT
+
+pytestmark = pytest.mark.gpu
+
+SOFTMAX, SILU, GELU = W.SOFTMAX, W.SILU, W.GELU_TANH
+
+# (name, lq, lk, H, D, bias_buckets, act, block, dtype)
+CASES = [
+    ("self_d128_tails", [1, 127, 128, 129, 300], None, 2, 128, 0, SOFTMAX, 0, torch.bfloat16),
+    ("self_d128_bias", [45, 200, 129, 1, 390], None, 4, 128, 64, SOFTMAX, 0, torch.bfloat16),
+    ("self_d64", [70, 256, 3, 190], None, 3, 64, 0, SOFTMAX, 0, torch.bfloat16),
+    ("self_d64_bias", [70, 256, 3, 190], None, 2, 64, 16, SOFTMAX, 0, torch.bfloat16),
+    ("cross_short_kv", [200, 35, 129, 511], [8, 64, 17, 40], 2, 128, 0, SOFTMAX, 0, torch.bfloat16),
+    ("short_q_long_kv", [32, 32, 5], [600, 257, 1000], 2, 128, 0, SOFTMAX, 0, torch.bfloat16),
+    ("empty_sequences", [10, 0, 140, 7], [0, 5, 30, 0], 2, 128, 0, SOFTMAX, 0, torch.bfloat16),
+    ("gdpa_silu", [32, 32, 100], [700, 1500, 129], 2, 128, 0, SILU, 0, torch.bfloat16),
+    ("gdpa_gelu", [32, 32, 100], [700, 1500, 129], 2, 128, 0, GELU, 0, torch.bfloat16),
+    ("gdpa_silu_d64_bias", [150, 3], [90, 400], 2, 64, 8, SILU, 0, torch.bfloat16),
+    ("block64_d64", [1, 63, 64, 65, 200, 513], None, 4, 64, 0, SOFTMAX, 64, torch.bfloat16),
+    ("block64_d128_bias", [130, 64, 7, 300], None, 2, 128, 64, SOFTMAX, 64, torch.bfloat16),
+    ("block64_silu", [100, 257], None, 2, 64, 0, SILU, 64, torch.bfloat16),
+    ("fp32_d32", [31, 33, 49, 61], None, 2, 32, 0, SOFTMAX, 0, torch.float32),
+    ("bf16_d32", [5, 140, 64], [9, 130, 1], 2, 32, 0, SOFTMAX, 0, torch.bfloat16),
+    ("fp32_d128_gelu", [40, 130], [300, 20], 2, 128, 0, GELU, 0, torch.float32),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_parity_small(case):
+    name, lq, lk, H, D, nb, act, block, dtype = case
+    lk = lq if lk is None else lk
+    bt = W.random_batch(zlib.crc32(name.encode()) % 10000, lq, lk, H, D, dtype=dtype, bias_buckets=nb)
+    gpu = PT.run_library(bt, act=act, block=block, dtype="fp32" if dtype == torch.float32 else "bf16")
+    if dtype == torch.float32 and act != SOFTMAX:
+        # float32 data enters the tensor cores as bf16 (the library's stated
+        # precision); unnormalised activation sums over hundreds of keys turn
+        # that input rounding alone into more than the bf16 tolerance, so the
+        # oracle sees the same bf16-rounded values.  Softmax fp32 cases compare
+        # against the unrounded inputs.
+        bt = dict(bt, **{n: bt[n].to(torch.bfloat16).float() for n in ("q", "k", "v", "dout")})
+    ref = PT.run_oracle(bt, act=act, block=block)
+    PT.compare(gpu, ref)
+
+
+def test_tiny_workload_fp32():
+    """The tiny fp32 workload, exactly as drawn (B=4, H=2, D=32)."""
+    b = W.make_batch(1)
+    bt = dict(q_off=b.q_off, kv_off=b.kv_off, q=b.q, k=b.k, v=b.v, bias=None, dout=b.dout, scale=b.scale)
+    gpu = PT.run_library(bt, dtype="fp32")
+    PT.compare(gpu, PT.run_oracle(bt))
+
+
+def test_run_to_run_bitwise_deterministic():
+    bt = W.random_batch(7, [300, 129, 17], [300, 129, 17], 2, 128, bias_buckets=8)
+    a = PT.run_library(bt)
+    b = PT.run_library(bt)
+    for n in ("out", "lse", "dq", "dk", "dv"):
+        assert np.array_equal(a[n], b[n]), n
+
+
+def _sample_seqs(q_off, kv_off, k=6, seed=0):
+    lq = np.diff(q_off.astype(np.int64))
+    lk = np.diff(kv_off.astype(np.int64))
+    work = lq * np.maximum(lk, 1)
+    rng = np.random.default_rng(seed)
+    picks = {int(np.argmax(work)), int(np.argmin(work))}
+    while len(picks) < min(k, len(lq)):
+        picks.add(int(rng.integers(len(lq))))
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("wid,act", [(2, SOFTMAX), (3, SOFTMAX), (4, SILU), (4, GELU), (5, SOFTMAX)])
+def test_full_size_workload_sampled(wid, act):
+    """Full-size workload on the GPU; sampled sequences checked against the oracle."""
+    b = W.make_batch(wid, act=act)
+    w = b.w
+    bt = dict(q_off=b.q_off, kv_off=b.kv_off, q=b.q, k=b.k, v=b.v, bias=b.bias, dout=b.dout, scale=b.scale)
+    gpu = PT.run_library(bt, act=act, block=w.block)
+    for n in ("out", "dq", "dk", "dv"):
+        assert np.isfinite(gpu[n]).all(), n
+    seqs = _sample_seqs(b.q_off, b.kv_off, k=4 if wid == 5 else 6)
+    qo, ko, (q, dout), (k, v), qidx, kidx = oracle.sub_batch(b.q_off, b.kv_off, seqs, b.q, b.dout,
+                                                             tensors_kv=(b.k, b.v))
+    sub = dict(q_off=qo, kv_off=ko, q=q, k=k, v=v, bias=b.bias, dout=dout, scale=b.scale)
+    ref = PT.run_oracle(sub, act=act, block=w.block)
+    PT.assert_close(gpu["out"][qidx], ref["out"], PT.FWD_TOL, "out")
+    if ref["lse"] is not None:
+        PT.assert_close(gpu["lse"][:, qidx], ref["lse"], PT.FWD_TOL, "lse")
+    PT.assert_close(gpu["dq"][qidx], ref["dq"], PT.BWD_TOL, "dq")
+    PT.assert_close(gpu["dk"][kidx], ref["dk"], PT.BWD_TOL, "dk")
+    PT.assert_close(gpu["dv"][kidx], ref["dv"], PT.BWD_TOL, "dv")
+
+
+def test_plan_update_between_batches():
+    """One plan re-planned for a second batch gives the same result as a fresh plan."""
+    bt1 = W.random_batch(21, [100, 300], [100, 300], 2, 128)
+    bt2 = W.random_batch(22, [5, 129, 260, 1], [5, 129, 260, 1], 2, 128)
+    plan = J.Plan(bt1["q_off"], bt1["kv_off"], 2, 128, device=0)
+    PT.run_library(bt1, plan=plan)
+    plan.update(bt2["q_off"], bt2["kv_off"])
+    a = PT.run_library(bt2, plan=plan)
+    PT.compare(a, PT.run_oracle(bt2))
