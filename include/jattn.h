@@ -160,7 +160,9 @@ jattn_status jattn_bwd(const jattn_plan *plan, const void *dout, const void *q, 
  * events[i] right after its i-th kernel (i < n_events), so elapsed times
  * between consecutive events are per-kernel device durations.  `events` is a
  * HOST array of cudaEvent_t handles owned by the caller (copied; the handles
- * must stay valid while set); NULL or n_events = 0 turns the hook off.
+ * must stay valid while set; a NULL handle is JATTN_ERR_INVALID_ARG); NULL or
+ * n_events = 0 turns the hook off.  A failed event record fails the call with
+ * JATTN_ERR_CUDA.
  */
 jattn_status jattn_plan_set_events(jattn_plan *plan, void *const *events, int32_t n_events);
 
@@ -169,6 +171,10 @@ int64_t jattn_plan_launch_count(const jattn_plan *plan);
 
 /* Synchronises `stream`, then returns and clears the plan's device status word. */
 jattn_status jattn_check_device_status(const jattn_plan *plan, void *stream);
+
+/* Text of the CUDA error behind the calling thread's most recent JATTN_ERR_CUDA
+ * return (thread-local, static storage; "" if none). */
+const char *jattn_last_cuda_error(void);
 
 /* Static, human-readable name of a status code. */
 const char *jattn_status_str(jattn_status status);

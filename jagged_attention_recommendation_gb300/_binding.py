@@ -23,13 +23,16 @@ TILES_Q, TILES_KV = 0, 1
 
 EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd_workspace_bytes",
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
-            "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count")
+            "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error")
 
 
 class JattnError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
-        super().__init__("%s failed: %s (status %d)" % (what, status_str(code), code))
+        detail = ""
+        if code == ERR_CUDA:
+            detail = " [%s]" % load().jattn_last_cuda_error().decode()
+        super().__init__("%s failed: %s (status %d)%s" % (what, status_str(code), code, detail))
 
 
 class Mode(ctypes.Structure):
@@ -67,6 +70,8 @@ def load():
     lib.jattn_plan_set_events.restype = i32
     lib.jattn_plan_launch_count.argtypes = [P]
     lib.jattn_plan_launch_count.restype = i64
+    lib.jattn_last_cuda_error.argtypes = []
+    lib.jattn_last_cuda_error.restype = ctypes.c_char_p
     lib.jattn_status_str.argtypes = [i32]
     lib.jattn_status_str.restype = ctypes.c_char_p
     for f in ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd", "jattn_bwd",
@@ -192,6 +197,9 @@ class Plan:
             self._events = None
             return
         self._events = list(events)  # keep the handles alive
+        for e in self._events:
+            if not e.cuda_event:  # torch creates the CUDA event on its first record
+                e.record()
         arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in self._events])
         _check(load().jattn_plan_set_events(self._h, arr, len(events)), "jattn_plan_set_events")
 

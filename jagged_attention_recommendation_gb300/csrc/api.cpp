@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <climits>
 #include <cmath>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -158,7 +159,26 @@ void build_lists(jattn_plan *p) {
     schedule(tk, p->cta[JATTN_TILES_KV], p->num_sms, true, block);
 }
 
-jattn_status cuda_status(cudaError_t e) { return e == cudaSuccess ? JATTN_OK : JATTN_ERR_CUDA; }
+thread_local char g_last_cuda_error[256] = "";
+
+// Map a CUDA result to a status, remembering the error text for jattn_last_cuda_error.
+jattn_status cuda_status(cudaError_t e, const char *where = "") {
+    if (e == cudaSuccess) return JATTN_OK;
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s: %s (%s)", where, cudaGetErrorString(e),
+                  cudaGetErrorName(e));
+    return JATTN_ERR_CUDA;
+}
+
+#define CUDA_TRY(expr)                                      \
+    do {                                                    \
+        const cudaError_t e_ = (expr);                      \
+        if (e_ != cudaSuccess) return cuda_status(e_, #expr); \
+    } while (0)
+
+jattn_status note_error(const char *where) {
+    std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s", where);
+    return JATTN_ERR_CUDA;
+}
 
 // Lay out and upload tiles, schedules and offsets (asynchronously on `stream`).
 jattn_status upload(jattn_plan *p, cudaStream_t stream) {
@@ -178,26 +198,25 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
     const size_t bytes = off;
 
     if (bytes > p->d_cap) {
-        cudaError_t e = cudaStreamSynchronize(stream);  // earlier launches may still read the old buffer
-        if (e != cudaSuccess) return JATTN_ERR_CUDA;
+        CUDA_TRY(cudaStreamSynchronize(stream));  // earlier launches may still read the old buffer
         if (p->d_buf) cudaFree(p->d_buf);
         p->d_buf = nullptr;
         p->d_cap = 0;
         const size_t cap = std::max(bytes + bytes / 2, static_cast<size_t>(4096));
-        if (cudaMalloc(&p->d_buf, cap) != cudaSuccess) return JATTN_ERR_CUDA;
+        CUDA_TRY(cudaMalloc(&p->d_buf, cap));
         p->d_cap = cap;
     }
     const int k = p->pin_next;
     p->pin_next ^= 1;
     if (p->ev_used[k]) {
-        if (cudaEventSynchronize(p->ev[k]) != cudaSuccess) return JATTN_ERR_CUDA;
+        CUDA_TRY(cudaEventSynchronize(p->ev[k]));
     }
     if (bytes > p->h_cap[k]) {
         if (p->h_pin[k]) cudaFreeHost(p->h_pin[k]);
         p->h_pin[k] = nullptr;
         p->h_cap[k] = 0;
         const size_t cap = std::max(bytes + bytes / 2, static_cast<size_t>(4096));
-        if (cudaMallocHost(&p->h_pin[k], cap) != cudaSuccess) return JATTN_ERR_CUDA;
+        CUDA_TRY(cudaMallocHost(&p->h_pin[k], cap));
         p->h_cap[k] = cap;
     }
     uint8_t *h = static_cast<uint8_t *>(p->h_pin[k]);
@@ -208,8 +227,8 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
     }
     std::memcpy(h + p->off_qoff, p->q_off.data(), p->q_off.size() * sizeof(int32_t));
     std::memcpy(h + p->off_kvoff, p->kv_off.data(), p->kv_off.size() * sizeof(int32_t));
-    if (cudaMemcpyAsync(p->d_buf, h, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return JATTN_ERR_CUDA;
-    if (cudaEventRecord(p->ev[k], stream) != cudaSuccess) return JATTN_ERR_CUDA;
+    CUDA_TRY(cudaMemcpyAsync(p->d_buf, h, bytes, cudaMemcpyHostToDevice, stream));
+    CUDA_TRY(cudaEventRecord(p->ev[k], stream));
     p->ev_used[k] = true;
     return JATTN_OK;
 }
@@ -306,19 +325,22 @@ int n_ctas(const jattn_plan *p, int which) { return static_cast<int>(p->cta[whic
 struct LaunchLog {
     const jattn_plan *p;
     cudaStream_t st;
+    cudaError_t first = cudaSuccess;  // result of recording the call's first event
     LaunchLog(const jattn_plan *plan, cudaStream_t stream) : p(plan), st(stream) {
         p->prof_next = 0;
-        mark();
+        first = mark();
     }
-    void mark() {
+    cudaError_t mark() {
         if (p->prof_next < static_cast<int>(p->prof_events.size()))
-            cudaEventRecord(p->prof_events[p->prof_next++], st);
+            return cudaEventRecord(p->prof_events[p->prof_next++], st);
+        return cudaSuccess;
     }
     // one kernel was launched (launch functions that skip an empty grid still count as one)
     cudaError_t done(cudaError_t e) {
+        if (e == cudaSuccess && first != cudaSuccess) e = first;
         if (e == cudaSuccess) {
             ++p->launches;
-            mark();
+            e = mark();
         }
         return e;
     }
@@ -388,7 +410,7 @@ jattn_status jattn_plan_update(jattn_plan *plan, const int32_t *q_offsets, const
     set_batch(plan, q_offsets, kv_offsets, B);
     if (plan->device < 0) return JATTN_OK;
     DeviceGuard g(plan->device);
-    if (!g.ok) return JATTN_ERR_CUDA;
+    if (!g.ok) return note_error("jattn_plan_update: cudaSetDevice failed");
     return upload(plan, static_cast<cudaStream_t>(stream));
 }
 
@@ -442,7 +464,8 @@ jattn_status jattn_fwd(const jattn_plan *p, const void *q, const void *k, const 
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return JATTN_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
     DeviceGuard guard(p->device);
-    if (!guard.ok) return JATTN_ERR_CUDA;
+    if (!guard.ok) return note_error("jattn_fwd: cudaSetDevice failed");
+    (void)cudaGetLastError();  // report only errors of this call
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int f32 = p->mode.dtype == JATTN_FP32;
     const void *qq = q, *kk = k, *vv = v;
@@ -450,9 +473,9 @@ jattn_status jattn_fwd(const jattn_plan *p, const void *q, const void *k, const 
     if (p->staged) {
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         void *qs = ws, *ks = ws + stage_bytes(p, p->Tq), *vs = ws + stage_bytes(p, p->Tq) + stage_bytes(p, p->Tk);
-        if (log.done(launch_stage(q, f32, p->Tq * p->H, p->D, p->Dp, qs, st)) != cudaSuccess) return JATTN_ERR_CUDA;
-        if (log.done(launch_stage(k, f32, p->Tk * p->H, p->D, p->Dp, ks, st)) != cudaSuccess) return JATTN_ERR_CUDA;
-        if (log.done(launch_stage(v, f32, p->Tk * p->H, p->D, p->Dp, vs, st)) != cudaSuccess) return JATTN_ERR_CUDA;
+        CUDA_TRY(log.done(launch_stage(q, f32, p->Tq * p->H, p->D, p->Dp, qs, st)));
+        CUDA_TRY(log.done(launch_stage(k, f32, p->Tk * p->H, p->D, p->Dp, ks, st)));
+        CUDA_TRY(log.done(launch_stage(v, f32, p->Tk * p->H, p->D, p->Dp, vs, st)));
         qq = qs;
         kk = ks;
         vv = vs;
@@ -460,14 +483,15 @@ jattn_status jattn_fwd(const jattn_plan *p, const void *q, const void *k, const 
     TmapSet tm;
     if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
         !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
-        return JATTN_ERR_CUDA;
+        return note_error("jattn_fwd: cuTensorMapEncodeTiled failed");
     tm.dout = tm.q;
     FwdArgs a;
     a.g = make_geom(p, JATTN_TILES_Q);
     a.g.bias = bias;
     a.out = out_desc(p, out);
     a.lse = lse;
-    return cuda_status(log.done(launch_fwd(p->Dp, p->mode.act != JATTN_SOFTMAX, tm, a, n_ctas(p, JATTN_TILES_Q), st)));
+    return cuda_status(log.done(launch_fwd(p->Dp, p->mode.act != JATTN_SOFTMAX, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
+                       "jattn_fwd: forward kernel launch");
 }
 
 jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, const void *k, const void *v,
@@ -486,7 +510,8 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return JATTN_ERR_WORKSPACE;
     if (need > 0 && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
     DeviceGuard guard(p->device);
-    if (!guard.ok) return JATTN_ERR_CUDA;
+    if (!guard.ok) return note_error("jattn_bwd: cudaSetDevice failed");
+    (void)cudaGetLastError();  // report only errors of this call
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int f32 = p->mode.dtype == JATTN_FP32;
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -522,35 +547,43 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
     if (p->mode.block != 0) {
         if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
             !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128))
-            return JATTN_ERR_CUDA;
+            return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
         a.g = make_geom(p, JATTN_TILES_Q);
         a.g.bias = bias;
-        return cuda_status(log.done(launch_bwd_block(p->Dp, tm, a, n_ctas(p, JATTN_TILES_Q), st)));
+        return cuda_status(log.done(launch_bwd_block(p->Dp, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
+                           "jattn_bwd: block kernel launch");
     }
     if (delta != nullptr) {
-        if (log.done(launch_delta(out, dout, f32, p->Tq, p->H, p->D, delta, st)) != cudaSuccess)
-            return JATTN_ERR_CUDA;
+        jattn_status e = cuda_status(log.done(launch_delta(out, dout, f32, p->Tq, p->H, p->D, delta, st)),
+                                     "jattn_bwd: delta kernel launch");
+        if (e != JATTN_OK) return e;
     }
     const bool act = p->mode.act != JATTN_SOFTMAX;
     // pass 1: dQ over query-major tiles (128 query rows, keys in blocks of 64)
     if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128) ||
         !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 64) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 64))
-        return JATTN_ERR_CUDA;
+        return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
     a.g = make_geom(p, JATTN_TILES_Q);
     a.g.bias = bias;
-    if (log.done(launch_bwd_dq(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)) != cudaSuccess)
-        return JATTN_ERR_CUDA;
+    {
+        jattn_status e = cuda_status(log.done(launch_bwd_dq(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
+                                     "jattn_bwd: dQ kernel launch");
+        if (e != JATTN_OK) return e;
+    }
     // pass 2: dK, dV over key-major tiles (128 key rows, queries in blocks of 64)
     if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 64) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 64) ||
         !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
-        return JATTN_ERR_CUDA;
+        return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
     a.g = make_geom(p, JATTN_TILES_KV);
     a.g.bias = bias;
-    return cuda_status(log.done(launch_bwd_dkdv(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_KV), st)));
+    return cuda_status(log.done(launch_bwd_dkdv(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_KV), st)),
+                       "jattn_bwd: dK/dV kernel launch");
 }
 
 jattn_status jattn_plan_set_events(jattn_plan *p, void *const *events, int32_t n_events) {
     if (p == nullptr || n_events < 0 || (n_events > 0 && events == nullptr)) return JATTN_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n_events; ++i)
+        if (events[i] == nullptr) return JATTN_ERR_INVALID_ARG;
     p->prof_events.clear();
     for (int32_t i = 0; i < n_events; ++i) p->prof_events.push_back(static_cast<cudaEvent_t>(events[i]));
     return JATTN_OK;
@@ -562,14 +595,16 @@ jattn_status jattn_check_device_status(const jattn_plan *p, void *stream) {
     if (p == nullptr) return JATTN_ERR_INVALID_ARG;
     if (p->device < 0) return JATTN_ERR_NO_DEVICE;
     DeviceGuard guard(p->device);
-    if (!guard.ok) return JATTN_ERR_CUDA;
+    if (!guard.ok) return note_error("jattn_check_device_status: cudaSetDevice failed");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(st) != cudaSuccess) return JATTN_ERR_CUDA;
+    CUDA_TRY(cudaStreamSynchronize(st));
     int code = 0;
-    if (cudaMemcpy(&code, p->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return JATTN_ERR_CUDA;
-    if (code != 0 && cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess) return JATTN_ERR_CUDA;
+    CUDA_TRY(cudaMemcpy(&code, p->d_status, sizeof(int), cudaMemcpyDeviceToHost));
+    if (code != 0) CUDA_TRY(cudaMemset(p->d_status, 0, sizeof(int)));
     return static_cast<jattn_status>(code);
 }
+
+const char *jattn_last_cuda_error(void) { return g_last_cuda_error; }
 
 const char *jattn_status_str(jattn_status s) {
     switch (s) {

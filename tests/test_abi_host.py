@@ -153,3 +153,13 @@ def test_status_strings(lib):
         s = J.status_str(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert J.status_str(99) == "unknown status"
+
+
+def test_set_events_rejects_null_handles(lib):
+    p = J.Plan([0, 3], [0, 3], 1, 64, device=-1)
+    arr = (ctypes.c_void_p * 2)(None, None)
+    assert lib.jattn_plan_set_events(p._h, arr, 2) == J.ERR_INVALID_ARG
+    assert lib.jattn_plan_set_events(p._h, None, 0) == J.OK
+    assert lib.jattn_plan_set_events(p._h, None, 3) == J.ERR_INVALID_ARG
+    assert lib.jattn_plan_launch_count(p._h) == 0
+    assert lib.jattn_last_cuda_error() == b""
