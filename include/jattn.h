@@ -169,6 +169,33 @@ jattn_status jattn_plan_set_events(jattn_plan *plan, void *const *events, int32_
 /* Number of kernels launched through this plan since it was created (host counter). */
 int64_t jattn_plan_launch_count(const jattn_plan *plan);
 
+/*
+ * Backward without a caller-provided workspace.  The paper has no counterpart;
+ * this entry point exists for callers that cannot call cudaMalloc or hand the
+ * library device memory: code running where a framework's allocator owns the
+ * whole device, plug-ins and sandboxes without allocation rights, or latency-
+ * critical paths that must not take an allocation (which can synchronise the
+ * device).  Arguments and results are those of jattn_bwd, minus the workspace.
+ *
+ * The scratch the backward needs (Delta = rowsum(dO * O), [H, Tq] floats, plus
+ * bf16 staging copies for float32 or D = 32 data) lives in a fixed 16 MiB
+ * device array inside the library, reserved on every GPU that loads it until
+ * the process exits.  A batch whose jattn_bwd_workspace_bytes exceeds 16 MiB is
+ * rejected with JATTN_ERR_WORKSPACE before anything runs (softmax, bf16: up to
+ * H * Tq = 4,194,304).  Nothing is allocated: no cudaMalloc, cudaFree or
+ * allocating library routine is called.
+ *
+ * The first call on a device looks up the array's device address with that
+ * device current (cudaGetSymbolAddress, once per device); make that first call
+ * before any stream capture.  All calls share the one array and each call
+ * overwrites the part it uses (nothing in it has to start at zero), so calls
+ * whose work overlaps on the GPU (different streams, or different host threads
+ * without ordering) race on it: order them.
+ */
+jattn_status jattn_bwd_noalloc(const jattn_plan *plan, const void *dout, const void *q, const void *k, const void *v,
+                               const float *bias, const void *out, const float *lse, void *dq, void *dk, void *dv,
+                               float *dbias, void *stream);
+
 /* Synchronises `stream`, then returns and clears the plan's device status word. */
 jattn_status jattn_check_device_status(const jattn_plan *plan, void *stream);
 

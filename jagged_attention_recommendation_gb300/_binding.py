@@ -23,7 +23,7 @@ TILES_Q, TILES_KV = 0, 1
 
 EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd_workspace_bytes",
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
-            "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error")
+            "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc")
 
 
 class JattnError(RuntimeError):
@@ -65,6 +65,8 @@ def load():
     lib.jattn_plan_destroy.restype = None
     lib.jattn_fwd.argtypes = [P, P, P, P, P, P, P, P, sz, P]
     lib.jattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.jattn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
+    lib.jattn_bwd_noalloc.restype = i32
     lib.jattn_check_device_status.argtypes = [P, P]
     lib.jattn_plan_set_events.argtypes = [P, P, i32]
     lib.jattn_plan_set_events.restype = i32
@@ -188,6 +190,19 @@ class Plan:
         _check(load().jattn_bwd(self._h, _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(ws), nbytes, _stream(stream)),
                "jattn_bwd")
+        return dq, dk, dv
+
+    def bwd_noalloc(self, dout, q, k, v, out, lse=None, bias=None, dq=None, dk=None, dv=None, dbias=None,
+                    stream=None):
+        """Backward with the library's fixed device scratch instead of a workspace.
+        Returns (dq, dk, dv); the output tensors are allocated here unless given."""
+        dt = self._tdtype()
+        dq = torch.empty(self.Tq, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
+        dk = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dk is None else dk
+        dv = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dv is None else dv
+        _check(load().jattn_bwd_noalloc(self._h, _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out),
+                                        _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _stream(stream)),
+               "jattn_bwd_noalloc")
         return dq, dk, dv
 
     def set_events(self, events):

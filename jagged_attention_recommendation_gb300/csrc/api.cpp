@@ -348,6 +348,11 @@ struct LaunchLog {
 
 }  // namespace
 
+namespace jattn {
+// Device ordinal of a plan (-1 for a host-only plan), for other translation units.
+int plan_device(const jattn_plan *plan) { return plan == nullptr ? -1 : plan->device; }
+}  // namespace jattn
+
 extern "C" {
 
 jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B, int32_t H, int32_t D,
