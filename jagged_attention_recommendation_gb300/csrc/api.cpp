@@ -21,8 +21,8 @@
 
 using namespace jattn;
 
-static_assert(sizeof(jattn_tile) == sizeof(Tile), "tile record layout");
 static_assert(sizeof(jattn_tile) == 24, "tile record is 24 bytes");
+static_assert(sizeof(Tile) == 32, "device tile record is 32 bytes");
 
 namespace {
 
@@ -185,7 +185,7 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
     size_t off = 0;
     for (int w = 0; w < 2; ++w) {
         p->off_tiles[w] = off;
-        off = align_up(off + p->tiles[w].size() * sizeof(jattn_tile), 16);
+        off = align_up(off + p->tiles[w].size() * sizeof(Tile), 16);
     }
     for (int w = 0; w < 2; ++w) {
         p->off_cta[w] = off;
@@ -221,8 +221,12 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
     }
     uint8_t *h = static_cast<uint8_t *>(p->h_pin[k]);
     for (int w = 0; w < 2; ++w) {
-        if (!p->tiles[w].empty())
-            std::memcpy(h + p->off_tiles[w], p->tiles[w].data(), p->tiles[w].size() * sizeof(jattn_tile));
+        Tile *dst = reinterpret_cast<Tile *>(h + p->off_tiles[w]);
+        for (size_t i = 0; i < p->tiles[w].size(); ++i) {
+            const jattn_tile &t = p->tiles[w][i];
+            dst[i] = Tile{t.b, t.h, t.q_start, t.q_len, t.kv_start, t.kv_len, t.q_start - p->q_off[t.b],
+                          t.kv_start - p->kv_off[t.b]};
+        }
         std::memcpy(h + p->off_cta[w], p->cta[w].data(), p->cta[w].size() * sizeof(int32_t));
     }
     std::memcpy(h + p->off_qoff, p->q_off.data(), p->q_off.size() * sizeof(int32_t));

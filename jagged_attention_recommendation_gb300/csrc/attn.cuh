@@ -18,18 +18,34 @@ __device__ __forceinline__ uint8_t *align1024(uint8_t *p) {
     return reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~static_cast<uintptr_t>(1023));
 }
 
-// Reads tile record `idx` and checks it against the batch geometry.  A record
-// that fails the checks is reported on the status word and skipped by every
-// role of the CTA alike (they all read the same record).
-__device__ __forceinline__ bool load_tile(const Geom &g, int idx, Tile &t, const ErrCtx &e, bool report) {
-    t = g.tiles[idx];
+// Checks a tile record against the batch geometry.  A record that fails is
+// reported on the status word and skipped by every role of the CTA alike (they
+// all read the same record).
+__device__ __forceinline__ bool check_tile(const Geom &g, const Tile &t, const ErrCtx &e, bool report) {
     bool ok = t.b >= 0 && t.b < g.B && t.h >= 0 && t.h < g.H && t.q_len >= 0 && t.q_len <= g.max_q_len &&
               t.kv_len >= 0 && t.kv_len <= g.max_kv_len && t.q_start >= 0 && t.kv_start >= 0 &&
-              static_cast<int64_t>(t.q_start) + t.q_len <= g.Tq &&
+              t.q_loc0 >= 0 && t.kv_loc0 >= 0 && static_cast<int64_t>(t.q_start) + t.q_len <= g.Tq &&
               static_cast<int64_t>(t.kv_start) + t.kv_len <= g.Tk;
     if (!ok && report) raise_error(e, kStatusDeviceCheck);
     return ok;
 }
+
+// A CTA's tile range, read one record ahead so that the global load of the
+// next record overlaps the current tile's work.
+struct TileStream {
+    const Tile *p;
+    int i, end;
+    Tile nxt;
+    __device__ __forceinline__ TileStream(const Geom &g, int begin, int stop) : p(g.tiles), i(begin), end(stop) {
+        if (i < end) nxt = p[i];
+    }
+    __device__ __forceinline__ bool next(Tile &t) {
+        if (i >= end) return false;
+        t = nxt;
+        if (++i < end) nxt = p[i];
+        return true;
+    }
+};
 
 // Copy the whole bias table [H, nb] into shared memory, times `mul`
 // (all threads of the CTA, before the roles split; a __syncthreads follows).
@@ -114,7 +130,9 @@ __device__ __forceinline__ void store_out32(const OutDesc &o, int64_t row, int h
                 reinterpret_cast<float4 *>(p)[k] =
                     make_float4(v[4 * k] * mul, v[4 * k + 1] * mul, v[4 * k + 2] * mul, v[4 * k + 3] * mul);
         } else {
-            for (int i = 0; i < n; ++i) p[i] = v[i] * mul;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < n) p[i] = v[i] * mul;
         }
     } else {
         __nv_bfloat16 *p = static_cast<__nv_bfloat16 *>(o.ptr) + row * o.ld + static_cast<int64_t>(h) * o.cols + c0;
@@ -129,9 +147,66 @@ __device__ __forceinline__ void store_out32(const OutDesc &o, int64_t row, int h
                 reinterpret_cast<uint4 *>(p)[k] = w;
             }
         } else {
-            for (int i = 0; i < n; ++i) p[i] = __float2bfloat16_rn(v[i] * mul);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                if (i < n) p[i] = __float2bfloat16_rn(v[i] * mul);
         }
     }
+}
+
+// Copy a warp's 32 staged rows (row0 .. row0+31 of a 128B-swizzled bf16 tile,
+// sub-tiles of 64 columns `sub_bytes` apart) to the bf16 result rows
+// grow0 + row, head h; rows >= nvalid are skipped.  Consecutive lanes write
+// consecutive 16-byte pieces of a row, so every store is a full row segment.
+template <int D>
+__device__ __forceinline__ void copy_rows_out(uint32_t tile, uint32_t sub_bytes, int row0, int nvalid,
+                                              const OutDesc &o, int64_t grow0, int h, uint32_t lane) {
+    constexpr int CPR = D / 8;      // 16-byte pieces per row
+    constexpr int RPI = 32 / CPR;   // rows per warp instruction
+    const int cc = static_cast<int>(lane) % CPR, rsub = static_cast<int>(lane) / CPR;
+    uint4 v[32 / RPI];
+#pragma unroll
+    for (int k = 0; k < 32 / RPI; ++k)
+        v[k] = ld_shared_v4(tile + (cc >> 3) * sub_bytes + sw128_offset(row0 + k * RPI + rsub, cc & 7));
+#pragma unroll
+    for (int k = 0; k < 32 / RPI; ++k) {
+        const int r = row0 + k * RPI + rsub;
+        if (r < nvalid) {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(o.ptr) + (grow0 + r) * o.ld +
+                                 static_cast<int64_t>(h) * D + cc * 8;
+            *reinterpret_cast<uint4 *>(dst) = v[k];
+        }
+    }
+}
+
+// Same, for a W-column slice [c0, c0 + W) of rows of width D: lanes write
+// consecutive 16-byte pieces of each row slice.
+template <int W, int D>
+__device__ __forceinline__ void copy_rows_cols(uint32_t tile, uint32_t sub_bytes, int c0, int row0, int nvalid,
+                                               const OutDesc &o, int64_t grow0, int h, uint32_t lane) {
+    constexpr int CPR = W / 8;
+    constexpr int RPI = 32 / CPR;
+    const int cc = static_cast<int>(lane) % CPR, rsub = static_cast<int>(lane) / CPR;
+    const int col = c0 + cc * 8;
+    const uint32_t src = tile + (col >> 6) * sub_bytes;
+    uint4 v[32 / RPI];
+#pragma unroll
+    for (int k = 0; k < 32 / RPI; ++k) v[k] = ld_shared_v4(src + sw128_offset(row0 + k * RPI + rsub, (col & 63) >> 3));
+#pragma unroll
+    for (int k = 0; k < 32 / RPI; ++k) {
+        const int r = row0 + k * RPI + rsub;
+        if (r < nvalid) {
+            __nv_bfloat16 *dst =
+                static_cast<__nv_bfloat16 *>(o.ptr) + (grow0 + r) * o.ld + static_cast<int64_t>(h) * D + col;
+            *reinterpret_cast<uint4 *>(dst) = v[k];
+        }
+    }
+}
+
+// True when results can be staged and written as whole bf16 rows of width D.
+template <int D>
+__device__ __forceinline__ bool rows_fast(const OutDesc &o) {
+    return o.f32 == 0 && o.cols == D;
 }
 
 // act(x) = x * sigmoid(z) with z = x (SiLU) or z = 2 sqrt(2/pi) (x + 0.044715 x^3)
@@ -157,6 +232,132 @@ __device__ __forceinline__ float act_bwd(int act, float x, float &a) {
     const float sg = sigmoid_f(z);
     a = x * sg;
     return fmaf(x * sg * (1.0f - sg), dz, sg);
+}
+
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (sm_100 family f32x2 arithmetic) and 3-input max
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+// (a0, a1) <- (a0, a1) * (b0, b1) + (c0, c1)
+__device__ __forceinline__ void fma2(float &a0, float &a1, float b0, float b1, float c0, float c1) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a0, a1)), "l"(pk(b0, b1)), "l"(pk(c0, c1)));
+    upk(r, a0, a1);
+}
+// (a0, a1) <- (a0, a1) + (b0, b1)
+__device__ __forceinline__ void add2(float &a0, float &a1, float b0, float b1) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a0, a1)), "l"(pk(b0, b1)));
+    upk(r, a0, a1);
+}
+// (a0, a1) <- (a0, a1) * (b0, b1)
+__device__ __forceinline__ void mul2(float &a0, float &a1, float b0, float b1) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a0, a1)), "l"(pk(b0, b1)));
+    upk(r, a0, a1);
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Maximum of 32 values with a tree of 3-input max operations.
+__device__ __forceinline__ float max32(const float (&v)[32]) {
+    float m[11];
+#pragma unroll
+    for (int k = 0; k < 10; ++k) m[k] = max3(v[3 * k], v[3 * k + 1], v[3 * k + 2]);
+    m[10] = fmaxf(v[30], v[31]);
+    const float a = max3(m[0], m[1], m[2]), b = max3(m[3], m[4], m[5]), c = max3(m[6], m[7], m[8]);
+    return max3(max3(a, b, c), m[9], m[10]);
+}
+
+// Sum of 32 values with four independent packed accumulators.
+__device__ __forceinline__ float sum32(const float (&v)[32]) {
+    float a0 = v[0], a1 = v[1], b0 = v[2], b1 = v[3];
+#pragma unroll
+    for (int k = 4; k < 32; k += 4) {
+        add2(a0, a1, v[k], v[k + 1]);
+        add2(b0, b1, v[k + 2], v[k + 3]);
+    }
+    add2(a0, a1, b0, b1);
+    return a0 + a1;
+}
+
+// ---------------------------------------------------------------------------
+// relative-position bias as a reflected table: ext[x + kExtPad] =
+// T[min(|x|, nb-1)] * mul for |x| <= nb - 1 + 31, so that the 32 biases of a
+// chunk that touches the band are a contiguous (reversed) window.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr int ext_pad(int nb) { return nb - 1 + 31; }
+__host__ __device__ constexpr int ext_len(int nb) { return 2 * ext_pad(nb) + 1; }
+
+__device__ __forceinline__ void stage_bias_ext(const Geom &g, float *sext, float mul) {
+    if (g.nb <= 0) return;
+    const int pad = ext_pad(g.nb), len = ext_len(g.nb);
+    for (int i = threadIdx.x; i < g.H * len; i += blockDim.x) {
+        const int h = i / len;
+        int x = i - h * len - pad;
+        x = x < 0 ? -x : x;
+        sext[i] = g.bias[h * g.nb + (x < g.nb - 1 ? x : g.nb - 1)] * mul;
+    }
+}
+
+// Bias of keys kv0..kv0+31 for local query position q (or, symmetrically, of
+// queries for a key): returns false and a constant when the chunk lies
+// entirely beyond the last bucket, else fills bv from the reflected table.
+__device__ __forceinline__ bool bias32_ext(const float *ext_h, int nb, int q, int kv0, float (&bv)[32], float &cst) {
+    const int lo = q - (kv0 + 31), hi = kv0 - q;
+    const int dmin = lo > 0 ? lo : (hi > 0 ? hi : 0);
+    if (dmin >= nb - 1) {
+        cst = ext_h[0];  // |x| = pad >= nb - 1: the last bucket
+        return false;
+    }
+    const float *p = ext_h + ext_pad(nb) + (q - kv0);  // p[-i] = bias of key kv0 + i
+#pragma unroll
+    for (int i = 0; i < 32; ++i) bv[i] = p[-i];
+    return true;
+}
+
+// One accumulator row of D fp32 columns from TMEM (one round trip).
+template <int D>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[D]) {
+    if constexpr (D == 128) {
+        tmem_ld128(taddr, v);
+    } else if constexpr (D == 64) {
+        tmem_ld64(taddr, v);
+    } else {
+        static_assert(D == 32, "32, 64 or 128 columns");
+        tmem_ld32(taddr, v);
+    }
+}
+
+// x[i] = x[i] * sc + bias(key kv0 + i) for a 32-column chunk, bias read straight
+// from the reflected table (or the constant last bucket when the chunk is past it).
+__device__ __forceinline__ void scale_bias32(float (&x)[32], float sc, const float *ext_h, int nb, int q, int kv0) {
+    const int lo = q - (kv0 + 31), hi = kv0 - q;
+    const int dmin = lo > 0 ? lo : (hi > 0 ? hi : 0);
+    if (dmin >= nb - 1) {
+        const float c = ext_h[0];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) fma2(x[i], x[i + 1], sc, sc, c, c);
+    } else {
+        const float *p = ext_h + ext_pad(nb) + (q - kv0);
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) fma2(x[i], x[i + 1], sc, sc, p[-i], p[-i - 1]);
+    }
+}
+
+template <int N>
+__device__ __forceinline__ float (&sub64(float (&a)[N], int c))[64] {
+    return *reinterpret_cast<float(*)[64]>(&a[64 * c]);
 }
 
 template <int N>

@@ -17,25 +17,52 @@ __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 x) {
     return __bfloat162float(x);
 }
 
-// Delta_i = <dO_i, O_i> for every (token, head) row: one warp per row, fp32
-// accumulation; rows are [T, H, D] and the result is laid out [H, T].
+// Delta_i = <dO_i, O_i> for every (token, head) row, fp32 accumulation; rows
+// are [T, H, D] and the result is laid out [H, T].  Every thread reads 16-byte
+// vectors of both rows; TPR = D / (elements per vector) consecutive lanes share
+// a row and reduce with shuffles.
+template <typename T>
+__device__ __forceinline__ float dot16(const uint4 &a, const uint4 &b);
+template <>
+__device__ __forceinline__ float dot16<float>(const uint4 &a, const uint4 &b) {
+    return __uint_as_float(a.x) * __uint_as_float(b.x) + __uint_as_float(a.y) * __uint_as_float(b.y) +
+           __uint_as_float(a.z) * __uint_as_float(b.z) + __uint_as_float(a.w) * __uint_as_float(b.w);
+}
+template <>
+__device__ __forceinline__ float dot16<__nv_bfloat16>(const uint4 &a, const uint4 &b) {
+    const __nv_bfloat162 *x = reinterpret_cast<const __nv_bfloat162 *>(&a);
+    const __nv_bfloat162 *y = reinterpret_cast<const __nv_bfloat162 *>(&b);
+    float acc = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 u = __bfloat1622float2(x[k]), w = __bfloat1622float2(y[k]);
+        acc = fmaf(u.x, w.x, fmaf(u.y, w.y, acc));
+    }
+    return acc;
+}
+
 template <typename T>
 __global__ void delta_kernel(const T *__restrict__ out, const T *__restrict__ dout, int64_t Tq, int H, int D,
                              float *__restrict__ delta) {
+    constexpr int E = 16 / sizeof(T);  // elements per 16-byte vector
+    const int tpr = D / E;             // lanes per row (4..32, a power of two)
     const int64_t nrows = Tq * H;
-    const int lane = threadIdx.x & 31;
-    int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t stride = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    for (; r < nrows; r += stride) {
-        const T *o = out + r * D;
-        const T *d = dout + r * D;
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int sub = threadIdx.x & (tpr - 1);
+    // whole warps stay in the loop together so the shuffles see every lane
+    for (int64_t base = (gtid / tpr) - ((threadIdx.x & 31) / tpr); base < nrows; base += nthreads / tpr) {
+        const int64_t r = base + (threadIdx.x & 31) / tpr;
         float acc = 0.0f;
-        for (int c = lane; c < D; c += 32) acc = fmaf(to_f(o[c]), to_f(d[c]), acc);
-#pragma unroll
-        for (int k = 16; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
-        if (lane == 0) {
+        if (r < nrows) {
+            const uint4 *o = reinterpret_cast<const uint4 *>(out + r * D);
+            const uint4 *d = reinterpret_cast<const uint4 *>(dout + r * D);
+            acc = dot16<T>(__ldg(o + sub), __ldg(d + sub));
+        }
+        for (int k = tpr >> 1; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
+        if (sub == 0 && r < nrows) {
             const int64_t t = r / H;
-            const int h = static_cast<int>(r % H);
+            const int h = static_cast<int>(r - t * H);
             delta[static_cast<int64_t>(h) * Tq + t] = acc;
         }
     }
@@ -62,7 +89,9 @@ static int grid_for(int64_t work, int per_block) {
 cudaError_t launch_delta(const void *out, const void *dout, int f32, int64_t Tq, int H, int D, float *delta,
                          cudaStream_t stream) {
     if (Tq <= 0) return cudaSuccess;
-    const int grid = grid_for(Tq * H, 8);  // 8 warps of 32 per block
+    const int per_vec = f32 ? 4 : 8;
+    if (D % per_vec != 0 || D / per_vec > 32 || ((D / per_vec) & (D / per_vec - 1)) != 0) return cudaErrorInvalidValue;
+    const int grid = grid_for(Tq * H * (D / per_vec), 256);
     if (f32)
         delta_kernel<float><<<grid, 256, 0, stream>>>(static_cast<const float *>(out),
                                                        static_cast<const float *>(dout), Tq, H, D, delta);

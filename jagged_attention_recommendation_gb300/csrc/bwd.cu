@@ -49,7 +49,8 @@ struct DqCfg {
     static constexpr int NBAR = 2 + 2 * NST + 8 + 3;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
-    static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + kMaxBiasFloats * 4;
+    static constexpr uint32_t SMEM = OFF_BEXT + (ACT ? 0 : kMaxBiasExtFloats * 4);
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;     // S[2]:  0, 64
@@ -84,6 +85,8 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
+    float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
+    const bool use_ext = !ACT && g.nb > 0 && g.H * ext_len(g.nb) <= kMaxBiasExtFloats;
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
     const uint32_t sDO = smem_u32(smem + C::OFF_DO);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(192, 1)
         tmem_relinquish();
     }
     stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (use_ext) stage_bias_ext(g, sext, kLog2e);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -132,9 +136,10 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, t_local = 0;
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, true)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, true)) continue;
                 if (!(ok = mbar_wait(qd_empty, (t_local & 1) ^ 1, err))) break;
                 ++t_local;
                 mbar_arrive_expect_tx(qd_full, 2 * C::Q_BYTES);
@@ -169,9 +174,10 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t kv_it = 0, s_it = 0, ds_it = 0, t_local = 0;
             const uint32_t idesc_dq = idesc_bf16(128, D, false, true);
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, false)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, false)) continue;
                 const int nkv = cdiv(t.kv_len, C::BN);
                 if (!(ok = mbar_wait(qd_full, t_local & 1, err))) break;
                 if (!(ok = mbar_wait(dq_empty, (t_local & 1) ^ 1, err))) break;
@@ -242,13 +248,15 @@ __global__ void __launch_bounds__(192, 1)
         const float sc = ACT ? g.scale : g.scale * kLog2e;
         uint32_t s_it = 0, ds_it = 0, t_local = 0;
         bool ok = true;
-        for (int ti = tbeg; ti < tend && ok; ++ti) {
-            Tile t;
-            if (!load_tile(g, ti, t, err, false)) continue;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
             const int nkv = cdiv(t.kv_len, C::BN);
             const float *bt = sbias + t.h * g.nb;
-            const int q_loc = t.q_start - g.q_off[t.b] + row;
-            const int kv_loc0 = t.kv_start - g.kv_off[t.b];
+            const float *ext_h = sext + t.h * ext_len(g.nb);
+            const int q_loc = t.q_loc0 + row;
+            const int kv_loc0 = t.kv_loc0;
             const bool row_ok = row < t.q_len;
             const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
             float lse2 = 0.0f, dlt = 0.0f;
@@ -265,13 +273,9 @@ __global__ void __launch_bounds__(192, 1)
                 float s[C::BN], dp[C::BN];
                 bool live[2];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    live[c] = c * 32 < nvalid;
-                    if (live[c]) {
-                        tmem_ld32(tmem + lane_base + C::COL_S + sb * C::BN + c * 32, sub32(s, c));
-                        tmem_ld32(tmem + lane_base + C::COL_DP + sb * C::BN + c * 32, sub32(dp, c));
-                    }
-                }
+                for (int c = 0; c < 2; ++c) live[c] = c * 32 < nvalid;
+                tmem_ld64x2(tmem + lane_base + C::COL_S + sb * C::BN, tmem + lane_base + C::COL_DP + sb * C::BN, s,
+                            dp);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
@@ -281,25 +285,51 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     if (!live[c]) continue;
-                    float bv[32];
+                    float(&xs)[32] = sub32(s, c);
+                    float(&dpc)[32] = sub32(dp, c);
+                    // x = scale * s + bias (softmax: minus lse, in log2 units)
+                    const float off = ACT ? 0.0f : -lse2;
+                    float bv[32], cst = 0.0f;
+                    bool band = false;
                     if (g.nb > 0) {
-                        bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) bv[i] = 0.0f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const int cc = c * 32 + i;
-                        const float x = fmaf(s[cc], sc, bv[i]);
-                        float ds;
-                        if (ACT) {
-                            float av;
-                            ds = act_bwd(g.act, x, av) * dp[cc];
+                        if (use_ext) {
+                            band = bias32_ext(ext_h, g.nb, q_loc, kvb + c * 32, bv, cst);
                         } else {
-                            ds = ex2_approx(x - lse2) * (dp[cc] - dlt);
+                            bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
+                            band = true;
                         }
-                        s[cc] = cc < nvalid ? ds : 0.0f;
+                    }
+                    if (band) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            add2(bv[i], bv[i + 1], off, off);
+                            fma2(xs[i], xs[i + 1], sc, sc, bv[i], bv[i + 1]);
+                        }
+                    } else {
+                        const float o2 = cst + off;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) fma2(xs[i], xs[i + 1], sc, sc, o2, o2);
+                    }
+                    if (ACT) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float av;
+                            xs[i] = act_bwd(g.act, xs[i], av) * dpc[i];
+                        }
+                    } else {
+                        const float nd = -dlt;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) xs[i] = ex2_approx(xs[i]);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {
+                            add2(dpc[i], dpc[i + 1], nd, nd);
+                            mul2(xs[i], xs[i + 1], dpc[i], dpc[i + 1]);
+                        }
+                    }
+                    if (c * 32 + 32 > nvalid) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i >= nvalid) xs[i] = 0.0f;
                     }
                 }
                 const uint32_t db = ds_it & 1, duse = ds_it >> 1;
@@ -325,16 +355,30 @@ __global__ void __launch_bounds__(192, 1)
             if (!ok) break;
             if (!(ok = mbar_wait_warp(dq_full, t_local & 1, err))) break;
             tc_fence_after();
+            const bool fast = rows_fast<D>(a.dq);
+            float oa[D];
+            if (nkv > 0) {
+                tmem_ld_row<D>(tmem + lane_base + C::COL_DQ, oa);
+            } else {
+#pragma unroll
+                for (int i = 0; i < D; ++i) oa[i] = 0.0f;
+            }
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                if (nkv > 0) {
-                    tmem_ld32(tmem + lane_base + C::COL_DQ + c * 32, o);
-                } else {
+                float(&o)[32] = sub32(oa, c);
+                if (fast) {
+                    // stage in this warp's rows of the two dS buffers (every dQ MMA is done)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+                    for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], g.scale, g.scale);
+                    st_row32_bf16(sDS, C::NDS * C::DS_BYTES, row, c * 32, o);
+                } else if (row_ok) {
+                    store_out32(a.dq, qrow, t.h, c * 32, o, g.scale);
                 }
-                if (row_ok) store_out32(a.dq, qrow, t.h, c * 32, o, g.scale);
+            }
+            if (fast) {
+                __syncwarp();
+                copy_rows_out<D>(sDS, C::NDS * C::DS_BYTES, quad * 32, t.q_len, a.dq, t.q_start, t.h, lane);
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -378,7 +422,8 @@ struct DkvCfg {
     static constexpr int NBAR = 2 + 2 * NST + 4 + 2 + 2 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
-    static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + kMaxBiasFloats * 4;
+    static constexpr uint32_t SMEM = OFF_BEXT + (ACT ? 0 : kMaxBiasExtFloats * 4);
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_ST = 0;
@@ -414,6 +459,8 @@ __global__ void __launch_bounds__(192, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
+    float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
+    const bool use_ext = !ACT && g.nb > 0 && g.H * ext_len(g.nb) <= kMaxBiasExtFloats;
     float *sLD = reinterpret_cast<float *>(smem + C::OFF_LD);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
@@ -446,6 +493,7 @@ __global__ void __launch_bounds__(192, 1)
         tmem_relinquish();
     }
     stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (use_ext) stage_bias_ext(g, sext, kLog2e);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -465,9 +513,10 @@ __global__ void __launch_bounds__(192, 1)
         // query block into the stage's shared-memory slot before it is published.
         uint32_t q_it = 0, t_local = 0;
         bool ok = true;
-        for (int ti = tbeg; ti < tend && ok; ++ti) {
-            Tile t;
-            if (!load_tile(g, ti, t, err, lane == 0)) continue;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, lane == 0)) continue;
             if (!(ok = mbar_wait_warp(kv_empty, (t_local & 1) ^ 1, err))) break;
             ++t_local;
             if (lane == 0) {
@@ -485,11 +534,11 @@ __global__ void __launch_bounds__(192, 1)
                     float *ld = sLD + slot * 2 * C::BQ;
                     for (int k = lane; k < C::BQ; k += 32) {
                         const int qi = i * C::BQ + k;
-                        float l2 = 0.0f, dl = 0.0f;
+                        float l2 = 0.0f, dl = 0.0f;  // stored negated: the consumer adds them
                         if (qi < t.q_len) {
                             const int64_t idx = static_cast<int64_t>(t.h) * g.Tq + t.q_start + qi;
-                            l2 = a.lse[idx] * kLog2e;
-                            dl = a.delta[idx];
+                            l2 = -a.lse[idx] * kLog2e;
+                            dl = -a.delta[idx];
                         }
                         ld[k] = l2;
                         ld[C::BQ + k] = dl;
@@ -520,9 +569,10 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t q_it = 0, st_it = 0, p_it = 0, t_local = 0;
             const uint32_t idesc_acc = idesc_bf16(128, D, false, true);
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, false)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, false)) continue;
                 const int nq = cdiv(t.q_len, C::BQ);
                 if (!(ok = mbar_wait(kv_full, t_local & 1, err))) break;
                 if (!(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
@@ -594,13 +644,15 @@ __global__ void __launch_bounds__(192, 1)
         const float sc = ACT ? g.scale : g.scale * kLog2e;
         uint32_t q_it = 0, st_it = 0, p_it = 0, t_local = 0;
         bool ok = true;
-        for (int ti = tbeg; ti < tend && ok; ++ti) {
-            Tile t;
-            if (!load_tile(g, ti, t, err, false)) continue;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
             const int nq = cdiv(t.q_len, C::BQ);
             const float *bt = sbias + t.h * g.nb;
-            const int kv_loc = t.kv_start - g.kv_off[t.b] + row;
-            const int q_loc0 = t.q_start - g.q_off[t.b];
+            const float *ext_h = sext + t.h * ext_len(g.nb);
+            const int kv_loc = t.kv_loc0 + row;
+            const int q_loc0 = t.q_loc0;
             for (int i = 0; i < nq; ++i, ++q_it) {
                 const uint32_t slot = q_it % C::NST;
                 const uint32_t sb = st_it & 1, suse = st_it >> 1;
@@ -611,44 +663,68 @@ __global__ void __launch_bounds__(192, 1)
                 float st[C::BQ], dpt[C::BQ];
                 bool live[2];
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    live[c] = c * 32 < nvalid;
-                    if (live[c]) {
-                        tmem_ld32(tmem + lane_base + C::COL_ST + sb * C::BQ + c * 32, sub32(st, c));
-                        tmem_ld32(tmem + lane_base + C::COL_DPT + sb * C::BQ + c * 32, sub32(dpt, c));
-                    }
-                }
+                for (int c = 0; c < 2; ++c) live[c] = c * 32 < nvalid;
+                tmem_ld64x2(tmem + lane_base + C::COL_ST + sb * C::BQ, tmem + lane_base + C::COL_DPT + sb * C::BQ, st,
+                            dpt);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&st_empty[sb]);
                 ++st_it;
 
-                const float *ld = sLD + slot * 2 * C::BQ;
+                const float *ld = sLD + slot * 2 * C::BQ;  // [-lse * log2 e | -Delta] of the 64 queries
                 const int qb = q_loc0 + i * C::BQ;
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     if (!live[c]) continue;
-                    float bv[32];
+                    float(&xs)[32] = sub32(st, c);
+                    float(&dpc)[32] = sub32(dpt, c);
+                    float bv[32], cst = 0.0f;
+                    bool band = false;
                     if (g.nb > 0) {
-                        bias32(bt, g.nb, kv_loc, qb + c * 32, bv);
+                        if (use_ext) {
+                            band = bias32_ext(ext_h, g.nb, kv_loc, qb + c * 32, bv, cst);
+                        } else {
+                            bias32(bt, g.nb, kv_loc, qb + c * 32, bv);
+                            band = true;
+                        }
+                    }
+                    if (band) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2) fma2(xs[k], xs[k + 1], sc, sc, bv[k], bv[k + 1]);
                     } else {
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) bv[k] = 0.0f;
+                        for (int k = 0; k < 32; k += 2) fma2(xs[k], xs[k + 1], sc, sc, cst, cst);
                     }
+                    if (ACT) {
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const int cc = c * 32 + k;
-                        const float x = fmaf(st[cc], sc, bv[k]);
-                        float p, ds;
-                        if (ACT) {
-                            ds = act_bwd(g.act, x, p) * dpt[cc];
-                        } else {
-                            p = ex2_approx(x - ld[cc]);
-                            ds = p * (dpt[cc] - ld[C::BQ + cc]);
+                        for (int k = 0; k < 32; ++k) {
+                            float pv;
+                            dpc[k] = act_bwd(g.act, xs[k], pv) * dpc[k];
+                            xs[k] = pv;
                         }
-                        const bool in = cc < nvalid;
-                        st[cc] = in ? p : 0.0f;
-                        dpt[cc] = in ? ds : 0.0f;
+                    } else {
+                        const float4 *l4 = reinterpret_cast<const float4 *>(ld + c * 32);
+                        const float4 *d4 = reinterpret_cast<const float4 *>(ld + C::BQ + c * 32);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const float4 lz = l4[k], dz = d4[k];
+                            add2(xs[4 * k], xs[4 * k + 1], lz.x, lz.y);
+                            add2(xs[4 * k + 2], xs[4 * k + 3], lz.z, lz.w);
+                            add2(dpc[4 * k], dpc[4 * k + 1], dz.x, dz.y);
+                            add2(dpc[4 * k + 2], dpc[4 * k + 3], dz.z, dz.w);
+                        }
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) xs[k] = ex2_approx(xs[k]);
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2) mul2(dpc[k], dpc[k + 1], xs[k], xs[k + 1]);
+                    }
+                    if (c * 32 + 32 > nvalid) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k)
+                            if (c * 32 + k >= nvalid) {
+                                xs[k] = 0.0f;
+                                dpc[k] = 0.0f;
+                            }
                     }
                 }
                 if (!(ok = mbar_wait_warp(p_empty, (p_it & 1) ^ 1, err))) break;
@@ -678,18 +754,43 @@ __global__ void __launch_bounds__(192, 1)
             tc_fence_after();
             const bool row_ok = row < t.kv_len;
             const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
+            if (rows_fast<D>(a.dv)) {
+                // stage dV, then dK, in this warp's rows of the P^T / dS^T planes (all MMAs are done)
+                for (int pass = 0; pass < 2; ++pass) {
+                    const float mul = pass == 0 ? 1.0f : g.scale;
+                    float oa[D];
+                    if (nq > 0) {
+                        tmem_ld_row<D>(tmem + lane_base + (pass == 0 ? C::COL_DV : C::COL_DK), oa);
+                    } else {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                if (nq > 0) {
-                    tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
-                } else {
+                        for (int k = 0; k < D; ++k) oa[k] = 0.0f;
+                    }
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) o[k] = 0.0f;
+                    for (int c = 0; c < D / 32; ++c) {
+                        float(&o)[32] = sub32(oa, c);
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2) mul2(o[k], o[k + 1], mul, mul);
+                        st_row32_bf16(sPT, C::PT_BYTES, row, c * 32, o);
+                    }
+                    __syncwarp();
+                    copy_rows_out<D>(sPT, C::PT_BYTES, quad * 32, t.kv_len, pass == 0 ? a.dv : a.dk, t.kv_start,
+                                     t.h, lane);
+                    __syncwarp();
                 }
-                if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
-                if (nq > 0) tmem_ld32(tmem + lane_base + C::COL_DK + c * 32, o);
-                if (row_ok) store_out32(a.dk, krow, t.h, c * 32, o, g.scale);
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    if (nq > 0) {
+                        tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = 0.0f;
+                    }
+                    if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
+                    if (nq > 0) tmem_ld32(tmem + lane_base + C::COL_DK + c * 32, o);
+                    if (row_ok) store_out32(a.dk, krow, t.h, c * 32, o, g.scale);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -119,9 +119,10 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t t_local = 0;
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, true)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, true)) continue;
                 const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
                 if (!(ok = mbar_wait(&in_empty[buf], (use & 1) ^ 1, err))) break;
                 ++t_local;
@@ -148,9 +149,10 @@ __global__ void __launch_bounds__(192, 1)
             const uint32_t idesc_mn = idesc_bf16(128, D, true, true);   // dV, dK
             const uint32_t idesc_kmn = idesc_bf16(128, D, false, true); // dQ
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, false)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, false)) continue;
                 const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
                 if (!(ok = mbar_wait(&in_full[buf], use & 1, err))) break;
                 if (!(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
@@ -203,13 +205,14 @@ __global__ void __launch_bounds__(192, 1)
         const float sc = ACT ? g.scale : g.scale * kLog2e;
         uint32_t t_local = 0;
         bool ok = true;
-        for (int ti = tbeg; ti < tend && ok; ++ti) {
-            Tile t;
-            if (!load_tile(g, ti, t, err, false)) continue;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
             const float *bt = sbias + t.h * g.nb;
             const int len = t.q_len;
-            const int q_loc = t.q_start - g.q_off[t.b] + row;
-            const int kv_loc0 = t.kv_start - g.kv_off[t.b] + half * 64;  // first key of this row's block
+            const int q_loc = t.q_loc0 + row;
+            const int kv_loc0 = t.kv_loc0 + half * 64;  // first key of this row's block
             const int nvalid = min(64, max(0, len - half * 64));          // valid keys in the block
             // Query rows past the sequence end must contribute nothing to dK / dV.
             const bool row_valid = row < len;
@@ -218,13 +221,9 @@ __global__ void __launch_bounds__(192, 1)
             float s[64], dp[64];
             bool live[2];
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                live[c] = c * 32 < nvalid;  // uniform across the warp (one warp lies in one block)
-                if (live[c]) {
-                    tmem_ld32(tmem + lane_base + C::COL_S + half * 64 + c * 32, sub32(s, c));
-                    tmem_ld32(tmem + lane_base + C::COL_DP + half * 64 + c * 32, sub32(dp, c));
-                }
-            }
+            for (int c = 0; c < 2; ++c) live[c] = c * 32 < nvalid;  // uniform: one warp lies in one block
+            if (nvalid > 0)
+                tmem_ld64x2(tmem + lane_base + C::COL_S + half * 64, tmem + lane_base + C::COL_DP + half * 64, s, dp);
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 if (!live[c]) continue;
@@ -323,15 +322,36 @@ __global__ void __launch_bounds__(192, 1)
             const bool row_ok = row < len;
             const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
             const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
+            if (rows_fast<D>(a.dq)) {
+                // stage dQ, dK, dV in turn in this warp's rows of the P tile (every MMA is done)
+                for (int pass = 0; pass < 3; ++pass) {
+                    const uint32_t col = pass == 0 ? C::COL_S : (pass == 1 ? C::COL_DK : C::COL_DV);
+                    const float mul = pass == 2 ? 1.0f : g.scale;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                tmem_ld32(tmem + lane_base + C::COL_S + c * 32, o);
-                if (row_ok) store_out32(a.dq, qrow, t.h, c * 32, o, g.scale);
-                tmem_ld32(tmem + lane_base + C::COL_DK + c * 32, o);
-                if (row_ok) store_out32(a.dk, krow, t.h, c * 32, o, g.scale);
-                tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
-                if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
+                    for (int hc = 0; hc < D / 64; ++hc) {
+                        float oa[64];
+                        tmem_ld64(tmem + lane_base + col + hc * 64, oa);
+#pragma unroll
+                        for (int i = 0; i < 64; i += 2) mul2(oa[i], oa[i + 1], mul, mul);
+                        st_row32_bf16(sP, C::SUB, row, hc * 64, sub32(oa, 0));
+                        st_row32_bf16(sP, C::SUB, row, hc * 64 + 32, sub32(oa, 1));
+                    }
+                    __syncwarp();
+                    copy_rows_out<D>(sP, C::SUB, quad * 32, len, pass == 0 ? a.dq : (pass == 1 ? a.dk : a.dv),
+                                     pass == 0 ? t.q_start : t.kv_start, t.h, lane);
+                    __syncwarp();
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + C::COL_S + c * 32, o);
+                    if (row_ok) store_out32(a.dq, qrow, t.h, c * 32, o, g.scale);
+                    tmem_ld32(tmem + lane_base + C::COL_DK + c * 32, o);
+                    if (row_ok) store_out32(a.dk, krow, t.h, c * 32, o, g.scale);
+                    tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
+                    if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
+                }
             }
             tc_fence_before();
             __syncwarp();

@@ -18,14 +18,18 @@ constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 // largest bias table (H * NB floats) the kernels stage in shared memory
 constexpr int kMaxBiasFloats = 256;
+// largest reflected bias table (H * (2 * (NB + 30) + 1) floats) the softmax kernels stage
+constexpr int kMaxBiasExtFloats = 1024;
 
 // online-softmax rescale threshold (log2 units): the running max is only moved,
 // and O rescaled, when a row's max grows by more than this, so unnormalised
 // probabilities stay below 2^8.
 constexpr float kRescaleThreshold = 8.0f;
 
+// Device tile record: the ABI's 24-byte record plus the tile's first query and
+// key positions local to its sequence (precomputed by the planner).
 struct Tile {
-    int32_t b, h, q_start, q_len, kv_start, kv_len;
+    int32_t b, h, q_start, q_len, kv_start, kv_len, q_loc0, kv_loc0;
 };
 
 enum Act : int32_t { kSoftmax = 0, kSilu = 1, kGeluTanh = 2 };

@@ -46,11 +46,14 @@ struct FwdCfg {
     static constexpr uint32_t OFF_PLO = OFF_P + P_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_PLO + (ACT ? P_BYTES : 0);
     // q_full, q_empty, kv_full[NST], kv_empty[NST], s_full[2], s_empty[2], p_full, pv_done,
-    // o_full[2], o_empty[2], drain
-    static constexpr int NBAR = 2 + 2 * NST + 4 + 2 + 4 + 1;
+    // o_full[2], o_empty[2], drain, xbar[4]
+    static constexpr int NBAR = 2 + 2 * NST + 4 + 2 + 4 + 1 + 4;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
-    static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + kMaxBiasFloats * 4;  // reflected table (softmax only)
+    static constexpr uint32_t OFF_XCHG = OFF_BEXT + (ACT ? 0 : kMaxBiasExtFloats * 4);  // [2][2][128] floats
+    static constexpr uint32_t SMEM = OFF_XCHG + (ACT ? 0 : 2 * 2 * 128 * 4);
+    static constexpr int THREADS = 320;  // producer, MMA issuer, two softmax warpgroups
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;  // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;    // two score buffers of BN columns
@@ -59,7 +62,7 @@ struct FwdCfg {
 };
 
 template <int D, bool ACT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
     using C = FwdCfg<D, ACT>;
@@ -81,9 +84,13 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *o_full = pv_done + 1;
     uint64_t *o_empty = o_full + 2;
     uint64_t *drain = o_empty + 2;
+    uint64_t *xbar = drain + 1;  // [4]: the two groups' warps of one TMEM lane quadrant
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
+    float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
+    float *xchg = reinterpret_cast<float *>(smem + C::OFF_XCHG);
+    const bool use_ext = !ACT && g.nb > 0 && g.H * ext_len(g.nb) <= kMaxBiasExtFloats;
 
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
@@ -100,11 +107,12 @@ __global__ void __launch_bounds__(192, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 4);
+            mbar_init(&s_empty[b], 8);
             mbar_init(&o_full[b], 1);
-            mbar_init(&o_empty[b], 4);
+            mbar_init(&o_empty[b], 8);
         }
-        mbar_init(p_full, 4);
+        for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 2);
+        mbar_init(p_full, 8);
         mbar_init(pv_done, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -115,6 +123,7 @@ __global__ void __launch_bounds__(192, 1)
         tmem_relinquish();
     }
     stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (use_ext) stage_bias_ext(g, sext, kLog2e);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -133,9 +142,10 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) {
             uint32_t kv_it = 0, t_local = 0;
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, true)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, true)) continue;
                 if (!(ok = mbar_wait(q_empty, (t_local & 1) ^ 1, err))) break;
                 ++t_local;
                 mbar_arrive_expect_tx(q_full, C::Q_BYTES);
@@ -170,9 +180,10 @@ __global__ void __launch_bounds__(192, 1)
             uint32_t kv_it = 0, s_it = 0, p_it = 0, t_local = 0;
             const uint32_t idesc_pv = idesc_bf16(128, D, false, true);
             bool ok = true;
-            for (int ti = tbeg; ti < tend && ok; ++ti) {
-                Tile t;
-                if (!load_tile(g, ti, t, err, false)) continue;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, false)) continue;
                 const int nkv = cdiv(t.kv_len, C::BN);
                 const uint32_t ob = t_local & 1, ouse = t_local >> 1;
                 if (!(ok = mbar_wait(q_full, t_local & 1, err))) break;
@@ -238,20 +249,41 @@ __global__ void __launch_bounds__(192, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax / epilogue
+        // Two warpgroups share every score row: group wg handles key columns
+        // [64 wg, 64 wg + 64) of each 128-key block and output columns
+        // [wg D/2, (wg + 1) D/2).  Per key block they exchange their partial row
+        // maxima through shared memory (one bounded mbarrier per TMEM lane
+        // quadrant); their partial row sums are added once per tile.
+        constexpr int HC = C::BN / 2;  // key columns per group
+        constexpr int HD = D / 2;      // output columns per group
+        const int wg = (warp - 2) >> 2;
         const int quad = warp & 3;            // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;     // query row within the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const float sc = ACT ? g.scale : g.scale * kLog2e;
-        uint32_t s_it = 0, p_it = 0, t_local = 0;
+        const int cbase = wg * HC;            // first key column of this group in a block
+        uint32_t s_it = 0, p_it = 0, t_local = 0, x_it = 0;
         bool ok = true;
-        for (int ti = tbeg; ti < tend && ok; ++ti) {
-            Tile t;
-            if (!load_tile(g, ti, t, err, false)) continue;
+        // Swap one value per row with the partner warp (same quadrant, other group).
+        auto exchange = [&](float mine, float &theirs) -> bool {
+            const uint32_t slot = x_it & 1;
+            xchg[(slot * 2 + wg) * 128 + row] = mine;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&xbar[quad]);
+            if (!mbar_wait_warp(&xbar[quad], x_it & 1, err)) return false;
+            theirs = xchg[(slot * 2 + (wg ^ 1)) * 128 + row];
+            ++x_it;
+            return true;
+        };
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
             const int nkv = cdiv(t.kv_len, C::BN);
             const float *bt = sbias + t.h * g.nb;
-            const int q_loc = t.q_start - g.q_off[t.b] + row;
-            const int kv_loc0 = t.kv_start - g.kv_off[t.b];
-            float m = -INFINITY, l = 0.0f;
+            const float *ext_h = sext + t.h * ext_len(g.nb);
+            const int q_loc = t.q_loc0 + row;
+            float m = -INFINITY, l = 0.0f;  // l: this group's partial row sum
 
             for (int j = 0; j < nkv; ++j) {
                 const uint32_t sb = s_it & 1, suse = s_it >> 1;
@@ -259,103 +291,128 @@ __global__ void __launch_bounds__(192, 1)
                 tc_fence_after();
                 const int nvalid = min(C::BN, t.kv_len - j * C::BN);
                 const int ncols = round_up16(nvalid);
-                float x[C::BN];
-                bool live[4];
+                float x[HC];
+                bool live[2];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    live[c] = (c * 32 < nvalid) && (g.block == 0 || (c >> 1) == (row >> 6));
-                    if (live[c]) tmem_ld32(tmem + lane_base + C::COL_S + sb * C::BN + c * 32, sub32(x, c));
+                for (int c = 0; c < 2; ++c) {
+                    const int cg = cbase + c * 32;
+                    live[c] = (cg < nvalid) && (g.block == 0 || (cg >> 6) == (row >> 6));
                 }
+                if (cbase < ncols) tmem_ld64(tmem + lane_base + C::COL_S + sb * C::BN + cbase, x);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_empty[sb]);
                 ++s_it;
 
-                // scores (log2 units for softmax) with bias and key mask
-                const int kvb = kv_loc0 + j * C::BN;
+                // scores with bias and key mask (softmax: log2 units; without a
+                // bias the scale is folded into the exponent's FMA below)
+                const int kvb = t.kv_loc0 + j * C::BN + cbase;
+                const bool scaled = ACT || g.nb > 0;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 2; ++c) {
                     if (!live[c]) continue;
-                    float bv[32];
+                    float(&xc)[32] = sub32(x, c);
                     if (g.nb > 0) {
-                        bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
-                    } else {
+                        if (use_ext) {
+                            scale_bias32(xc, sc, ext_h, g.nb, q_loc, kvb + c * 32);
+                        } else {
+                            float bv[32];
+                            bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) bv[i] = 0.0f;
-                    }
+                            for (int i = 0; i < 32; i += 2) fma2(xc[i], xc[i + 1], sc, sc, bv[i], bv[i + 1]);
+                        }
+                    } else if (ACT) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const bool in = c * 32 + i < nvalid;
-                        const float v = fmaf(x[c * 32 + i], sc, bv[i]);
-                        x[c * 32 + i] = in ? v : (ACT ? 0.0f : -INFINITY);
+                        for (int i = 0; i < 32; i += 2) mul2(xc[i], xc[i + 1], sc, sc);
                     }
+                    const int cg = cbase + c * 32;
+                    if (cg + 32 > nvalid) {  // the sequence's last keys end inside this chunk
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (cg + i >= nvalid) xc[i] = ACT ? 0.0f : -INFINITY;
+                    }
+                }
+                float mloc = -INFINITY;
+                if (!ACT) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c)
+                        if (live[c]) mloc = fmaxf(mloc, max32(sub32(x, c)));
+                    if (!scaled) mloc *= sc;
+                    float mo;
+                    if (!(ok = exchange(mloc, mo))) break;
+                    mloc = fmaxf(mloc, mo);
                 }
                 // the previous P @ V must be done before P is overwritten or O touched
                 if (p_it > 0) {
                     if (!(ok = mbar_wait_warp(pv_done, (p_it - 1) & 1, err))) break;
                 }
                 if (!ACT) {
-                    float mloc = -INFINITY;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (!live[c]) continue;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) mloc = fmaxf(mloc, x[c * 32 + i]);
-                    }
                     const float m_new = fmaxf(m, mloc);
                     if (j == 0) {
                         m = m_new;
                     } else {
+                        // both groups see the same maxima, so they take the same decision
                         const bool need = m_new > m + kRescaleThreshold;
                         if (__any_sync(0xffffffffu, need)) {
                             const float alpha = ex2_approx(m - m_new);
                             tc_fence_after();
+                            const uint32_t ta = tmem + lane_base + C::COL_O + (t_local & 1) * D + wg * HD;
+                            if constexpr (HD == 64) {
+                                float o[64];
+                                tmem_ld64(ta, o);
 #pragma unroll
-                            for (int c = 0; c < D / 32; ++c) {
+                                for (int i = 0; i < 64; i += 2) mul2(o[i], o[i + 1], alpha, alpha);
+                                tmem_st32(ta, sub32(o, 0));
+                                tmem_st32(ta + 32, sub32(o, 1));
+                            } else {
                                 float o[32];
-                                const uint32_t ta = tmem + lane_base + C::COL_O + (t_local & 1) * D + c * 32;
                                 tmem_ld32(ta, o);
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                                for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], alpha, alpha);
                                 tmem_st32(ta, o);
                             }
                             l *= alpha;
                             m = m_new;
                         }
                     }
-                    const float msub = (m == -INFINITY) ? 0.0f : m;
+                    const float nm = (m == -INFINITY) ? 0.0f : -m;
                     float rs = 0.0f;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c * 32 >= ncols) continue;
+                    for (int c = 0; c < 2; ++c) {
+                        const int cg = cbase + c * 32;
+                        if (cg >= ncols) continue;
                         if (!live[c]) {
-                            st_row32_zero(sP, C::BM * 128, row, c * 32);
+                            st_row32_zero(sP, C::BM * 128, row, cg);
                             continue;
                         }
+                        float(&xc)[32] = sub32(x, c);
+                        if (scaled) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float p = ex2_approx(x[c * 32 + i] - msub);
-                            x[c * 32 + i] = p;
-                            rs += p;
+                            for (int i = 0; i < 32; i += 2) add2(xc[i], xc[i + 1], nm, nm);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) fma2(xc[i], xc[i + 1], sc, sc, nm, nm);
                         }
-                        st_row32_bf16(sP, C::BM * 128, row, c * 32, sub32(x, c));
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) xc[i] = ex2_approx(xc[i]);
+                        rs += sum32(xc);
+                        st_row32_bf16(sP, C::BM * 128, row, cg, xc);
                     }
                     l += rs;
                 } else {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        if (c * 32 >= ncols) continue;
+                    for (int c = 0; c < 2; ++c) {
+                        const int cg = cbase + c * 32;
+                        if (cg >= ncols) continue;
                         if (!live[c]) {
-                            st_row32_zero(sP, C::BM * 128, row, c * 32);
-                            st_row32_zero(sPlo, C::BM * 128, row, c * 32);
+                            st_row32_zero(sP, C::BM * 128, row, cg);
+                            st_row32_zero(sPlo, C::BM * 128, row, cg);
                             continue;
                         }
+                        float(&xc)[32] = sub32(x, c);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const bool in = c * 32 + i < nvalid;
-                            x[c * 32 + i] = in ? act_fwd(g.act, x[c * 32 + i]) : 0.0f;
-                        }
-                        st_row32_bf16_hilo(sP, sPlo, C::BM * 128, row, c * 32, sub32(x, c));
+                        for (int i = 0; i < 32; ++i) xc[i] = cg + i < nvalid ? act_fwd(g.act, xc[i]) : 0.0f;
+                        st_row32_bf16_hilo(sP, sPlo, C::BM * 128, row, cg, xc);
                     }
                 }
                 fence_async_smem();
@@ -366,27 +423,48 @@ __global__ void __launch_bounds__(192, 1)
             }
             if (!ok) break;
 
-            // ---- epilogue: O (/ l) -> global, lse
+            // ---- epilogue: this group's half of O (/ l) -> global; lse from group 0
             const uint32_t ob = t_local & 1, ouse = t_local >> 1;
             if (!(ok = mbar_wait_warp(&o_full[ob], ouse & 1, err))) break;
             tc_fence_after();
+            float lt = l;
+            if (!ACT) {
+                float lo_;
+                if (!(ok = exchange(l, lo_))) break;
+                lt = wg == 0 ? l + lo_ : lo_ + l;  // same order in both groups
+            }
             const bool row_ok = row < t.q_len;
             const int64_t orow = static_cast<int64_t>(t.q_start) + row;
-            const float mul = ACT ? 1.0f : (l > 0.0f ? 1.0f / l : 0.0f);
+            const float mul = ACT ? 1.0f : (lt > 0.0f ? 1.0f / lt : 0.0f);
+            const bool fast = rows_fast<D>(a.out);
+            float oa[HD];
+            if (nkv > 0) {
+                tmem_ld_row<HD>(tmem + lane_base + C::COL_O + ob * D + wg * HD, oa);
+            } else {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float o[32];
-                if (nkv > 0) {
-                    tmem_ld32(tmem + lane_base + C::COL_O + ob * D + c * 32, o);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0.0f;
-                }
-                if (row_ok) store_out32(a.out, orow, t.h, c * 32, o, mul);
+                for (int i = 0; i < HD; ++i) oa[i] = 0.0f;
             }
-            if (!ACT && a.lse != nullptr && row_ok) {
+#pragma unroll
+            for (int c = 0; c < HD / 32; ++c) {
+                float(&o)[32] = sub32(oa, c);
+                const int col = wg * HD + c * 32;
+                if (fast) {
+                    // stage the row in this warp's own rows of the P tile (all P @ V are done)
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], mul, mul);
+                    st_row32_bf16(sP, C::BM * 128, row, col, o);
+                } else if (row_ok) {
+                    store_out32(a.out, orow, t.h, col, o, mul);
+                }
+            }
+            if (fast) {
+                __syncwarp();
+                copy_rows_cols<HD, D>(sP, C::BM * 128, wg * HD, quad * 32, t.q_len, a.out, t.q_start, t.h, lane);
+                __syncwarp();
+            }
+            if (!ACT && wg == 0 && a.lse != nullptr && row_ok) {
                 a.lse[static_cast<int64_t>(t.h) * g.Tq + orow] =
-                    (nkv > 0 && l > 0.0f) ? (m + __log2f(l)) * kLn2 : -INFINITY;
+                    (nkv > 0 && lt > 0.0f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
             }
             tc_fence_before();
             __syncwarp();
@@ -410,7 +488,7 @@ static cudaError_t launch_fwd_t(const TmapSet &tm, const FwdArgs &a, int n_ctas,
     static bool done[64] = {};
     cudaError_t e = ensure_smem(kern, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    kern<<<n_ctas, 192, C::SMEM_ALLOC, stream>>>(tm.q, tm.k, tm.v, a);
+    kern<<<n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(tm.q, tm.k, tm.v, a);
     return cudaGetLastError();
 }
 
