@@ -179,6 +179,28 @@ __device__ __forceinline__ void copy_rows_out(uint32_t tile, uint32_t sub_bytes,
     }
 }
 
+// Copy a warp's 32 staged rows of one 64-column sub-tile (128B-swizzled bf16,
+// rows row0 .. row0+31) to columns gcol0 .. gcol0+63 of the bf16 result rows
+// grow0 + row, head h; rows >= nvalid are skipped.  Eight lanes cover one
+// 128-byte row segment, so each warp store writes four whole segments.
+template <int D>
+__device__ __forceinline__ void copy_seg64(uint32_t sub, int row0, int nvalid, const OutDesc &o, int64_t grow0,
+                                           int h, int gcol0, uint32_t lane) {
+    const int cc = static_cast<int>(lane) & 7, rsub = static_cast<int>(lane) >> 3;
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] = ld_shared_v4(sub + sw128_offset(row0 + 4 * k + rsub, cc));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int r = row0 + 4 * k + rsub;
+        if (r < nvalid) {
+            __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(o.ptr) + (grow0 + r) * o.ld +
+                                 static_cast<int64_t>(h) * D + gcol0 + cc * 8;
+            *reinterpret_cast<uint4 *>(dst) = v[k];
+        }
+    }
+}
+
 // Same, for a W-column slice [c0, c0 + W) of rows of width D: lanes write
 // consecutive 16-byte pieces of each row slice.
 template <int W, int D>

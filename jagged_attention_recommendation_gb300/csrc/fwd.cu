@@ -7,15 +7,36 @@
 // softmax replaced by GELU / SiLU with no normalisation (no max, no rescale);
 // section "BlockAttention": each 64-token query block sees only its own block.
 //
-// One CTA = 6 warps, persistent over the tiles the planner gave it:
-//   warp 0     TMA producer: Q tile (128 rows) once per tile, then K/V tiles
-//              (128 rows each) through an NST-deep ring.
-//   warp 1     allocates TMEM; one thread issues every tcgen05.mma:
-//              S_j = Q K_j^T into one of two TMEM score buffers, then
-//              O += P_j V_j into one of two TMEM output buffers.
-//   warps 2-5  one thread per query row (TMEM lane): scores -> bias, mask,
-//              online softmax (or activation) -> P (bf16, 128B-swizzled smem),
-//              rare O rescales in TMEM, epilogue O / l -> global, lse.
+// One CTA = 16 warps (four warpgroups), persistent over the tiles the planner
+// gave it.  A tile is 128 query rows of one (sequence, head) against all of its
+// keys, in blocks of 128 keys.  The CTA numbers the key blocks of its tiles
+// consecutively (block n), across tile boundaries.
+//   warp 0      TMA producer for K and V (128-row tiles) through NST-deep rings
+//               with separate release barriers: a K slot refills as soon as
+//               its S = Q K^T is done, a V slot once its P V is done.
+//   warp 1      allocates TMEM; one thread issues every tcgen05.mma.
+//   warp 2      TMA producer for Q, double-buffered so the next tile's rows
+//               arrive while the current tile runs.
+//   warp 3      idle (its registers go to the softmax warpgroups).
+//   warps 4-7   softmax group 0: blocks n = 0, 2, 4, ...
+//   warps 8-11  softmax group 1: blocks n = 1, 3, 5, ...
+//   warps 12-15 output group: merges the two groups' partial results of a
+//               tile, O / l -> global, lse.
+// Each softmax group runs its own online softmax (row max m_g, row sum l_g)
+// over its blocks of a tile into its own TMEM accumulator O_g, so the groups
+// never wait for each other, their exp, scale and max phases interleave on
+// the SM sub-partitions, and at a tile boundary one group starts the next tile
+// while the other finishes the current one.  The output group combines
+//   O = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),
+// m = max(m_0, m_1), over the groups that had blocks in the tile (in the
+// activation modes simply O_0 + O_1).
+// P never touches shared memory: the softmax writes it as bf16 over the
+// group's own score columns in TMEM and P V reads it from there (the A operand
+// of tcgen05.mma may live in TMEM).  The issuer orders
+//   S_0, S_1, PV_0, S_2, PV_1, S_3, ...
+// and tcgen05.mma operations of one thread execute in issue order, so S_{n+2}
+// overwrites P_n only after PV_n has read it, while S_{n+1} is computed during
+// the softmax of block n.
 // Rows past a sequence's end are loaded (they belong to the next sequence or
 // are zero-filled past the tensor end) but masked as keys and never stored as
 // queries; the last key block of a sequence runs a narrower MMA (N rounded up
@@ -23,49 +44,59 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#define JATTN_INLINE_WAITS 1
 #include "attn.cuh"
 #include "kernels.h"
 
 namespace jattn {
 using namespace dev;
 
-template <int D, bool ACT>
+// How the relative-position bias reaches the scores.
+enum : int {
+    kBiasNone = 0,
+    kBiasExt = 1,    // reflected per-head table in shared memory (contiguous windows)
+    kBiasTable = 2,  // the [H, nb] table in shared memory, bucket computed per element
+};
+
+template <int D, bool ACT, int BIAS>
 struct FwdCfg {
     static constexpr int BM = 128, BN = 128;
     static constexpr int NKB = D / 64;  // 64-column sub-tiles along D
-    static constexpr int NST = (D == 64) ? 4 : 2;
-    static constexpr uint32_t SUB_Q = BM * 128;   // bytes of one 64-column sub-tile
+    static constexpr int NST = (D == 64) ? 4 : 2;  // depth of the K ring and of the V ring
+    static constexpr uint32_t SUB_Q = BM * 128;    // bytes of one 64-column sub-tile
     static constexpr uint32_t SUB_KV = BN * 128;
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;
-    static constexpr uint32_t P_BYTES = BM * BN * 2;
+    // q_full[2], q_empty[2], k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
+    // s_full[2], p_full[2], o_full, o_empty[2], l_full[2], drain
+    static constexpr int NBAR = 4 + 4 * NST + 2 + 2 + 1 + 2 + 2 + 1;
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
+    static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + NST * KV_BYTES;
-    static constexpr uint32_t OFF_PLO = OFF_P + P_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_PLO + (ACT ? P_BYTES : 0);
-    // q_full, q_empty, kv_full[NST], kv_empty[NST], s_full[2], s_empty[2], p_full, pv_done,
-    // o_full[2], o_empty[2], drain, xbar[4]
-    static constexpr int NBAR = 2 + 2 * NST + 4 + 2 + 4 + 1 + 4;
+    static constexpr uint32_t OFF_BAR = OFF_V + NST * KV_BYTES;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
-    static constexpr uint32_t OFF_BEXT = OFF_BIAS + kMaxBiasFloats * 4;  // reflected table (softmax only)
-    static constexpr uint32_t OFF_XCHG = OFF_BEXT + (ACT ? 0 : kMaxBiasExtFloats * 4);  // [2][2][128] floats
-    static constexpr uint32_t SMEM = OFF_XCHG + (ACT ? 0 : 2 * 2 * 128 * 4);
-    static constexpr int THREADS = 320;  // producer, MMA issuer, two softmax warpgroups
+    static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;  // [H, nb] table (kBiasTable)
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
+    static constexpr uint32_t OFF_ROWS = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
+    static constexpr uint32_t SMEM = OFF_ROWS + (ACT ? 0 : 2 * 4 * 128 * 4);  // [2][m0 l0 m1 l1][128]
+    static constexpr int THREADS = 512;
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;  // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0;    // two score buffers of BN columns
-    static constexpr uint32_t COL_O = 256;  // two output buffers of D columns
+    static constexpr uint32_t COL_S = 0;    // S_g / P_g: BN columns per group
+    static constexpr uint32_t COL_O = 256;  // O_g: D columns per group
+    // registers per thread after the split (launch: 512 threads x 128)
+    static constexpr uint32_t REG_CTRL = 56, REG_SOFTMAX = 176, REG_OUT = 104;
+    static_assert(REG_CTRL * 128 + REG_SOFTMAX * 256 + REG_OUT * 128 <= 128 * 512, "register split");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "operand alignment");
+    static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D, bool ACT>
-__global__ void __launch_bounds__(320, 1)
+template <int D, bool ACT, int BIAS>
+__global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
-    using C = FwdCfg<D, ACT>;
+    using C = FwdCfg<D, ACT, BIAS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -73,47 +104,44 @@ __global__ void __launch_bounds__(320, 1)
     const int lane = threadIdx.x & 31;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *q_full = bars + 0;
-    uint64_t *q_empty = bars + 1;
-    uint64_t *kv_full = bars + 2;
-    uint64_t *kv_empty = bars + 2 + C::NST;
-    uint64_t *s_full = bars + 2 + 2 * C::NST;
-    uint64_t *s_empty = s_full + 2;
-    uint64_t *p_full = s_empty + 2;
-    uint64_t *pv_done = p_full + 1;
-    uint64_t *o_full = pv_done + 1;
-    uint64_t *o_empty = o_full + 2;
-    uint64_t *drain = o_empty + 2;
-    uint64_t *xbar = drain + 1;  // [4]: the two groups' warps of one TMEM lane quadrant
+    uint64_t *q_full = bars + 0;   // [2]
+    uint64_t *q_empty = bars + 2;  // [2]
+    uint64_t *k_full = bars + 4;
+    uint64_t *k_empty = k_full + C::NST;
+    uint64_t *v_full = k_empty + C::NST;
+    uint64_t *v_empty = v_full + C::NST;
+    uint64_t *s_full = v_empty + C::NST;  // [2] per softmax group
+    uint64_t *p_full = s_full + 2;        // [2] per softmax group
+    uint64_t *o_full = p_full + 2;
+    uint64_t *o_empty = o_full + 1;  // [2] per tile parity
+    uint64_t *l_full = o_empty + 2;  // [2] per tile parity
+    uint64_t *drain = l_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
     float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
-    float *xchg = reinterpret_cast<float *>(smem + C::OFF_XCHG);
-    const bool use_ext = !ACT && g.nb > 0 && g.H * ext_len(g.nb) <= kMaxBiasExtFloats;
+    float *srows = reinterpret_cast<float *>(smem + C::OFF_ROWS);  // [tile & 1][m0 | l0 | m1 | l1][row]
 
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
-    const uint32_t sP = smem_u32(smem + C::OFF_P);
-    const uint32_t sPlo = smem_u32(smem + C::OFF_PLO);
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&p_full[s], 4);
+            mbar_init(&o_empty[s], 4);
+            mbar_init(&l_full[s], 8);
+        }
         for (int s = 0; s < C::NST; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 8);
-            mbar_init(&o_full[b], 1);
-            mbar_init(&o_empty[b], 8);
-        }
-        for (int q = 0; q < 4; ++q) mbar_init(&xbar[q], 2);
-        mbar_init(p_full, 8);
-        mbar_init(pv_done, 1);
+        mbar_init(o_full, 1);
         mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -122,8 +150,9 @@ __global__ void __launch_bounds__(320, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
-    if (use_ext) stage_bias_ext(g, sext, kLog2e);
+    // softmax works in log2 units: the bias goes in times log2(e)
+    if (BIAS == kBiasTable) stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (BIAS == kBiasExt) stage_bias_ext(g, sext, ACT ? 1.0f : kLog2e);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -137,144 +166,225 @@ __global__ void __launch_bounds__(320, 1)
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            uint32_t kv_it = 0, t_local = 0;
+    // Role of this warp's warpgroup, warp-uniform by construction; each role
+    // sets its warpgroup's register budget first.
+    const int wgi = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 7, 0);
+    if (wgi == 0) {
+        regs_release<C::REG_CTRL>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- K/V producer
+            // Issue order per key block: K_n, then V_{n-1}, so a V slot that still
+            // waits for its P V never holds back the next S = Q K^T.
+            uint32_t k_it = 0, v_it = 0;
             bool ok = true;
+            bool v_pending = false;
+            int v_col = 0, v_row = 0;
+            auto load_v = [&]() -> bool {
+                const uint32_t slot = v_it % C::NST, use = v_it / C::NST;
+                if (!mbar_wait(&v_empty[slot], (use & 1) ^ 1, err)) return false;
+                mbar_arrive_expect_tx(&v_full[slot], C::KV_BYTES);
+                for (int kb = 0; kb < C::NKB; ++kb)
+                    tma_load_2d(smem + C::OFF_V + slot * C::KV_BYTES + kb * C::SUB_KV, &tmV, &v_full[slot],
+                                v_col + kb * 64, v_row);
+                ++v_it;
+                v_pending = false;
+                return true;
+            };
             TileStream ts(g, tbeg, tend);
             Tile t;
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, true)) continue;
-                if (!(ok = mbar_wait(q_empty, (t_local & 1) ^ 1, err))) break;
-                ++t_local;
-                mbar_arrive_expect_tx(q_full, C::Q_BYTES);
-                for (int kb = 0; kb < C::NKB; ++kb)
-                    tma_load_2d(smem + C::OFF_Q + kb * C::SUB_Q, &tmQ, q_full, t.h * D + kb * 64, t.q_start);
                 const int nkv = cdiv(t.kv_len, C::BN);
-                for (int j = 0; j < nkv; ++j, ++kv_it) {
-                    const uint32_t slot = kv_it % C::NST, use = kv_it / C::NST;
-                    if (!(ok = mbar_wait(&kv_empty[slot], (use & 1) ^ 1, err))) break;
-                    mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
+                for (int j = 0; j < nkv; ++j) {
+                    const uint32_t slot = k_it % C::NST, use = k_it / C::NST;
+                    if (!(ok = mbar_wait(&k_empty[slot], (use & 1) ^ 1, err))) break;
+                    mbar_arrive_expect_tx(&k_full[slot], C::KV_BYTES);
                     const int y = t.kv_start + j * C::BN;
-                    for (int kb = 0; kb < C::NKB; ++kb) {
-                        tma_load_2d(smem + C::OFF_K + slot * C::KV_BYTES + kb * C::SUB_KV, &tmK, &kv_full[slot],
+                    for (int kb = 0; kb < C::NKB; ++kb)
+                        tma_load_2d(smem + C::OFF_K + slot * C::KV_BYTES + kb * C::SUB_KV, &tmK, &k_full[slot],
                                     t.h * D + kb * 64, y);
-                        tma_load_2d(smem + C::OFF_V + slot * C::KV_BYTES + kb * C::SUB_KV, &tmV, &kv_full[slot],
-                                    t.h * D + kb * 64, y);
-                    }
+                    ++k_it;
+                    if (v_pending && !(ok = load_v())) break;
+                    v_pending = true;
+                    v_col = t.h * D;
+                    v_row = y;
                 }
             }
+            if (ok && v_pending) ok = load_v();
             // Do not leave the CTA with copies still landing in shared memory.
             if (!ok) {
-                if (t_local > 0) mbar_drain(q_full, (t_local - 1) & 1);
-                for (uint32_t s = 0; s < C::NST && s < kv_it; ++s) {
-                    const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % C::NST);  // last iteration using slot s
-                    mbar_drain(&kv_full[last % C::NST], (last / C::NST) & 1);
+                for (uint32_t s = 0; s < C::NST && s < k_it; ++s) {
+                    const uint32_t last = k_it - 1 - ((k_it - 1 - s) % C::NST);  // last load into slot s
+                    mbar_drain(&k_full[last % C::NST], (last / C::NST) & 1);
+                }
+                for (uint32_t s = 0; s < C::NST && s < v_it; ++s) {
+                    const uint32_t last = v_it - 1 - ((v_it - 1 - s) % C::NST);
+                    mbar_drain(&v_full[last % C::NST], (last / C::NST) & 1);
                 }
             }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            uint32_t kv_it = 0, s_it = 0, p_it = 0, t_local = 0;
-            const uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------------------- Q producer
+            uint32_t t_local = 0;
             bool ok = true;
             TileStream ts(g, tbeg, tend);
             Tile t;
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, false)) continue;
-                const int nkv = cdiv(t.kv_len, C::BN);
-                const uint32_t ob = t_local & 1, ouse = t_local >> 1;
-                if (!(ok = mbar_wait(q_full, t_local & 1, err))) break;
-                if (!(ok = mbar_wait(&o_empty[ob], (ouse & 1) ^ 1, err))) break;
-                tc_fence_after();
-
-                auto issue_S = [&](int j) -> bool {
-                    const uint32_t it = kv_it + j, slot = it % C::NST, use = it / C::NST;
-                    if (!mbar_wait(&kv_full[slot], use & 1, err)) return false;
-                    const uint32_t sb = s_it & 1, suse = s_it >> 1;
-                    if (!mbar_wait(&s_empty[sb], (suse & 1) ^ 1, err)) return false;
-                    tc_fence_after();
-                    const int ncols = round_up16(min(C::BN, t.kv_len - j * C::BN));
-                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
-                    const uint32_t kbase = sK + slot * C::KV_BYTES;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint64_t ad = sdesc_sw128(sQ + (ks >> 2) * C::SUB_Q + (ks & 3) * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(kbase + (ks >> 2) * C::SUB_KV + (ks & 3) * 32, 16, 1024);
-                        mma_bf16_ss(tmem + C::COL_S + sb * C::BN, ad, bd, idesc, ks > 0);
-                    }
-                    mma_commit(&s_full[sb]);
-                    ++s_it;
-                    return true;
-                };
-
-                if (nkv > 0) ok = issue_S(0);
-                for (int j = 0; ok && j < nkv; ++j) {
-                    if (j + 1 < nkv) {
-                        if (!(ok = issue_S(j + 1))) break;
-                    } else {
-                        mma_commit(q_empty);  // last read of Q for this tile is in flight
-                    }
-                    if (!(ok = mbar_wait(p_full, p_it & 1, err))) break;
-                    tc_fence_after();
-                    const uint32_t slot = (kv_it + j) % C::NST;
-                    const int ksteps = round_up16(min(C::BN, t.kv_len - j * C::BN)) / 16;
-                    const uint32_t vbase = sV + slot * C::KV_BYTES;
-                    const uint32_t dcol = tmem + C::COL_O + ob * D;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::SUB_KV, 1024);
-                        const uint64_t ad = sdesc_sw128(sP + (ks >> 2) * (C::BM * 128) + (ks & 3) * 32, 16, 1024);
-                        mma_bf16_ss(dcol, ad, bd, idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
-                        if (ACT) {
-                            const uint64_t al =
-                                sdesc_sw128(sPlo + (ks >> 2) * (C::BM * 128) + (ks & 3) * 32, 16, 1024);
-                            mma_bf16_ss(dcol, al, bd, idesc_pv, 1u);
-                        }
-                    }
-                    mma_commit(&kv_empty[slot]);
-                    mma_commit(pv_done);
-                    ++p_it;
-                }
-                if (!ok) break;
-                if (nkv == 0) mma_commit(q_empty);
-                mma_commit(&o_full[ob]);
-                kv_it += nkv;
+                const uint32_t s = t_local & 1, use = t_local >> 1;
+                if (!(ok = mbar_wait(&q_empty[s], (use & 1) ^ 1, err))) break;
+                mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES);
+                for (int kb = 0; kb < C::NKB; ++kb)
+                    tma_load_2d(smem + C::OFF_Q + s * C::Q_BYTES + kb * C::SUB_Q, &tmQ, &q_full[s],
+                                t.h * D + kb * 64, t.q_start);
                 ++t_local;
+            }
+            if (!ok) {
+                for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
+                    mbar_drain(&q_full[i & 1], (i >> 1) & 1);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            // Two cursors over the CTA's blocks: S runs two blocks ahead of P V,
+            // across tile boundaries.
+            const uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+            bool ok = true;
+            uint32_t p_cnt[2] = {0, 0};  // P blocks consumed per softmax group
+
+            // S cursor: tile ta (the ta_n-th valid tile), block ja of na, global block ns
+            TileStream tsa(g, tbeg, tend);
+            Tile ta;
+            int ja = 0, na = 0;
+            uint32_t ta_n = 0, ns = 0;
+            // moves to the next tile with keys; tiles without keys only hand back their Q slot
+            auto a_next = [&]() -> bool {
+                while (tsa.next(ta)) {
+                    if (!check_tile(g, ta, err, false)) continue;
+                    na = cdiv(ta.kv_len, C::BN);
+                    ja = 0;
+                    if (na > 0) return true;
+                    if (!(ok = mbar_wait(&q_full[ta_n & 1], (ta_n >> 1) & 1, err))) return false;
+                    mma_commit(&q_empty[ta_n & 1]);
+                    ++ta_n;
+                }
+                return false;
+            };
+            bool a_has = a_next();
+            // S_ns = Q K^T into the score columns of group ns & 1
+            auto issue_S = [&]() {
+                const uint32_t qs = ta_n & 1;
+                if (ja == 0) {
+                    if (!(ok = mbar_wait(&q_full[qs], (ta_n >> 1) & 1, err))) return;
+                }
+                const uint32_t slot = ns % C::NST, use = ns / C::NST;
+                if (!(ok = mbar_wait(&k_full[slot], use & 1, err))) return;
+                tc_fence_after();
+                const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
+                const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                const uint32_t qbase = sQ + qs * C::Q_BYTES;
+                const uint32_t kbase = sK + slot * C::KV_BYTES;
+                const uint32_t dS = tmem + C::COL_S + (ns & 1) * C::BN;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint64_t ad = sdesc_sw128(qbase + (ks >> 2) * C::SUB_Q + (ks & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc_sw128(kbase + (ks >> 2) * C::SUB_KV + (ks & 3) * 32, 16, 1024);
+                    mma_bf16_ss(dS, ad, bd, idesc, ks > 0);
+                }
+                mma_commit(&s_full[ns & 1]);
+                mma_commit(&k_empty[slot]);
+                ++ns;
+                if (++ja == na) {
+                    mma_commit(&q_empty[qs]);  // the last read of this Q slot is in flight
+                    ++ta_n;
+                    a_has = a_next();
+                }
+            };
+
+            // P V cursor: tile tb (the tb_n-th valid tile), block jb of nbk, global block np
+            TileStream tsb(g, tbeg, tend);
+            Tile tb;
+            int jb = 0, nbk = 0;
+            uint32_t tb_n = 0, np = 0;
+            // the output group must have read tile tb_n - 1 before O_0 / O_1 are reused
+            auto wait_out = [&]() -> bool {
+                if (tb_n == 0) return true;
+                return mbar_wait(&o_empty[(tb_n - 1) & 1], ((tb_n - 1) >> 1) & 1, err);
+            };
+            // moves to the next tile with keys; tiles without keys are handed to the
+            // output group (all-zero rows) in order
+            auto b_next = [&]() -> bool {
+                while (tsb.next(tb)) {
+                    if (!check_tile(g, tb, err, false)) continue;
+                    nbk = cdiv(tb.kv_len, C::BN);
+                    jb = 0;
+                    if (nbk > 0) return true;
+                    if (!(ok = wait_out())) return false;
+                    mma_commit(o_full);
+                    ++tb_n;
+                }
+                return false;
+            };
+            bool b_has = b_next();
+            // O_{np & 1} (+)= P_np V_np, P (bf16; activation: hi and lo parts) read from TMEM
+            auto issue_PV = [&]() {
+                const int grp = np & 1;
+                if (!(ok = mbar_wait(&p_full[grp], p_cnt[grp] & 1, err))) return;
+                ++p_cnt[grp];
+                if (jb == 0 && !(ok = wait_out())) return;
+                const uint32_t slot = np % C::NST, use = np / C::NST;
+                if (!(ok = mbar_wait(&v_full[slot], use & 1, err))) return;
+                tc_fence_after();
+                const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
+                const uint32_t vbase = sV + slot * C::KV_BYTES;
+                const uint32_t dO = tmem + C::COL_O + grp * D;
+                const uint32_t aP = tmem + C::COL_S + grp * C::BN;
+                // the first two blocks of a tile start their group's accumulator
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::SUB_KV, 1024);
+                    if (ACT) {  // hi at columns 16 ks .. +7, lo at 16 ks + 8 .. +15
+                        mma_bf16_ts(dO, aP + ks * 16, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
+                        mma_bf16_ts(dO, aP + ks * 16 + 8, bd, idesc_pv, 1u);
+                    } else {
+                        mma_bf16_ts(dO, aP + ks * 8, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
+                    }
+                }
+                mma_commit(&v_empty[slot]);
+                ++np;
+                if (++jb == nbk) {
+                    mma_commit(o_full);
+                    ++tb_n;
+                    b_has = b_next();
+                }
+            };
+
+            if (ok && a_has) issue_S();
+            if (ok && a_has) issue_S();
+            while (ok && b_has) {
+                issue_PV();
+                // S_{np+1} overwrites P_{np-1}: issued after that P V, executed after it
+                if (ok && a_has) issue_S();
             }
             // wait for every MMA this thread issued before TMEM is released
             mma_commit(drain);
             mbar_drain(drain, 0);
         }
-    } else {
-        // ------------------------------------------------------------ softmax / epilogue
-        // Two warpgroups share every score row: group wg handles key columns
-        // [64 wg, 64 wg + 64) of each 128-key block and output columns
-        // [wg D/2, (wg + 1) D/2).  Per key block they exchange their partial row
-        // maxima through shared memory (one bounded mbarrier per TMEM lane
-        // quadrant); their partial row sums are added once per tile.
-        constexpr int HC = C::BN / 2;  // key columns per group
-        constexpr int HD = D / 2;      // output columns per group
-        const int wg = (warp - 2) >> 2;
-        const int quad = warp & 3;            // TMEM lane quadrant of this warp
-        const int row = quad * 32 + lane;     // query row within the tile == TMEM lane
+        // warp 3 and the other lanes: idle
+    } else if (wgi < 3) {
+        regs_claim<C::REG_SOFTMAX>();
+        // ------------------------------------------------------------ softmax
+        // One thread per query row (TMEM lane) over all 128 columns of the
+        // group's blocks: scores -> bias, mask, online softmax (or activation)
+        // -> P as bf16 over the same TMEM columns; rare O rescales in TMEM; per
+        // tile the row max and row sum go to the output group.
+        const int grp = wgi - 1;                   // blocks n with n % 2 == grp
+        const int quad = warp & 3;                 // TMEM lane quadrant of this warp
+        const int row = quad * 32 + lane;          // query row within the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + C::COL_S + grp * C::BN;  // S, then P over it
+        const uint32_t tO = tmem + lane_base + C::COL_O + grp * D;
         const float sc = ACT ? g.scale : g.scale * kLog2e;
-        const int cbase = wg * HC;            // first key column of this group in a block
-        uint32_t s_it = 0, p_it = 0, t_local = 0, x_it = 0;
+        constexpr bool scaled = ACT || BIAS != kBiasNone;  // else the scale is folded into the exponent
+        uint32_t s_it = 0, t_local = 0, n0 = 0;  // n0: global number of the tile's first block
         bool ok = true;
-        // Swap one value per row with the partner warp (same quadrant, other group).
-        auto exchange = [&](float mine, float &theirs) -> bool {
-            const uint32_t slot = x_it & 1;
-            xchg[(slot * 2 + wg) * 128 + row] = mine;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&xbar[quad]);
-            if (!mbar_wait_warp(&xbar[quad], x_it & 1, err)) return false;
-            theirs = xchg[(slot * 2 + (wg ^ 1)) * 128 + row];
-            ++x_it;
-            return true;
-        };
         TileStream ts(g, tbeg, tend);
         Tile t;
         while (ok && ts.next(t)) {
@@ -283,192 +393,256 @@ __global__ void __launch_bounds__(320, 1)
             const float *bt = sbias + t.h * g.nb;
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int q_loc = t.q_loc0 + row;
-            float m = -INFINITY, l = 0.0f;  // l: this group's partial row sum
+            const int j0 = (grp - static_cast<int>(n0 & 1)) & 1;  // this group's first block of the tile
+            // A warp whose 32 rows all lie past the tile's end only keeps the hand-offs
+            // going: rows are independent through both products, so whatever its TMEM
+            // lanes hold reaches only output rows that are never stored.
+            const bool warp_live = quad * 32 < t.q_len;
+            float m = -INFINITY, l = 0.0f;
 
-            for (int j = 0; j < nkv; ++j) {
-                const uint32_t sb = s_it & 1, suse = s_it >> 1;
-                if (!(ok = mbar_wait_warp(&s_full[sb], suse & 1, err))) break;
-                tc_fence_after();
-                const int nvalid = min(C::BN, t.kv_len - j * C::BN);
-                const int ncols = round_up16(nvalid);
-                float x[HC];
-                bool live[2];
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    const int cg = cbase + c * 32;
-                    live[c] = (cg < nvalid) && (g.block == 0 || (cg >> 6) == (row >> 6));
-                }
-                if (cbase < ncols) tmem_ld64(tmem + lane_base + C::COL_S + sb * C::BN + cbase, x);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
+            for (int j = j0; j < nkv; j += 2) {
+                if (!(ok = mbar_wait_warp(&s_full[grp], s_it & 1, err))) break;
                 ++s_it;
-
-                // scores with bias and key mask (softmax: log2 units; without a
-                // bias the scale is folded into the exponent's FMA below)
-                const int kvb = t.kv_loc0 + j * C::BN + cbase;
-                const bool scaled = ACT || g.nb > 0;
+                if (!warp_live) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[grp]);
+                    continue;
+                }
+                tc_fence_after();
+                // The block is walked in 32-key chunks by compact loops (the whole
+                // unrolled block would not stay in the instruction cache); TMEM
+                // holds the scores between passes.
+                const int nvalid = min(C::BN, t.kv_len - j * C::BN);
+                const int kvb = t.kv_loc0 + j * C::BN;
+                // chunk c holds keys this row may see (block mode: its own 64-block)
+                auto live = [&](int c) {
+                    return c * 32 < nvalid && (g.block == 0 || ((c * 32) >> 6) == (row >> 6));
+                };
+                // scores of chunk c with scale, bias and key mask (softmax: log2 units;
+                // without a bias the scale waits for the exponent's FMA)
+                auto scores = [&](int c, float (&xc)[32]) {
+                    if constexpr (BIAS == kBiasExt) {
+                        scale_bias32(xc, sc, ext_h, g.nb, q_loc, kvb + c * 32);
+                    } else if constexpr (BIAS == kBiasTable) {
+                        float bv[32];
+                        bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (!live[c]) continue;
-                    float(&xc)[32] = sub32(x, c);
-                    if (g.nb > 0) {
-                        if (use_ext) {
-                            scale_bias32(xc, sc, ext_h, g.nb, q_loc, kvb + c * 32);
-                        } else {
-                            float bv[32];
-                            bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) fma2(xc[i], xc[i + 1], sc, sc, bv[i], bv[i + 1]);
-                        }
-                    } else if (ACT) {
+                        for (int i = 0; i < 32; i += 2) fma2(xc[i], xc[i + 1], sc, sc, bv[i], bv[i + 1]);
+                    } else if constexpr (ACT) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) mul2(xc[i], xc[i + 1], sc, sc);
                     }
-                    const int cg = cbase + c * 32;
-                    if (cg + 32 > nvalid) {  // the sequence's last keys end inside this chunk
+                    if (c * 32 + 32 > nvalid) {  // the sequence's last keys end inside this chunk
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            if (cg + i >= nvalid) xc[i] = ACT ? 0.0f : -INFINITY;
+                            if (c * 32 + i >= nvalid) xc[i] = ACT ? 0.0f : -INFINITY;
                     }
-                }
-                float mloc = -INFINITY;
-                if (!ACT) {
+                };
+
+                if constexpr (!ACT) {
+                    // pass 1: row max of the block (biased scores written back in place)
+                    float mloc = -INFINITY;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        if (!live(c)) continue;
+                        float xc[32];
+                        tmem_ld32(tS + 32 * c, xc);
+                        scores(c, xc);
+                        mloc = fmaxf(mloc, max32(xc));
+                        if constexpr (scaled) {
+                            uint32_t w[32];
 #pragma unroll
-                    for (int c = 0; c < 2; ++c)
-                        if (live[c]) mloc = fmaxf(mloc, max32(sub32(x, c)));
-                    if (!scaled) mloc *= sc;
-                    float mo;
-                    if (!(ok = exchange(mloc, mo))) break;
-                    mloc = fmaxf(mloc, mo);
-                }
-                // the previous P @ V must be done before P is overwritten or O touched
-                if (p_it > 0) {
-                    if (!(ok = mbar_wait_warp(pv_done, (p_it - 1) & 1, err))) break;
-                }
-                if (!ACT) {
-                    const float m_new = fmaxf(m, mloc);
-                    if (j == 0) {
-                        m = m_new;
-                    } else {
-                        // both groups see the same maxima, so they take the same decision
-                        const bool need = m_new > m + kRescaleThreshold;
-                        if (__any_sync(0xffffffffu, need)) {
-                            const float alpha = ex2_approx(m - m_new);
-                            tc_fence_after();
-                            const uint32_t ta = tmem + lane_base + C::COL_O + (t_local & 1) * D + wg * HD;
-                            if constexpr (HD == 64) {
-                                float o[64];
-                                tmem_ld64(ta, o);
-#pragma unroll
-                                for (int i = 0; i < 64; i += 2) mul2(o[i], o[i + 1], alpha, alpha);
-                                tmem_st32(ta, sub32(o, 0));
-                                tmem_st32(ta + 32, sub32(o, 1));
-                            } else {
-                                float o[32];
-                                tmem_ld32(ta, o);
-#pragma unroll
-                                for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], alpha, alpha);
-                                tmem_st32(ta, o);
-                            }
-                            l *= alpha;
-                            m = m_new;
+                            for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(xc[i]);
+                            tmem_st32_u32(tS + 32 * c, w);
                         }
+                    }
+                    if constexpr (scaled) tmem_wait_st();
+                    if (!scaled) mloc *= sc;
+                    const float m_new = fmaxf(m, mloc);
+                    // lazy rescale: keep the old max while it is within the threshold
+                    float alpha = 1.0f;
+                    bool resc = false;
+                    if (j == j0) {
+                        m = m_new;
+                    } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
+                        alpha = ex2_approx(m - m_new);
+                        resc = true;
+                        l *= alpha;
+                        m = m_new;
                     }
                     const float nm = (m == -INFINITY) ? 0.0f : -m;
+                    // pass 2: P = 2^(s - m) as bf16; chunk c goes to columns 16c..16c+15,
+                    // which hold scores already consumed
                     float rs = 0.0f;
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t pw[16];
+                        if (!live(c)) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int cg = cbase + c * 32;
-                        if (cg >= ncols) continue;
-                        if (!live[c]) {
-                            st_row32_zero(sP, C::BM * 128, row, cg);
-                            continue;
-                        }
-                        float(&xc)[32] = sub32(x, c);
-                        if (scaled) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 2) add2(xc[i], xc[i + 1], nm, nm);
+                            for (int i = 0; i < 16; ++i) pw[i] = 0u;
                         } else {
+                            float xc[32];
+                            tmem_ld32(tS + 32 * c, xc);
+                            if constexpr (scaled) {
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2) fma2(xc[i], xc[i + 1], sc, sc, nm, nm);
+                                for (int i = 0; i < 32; i += 2) add2(xc[i], xc[i + 1], nm, nm);
+                            } else {
+#pragma unroll
+                                for (int i = 0; i < 32; i += 2) fma2(xc[i], xc[i + 1], sc, sc, nm, nm);
+                            }
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) xc[i] = ex2_approx(xc[i]);
+                            if (!scaled && c * 32 + 32 > nvalid) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (c * 32 + i >= nvalid) xc[i] = 0.0f;
+                            }
+                            rs += sum32(xc);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(xc[2 * i], xc[2 * i + 1]);
                         }
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) xc[i] = ex2_approx(xc[i]);
-                        rs += sum32(xc);
-                        st_row32_bf16(sP, C::BM * 128, row, cg, xc);
+                        tmem_st16_u32(tS + 16 * c, pw);
                     }
                     l += rs;
-                } else {
+                    if (resc) {
+                        // O_grp holds this group's earlier blocks of the tile (its last
+                        // P V finished before S_j did); bring it to the new max first
+#pragma unroll 1
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[32];
+                            tmem_ld32(tO + c * 32, o);
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int cg = cbase + c * 32;
-                        if (cg >= ncols) continue;
-                        if (!live[c]) {
-                            st_row32_zero(sP, C::BM * 128, row, cg);
-                            st_row32_zero(sPlo, C::BM * 128, row, cg);
-                            continue;
+                            for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], alpha, alpha);
+                            tmem_st32(tO + c * 32, o);
                         }
-                        float(&xc)[32] = sub32(x, c);
+                    }
+                } else {
+                    // P = act(s) as bf16 hi + lo parts, interleaved per 16-key MMA step:
+                    // step k's hi at columns 16k..16k+7, its lo at 16k+8..16k+15, so
+                    // chunk c lands exactly on its own score columns 32c..32c+31
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t w[32];
+                        if (!live(c)) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) xc[i] = cg + i < nvalid ? act_fwd(g.act, xc[i]) : 0.0f;
-                        st_row32_bf16_hilo(sP, sPlo, C::BM * 128, row, cg, xc);
+                            for (int i = 0; i < 32; ++i) w[i] = 0u;
+                        } else {
+                            float xc[32];
+                            tmem_ld32(tS + 32 * c, xc);
+                            scores(c, xc);
+#pragma unroll
+                            for (int i = 0; i < 32; i += 2) {
+                                const float a0 = c * 32 + i < nvalid ? act_fwd(g.act, xc[i]) : 0.0f;
+                                const float a1 = c * 32 + i + 1 < nvalid ? act_fwd(g.act, xc[i + 1]) : 0.0f;
+                                __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+                                const int k = i >> 4, e = (i & 15) >> 1;  // MMA step within the chunk, pair
+                                w[16 * k + e] = *reinterpret_cast<uint32_t *>(&h2);
+                                w[16 * k + 8 + e] = pack_bf16x2(a0 - __bfloat162float(h2.x), a1 - __bfloat162float(h2.y));
+                            }
+                        }
+                        tmem_st32_u32(tS + 32 * c, w);
                     }
                 }
-                fence_async_smem();
+                tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
-                ++p_it;
+                if (lane == 0) mbar_arrive(&p_full[grp]);
             }
             if (!ok) break;
 
-            // ---- epilogue: this group's half of O (/ l) -> global; lse from group 0
-            const uint32_t ob = t_local & 1, ouse = t_local >> 1;
-            if (!(ok = mbar_wait_warp(&o_full[ob], ouse & 1, err))) break;
-            tc_fence_after();
-            float lt = l;
-            if (!ACT) {
-                float lo_;
-                if (!(ok = exchange(l, lo_))) break;
-                lt = wg == 0 ? l + lo_ : lo_ + l;  // same order in both groups
+            // ---- this group's row statistics for the output group
+            if constexpr (!ACT) {
+                const uint32_t sl = t_local & 1;
+                // the output group must be done with the tile that last used this slot
+                if (!(ok = mbar_wait_warp(&o_empty[sl], ((t_local >> 1) & 1) ^ 1, err))) break;
+                srows[(sl * 4 + 2 * grp) * 128 + row] = m;
+                srows[(sl * 4 + 2 * grp + 1) * 128 + row] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&l_full[sl]);
             }
+            n0 += nkv;
+            ++t_local;
+        }
+    } else {
+        regs_release<C::REG_OUT>();
+        // ------------------------------------------------------------ output
+        // One thread per query row: merge O_0 and O_1 (TMEM, fp32) of the groups
+        // that had blocks in the tile with their row statistics, write the
+        // output row (each thread stores whole 64-byte pieces of its row) and
+        // lse = ln 2 (m + log2 L).  The accumulators are handed back as soon as
+        // they have been read.
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tO0 = tmem + lane_base + C::COL_O, tO1 = tO0 + D;
+        uint32_t t_local = 0, n0 = 0;
+        bool ok = true;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
+            const int nkv = cdiv(t.kv_len, C::BN);
+            // group g has blocks in this tile when there are two or more, or one
+            // that is its turn
+            const bool has0 = nkv >= 2 || (nkv == 1 && (n0 & 1) == 0);
+            const bool has1 = nkv >= 2 || (nkv == 1 && (n0 & 1) == 1);
+            const uint32_t sl = t_local & 1;
+            if (!(ok = mbar_wait_warp(o_full, t_local & 1, err))) break;
+            float c0 = has0 ? 1.0f : 0.0f, c1 = has1 ? 1.0f : 0.0f, lse = -INFINITY;
+            if constexpr (!ACT) {
+                if (!(ok = mbar_wait_warp(&l_full[sl], (t_local >> 1) & 1, err))) break;
+                const float m0 = srows[(sl * 4 + 0) * 128 + row], l0 = srows[(sl * 4 + 1) * 128 + row];
+                const float m1 = srows[(sl * 4 + 2) * 128 + row], l1 = srows[(sl * 4 + 3) * 128 + row];
+                const float mm = fmaxf(m0, m1);
+                const float w0 = l0 > 0.0f ? ex2_approx(m0 - mm) : 0.0f;
+                const float w1 = l1 > 0.0f ? ex2_approx(m1 - mm) : 0.0f;
+                const float L = l0 * w0 + l1 * w1;
+                const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+                c0 = w0 * inv;
+                c1 = w1 * inv;
+                if (L > 0.0f) lse = (mm + __log2f(L)) * kLn2;
+            }
+            tc_fence_after();
             const bool row_ok = row < t.q_len;
             const int64_t orow = static_cast<int64_t>(t.q_start) + row;
-            const float mul = ACT ? 1.0f : (lt > 0.0f ? 1.0f / lt : 0.0f);
-            const bool fast = rows_fast<D>(a.out);
-            float oa[HD];
-            if (nkv > 0) {
-                tmem_ld_row<HD>(tmem + lane_base + C::COL_O + ob * D + wg * HD, oa);
-            } else {
-#pragma unroll
-                for (int i = 0; i < HD; ++i) oa[i] = 0.0f;
+            if (quad * 32 >= t.q_len) {  // no row of this warp is stored
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&o_empty[sl]);
+                n0 += nkv;
+                ++t_local;
+                continue;
             }
+#pragma unroll 1
+            for (int col = 0; col < D; col += 32) {
+                float o[32];
+                if (has0) {
+                    tmem_ld32(tO0 + col, o);
 #pragma unroll
-            for (int c = 0; c < HD / 32; ++c) {
-                float(&o)[32] = sub32(oa, c);
-                const int col = wg * HD + c * 32;
-                if (fast) {
-                    // stage the row in this warp's own rows of the P tile (all P @ V are done)
+                    for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], c0, c0);
+                } else {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], mul, mul);
-                    st_row32_bf16(sP, C::BM * 128, row, col, o);
-                } else if (row_ok) {
-                    store_out32(a.out, orow, t.h, col, o, mul);
+                    for (int i = 0; i < 32; ++i) o[i] = 0.0f;
                 }
+                if (has1) {
+                    float o1[32];
+                    tmem_ld32(tO1 + col, o1);
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) {  // o += c1 * o1
+                        fma2(o1[i], o1[i + 1], c1, c1, o[i], o[i + 1]);
+                        o[i] = o1[i];
+                        o[i + 1] = o1[i + 1];
+                    }
+                }
+                if (col + 32 >= D) {
+                    // every TMEM read of this tile is done: O_0 / O_1 are free
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&o_empty[sl]);
+                }
+                if (row_ok) store_out32(a.out, orow, t.h, col, o, 1.0f);
             }
-            if (fast) {
-                __syncwarp();
-                copy_rows_cols<HD, D>(sP, C::BM * 128, wg * HD, quad * 32, t.q_len, a.out, t.q_start, t.h, lane);
-                __syncwarp();
-            }
-            if (!ACT && wg == 0 && a.lse != nullptr && row_ok) {
-                a.lse[static_cast<int64_t>(t.h) * g.Tq + orow] =
-                    (nkv > 0 && lt > 0.0f) ? (m + __log2f(lt)) * kLn2 : -INFINITY;
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&o_empty[ob]);
+            if (!ACT && a.lse != nullptr && row_ok) a.lse[static_cast<int64_t>(t.h) * g.Tq + orow] = lse;
+            n0 += nkv;
             ++t_local;
         }
     }
@@ -481,10 +655,10 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
-template <int D, bool ACT>
+template <int D, bool ACT, int BIAS>
 static cudaError_t launch_fwd_t(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
-    using C = FwdCfg<D, ACT>;
-    auto kern = fwd_kernel<D, ACT>;
+    using C = FwdCfg<D, ACT, BIAS>;
+    auto kern = fwd_kernel<D, ACT, BIAS>;
     static bool done[64] = {};
     cudaError_t e = ensure_smem(kern, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
@@ -492,9 +666,18 @@ static cudaError_t launch_fwd_t(const TmapSet &tm, const FwdArgs &a, int n_ctas,
     return cudaGetLastError();
 }
 
+template <int D, bool ACT>
+static cudaError_t launch_fwd_b(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
+    if (a.g.nb <= 0) return launch_fwd_t<D, ACT, kBiasNone>(tm, a, n_ctas, stream);
+    if (a.g.H * ext_len(a.g.nb) <= kMaxBiasExtFloats) return launch_fwd_t<D, ACT, kBiasExt>(tm, a, n_ctas, stream);
+    return launch_fwd_t<D, ACT, kBiasTable>(tm, a, n_ctas, stream);
+}
+
 cudaError_t launch_fwd(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
-    if (D == 128) return act ? launch_fwd_t<128, true>(tm, a, n_ctas, stream) : launch_fwd_t<128, false>(tm, a, n_ctas, stream);
-    if (D == 64) return act ? launch_fwd_t<64, true>(tm, a, n_ctas, stream) : launch_fwd_t<64, false>(tm, a, n_ctas, stream);
+    if (D == 128)
+        return act ? launch_fwd_b<128, true>(tm, a, n_ctas, stream) : launch_fwd_b<128, false>(tm, a, n_ctas, stream);
+    if (D == 64)
+        return act ? launch_fwd_b<64, true>(tm, a, n_ctas, stream) : launch_fwd_b<64, false>(tm, a, n_ctas, stream);
     return cudaErrorInvalidValue;
 }
 
