@@ -241,6 +241,18 @@ __device__ __forceinline__ float act_fwd(int act, float x) {
     return x * sigmoid_f(z);
 }
 
+// The same with the activation fixed at compile time, so that a loop over
+// many elements carries no per-element test and its exponential / reciprocal
+// chains overlap.
+template <int AF>
+__device__ __forceinline__ float act_fwd_t(float x) {
+    if constexpr (AF == kSilu) {
+        return x * sigmoid_f(x);
+    } else {
+        return x * sigmoid_f(kGeluC2 * fmaf(kGeluA * x, x * x, x));
+    }
+}
+
 // act'(x) = sigmoid(z) + x sigmoid(z) (1 - sigmoid(z)) z'(x); also returns act(x).
 __device__ __forceinline__ float act_bwd(int act, float x, float &a) {
     float z, dz;

@@ -44,6 +44,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #define JATTN_INLINE_WAITS 1
 #include "attn.cuh"
 #include "kernels.h"
@@ -520,27 +522,36 @@ __global__ void __launch_bounds__(512, 1)
                     // P = act(s) as bf16 hi + lo parts, interleaved per 16-key MMA step:
                     // step k's hi at columns 16k..16k+7, its lo at 16k+8..16k+15, so
                     // chunk c lands exactly on its own score columns 32c..32c+31
+                    auto act_block = [&](auto af) {
+                        constexpr int AF = decltype(af)::value;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t w[32];
-                        if (!live(c)) {
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t w[32];
+                            if (!live(c)) {
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) w[i] = 0u;
-                        } else {
-                            float xc[32];
-                            tmem_ld32(tS + 32 * c, xc);
-                            scores(c, xc);
+                                for (int i = 0; i < 32; ++i) w[i] = 0u;
+                            } else {
+                                float xc[32];
+                                tmem_ld32(tS + 32 * c, xc);
+                                scores(c, xc);
 #pragma unroll
-                            for (int i = 0; i < 32; i += 2) {
-                                const float a0 = c * 32 + i < nvalid ? act_fwd(g.act, xc[i]) : 0.0f;
-                                const float a1 = c * 32 + i + 1 < nvalid ? act_fwd(g.act, xc[i + 1]) : 0.0f;
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
-                                const int k = i >> 4, e = (i & 15) >> 1;  // MMA step within the chunk, pair
-                                w[16 * k + e] = *reinterpret_cast<uint32_t *>(&h2);
-                                w[16 * k + 8 + e] = pack_bf16x2(a0 - __bfloat162float(h2.x), a1 - __bfloat162float(h2.y));
+                                for (int i = 0; i < 32; i += 2) {
+                                    const float a0 = c * 32 + i < nvalid ? act_fwd_t<AF>(xc[i]) : 0.0f;
+                                    const float a1 = c * 32 + i + 1 < nvalid ? act_fwd_t<AF>(xc[i + 1]) : 0.0f;
+                                    __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
+                                    const int k = i >> 4, e = (i & 15) >> 1;  // MMA step within the chunk, pair
+                                    w[16 * k + e] = *reinterpret_cast<uint32_t *>(&h2);
+                                    w[16 * k + 8 + e] =
+                                        pack_bf16x2(a0 - __bfloat162float(h2.x), a1 - __bfloat162float(h2.y));
+                                }
                             }
+                            tmem_st32_u32(tS + 32 * c, w);
                         }
-                        tmem_st32_u32(tS + 32 * c, w);
+                    };
+                    if (g.act == kSilu) {
+                        act_block(std::integral_constant<int, kSilu>{});
+                    } else {
+                        act_block(std::integral_constant<int, kGeluTanh>{});
                     }
                 }
                 tmem_wait_st();
