@@ -268,6 +268,22 @@ __device__ __forceinline__ float act_bwd(int act, float x, float &a) {
     return fmaf(x * sg * (1.0f - sg), dz, sg);
 }
 
+// The same with the activation fixed at compile time.
+template <int AF>
+__device__ __forceinline__ float act_bwd_t(float x, float &a) {
+    float z, dz;
+    if constexpr (AF == kSilu) {
+        z = x;
+        dz = 1.0f;
+    } else {
+        z = kGeluC2 * fmaf(kGeluA * x, x * x, x);
+        dz = kGeluC2 * fmaf(3.0f * kGeluA, x * x, 1.0f);
+    }
+    const float sg = sigmoid_f(z);
+    a = x * sg;
+    return fmaf(x * sg * (1.0f - sg), dz, sg);
+}
+
 // ---------------------------------------------------------------------------
 // packed fp32 pairs (sm_100 family f32x2 arithmetic) and 3-input max
 // ---------------------------------------------------------------------------
@@ -386,6 +402,37 @@ __device__ __forceinline__ void scale_bias32(float (&x)[32], float sc, const flo
         const float *p = ext_h + ext_pad(nb) + (q - kv0);
 #pragma unroll
         for (int i = 0; i < 32; i += 2) fma2(x[i], x[i + 1], sc, sc, p[-i], p[-i - 1]);
+    }
+}
+
+// Scale and relative-position bias of a 32-wide chunk, plus a constant offset:
+// x[i] = x[i] * sc + bias(position p, other positions o0 .. o0+31) + off.
+// BIAS: 0 none, 1 reflected table ext_h, 2 plain table bt (see the kernels).
+template <int BIAS>
+__device__ __forceinline__ void scale_bias_off32(float (&x)[32], float sc, float off, const float *ext_h,
+                                                 const float *bt, int nb, int p, int o0) {
+    if constexpr (BIAS == 0) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) fma2(x[i], x[i + 1], sc, sc, off, off);
+    } else {
+        float bv[32], cst = 0.0f;
+        bool band = true;
+        if constexpr (BIAS == 1) {
+            band = bias32_ext(ext_h, nb, p, o0, bv, cst);
+        } else {
+            bias32(bt, nb, p, o0, bv);
+        }
+        if (band) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                add2(bv[i], bv[i + 1], off, off);
+                fma2(x[i], x[i + 1], sc, sc, bv[i], bv[i + 1]);
+            }
+        } else {
+            const float o2 = cst + off;
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) fma2(x[i], x[i + 1], sc, sc, o2, o2);
+        }
     }
 }
 

@@ -3,67 +3,109 @@
 // "Training GEM at LLM scale", section "Jagged Sequence Flash Attention",
 // backward parallelisation: accumulating dQ across key tiles normally needs
 // atomic adds; for recommendation shapes (many batch x head pairs) a
-// non-sequence-parallel scheme that computes dQ in a separate pass removes both
-// the atomics and the redundant recompute.  Here:
+// non-sequence-parallel scheme that computes dQ in a separate pass removes the
+// atomics.  Here:
 //   pass 1 (dq_kernel, query-major tiles): per 128-row query tile, loop over the
 //     sequence's keys in 64-row blocks: S = Q K^T, dP = dO V^T (TMEM),
 //     dS = P (dP - Delta) or act'(S) dP, dQ += dS K (TMEM); one writer per dQ row.
 //   pass 2 (dkdv_kernel, key-major tiles): per 128-row key tile, loop over the
 //     sequence's queries in 64-row blocks: S^T = K Q^T, dP^T = V dO^T,
 //     dV += P^T dO, dK += dS^T Q (TMEM); one writer per dK / dV row.
-// Softmax mode recomputes P from the forward's lse; Delta_i = <dO_i, O_i> is
-// computed by a small pre-pass.  Activation mode needs neither; its dS and P
-// reach the tensor cores as a bf16 hi + lo pair (reductions over long key or
-// query ranges would otherwise lose the tolerance to bf16 rounding).
+// Softmax mode recomputes P from the forward's lse; Delta_i = <dO_i, O_i> comes
+// from a small pre-pass.  Activation mode needs neither; its dS and P reach the
+// tensor cores as a bf16 hi + lo pair (reductions over long key or query ranges
+// would otherwise lose the tolerance to bf16 rounding).
+//
+// Both passes share one layout, 16 warps (four warpgroups):
+//   warpgroup 0  warp 0: TMA producer of the looped-over blocks (K / V, or
+//                Q / dO with lse and Delta); warp 1: TMEM allocation and the
+//                single MMA-issuing thread; warp 2: TMA producer of the tile's
+//                own rows (Q / dO, or K / V); warp 3 idle.
+//   warpgroups 1, 2  two compute groups; the CTA numbers its blocks n across
+//                tile boundaries and group g takes the blocks with n % 2 == g,
+//                one thread per tile row (TMEM lane), 32 columns at a time.
+//   warpgroup 3  output group: reads the accumulators and writes the rows.
+// A block's two products land in its group's TMEM columns; the compute group
+// overwrites them in place with bf16 dS (and P^T) and the accumulating product
+// reads that operand from TMEM.  The issuer orders
+//   SdP_0, SdP_1, acc_0, SdP_2, acc_1, SdP_3, ...
+// and tcgen05.mma operations of one thread execute in issue order, so SdP_{n+2}
+// overwrites block n's operands only after acc_n has read them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
+#define JATTN_INLINE_WAITS 1
 #include "attn.cuh"
 #include "kernels.h"
 
 namespace jattn {
 using namespace dev;
 
+namespace {
+enum : int { kBiasNone = 0, kBiasExt = 1, kBiasTable = 2 };
+
+// registers per thread after the split (launch: 512 threads x 128)
+constexpr uint32_t kRegCtrl = 56, kRegCompute = 176, kRegOut = 104;
+static_assert(kRegCtrl * 128 + kRegCompute * 256 + kRegOut * 128 <= 128 * 512, "register split");
+
+// Packs 32 results of one row for a TMEM operand: bf16 pairs (16 words) or,
+// with the remainder, hi / lo pairs interleaved per 16-column MMA step (hi at
+// words 16k..16k+7, lo at 16k+8..16k+15 for step k of the chunk).
+__device__ __forceinline__ void pack16(const float (&v)[32], uint32_t (&w)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+}
+__device__ __forceinline__ void pack_hilo32(const float (&v)[32], uint32_t (&w)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(v[i], v[i + 1]);
+        const int k = i >> 4, e = (i & 15) >> 1;
+        w[16 * k + e] = *reinterpret_cast<uint32_t *>(&h2);
+        w[16 * k + 8 + e] = pack_bf16x2(v[i] - __bfloat162float(h2.x), v[i + 1] - __bfloat162float(h2.y));
+    }
+}
+}  // namespace
+
 // ============================================================================
 // pass 1: dQ
 // ============================================================================
-template <int D, bool ACT>
+template <int D, bool ACT, int BIAS>
 struct DqCfg {
     static constexpr int BM = 128, BN = 64;
     static constexpr int NKB = D / 64;
-    static constexpr int NST = 3;
-    static constexpr uint32_t SUB_Q = BM * 128;  // 16 KB sub-tile (128 rows x 64 cols)
-    static constexpr uint32_t SUB_KV = BN * 128; // 8 KB sub-tile (64 rows x 64 cols)
+    static constexpr int NSK = (D == 64) ? 4 : 3;  // K ring: S, then dQ, read each block
+    static constexpr int NSV = (D == 64) ? 3 : 2;  // V ring: dP only
+    static constexpr uint32_t SUB_Q = BM * 128;    // 16 KB sub-tile (128 rows x 64 cols)
+    static constexpr uint32_t SUB_KV = BN * 128;   // 8 KB sub-tile (64 rows x 64 cols)
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;
-    static constexpr uint32_t DS_BYTES = BM * BN * 2;  // one 16 KB sub-tile
-    static constexpr int NDS = ACT ? 2 : 1;            // hi (+ lo) planes
-    static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_DO = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_K = OFF_DO + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
-    static constexpr uint32_t OFF_DS = OFF_V + NST * KV_BYTES;  // [2 buffers][NDS planes]
-    static constexpr uint32_t OFF_BAR = OFF_DS + 2 * NDS * DS_BYTES;
-    // qd_full, qd_empty, kv_full[NST], kv_empty[NST], s_full[2], s_empty[2], ds_full[2], ds_empty[2],
-    // dq_full, dq_empty, drain
-    static constexpr int NBAR = 2 + 2 * NST + 8 + 3;
+    static constexpr uint32_t OFF_Q = 0;  // [2 slots][Q | dO]
+    static constexpr uint32_t OFF_K = OFF_Q + 4 * Q_BYTES;
+    static constexpr uint32_t OFF_V = OFF_K + NSK * KV_BYTES;
+    static constexpr uint32_t OFF_BAR = OFF_V + NSV * KV_BYTES;
+    // qd_full[2], qd_empty[2], k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV],
+    // s_full[2], ds_full[2], dq_full[2], dq_empty[2], drain
+    static constexpr int NBAR = 4 + 2 * NSK + 2 * NSV + 8 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
-    static constexpr uint32_t OFF_BEXT = OFF_BIAS + kMaxBiasFloats * 4;
-    static constexpr uint32_t SMEM = OFF_BEXT + (ACT ? 0 : kMaxBiasExtFloats * 4);
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
+    static constexpr uint32_t SMEM = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0;     // S[2]:  0, 64
-    static constexpr uint32_t COL_DP = 128;  // dP[2]: 128, 192
-    static constexpr uint32_t COL_DQ = 256;  // dQ: D columns
+    // group g: S at 128 g, dP at 128 g + 64 (dS over S); dQ[b] at 256 + b D
+    static constexpr uint32_t COL_DQ = 256;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "operand alignment");
+    static_assert(COL_DQ + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D, bool ACT>
-__global__ void __launch_bounds__(192, 1)
+template <int D, bool ACT, int BIAS>
+__global__ void __launch_bounds__(512, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
-    using C = DqCfg<D, ACT>;
+    using C = DqCfg<D, ACT, BIAS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -71,43 +113,42 @@ __global__ void __launch_bounds__(192, 1)
     const int lane = threadIdx.x & 31;
 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *qd_full = bars + 0;
-    uint64_t *qd_empty = bars + 1;
-    uint64_t *kv_full = bars + 2;
-    uint64_t *kv_empty = kv_full + C::NST;
-    uint64_t *s_full = kv_empty + C::NST;
-    uint64_t *s_empty = s_full + 2;
-    uint64_t *ds_full = s_empty + 2;
-    uint64_t *ds_empty = ds_full + 2;
-    uint64_t *dq_full = ds_empty + 2;
-    uint64_t *dq_empty = dq_full + 1;
-    uint64_t *drain = dq_empty + 1;
+    uint64_t *qd_full = bars + 0;   // [2]
+    uint64_t *qd_empty = bars + 2;  // [2]
+    uint64_t *k_full = bars + 4;
+    uint64_t *k_empty = k_full + C::NSK;
+    uint64_t *v_full = k_empty + C::NSK;
+    uint64_t *v_empty = v_full + C::NSV;
+    uint64_t *s_full = v_empty + C::NSV;  // [2] per compute group
+    uint64_t *ds_full = s_full + 2;       // [2] per compute group
+    uint64_t *dq_full = ds_full + 2;      // [2] per dQ buffer
+    uint64_t *dq_empty = dq_full + 2;     // [2] per dQ buffer
+    uint64_t *drain = dq_empty + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
     float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
-    const bool use_ext = !ACT && g.nb > 0 && g.H * ext_len(g.nb) <= kMaxBiasExtFloats;
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-    const uint32_t sDO = smem_u32(smem + C::OFF_DO);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
-    const uint32_t sDS = smem_u32(smem + C::OFF_DS);
 
     if (threadIdx.x == 0) {
-        mbar_init(qd_full, 1);
-        mbar_init(qd_empty, 1);
-        for (int s = 0; s < C::NST; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&qd_full[s], 1);
+            mbar_init(&qd_empty[s], 1);
+            mbar_init(&s_full[s], 1);
+            mbar_init(&ds_full[s], 4);
+            mbar_init(&dq_full[s], 1);
+            mbar_init(&dq_empty[s], 4);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&s_empty[b], 4);
-            mbar_init(&ds_full[b], 4);
-            mbar_init(&ds_empty[b], 1);
+        for (int s = 0; s < C::NSK; ++s) {
+            mbar_init(&k_full[s], 1);
+            mbar_init(&k_empty[s], 1);
         }
-        mbar_init(dq_full, 1);
-        mbar_init(dq_empty, 4);
+        for (int s = 0; s < C::NSV; ++s) {
+            mbar_init(&v_full[s], 1);
+            mbar_init(&v_empty[s], 1);
+        }
         mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -116,8 +157,8 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
-    if (use_ext) stage_bias_ext(g, sext, kLog2e);
+    if (BIAS == kBiasTable) stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (BIAS == kBiasExt) stage_bias_ext(g, sext, ACT ? 1.0f : kLog2e);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -132,121 +173,201 @@ __global__ void __launch_bounds__(192, 1)
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
-    if (warp == 0) {
-        if (lane == 0) {
-            uint32_t kv_it = 0, t_local = 0;
+    const int wgi = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 7, 0);
+    if (wgi == 0) {
+        regs_release<kRegCtrl>();
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------------- K / V producer
+            uint32_t k_it = 0, v_it = 0;
             bool ok = true;
             TileStream ts(g, tbeg, tend);
             Tile t;
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, true)) continue;
-                if (!(ok = mbar_wait(qd_empty, (t_local & 1) ^ 1, err))) break;
-                ++t_local;
-                mbar_arrive_expect_tx(qd_full, 2 * C::Q_BYTES);
-                for (int kb = 0; kb < C::NKB; ++kb) {
-                    tma_load_2d(smem + C::OFF_Q + kb * C::SUB_Q, &tmQ, qd_full, t.h * D + kb * 64, t.q_start);
-                    tma_load_2d(smem + C::OFF_DO + kb * C::SUB_Q, &tmDO, qd_full, t.h * D + kb * 64, t.q_start);
-                }
                 const int nkv = cdiv(t.kv_len, C::BN);
-                for (int j = 0; j < nkv; ++j, ++kv_it) {
-                    const uint32_t slot = kv_it % C::NST, use = kv_it / C::NST;
-                    if (!(ok = mbar_wait(&kv_empty[slot], (use & 1) ^ 1, err))) break;
-                    mbar_arrive_expect_tx(&kv_full[slot], 2 * C::KV_BYTES);
+                for (int j = 0; j < nkv; ++j) {
                     const int y = t.kv_start + j * C::BN;
-                    for (int kb = 0; kb < C::NKB; ++kb) {
-                        tma_load_2d(smem + C::OFF_K + slot * C::KV_BYTES + kb * C::SUB_KV, &tmK, &kv_full[slot],
+                    const uint32_t ks = k_it % C::NSK, ku = k_it / C::NSK;
+                    if (!(ok = mbar_wait(&k_empty[ks], (ku & 1) ^ 1, err))) break;
+                    mbar_arrive_expect_tx(&k_full[ks], C::KV_BYTES);
+                    for (int kb = 0; kb < C::NKB; ++kb)
+                        tma_load_2d(smem + C::OFF_K + ks * C::KV_BYTES + kb * C::SUB_KV, &tmK, &k_full[ks],
                                     t.h * D + kb * 64, y);
-                        tma_load_2d(smem + C::OFF_V + slot * C::KV_BYTES + kb * C::SUB_KV, &tmV, &kv_full[slot],
+                    ++k_it;
+                    const uint32_t vs = v_it % C::NSV, vu = v_it / C::NSV;
+                    if (!(ok = mbar_wait(&v_empty[vs], (vu & 1) ^ 1, err))) break;
+                    mbar_arrive_expect_tx(&v_full[vs], C::KV_BYTES);
+                    for (int kb = 0; kb < C::NKB; ++kb)
+                        tma_load_2d(smem + C::OFF_V + vs * C::KV_BYTES + kb * C::SUB_KV, &tmV, &v_full[vs],
                                     t.h * D + kb * 64, y);
-                    }
+                    ++v_it;
                 }
             }
             if (!ok) {
-                if (t_local > 0) mbar_drain(qd_full, (t_local - 1) & 1);
-                for (uint32_t s = 0; s < C::NST && s < kv_it; ++s) {
-                    const uint32_t last = kv_it - 1 - ((kv_it - 1 - s) % C::NST);
-                    mbar_drain(&kv_full[last % C::NST], (last / C::NST) & 1);
+                for (uint32_t s = 0; s < C::NSK && s < k_it; ++s) {
+                    const uint32_t last = k_it - 1 - ((k_it - 1 - s) % C::NSK);
+                    mbar_drain(&k_full[last % C::NSK], (last / C::NSK) & 1);
+                }
+                for (uint32_t s = 0; s < C::NSV && s < v_it; ++s) {
+                    const uint32_t last = v_it - 1 - ((v_it - 1 - s) % C::NSV);
+                    mbar_drain(&v_full[last % C::NSV], (last / C::NSV) & 1);
                 }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            uint32_t kv_it = 0, s_it = 0, ds_it = 0, t_local = 0;
-            const uint32_t idesc_dq = idesc_bf16(128, D, false, true);
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------------------- Q / dO producer
+            uint32_t t_local = 0;
             bool ok = true;
             TileStream ts(g, tbeg, tend);
             Tile t;
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, false)) continue;
-                const int nkv = cdiv(t.kv_len, C::BN);
-                if (!(ok = mbar_wait(qd_full, t_local & 1, err))) break;
-                if (!(ok = mbar_wait(dq_empty, (t_local & 1) ^ 1, err))) break;
-                tc_fence_after();
-
-                auto issue_sdp = [&](int j) -> bool {
-                    const uint32_t it = kv_it + j, slot = it % C::NST, use = it / C::NST;
-                    if (!mbar_wait(&kv_full[slot], use & 1, err)) return false;
-                    const uint32_t sb = s_it & 1, suse = s_it >> 1;
-                    if (!mbar_wait(&s_empty[sb], (suse & 1) ^ 1, err)) return false;
-                    tc_fence_after();
-                    const int ncols = round_up16(min(C::BN, t.kv_len - j * C::BN));
-                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
-                    const uint32_t kb = sK + slot * C::KV_BYTES, vb = sV + slot * C::KV_BYTES;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t ao = (ks >> 2) * C::SUB_Q + (ks & 3) * 32;
-                        const uint32_t bo = (ks >> 2) * C::SUB_KV + (ks & 3) * 32;
-                        mma_bf16_ss(tmem + C::COL_S + sb * C::BN, sdesc_sw128(sQ + ao, 16, 1024),
-                                    sdesc_sw128(kb + bo, 16, 1024), idesc, ks > 0);
-                        mma_bf16_ss(tmem + C::COL_DP + sb * C::BN, sdesc_sw128(sDO + ao, 16, 1024),
-                                    sdesc_sw128(vb + bo, 16, 1024), idesc, ks > 0);
-                    }
-                    mma_commit(&s_full[sb]);
-                    ++s_it;
-                    return true;
-                };
-
-                if (nkv > 0) ok = issue_sdp(0);
-                for (int j = 0; ok && j < nkv; ++j) {
-                    if (j + 1 < nkv) {
-                        if (!(ok = issue_sdp(j + 1))) break;
-                    } else {
-                        mma_commit(qd_empty);
-                    }
-                    const uint32_t db = ds_it & 1, duse = ds_it >> 1;
-                    if (!(ok = mbar_wait(&ds_full[db], duse & 1, err))) break;
-                    tc_fence_after();
-                    const uint32_t slot = (kv_it + j) % C::NST;
-                    const int ksteps = round_up16(min(C::BN, t.kv_len - j * C::BN)) / 16;
-                    const uint32_t kb = sK + slot * C::KV_BYTES;
-                    const uint32_t dsb = sDS + db * C::NDS * C::DS_BYTES;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint64_t bd = sdesc_sw128(kb + ks * 2048, C::SUB_KV, 1024);
-                        mma_bf16_ss(tmem + C::COL_DQ, sdesc_sw128(dsb + ks * 32, 16, 1024), bd, idesc_dq,
-                                    (j > 0 || ks > 0) ? 1u : 0u);
-                        if (ACT)
-                            mma_bf16_ss(tmem + C::COL_DQ, sdesc_sw128(dsb + C::DS_BYTES + ks * 32, 16, 1024), bd,
-                                        idesc_dq, 1u);
-                    }
-                    mma_commit(&kv_empty[slot]);
-                    mma_commit(&ds_empty[db]);
-                    ++ds_it;
+                const uint32_t s = t_local & 1, use = t_local >> 1;
+                if (!(ok = mbar_wait(&qd_empty[s], (use & 1) ^ 1, err))) break;
+                mbar_arrive_expect_tx(&qd_full[s], 2 * C::Q_BYTES);
+                uint8_t *base = smem + C::OFF_Q + s * 2 * C::Q_BYTES;
+                for (int kb = 0; kb < C::NKB; ++kb) {
+                    tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qd_full[s], t.h * D + kb * 64, t.q_start);
+                    tma_load_2d(base + C::Q_BYTES + kb * C::SUB_Q, &tmDO, &qd_full[s], t.h * D + kb * 64, t.q_start);
                 }
-                if (!ok) break;
-                if (nkv == 0) mma_commit(qd_empty);
-                mma_commit(dq_full);
-                kv_it += nkv;
                 ++t_local;
+            }
+            if (!ok) {
+                for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
+                    mbar_drain(&qd_full[i & 1], (i >> 1) & 1);
+            }
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            // S / dP run two blocks ahead of dQ, across tile boundaries.
+            const uint32_t idesc_dq = idesc_bf16(128, D, false, true);
+            bool ok = true;
+            uint32_t d_cnt[2] = {0, 0};  // dS blocks consumed per compute group
+
+            TileStream tsa(g, tbeg, tend);
+            Tile ta;
+            int ja = 0, na = 0;
+            uint32_t ta_n = 0, ns = 0;
+            // next tile with keys; a tile without keys only hands back its Q / dO slot
+            auto a_next = [&]() -> bool {
+                while (tsa.next(ta)) {
+                    if (!check_tile(g, ta, err, false)) continue;
+                    na = cdiv(ta.kv_len, C::BN);
+                    ja = 0;
+                    if (na > 0) return true;
+                    if (!(ok = mbar_wait(&qd_full[ta_n & 1], (ta_n >> 1) & 1, err))) return false;
+                    mma_commit(&qd_empty[ta_n & 1]);
+                    ++ta_n;
+                }
+                return false;
+            };
+            bool a_has = a_next();
+            // S_ns = Q K^T and dP_ns = dO V^T into the columns of group ns & 1
+            auto issue_SdP = [&]() {
+                const uint32_t qs = ta_n & 1;
+                if (ja == 0 && !(ok = mbar_wait(&qd_full[qs], (ta_n >> 1) & 1, err))) return;
+                const uint32_t ks = ns % C::NSK, vs = ns % C::NSV;
+                if (!(ok = mbar_wait(&k_full[ks], (ns / C::NSK) & 1, err))) return;
+                if (!(ok = mbar_wait(&v_full[vs], (ns / C::NSV) & 1, err))) return;
+                tc_fence_after();
+                const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
+                const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                const uint32_t qb = sQ + qs * 2 * C::Q_BYTES;
+                const uint64_t dq0 = sdesc_sw128(qb, 16, 1024), ddo0 = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
+                const uint64_t dk0 = sdesc_sw128(sK + ks * C::KV_BYTES, 16, 1024);
+                const uint64_t dv0 = sdesc_sw128(sV + vs * C::KV_BYTES, 16, 1024);
+                const uint32_t dS = tmem + (ns & 1) * 128, dDP = dS + 64;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ao = (k >> 2) * C::SUB_Q + (k & 3) * 32;
+                    const uint32_t bo = (k >> 2) * C::SUB_KV + (k & 3) * 32;
+                    mma_bf16_ss(dS, sdesc_add(dq0, ao), sdesc_add(dk0, bo), idesc, k > 0);
+                    mma_bf16_ss(dDP, sdesc_add(ddo0, ao), sdesc_add(dv0, bo), idesc, k > 0);
+                }
+                mma_commit(&s_full[ns & 1]);
+                mma_commit(&v_empty[vs]);
+                ++ns;
+                if (++ja == na) {
+                    mma_commit(&qd_empty[qs]);  // the last reads of this Q / dO slot are in flight
+                    ++ta_n;
+                    a_has = a_next();
+                }
+            };
+
+            TileStream tsb(g, tbeg, tend);
+            Tile tb;
+            int jb = 0, nbk = 0;
+            uint32_t tb_n = 0, np = 0;
+            // dQ buffer tb_n & 1 must have been read out for tile tb_n - 2
+            auto wait_out = [&]() -> bool {
+                return mbar_wait(&dq_empty[tb_n & 1], ((tb_n >> 1) & 1) ^ 1, err);
+            };
+            // next tile with keys; a tile without keys is handed to the output group in order
+            auto b_next = [&]() -> bool {
+                while (tsb.next(tb)) {
+                    if (!check_tile(g, tb, err, false)) continue;
+                    nbk = cdiv(tb.kv_len, C::BN);
+                    jb = 0;
+                    if (nbk > 0) return true;
+                    if (!(ok = wait_out())) return false;
+                    mma_commit(&dq_full[tb_n & 1]);
+                    ++tb_n;
+                }
+                return false;
+            };
+            bool b_has = b_next();
+            // dQ += dS_np K_np, dS (bf16; activation: hi and lo parts) read from TMEM
+            auto issue_dQ = [&]() {
+                const int grp = np & 1;
+                if (!(ok = mbar_wait(&ds_full[grp], d_cnt[grp] & 1, err))) return;
+                ++d_cnt[grp];
+                if (jb == 0 && !(ok = wait_out())) return;
+                tc_fence_after();
+                const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
+                const uint32_t ks = np % C::NSK;
+                const uint64_t bd0 = sdesc_sw128(sK + ks * C::KV_BYTES, C::SUB_KV, 1024);
+                const uint32_t dq = tmem + C::COL_DQ + (tb_n & 1) * D;
+                const uint32_t aS = tmem + grp * 128;
+                for (int k = 0; k < ksteps; ++k) {
+                    const uint64_t bd = sdesc_add(bd0, k * 2048);
+                    const uint32_t acc = (jb > 0 || k > 0) ? 1u : 0u;
+                    if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                        mma_bf16_ts(dq, aS + k * 16, bd, idesc_dq, acc);
+                        mma_bf16_ts(dq, aS + k * 16 + 8, bd, idesc_dq, 1u);
+                    } else {
+                        mma_bf16_ts(dq, aS + k * 8, bd, idesc_dq, acc);
+                    }
+                }
+                mma_commit(&k_empty[ks]);
+                ++np;
+                if (++jb == nbk) {
+                    mma_commit(&dq_full[tb_n & 1]);
+                    ++tb_n;
+                    b_has = b_next();
+                }
+            };
+
+            if (ok && a_has) issue_SdP();
+            if (ok && a_has) issue_SdP();
+            while (ok && b_has) {
+                issue_dQ();
+                // SdP_{np+1} overwrites block np-1's dS: issued after its dQ, executed after it
+                if (ok && a_has) issue_SdP();
             }
             mma_commit(drain);
             mbar_drain(drain, 0);
         }
-    } else {
+    } else if (wgi < 3) {
+        regs_claim<kRegCompute>();
+        // ------------------------------------------------------------ compute groups
+        // One thread per query row (TMEM lane): dS of the group's key blocks,
+        // 32 keys at a time, written as bf16 over the block's S columns
+        // (chunk c: columns 16c..16c+15, or 32c..32c+31 as hi / lo pairs).
+        const int grp = wgi - 1;
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + grp * 128, tDP = tS + 64;
         const float sc = ACT ? g.scale : g.scale * kLog2e;
-        uint32_t s_it = 0, ds_it = 0, t_local = 0;
+        uint32_t s_it = 0, n0 = 0;
         bool ok = true;
         TileStream ts(g, tbeg, tend);
         Tile t;
@@ -256,134 +377,119 @@ __global__ void __launch_bounds__(192, 1)
             const float *bt = sbias + t.h * g.nb;
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int q_loc = t.q_loc0 + row;
-            const int kv_loc0 = t.kv_loc0;
             const bool row_ok = row < t.q_len;
-            const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
-            float lse2 = 0.0f, dlt = 0.0f;
-            if (!ACT && row_ok) {
-                lse2 = a.lse[static_cast<int64_t>(t.h) * g.Tq + qrow] * kLog2e;
-                dlt = a.delta[static_cast<int64_t>(t.h) * g.Tq + qrow];
+            const bool warp_live = quad * 32 < t.q_len;  // else its rows reach nothing that is stored
+            const int j0 = (grp - static_cast<int>(n0 & 1)) & 1;
+            float lse2 = 0.0f, dlt = 0.0f;  // log2 units / Delta of this row
+            if (!ACT && row_ok && j0 < nkv) {
+                const int64_t idx = static_cast<int64_t>(t.h) * g.Tq + t.q_start + row;
+                lse2 = a.lse[idx] * kLog2e;
+                dlt = a.delta[idx];
             }
-            for (int j = 0; j < nkv; ++j) {
-                const uint32_t sb = s_it & 1, suse = s_it >> 1;
-                if (!(ok = mbar_wait_warp(&s_full[sb], suse & 1, err))) break;
-                tc_fence_after();
-                const int nvalid = min(C::BN, t.kv_len - j * C::BN);
-                const int ncols = round_up16(nvalid);
-                float s[C::BN], dp[C::BN];
-                bool live[2];
+            auto blocks = [&](auto af) {
+                constexpr int AF = decltype(af)::value;
+                for (int j = j0; j < nkv; j += 2) {
+                    if (!(ok = mbar_wait_warp(&s_full[grp], s_it & 1, err))) return;
+                    ++s_it;
+                    if (warp_live) {
+                        tc_fence_after();
+                        const int nvalid = min(C::BN, t.kv_len - j * C::BN);
+                        const int kvb = t.kv_loc0 + j * C::BN;
+#pragma unroll 1
+                        for (int c = 0; c < 2 && c * 32 < nvalid; ++c) {
+                            float x[32], dp[32];
+                            tmem_ld32x2(tS + 32 * c, tDP + 32 * c, x, dp);
+                            // x = scale * s + bias (softmax: minus lse, log2 units)
+                            scale_bias_off32<BIAS>(x, sc, ACT ? 0.0f : -lse2, ext_h, bt, g.nb, q_loc, kvb + c * 32);
+                            if constexpr (ACT) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) live[c] = c * 32 < nvalid;
-                tmem_ld64x2(tmem + lane_base + C::COL_S + sb * C::BN, tmem + lane_base + C::COL_DP + sb * C::BN, s,
-                            dp);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&s_empty[sb]);
-                ++s_it;
-
-                const int kvb = kv_loc0 + j * C::BN;
+                                for (int i = 0; i < 32; ++i) {
+                                    float av;
+                                    x[i] = act_bwd_t<AF>(x[i], av) * dp[i];
+                                }
+                            } else {
+                                const float nd = -dlt;
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (!live[c]) continue;
-                    float(&xs)[32] = sub32(s, c);
-                    float(&dpc)[32] = sub32(dp, c);
-                    // x = scale * s + bias (softmax: minus lse, in log2 units)
-                    const float off = ACT ? 0.0f : -lse2;
-                    float bv[32], cst = 0.0f;
-                    bool band = false;
-                    if (g.nb > 0) {
-                        if (use_ext) {
-                            band = bias32_ext(ext_h, g.nb, q_loc, kvb + c * 32, bv, cst);
-                        } else {
-                            bias32(bt, g.nb, q_loc, kvb + c * 32, bv);
-                            band = true;
+                                for (int i = 0; i < 32; ++i) x[i] = ex2_approx(x[i]);
+#pragma unroll
+                                for (int i = 0; i < 32; i += 2) {
+                                    add2(dp[i], dp[i + 1], nd, nd);
+                                    mul2(x[i], x[i + 1], dp[i], dp[i + 1]);
+                                }
+                            }
+                            if (c * 32 + 32 > nvalid) {
+#pragma unroll
+                                for (int i = 0; i < 32; ++i)
+                                    if (c * 32 + i >= nvalid) x[i] = 0.0f;
+                            }
+                            if constexpr (ACT) {
+                                uint32_t w[32];
+                                pack_hilo32(x, w);
+                                tmem_st32_u32(tS + 32 * c, w);
+                            } else {
+                                uint32_t w[16];
+                                pack16(x, w);
+                                tmem_st16_u32(tS + 16 * c, w);
+                            }
                         }
+                        tmem_wait_st();
+                        tc_fence_before();
                     }
-                    if (band) {
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            add2(bv[i], bv[i + 1], off, off);
-                            fma2(xs[i], xs[i + 1], sc, sc, bv[i], bv[i + 1]);
-                        }
-                    } else {
-                        const float o2 = cst + off;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) fma2(xs[i], xs[i + 1], sc, sc, o2, o2);
-                    }
-                    if (ACT) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            float av;
-                            xs[i] = act_bwd(g.act, xs[i], av) * dpc[i];
-                        }
-                    } else {
-                        const float nd = -dlt;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) xs[i] = ex2_approx(xs[i]);
-#pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            add2(dpc[i], dpc[i + 1], nd, nd);
-                            mul2(xs[i], xs[i + 1], dpc[i], dpc[i + 1]);
-                        }
-                    }
-                    if (c * 32 + 32 > nvalid) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (c * 32 + i >= nvalid) xs[i] = 0.0f;
-                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ds_full[grp]);
                 }
-                const uint32_t db = ds_it & 1, duse = ds_it >> 1;
-                if (!(ok = mbar_wait_warp(&ds_empty[db], (duse & 1) ^ 1, err))) break;
-                const uint32_t dsb = sDS + db * C::NDS * C::DS_BYTES;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (c * 32 >= ncols) continue;
-                    if (!live[c]) {
-                        st_row32_zero(dsb, C::DS_BYTES, row, c * 32);
-                        if (ACT) st_row32_zero(dsb + C::DS_BYTES, C::DS_BYTES, row, c * 32);
-                    } else if (ACT) {
-                        st_row32_bf16_hilo(dsb, dsb + C::DS_BYTES, C::DS_BYTES, row, c * 32, sub32(s, c));
-                    } else {
-                        st_row32_bf16(dsb, C::DS_BYTES, row, c * 32, sub32(s, c));
-                    }
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ds_full[db]);
-                ++ds_it;
+            };
+            if (!ACT || g.act == kSilu) {
+                blocks(std::integral_constant<int, kSilu>{});
+            } else {
+                blocks(std::integral_constant<int, kGeluTanh>{});
             }
             if (!ok) break;
-            if (!(ok = mbar_wait_warp(dq_full, t_local & 1, err))) break;
-            tc_fence_after();
-            const bool fast = rows_fast<D>(a.dq);
-            float oa[D];
-            if (nkv > 0) {
-                tmem_ld_row<D>(tmem + lane_base + C::COL_DQ, oa);
-            } else {
-#pragma unroll
-                for (int i = 0; i < D; ++i) oa[i] = 0.0f;
-            }
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float(&o)[32] = sub32(oa, c);
-                if (fast) {
-                    // stage in this warp's rows of the two dS buffers (every dQ MMA is done)
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], g.scale, g.scale);
-                    st_row32_bf16(sDS, C::NDS * C::DS_BYTES, row, c * 32, o);
-                } else if (row_ok) {
-                    store_out32(a.dq, qrow, t.h, c * 32, o, g.scale);
-                }
-            }
-            if (fast) {
-                __syncwarp();
-                copy_rows_out<D>(sDS, C::NDS * C::DS_BYTES, quad * 32, t.q_len, a.dq, t.q_start, t.h, lane);
-                __syncwarp();
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dq_empty);
+            n0 += nkv;
+        }
+    } else {
+        regs_release<kRegOut>();
+        // ------------------------------------------------------------ output
+        // One thread per query row: dQ (TMEM, fp32) times the score scale ->
+        // the row of dq (each thread stores whole 64-byte pieces of its row).
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t t_local = 0;
+        bool ok = true;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
+            const int nkv = cdiv(t.kv_len, C::BN);
+            const uint32_t b = t_local & 1;
+            if (!(ok = mbar_wait_warp(&dq_full[b], (t_local >> 1) & 1, err))) break;
             ++t_local;
+            if (quad * 32 >= t.q_len) {  // no row of this warp is stored
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&dq_empty[b]);
+                continue;
+            }
+            tc_fence_after();
+            const bool row_ok = row < t.q_len;
+            const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
+            const uint32_t tq = tmem + lane_base + C::COL_DQ + b * D;
+#pragma unroll 1
+            for (int col = 0; col < D; col += 32) {
+                float o[32];
+                if (nkv > 0) {
+                    tmem_ld32(tq + col, o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+                }
+                if (col + 32 >= D) {  // every TMEM read of this tile is done
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&dq_empty[b]);
+                }
+                if (row_ok) store_out32(a.dq, qrow, t.h, col, o, g.scale);
+            }
         }
     }
 
@@ -398,46 +504,41 @@ __global__ void __launch_bounds__(192, 1)
 // ============================================================================
 // pass 2: dK, dV
 // ============================================================================
-template <int D, bool ACT>
+template <int D, bool ACT, int BIAS>
 struct DkvCfg {
     static constexpr int BKV = 128, BQ = 64;
     static constexpr int NKB = D / 64;
-    static constexpr int NST = (ACT && D == 128) ? 2 : 3;
+    static constexpr int NSQ = (D == 64) ? 5 : 3;   // Q / dO / lse / Delta ring
     static constexpr uint32_t SUB_KV = BKV * 128;  // 16 KB
     static constexpr uint32_t SUB_Q = BQ * 128;    // 8 KB
     static constexpr uint32_t KV_BYTES = BKV * D * 2;
     static constexpr uint32_t Q_BYTES = BQ * D * 2;
-    static constexpr uint32_t PT_BYTES = BKV * BQ * 2;  // 16 KB
-    static constexpr int NPL = ACT ? 2 : 1;
     static constexpr uint32_t OFF_K = 0;
     static constexpr uint32_t OFF_V = KV_BYTES;
-    static constexpr uint32_t OFF_Q = 2 * KV_BYTES;
-    static constexpr uint32_t OFF_DO = OFF_Q + NST * Q_BYTES;
-    static constexpr uint32_t OFF_PT = OFF_DO + NST * Q_BYTES;    // P^T planes
-    static constexpr uint32_t OFF_DST = OFF_PT + NPL * PT_BYTES;  // dS^T planes
-    static constexpr uint32_t OFF_LD = OFF_DST + NPL * PT_BYTES;  // [NST][lse | delta][64] floats
-    static constexpr uint32_t OFF_BAR = OFF_LD + NST * 2 * BQ * 4;
-    // kv_full, kv_empty, qs_full[NST], qs_empty[NST], st_full[2], st_empty[2], p_full, p_empty,
-    // acc_full, acc_empty, drain
-    static constexpr int NBAR = 2 + 2 * NST + 4 + 2 + 2 + 1;
+    static constexpr uint32_t OFF_Q = 2 * KV_BYTES;  // [NSQ][Q | dO]
+    static constexpr uint32_t OFF_LD = OFF_Q + NSQ * 2 * Q_BYTES;  // [NSQ][-lse log2 e | -Delta][64] floats
+    static constexpr uint32_t OFF_BAR = OFF_LD + NSQ * 2 * BQ * 4;
+    // kv_full, kv_empty, qs_full[NSQ], qs_empty[NSQ], st_full[2], p_full[2], acc_full, acc_empty, drain
+    static constexpr int NBAR = 2 + 2 * NSQ + 4 + 2 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
-    static constexpr uint32_t OFF_BEXT = OFF_BIAS + kMaxBiasFloats * 4;
-    static constexpr uint32_t SMEM = OFF_BEXT + (ACT ? 0 : kMaxBiasExtFloats * 4);
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
+    static constexpr uint32_t SMEM = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_ST = 0;
-    static constexpr uint32_t COL_DPT = 128;
+    // group g: S^T at 128 g (P^T over it), dP^T at 128 g + 64 (dS^T over it); dV, dK
     static constexpr uint32_t COL_DV = 256;
     static constexpr uint32_t COL_DK = 256 + D;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "operand alignment");
+    static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D, bool ACT>
-__global__ void __launch_bounds__(192, 1)
+template <int D, bool ACT, int BIAS>
+__global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
-    using C = DkvCfg<D, ACT>;
+    using C = DkvCfg<D, ACT, BIAS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -448,40 +549,32 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *kv_full = bars + 0;
     uint64_t *kv_empty = bars + 1;
     uint64_t *qs_full = bars + 2;
-    uint64_t *qs_empty = qs_full + C::NST;
-    uint64_t *st_full = qs_empty + C::NST;
-    uint64_t *st_empty = st_full + 2;
-    uint64_t *p_full = st_empty + 2;
-    uint64_t *p_empty = p_full + 1;
-    uint64_t *acc_full = p_empty + 1;
+    uint64_t *qs_empty = qs_full + C::NSQ;
+    uint64_t *st_full = qs_empty + C::NSQ;  // [2] per compute group
+    uint64_t *p_full = st_full + 2;         // [2] per compute group
+    uint64_t *acc_full = p_full + 2;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *drain = acc_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
     float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
-    const bool use_ext = !ACT && g.nb > 0 && g.H * ext_len(g.nb) <= kMaxBiasExtFloats;
     float *sLD = reinterpret_cast<float *>(smem + C::OFF_LD);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-    const uint32_t sDO = smem_u32(smem + C::OFF_DO);
-    const uint32_t sPT = smem_u32(smem + C::OFF_PT);
-    const uint32_t sDST = smem_u32(smem + C::OFF_DST);
 
     if (threadIdx.x == 0) {
         mbar_init(kv_full, 1);
         mbar_init(kv_empty, 1);
-        for (int s = 0; s < C::NST; ++s) {
+        for (int s = 0; s < C::NSQ; ++s) {
             mbar_init(&qs_full[s], 1);
             mbar_init(&qs_empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st_full[b], 1);
-            mbar_init(&st_empty[b], 4);
+            mbar_init(&p_full[b], 4);
         }
-        mbar_init(p_full, 4);
-        mbar_init(p_empty, 1);
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         mbar_init(drain, 1);
@@ -492,8 +585,8 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(tmem_slot, C::TMEM_COLS);
         tmem_relinquish();
     }
-    stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
-    if (use_ext) stage_bias_ext(g, sext, kLog2e);
+    if (BIAS == kBiasTable) stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (BIAS == kBiasExt) stage_bias_ext(g, sext, ACT ? 1.0f : kLog2e);
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -508,141 +601,207 @@ __global__ void __launch_bounds__(192, 1)
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
-    if (warp == 0) {
-        // producer warp: lane 0 issues TMA; all lanes copy lse / Delta of each
-        // query block into the stage's shared-memory slot before it is published.
-        uint32_t q_it = 0, t_local = 0;
-        bool ok = true;
-        TileStream ts(g, tbeg, tend);
-        Tile t;
-        while (ok && ts.next(t)) {
-            if (!check_tile(g, t, err, lane == 0)) continue;
-            if (!(ok = mbar_wait_warp(kv_empty, (t_local & 1) ^ 1, err))) break;
-            ++t_local;
-            if (lane == 0) {
+    const int wgi = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 7, 0);
+    if (wgi == 0) {
+        regs_release<kRegCtrl>();
+        if (warp == 0) {
+            // -------------------------------------------------------- Q / dO producer
+            // lane 0 issues the copies; all lanes first write lse / Delta of the
+            // block's queries (negated, lse in log2 units) into the stage's slot.
+            uint32_t q_it = 0;
+            bool ok = true;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, lane == 0)) continue;
+                const int nq = cdiv(t.q_len, C::BQ);
+                for (int i = 0; i < nq; ++i, ++q_it) {
+                    const uint32_t slot = q_it % C::NSQ, use = q_it / C::NSQ;
+                    if (!(ok = mbar_wait_warp(&qs_empty[slot], (use & 1) ^ 1, err))) break;
+                    if (!ACT) {
+                        float *ld = sLD + slot * 2 * C::BQ;
+                        for (int k = lane; k < C::BQ; k += 32) {
+                            const int qi = i * C::BQ + k;
+                            float l2 = 0.0f, dl = 0.0f;
+                            if (qi < t.q_len) {
+                                const int64_t idx = static_cast<int64_t>(t.h) * g.Tq + t.q_start + qi;
+                                l2 = -a.lse[idx] * kLog2e;
+                                dl = -a.delta[idx];
+                            }
+                            ld[k] = l2;
+                            ld[C::BQ + k] = dl;
+                        }
+                        __syncwarp();
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&qs_full[slot], 2 * C::Q_BYTES);
+                        const int y = t.q_start + i * C::BQ;
+                        uint8_t *base = smem + C::OFF_Q + slot * 2 * C::Q_BYTES;
+                        for (int kb = 0; kb < C::NKB; ++kb) {
+                            tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qs_full[slot], t.h * D + kb * 64, y);
+                            tma_load_2d(base + C::Q_BYTES + kb * C::SUB_Q, &tmDO, &qs_full[slot], t.h * D + kb * 64,
+                                        y);
+                        }
+                    }
+                }
+            }
+            if (!ok && lane == 0) {
+                for (uint32_t s = 0; s < C::NSQ && s < q_it; ++s) {
+                    const uint32_t last = q_it - 1 - ((q_it - 1 - s) % C::NSQ);
+                    mbar_drain(&qs_full[last % C::NSQ], (last / C::NSQ) & 1);
+                }
+            }
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------------------- K / V producer
+            // one buffer: the tile's K and V are last read by its final S^T / dP^T,
+            // two blocks before the tile ends, so the next tile's rows load early
+            uint32_t t_local = 0;
+            bool ok = true;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, false)) continue;
+                if (!(ok = mbar_wait(kv_empty, (t_local & 1) ^ 1, err))) break;
+                ++t_local;
                 mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
                 for (int kb = 0; kb < C::NKB; ++kb) {
                     tma_load_2d(smem + C::OFF_K + kb * C::SUB_KV, &tmK, kv_full, t.h * D + kb * 64, t.kv_start);
                     tma_load_2d(smem + C::OFF_V + kb * C::SUB_KV, &tmV, kv_full, t.h * D + kb * 64, t.kv_start);
                 }
             }
-            const int nq = cdiv(t.q_len, C::BQ);
-            for (int i = 0; i < nq; ++i, ++q_it) {
-                const uint32_t slot = q_it % C::NST, use = q_it / C::NST;
-                if (!(ok = mbar_wait_warp(&qs_empty[slot], (use & 1) ^ 1, err))) break;
-                if (!ACT) {
-                    float *ld = sLD + slot * 2 * C::BQ;
-                    for (int k = lane; k < C::BQ; k += 32) {
-                        const int qi = i * C::BQ + k;
-                        float l2 = 0.0f, dl = 0.0f;  // stored negated: the consumer adds them
-                        if (qi < t.q_len) {
-                            const int64_t idx = static_cast<int64_t>(t.h) * g.Tq + t.q_start + qi;
-                            l2 = -a.lse[idx] * kLog2e;
-                            dl = -a.delta[idx];
-                        }
-                        ld[k] = l2;
-                        ld[C::BQ + k] = dl;
-                    }
-                    __syncwarp();
-                }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(&qs_full[slot], 2 * C::Q_BYTES);
-                    const int y = t.q_start + i * C::BQ;
-                    for (int kb = 0; kb < C::NKB; ++kb) {
-                        tma_load_2d(smem + C::OFF_Q + slot * C::Q_BYTES + kb * C::SUB_Q, &tmQ, &qs_full[slot],
-                                    t.h * D + kb * 64, y);
-                        tma_load_2d(smem + C::OFF_DO + slot * C::Q_BYTES + kb * C::SUB_Q, &tmDO, &qs_full[slot],
-                                    t.h * D + kb * 64, y);
-                    }
-                }
-            }
-        }
-        if (!ok && lane == 0) {
-            if (t_local > 0) mbar_drain(kv_full, (t_local - 1) & 1);
-            for (uint32_t s = 0; s < C::NST && s < q_it; ++s) {
-                const uint32_t last = q_it - 1 - ((q_it - 1 - s) % C::NST);
-                mbar_drain(&qs_full[last % C::NST], (last / C::NST) & 1);
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            uint32_t q_it = 0, st_it = 0, p_it = 0, t_local = 0;
+            if (!ok && t_local > 0) mbar_drain(kv_full, (t_local - 1) & 1);
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- MMA issuer
+            // S^T / dP^T run two blocks ahead of dV / dK, across tile boundaries.
             const uint32_t idesc_acc = idesc_bf16(128, D, false, true);
             bool ok = true;
-            TileStream ts(g, tbeg, tend);
-            Tile t;
-            while (ok && ts.next(t)) {
-                if (!check_tile(g, t, err, false)) continue;
-                const int nq = cdiv(t.q_len, C::BQ);
-                if (!(ok = mbar_wait(kv_full, t_local & 1, err))) break;
-                if (!(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
-                tc_fence_after();
+            uint32_t p_cnt[2] = {0, 0};  // P^T / dS^T blocks consumed per compute group
 
-                auto issue_st = [&](int i) -> bool {
-                    const uint32_t it = q_it + i, slot = it % C::NST, use = it / C::NST;
-                    if (!mbar_wait(&qs_full[slot], use & 1, err)) return false;
-                    const uint32_t sb = st_it & 1, suse = st_it >> 1;
-                    if (!mbar_wait(&st_empty[sb], (suse & 1) ^ 1, err)) return false;
-                    tc_fence_after();
-                    const int ncols = round_up16(min(C::BQ, t.q_len - i * C::BQ));
-                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
-                    const uint32_t qb = sQ + slot * C::Q_BYTES, dob = sDO + slot * C::Q_BYTES;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t ao = (ks >> 2) * C::SUB_KV + (ks & 3) * 32;
-                        const uint32_t bo = (ks >> 2) * C::SUB_Q + (ks & 3) * 32;
-                        mma_bf16_ss(tmem + C::COL_ST + sb * C::BQ, sdesc_sw128(sK + ao, 16, 1024),
-                                    sdesc_sw128(qb + bo, 16, 1024), idesc, ks > 0);
-                        mma_bf16_ss(tmem + C::COL_DPT + sb * C::BQ, sdesc_sw128(sV + ao, 16, 1024),
-                                    sdesc_sw128(dob + bo, 16, 1024), idesc, ks > 0);
-                    }
-                    mma_commit(&st_full[sb]);
-                    ++st_it;
-                    return true;
-                };
-
-                if (nq > 0) ok = issue_st(0);
-                for (int i = 0; ok && i < nq; ++i) {
-                    if (i + 1 < nq) {
-                        if (!(ok = issue_st(i + 1))) break;
-                    }
-                    if (!(ok = mbar_wait(p_full, p_it & 1, err))) break;
-                    tc_fence_after();
-                    const uint32_t slot = (q_it + i) % C::NST;
-                    const int ksteps = round_up16(min(C::BQ, t.q_len - i * C::BQ)) / 16;
-                    const uint32_t qb = sQ + slot * C::Q_BYTES, dob = sDO + slot * C::Q_BYTES;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint32_t acc = (i > 0 || ks > 0) ? 1u : 0u;
-                        const uint64_t bdo = sdesc_sw128(dob + ks * 2048, C::SUB_Q, 1024);
-                        const uint64_t bq = sdesc_sw128(qb + ks * 2048, C::SUB_Q, 1024);
-                        mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sPT + ks * 32, 16, 1024), bdo, idesc_acc, acc);
-                        mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDST + ks * 32, 16, 1024), bq, idesc_acc, acc);
-                        if (ACT) {
-                            mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sPT + C::PT_BYTES + ks * 32, 16, 1024), bdo,
-                                        idesc_acc, 1u);
-                            mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDST + C::PT_BYTES + ks * 32, 16, 1024), bq,
-                                        idesc_acc, 1u);
-                        }
-                    }
-                    mma_commit(&qs_empty[slot]);
-                    mma_commit(p_empty);
-                    ++p_it;
+            TileStream tsa(g, tbeg, tend);
+            Tile ta;
+            int ia = 0, na = 0;
+            uint32_t ta_n = 0, ns = 0;
+            // next tile with queries; a tile without queries only hands back its K / V
+            auto a_next = [&]() -> bool {
+                while (tsa.next(ta)) {
+                    if (!check_tile(g, ta, err, false)) continue;
+                    na = cdiv(ta.q_len, C::BQ);
+                    ia = 0;
+                    if (na > 0) return true;
+                    if (!(ok = mbar_wait(kv_full, ta_n & 1, err))) return false;
+                    mma_commit(kv_empty);
+                    ++ta_n;
                 }
-                if (!ok) break;
-                mma_commit(kv_empty);
-                mma_commit(acc_full);
-                q_it += nq;
-                ++t_local;
+                return false;
+            };
+            bool a_has = a_next();
+            // S^T_ns = K Q^T and dP^T_ns = V dO^T into the columns of group ns & 1
+            auto issue_SdPT = [&]() {
+                if (ia == 0 && !(ok = mbar_wait(kv_full, ta_n & 1, err))) return;
+                const uint32_t slot = ns % C::NSQ;
+                if (!(ok = mbar_wait(&qs_full[slot], (ns / C::NSQ) & 1, err))) return;
+                tc_fence_after();
+                const int ncols = round_up16(min(C::BQ, ta.q_len - ia * C::BQ));
+                const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
+                const uint64_t dqq = sdesc_sw128(qb, 16, 1024), ddo = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
+                const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, 16, 1024);
+                const uint32_t dS = tmem + (ns & 1) * 128, dDP = dS + 64;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t ao = (k >> 2) * C::SUB_KV + (k & 3) * 32;
+                    const uint32_t bo = (k >> 2) * C::SUB_Q + (k & 3) * 32;
+                    mma_bf16_ss(dS, sdesc_add(dk0, ao), sdesc_add(dqq, bo), idesc, k > 0);
+                    mma_bf16_ss(dDP, sdesc_add(dv0, ao), sdesc_add(ddo, bo), idesc, k > 0);
+                }
+                mma_commit(&st_full[ns & 1]);
+                ++ns;
+                if (++ia == na) {
+                    mma_commit(kv_empty);  // the tile's last reads of K and V are in flight
+                    ++ta_n;
+                    a_has = a_next();
+                }
+            };
+
+            TileStream tsb(g, tbeg, tend);
+            Tile tb;
+            int ib = 0, nbq = 0;
+            uint32_t tb_n = 0, np = 0;
+            // dV / dK must have been read out for tile tb_n - 1
+            auto wait_out = [&]() -> bool {
+                return mbar_wait(acc_empty, (tb_n & 1) ^ 1, err);
+            };
+            auto b_next = [&]() -> bool {
+                while (tsb.next(tb)) {
+                    if (!check_tile(g, tb, err, false)) continue;
+                    nbq = cdiv(tb.q_len, C::BQ);
+                    ib = 0;
+                    if (nbq > 0) return true;
+                    if (!(ok = wait_out())) return false;
+                    mma_commit(acc_full);
+                    ++tb_n;
+                }
+                return false;
+            };
+            bool b_has = b_next();
+            // dV += P^T dO and dK += dS^T Q, P^T and dS^T (bf16; activation: hi and lo) from TMEM
+            auto issue_acc = [&]() {
+                const int grp = np & 1;
+                if (!(ok = mbar_wait(&p_full[grp], p_cnt[grp] & 1, err))) return;
+                ++p_cnt[grp];
+                if (ib == 0 && !(ok = wait_out())) return;
+                tc_fence_after();
+                const int ksteps = round_up16(min(C::BQ, tb.q_len - ib * C::BQ)) / 16;
+                const uint32_t slot = np % C::NSQ;
+                const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
+                const uint64_t bq0 = sdesc_sw128(qb, C::SUB_Q, 1024), bdo0 = sdesc_sw128(qb + C::Q_BYTES, C::SUB_Q, 1024);
+                const uint32_t aP = tmem + grp * 128, aDS = aP + 64;
+                for (int k = 0; k < ksteps; ++k) {
+                    const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
+                    const uint64_t bdo = sdesc_add(bdo0, k * 2048);
+                    const uint64_t bq = sdesc_add(bq0, k * 2048);
+                    if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                        mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
+                        mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
+                        mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
+                        mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
+                    } else {
+                        mma_bf16_ts(tmem + C::COL_DV, aP + k * 8, bdo, idesc_acc, acc);
+                        mma_bf16_ts(tmem + C::COL_DK, aDS + k * 8, bq, idesc_acc, acc);
+                    }
+                }
+                mma_commit(&qs_empty[slot]);
+                ++np;
+                if (++ib == nbq) {
+                    mma_commit(acc_full);
+                    ++tb_n;
+                    b_has = b_next();
+                }
+            };
+
+            if (ok && a_has) issue_SdPT();
+            if (ok && a_has) issue_SdPT();
+            while (ok && b_has) {
+                issue_acc();
+                // SdPT_{np+1} overwrites block np-1's operands: issued after its products
+                if (ok && a_has) issue_SdPT();
             }
             mma_commit(drain);
             mbar_drain(drain, 0);
         }
-    } else {
+    } else if (wgi < 3) {
+        regs_claim<kRegCompute>();
+        // ------------------------------------------------------------ compute groups
+        // One thread per key row (TMEM lane): P^T and dS^T of the group's query
+        // blocks, 32 queries at a time, written as bf16 over the block's S^T and
+        // dP^T columns (chunk c: columns 16c..16c+15, or 32c..32c+31 as hi / lo).
+        const int grp = wgi - 1;
         const int quad = warp & 3;
-        const int row = quad * 32 + lane;  // key row within the tile == TMEM lane
+        const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + grp * 128, tDP = tS + 64;
         const float sc = ACT ? g.scale : g.scale * kLog2e;
-        uint32_t q_it = 0, st_it = 0, p_it = 0, t_local = 0;
+        uint32_t s_it = 0, n0 = 0;
         bool ok = true;
         TileStream ts(g, tbeg, tend);
         Tile t;
@@ -652,150 +811,128 @@ __global__ void __launch_bounds__(192, 1)
             const float *bt = sbias + t.h * g.nb;
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int kv_loc = t.kv_loc0 + row;
-            const int q_loc0 = t.q_loc0;
-            for (int i = 0; i < nq; ++i, ++q_it) {
-                const uint32_t slot = q_it % C::NST;
-                const uint32_t sb = st_it & 1, suse = st_it >> 1;
-                if (!(ok = mbar_wait_warp(&st_full[sb], suse & 1, err))) break;
-                tc_fence_after();
-                const int nvalid = min(C::BQ, t.q_len - i * C::BQ);
-                const int ncols = round_up16(nvalid);
-                float st[C::BQ], dpt[C::BQ];
-                bool live[2];
+            const bool warp_live = quad * 32 < t.kv_len;
+            const int i0 = (grp - static_cast<int>(n0 & 1)) & 1;
+            auto blocks = [&](auto af) {
+                constexpr int AF = decltype(af)::value;
+                for (int i = i0; i < nq; i += 2) {
+                    if (!(ok = mbar_wait_warp(&st_full[grp], s_it & 1, err))) return;
+                    ++s_it;
+                    if (warp_live) {
+                        tc_fence_after();
+                        const int nvalid = min(C::BQ, t.q_len - i * C::BQ);
+                        const int qb = t.q_loc0 + i * C::BQ;
+                        // [-lse log2 e | -Delta] of the block's queries (shared by all rows)
+                        const float *ld = sLD + ((n0 + i) % C::NSQ) * 2 * C::BQ;
+#pragma unroll 1
+                        for (int c = 0; c < 2 && c * 32 < nvalid; ++c) {
+                            float x[32], dp[32];
+                            tmem_ld32x2(tS + 32 * c, tDP + 32 * c, x, dp);
+                            scale_bias_off32<BIAS>(x, sc, 0.0f, ext_h, bt, g.nb, kv_loc, qb + c * 32);
+                            if constexpr (ACT) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) live[c] = c * 32 < nvalid;
-                tmem_ld64x2(tmem + lane_base + C::COL_ST + sb * C::BQ, tmem + lane_base + C::COL_DPT + sb * C::BQ, st,
-                            dpt);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&st_empty[sb]);
-                ++st_it;
-
-                const float *ld = sLD + slot * 2 * C::BQ;  // [-lse * log2 e | -Delta] of the 64 queries
-                const int qb = q_loc0 + i * C::BQ;
+                                for (int k = 0; k < 32; ++k) {
+                                    float pv;
+                                    dp[k] = act_bwd_t<AF>(x[k], pv) * dp[k];
+                                    x[k] = pv;
+                                }
+                            } else {
+                                const float4 *l4 = reinterpret_cast<const float4 *>(ld + c * 32);
+                                const float4 *d4 = reinterpret_cast<const float4 *>(ld + C::BQ + c * 32);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (!live[c]) continue;
-                    float(&xs)[32] = sub32(st, c);
-                    float(&dpc)[32] = sub32(dpt, c);
-                    float bv[32], cst = 0.0f;
-                    bool band = false;
-                    if (g.nb > 0) {
-                        if (use_ext) {
-                            band = bias32_ext(ext_h, g.nb, kv_loc, qb + c * 32, bv, cst);
-                        } else {
-                            bias32(bt, g.nb, kv_loc, qb + c * 32, bv);
-                            band = true;
-                        }
-                    }
-                    if (band) {
+                                for (int k = 0; k < 8; ++k) {
+                                    const float4 lz = l4[k], dz = d4[k];
+                                    add2(x[4 * k], x[4 * k + 1], lz.x, lz.y);
+                                    add2(x[4 * k + 2], x[4 * k + 3], lz.z, lz.w);
+                                    add2(dp[4 * k], dp[4 * k + 1], dz.x, dz.y);
+                                    add2(dp[4 * k + 2], dp[4 * k + 3], dz.z, dz.w);
+                                }
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) fma2(xs[k], xs[k + 1], sc, sc, bv[k], bv[k + 1]);
-                    } else {
+                                for (int k = 0; k < 32; ++k) x[k] = ex2_approx(x[k]);
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) fma2(xs[k], xs[k + 1], sc, sc, cst, cst);
-                    }
-                    if (ACT) {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) {
-                            float pv;
-                            dpc[k] = act_bwd(g.act, xs[k], pv) * dpc[k];
-                            xs[k] = pv;
-                        }
-                    } else {
-                        const float4 *l4 = reinterpret_cast<const float4 *>(ld + c * 32);
-                        const float4 *d4 = reinterpret_cast<const float4 *>(ld + C::BQ + c * 32);
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const float4 lz = l4[k], dz = d4[k];
-                            add2(xs[4 * k], xs[4 * k + 1], lz.x, lz.y);
-                            add2(xs[4 * k + 2], xs[4 * k + 3], lz.z, lz.w);
-                            add2(dpc[4 * k], dpc[4 * k + 1], dz.x, dz.y);
-                            add2(dpc[4 * k + 2], dpc[4 * k + 3], dz.z, dz.w);
-                        }
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) xs[k] = ex2_approx(xs[k]);
-#pragma unroll
-                        for (int k = 0; k < 32; k += 2) mul2(dpc[k], dpc[k + 1], xs[k], xs[k + 1]);
-                    }
-                    if (c * 32 + 32 > nvalid) {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            if (c * 32 + k >= nvalid) {
-                                xs[k] = 0.0f;
-                                dpc[k] = 0.0f;
+                                for (int k = 0; k < 32; k += 2) mul2(dp[k], dp[k + 1], x[k], x[k + 1]);
                             }
-                    }
-                }
-                if (!(ok = mbar_wait_warp(p_empty, (p_it & 1) ^ 1, err))) break;
+                            if (c * 32 + 32 > nvalid) {
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    if (c * 32 >= ncols) continue;
-                    if (!live[c]) {
-                        for (int pl = 0; pl < C::NPL; ++pl) {
-                            st_row32_zero(sPT + pl * C::PT_BYTES, C::PT_BYTES, row, c * 32);
-                            st_row32_zero(sDST + pl * C::PT_BYTES, C::PT_BYTES, row, c * 32);
+                                for (int k = 0; k < 32; ++k)
+                                    if (c * 32 + k >= nvalid) {
+                                        x[k] = 0.0f;
+                                        dp[k] = 0.0f;
+                                    }
+                            }
+                            if constexpr (ACT) {
+                                uint32_t w[32];
+                                pack_hilo32(x, w);
+                                tmem_st32_u32(tS + 32 * c, w);
+                                pack_hilo32(dp, w);
+                                tmem_st32_u32(tDP + 32 * c, w);
+                            } else {
+                                uint32_t w[16];
+                                pack16(x, w);
+                                tmem_st16_u32(tS + 16 * c, w);
+                                pack16(dp, w);
+                                tmem_st16_u32(tDP + 16 * c, w);
+                            }
                         }
-                    } else if (ACT) {
-                        st_row32_bf16_hilo(sPT, sPT + C::PT_BYTES, C::PT_BYTES, row, c * 32, sub32(st, c));
-                        st_row32_bf16_hilo(sDST, sDST + C::PT_BYTES, C::PT_BYTES, row, c * 32, sub32(dpt, c));
-                    } else {
-                        st_row32_bf16(sPT, C::PT_BYTES, row, c * 32, sub32(st, c));
-                        st_row32_bf16(sDST, C::PT_BYTES, row, c * 32, sub32(dpt, c));
+                        tmem_wait_st();
+                        tc_fence_before();
                     }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[grp]);
                 }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(p_full);
-                ++p_it;
+            };
+            if (!ACT || g.act == kSilu) {
+                blocks(std::integral_constant<int, kSilu>{});
+            } else {
+                blocks(std::integral_constant<int, kGeluTanh>{});
             }
             if (!ok) break;
+            n0 += nq;
+        }
+    } else {
+        regs_release<kRegOut>();
+        // ------------------------------------------------------------ output
+        // One thread per key row: dV and dK (times the score scale) from TMEM ->
+        // the rows of dv and dk (whole 64-byte pieces per thread).
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        uint32_t t_local = 0;
+        bool ok = true;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
+            const int nq = cdiv(t.q_len, C::BQ);
             if (!(ok = mbar_wait_warp(acc_full, t_local & 1, err))) break;
+            ++t_local;
+            if (quad * 32 >= t.kv_len) {  // no row of this warp is stored
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                continue;
+            }
             tc_fence_after();
             const bool row_ok = row < t.kv_len;
             const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
-            if (rows_fast<D>(a.dv)) {
-                // stage dV, then dK, in this warp's rows of the P^T / dS^T planes (all MMAs are done)
-                for (int pass = 0; pass < 2; ++pass) {
-                    const float mul = pass == 0 ? 1.0f : g.scale;
-                    float oa[D];
-                    if (nq > 0) {
-                        tmem_ld_row<D>(tmem + lane_base + (pass == 0 ? C::COL_DV : C::COL_DK), oa);
-                    } else {
+#pragma unroll 1
+            for (int col = 0; col < D; col += 32) {
+                float ov[32], ok_[32];
+                if (nq > 0) {
+                    tmem_ld32x2(tmem + lane_base + C::COL_DV + col, tmem + lane_base + C::COL_DK + col, ov, ok_);
+                } else {
 #pragma unroll
-                        for (int k = 0; k < D; ++k) oa[k] = 0.0f;
-                    }
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        float(&o)[32] = sub32(oa, c);
-#pragma unroll
-                        for (int k = 0; k < 32; k += 2) mul2(o[k], o[k + 1], mul, mul);
-                        st_row32_bf16(sPT, C::PT_BYTES, row, c * 32, o);
-                    }
-                    __syncwarp();
-                    copy_rows_out<D>(sPT, C::PT_BYTES, quad * 32, t.kv_len, pass == 0 ? a.dv : a.dk, t.kv_start,
-                                     t.h, lane);
-                    __syncwarp();
+                    for (int i = 0; i < 32; ++i) ov[i] = ok_[i] = 0.0f;
                 }
-            } else {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    if (nq > 0) {
-                        tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = 0.0f;
-                    }
-                    if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
-                    if (nq > 0) tmem_ld32(tmem + lane_base + C::COL_DK + c * 32, o);
-                    if (row_ok) store_out32(a.dk, krow, t.h, c * 32, o, g.scale);
+                if (col + 32 >= D) {  // every TMEM read of this tile is done
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty);
+                }
+                if (row_ok) {
+                    store_out32(a.dv, krow, t.h, col, ov, 1.0f);
+                    store_out32(a.dk, krow, t.h, col, ok_, g.scale);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
-            ++t_local;
         }
     }
 
@@ -807,37 +944,62 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-
-template <int D, bool ACT>
+// ============================================================================
+// launchers
+// ============================================================================
+template <int D, bool ACT, int BIAS>
 static cudaError_t launch_dq_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
-    using C = DqCfg<D, ACT>;
+    using C = DqCfg<D, ACT, BIAS>;
     static bool done[64] = {};
-    cudaError_t e = ensure_smem(dq_kernel<D, ACT>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(dq_kernel<D, ACT, BIAS>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    dq_kernel<D, ACT><<<n_ctas, 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    dq_kernel<D, ACT, BIAS><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 
-template <int D, bool ACT>
+template <int D, bool ACT, int BIAS>
 static cudaError_t launch_dkdv_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
-    using C = DkvCfg<D, ACT>;
+    using C = DkvCfg<D, ACT, BIAS>;
     static bool done[64] = {};
-    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    dkdv_kernel<D, ACT><<<n_ctas, 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    dkdv_kernel<D, ACT, BIAS><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
+}
+
+static int bias_form(const Geom &g) {
+    if (g.nb <= 0) return kBiasNone;
+    return g.H * ext_len(g.nb) <= kMaxBiasExtFloats ? kBiasExt : kBiasTable;
+}
+
+template <int D, bool ACT>
+static cudaError_t launch_dq_b(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    switch (bias_form(a.g)) {
+    case kBiasNone: return launch_dq_t<D, ACT, kBiasNone>(tm, a, n_ctas, st);
+    case kBiasExt: return launch_dq_t<D, ACT, kBiasExt>(tm, a, n_ctas, st);
+    default: return launch_dq_t<D, ACT, kBiasTable>(tm, a, n_ctas, st);
+    }
+}
+
+template <int D, bool ACT>
+static cudaError_t launch_dkdv_b(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    switch (bias_form(a.g)) {
+    case kBiasNone: return launch_dkdv_t<D, ACT, kBiasNone>(tm, a, n_ctas, st);
+    case kBiasExt: return launch_dkdv_t<D, ACT, kBiasExt>(tm, a, n_ctas, st);
+    default: return launch_dkdv_t<D, ACT, kBiasTable>(tm, a, n_ctas, st);
+    }
 }
 
 cudaError_t launch_bwd_dq(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
-    if (D == 128) return act ? launch_dq_t<128, true>(tm, a, n_ctas, st) : launch_dq_t<128, false>(tm, a, n_ctas, st);
-    if (D == 64) return act ? launch_dq_t<64, true>(tm, a, n_ctas, st) : launch_dq_t<64, false>(tm, a, n_ctas, st);
+    if (D == 128) return act ? launch_dq_b<128, true>(tm, a, n_ctas, st) : launch_dq_b<128, false>(tm, a, n_ctas, st);
+    if (D == 64) return act ? launch_dq_b<64, true>(tm, a, n_ctas, st) : launch_dq_b<64, false>(tm, a, n_ctas, st);
     return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_dkdv(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     if (D == 128)
-        return act ? launch_dkdv_t<128, true>(tm, a, n_ctas, st) : launch_dkdv_t<128, false>(tm, a, n_ctas, st);
-    if (D == 64) return act ? launch_dkdv_t<64, true>(tm, a, n_ctas, st) : launch_dkdv_t<64, false>(tm, a, n_ctas, st);
+        return act ? launch_dkdv_b<128, true>(tm, a, n_ctas, st) : launch_dkdv_b<128, false>(tm, a, n_ctas, st);
+    if (D == 64) return act ? launch_dkdv_b<64, true>(tm, a, n_ctas, st) : launch_dkdv_b<64, false>(tm, a, n_ctas, st);
     return cudaErrorInvalidValue;
 }
 

@@ -282,15 +282,13 @@ __global__ void __launch_bounds__(512, 1)
                 tc_fence_after();
                 const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
                 const uint32_t idesc = idesc_bf16(128, ncols, false, false);
-                const uint32_t qbase = sQ + qs * C::Q_BYTES;
-                const uint32_t kbase = sK + slot * C::KV_BYTES;
+                const uint64_t ad0 = sdesc_sw128(sQ + qs * C::Q_BYTES, 16, 1024);
+                const uint64_t bd0 = sdesc_sw128(sK + slot * C::KV_BYTES, 16, 1024);
                 const uint32_t dS = tmem + C::COL_S + (ns & 1) * C::BN;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t ad = sdesc_sw128(qbase + (ks >> 2) * C::SUB_Q + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(kbase + (ks >> 2) * C::SUB_KV + (ks & 3) * 32, 16, 1024);
-                    mma_bf16_ss(dS, ad, bd, idesc, ks > 0);
-                }
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_bf16_ss(dS, sdesc_add(ad0, (ks >> 2) * C::SUB_Q + (ks & 3) * 32),
+                                sdesc_add(bd0, (ks >> 2) * C::SUB_KV + (ks & 3) * 32), idesc, ks > 0);
                 mma_commit(&s_full[ns & 1]);
                 mma_commit(&k_empty[slot]);
                 ++ns;
@@ -336,12 +334,12 @@ __global__ void __launch_bounds__(512, 1)
                 if (!(ok = mbar_wait(&v_full[slot], use & 1, err))) return;
                 tc_fence_after();
                 const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
-                const uint32_t vbase = sV + slot * C::KV_BYTES;
+                const uint64_t bd0 = sdesc_sw128(sV + slot * C::KV_BYTES, C::SUB_KV, 1024);
                 const uint32_t dO = tmem + C::COL_O + grp * D;
                 const uint32_t aP = tmem + C::COL_S + grp * C::BN;
                 // the first two blocks of a tile start their group's accumulator
                 for (int ks = 0; ks < ksteps; ++ks) {
-                    const uint64_t bd = sdesc_sw128(vbase + ks * 2048, C::SUB_KV, 1024);
+                    const uint64_t bd = sdesc_add(bd0, ks * 2048);
                     if (ACT) {  // hi at columns 16 ks .. +7, lo at 16 ks + 8 .. +15
                         mma_bf16_ts(dO, aP + ks * 16, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
                         mma_bf16_ts(dO, aP + ks * 16 + 8, bd, idesc_pv, 1u);
