@@ -6,9 +6,11 @@ timed region starts; L2 is flushed (a 256 MiB write) between timed steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ID] [--impl ours|reference]
 
-With torchrun (N > 1) every rank runs the full batch on its own GPU (weak
-scaling, no collective on the data path); the reported time is the max over
-ranks and the value counts the work of all ranks.  --impl reference times the
+With torchrun (N > 1) the batch grows to N x B sequences drawn from the same
+length distribution and is split across the ranks by whole sequences, balanced
+by cost (jattn_shard): weak scaling with no collective on the attention path.
+The reported time is the max over ranks and the value counts the valid-token
+work of the whole global batch.  --impl reference times the
 fp64 CPU oracle instead (rank 0 only), on a bounded sample of the same batch.
 """
 from __future__ import annotations
@@ -49,13 +51,14 @@ def dist_env():
     return ws, rank, local
 
 
-def workload_config(w: W.Workload, act: int, Bn: int, flush: bool) -> dict:
+def workload_config(w: W.Workload, act: int, Bn: int, flush: bool, ws: int = 1, global_B=None) -> dict:
     return {"workload": "%s (B=%d, H=%d, D=%d, %s%s%s)" % (
         w.name, Bn, w.H, w.D, W.ACT_NAMES[act], ", rel-pos bias %d buckets" % w.bias_buckets if w.bias_buckets
         else "", ", block %d" % w.block if w.block else ""),
         "B": Bn, "H": w.H, "D": w.D, "act": W.ACT_NAMES[act], "block": w.block, "bias_buckets": w.bias_buckets,
         "input_dtype": w.dtype, "l2": "flushed between timed steps (256 MiB write)" if flush else "not flushed",
-        "parallelism": "one batch per GPU (data-parallel replicas)"}
+        "parallelism": ("single GPU" if ws == 1 else
+                        "dp%d: %d sequences split across ranks by cost (jattn_shard), no collective" % (ws, global_B))}
 
 
 # ---------------------------------------------------------------------------
@@ -317,7 +320,8 @@ def run_ours(args, w, batch):
         ms = float(t.item())
 
     f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block)
-    value = ws * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12
+    total_flops = args.global_flops if args.global_flops is not None else ws * (f_fwd + f_bwd)
+    value = total_flops / (ms * 1e-3) / 1e12
     pk, pk_kind = peaks()
 
     # roofline of the dominant kernel (largest share of the step's kernel time)
@@ -345,12 +349,12 @@ def run_ours(args, w, batch):
         t = torch.tensor([e2e["ms_per_step"]], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e["ms_per_step"] = float(t.item())
-        e2e["value"] = ws * (f_fwd + f_bwd) / (e2e["ms_per_step"] * 1e-3) / 1e12
+        e2e["value"] = total_flops / (e2e["ms_per_step"] * 1e-3) / 1e12
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, batch.act, batch.B, True),
+            "config": workload_config(w, batch.act, batch.B, True, ws, args.global_B),
             "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
             "pct_of_bf16_peak_sustained": 100.0 * value / ws / pk["bf16_tflops_sustained"],
             "per_kernel_ms": per_kernel, "gpu_launches": int(launches),
@@ -447,7 +451,23 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     act = None if args.act is None else {"softmax": 0, "silu": 1, "gelu_tanh": 2}[args.act]
-    batch = W.make_batch(args.workload, act=act)
+    ws, rank, _ = dist_env()
+    args.global_flops = None
+    args.global_B = None
+    if args.impl == "ours" and ws > 1:
+        # weak scaling: a global batch of N x B sequences from the same length
+        # distribution, split across the N ranks by cost (jattn_shard); each rank
+        # draws only its own sequences' tensors
+        import jagged_attention_recommendation_gb300 as J
+        w = W.WORKLOADS[args.workload]
+        lq, lk = W.lengths(args.workload, B=ws * w.B)
+        qo, ko = W.offsets(lq), W.offsets(lk)
+        mine = np.nonzero(J.shard(qo, ko, ws) == rank)[0]
+        batch = W.make_batch(args.workload, act=act, lens=(lq[mine], lk[mine]))
+        args.global_flops = float(sum(W.flops(qo, ko, w.H, w.D, w.block)))
+        args.global_B = int(ws * w.B)
+    else:
+        batch = W.make_batch(args.workload, act=act)
     if args.impl == "reference":
         run_reference(args, batch.w, batch)
     else:

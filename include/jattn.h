@@ -206,6 +206,27 @@ const char *jattn_last_cuda_error(void);
 /* Static, human-readable name of a status code. */
 const char *jattn_status_str(jattn_status status);
 
+/* ------------------------------------------------------------------------
+ * Multi-GPU data parallelism.  Every (sequence, head) pair is independent
+ * ("Training GEM at LLM scale", sections "Jagged Sequence Flash Attention"
+ * and the data-parallel training it serves), so a batch shards across ranks by
+ * whole sequences with no collective on the attention path.  Host only; touches
+ * no device.
+ *
+ * Assigns each of the B sequences of a jagged batch to one of `world` ranks:
+ * sequences in decreasing order of the cost Lq*Lk + 64*(Lq + Lk) (the pair
+ * work plus a per-row term for the tile set-up and the row traffic), each to
+ * the rank with the least cost so far (ties to the lower rank; equal costs keep
+ * their batch order), so the result is deterministic and the same on every
+ * rank.  q_offsets_host / kv_offsets_host: HOST int32 [B + 1] as for
+ * jattn_plan_create (block mode needs no special treatment).  rank_of: HOST
+ * int32 [B], caller-owned, receives the rank of each sequence.  Returns
+ * JATTN_ERR_INVALID_ARG for NULL pointers, B < 1, world < 1 or offsets that are
+ * not a valid prefix sum.
+ */
+jattn_status jattn_shard(const int32_t *q_offsets_host, const int32_t *kv_offsets_host, int32_t B, int32_t world,
+                         int32_t *rank_of);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ TILES_Q, TILES_KV = 0, 1
 
 EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd_workspace_bytes",
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
-            "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc")
+            "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
+            "jattn_shard")
 
 
 class JattnError(RuntimeError):
@@ -74,6 +75,8 @@ def load():
     lib.jattn_plan_launch_count.restype = i64
     lib.jattn_last_cuda_error.argtypes = []
     lib.jattn_last_cuda_error.restype = ctypes.c_char_p
+    lib.jattn_shard.argtypes = [P, P, i32, i32, P]
+    lib.jattn_shard.restype = i32
     lib.jattn_status_str.argtypes = [i32]
     lib.jattn_status_str.restype = ctypes.c_char_p
     for f in ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd", "jattn_bwd",
@@ -81,6 +84,16 @@ def load():
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
+
+
+def shard(q_offsets, kv_offsets, world: int) -> np.ndarray:
+    """Rank of every sequence (int32 [B]) for `world` data-parallel ranks (jattn_shard)."""
+    qo, ko = _i32(q_offsets), _i32(kv_offsets)
+    B = len(qo) - 1
+    out = np.zeros(max(B, 0), dtype=np.int32)
+    _check(load().jattn_shard(qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), B, int(world),
+                              out.ctypes.data_as(ctypes.c_void_p)), "jattn_shard")
+    return out
 
 
 def status_str(code: int) -> str:

@@ -615,6 +615,31 @@ jattn_status jattn_check_device_status(const jattn_plan *p, void *stream) {
 
 const char *jattn_last_cuda_error(void) { return g_last_cuda_error; }
 
+jattn_status jattn_shard(const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B, int32_t world,
+                         int32_t *rank_of) {
+    if (rank_of == nullptr || world < 1) return JATTN_ERR_INVALID_ARG;
+    const jattn_status st = check_offsets(q_offsets, kv_offsets, B, false);
+    if (st != JATTN_OK) return st;
+    std::vector<int64_t> cost(static_cast<size_t>(B));
+    for (int32_t b = 0; b < B; ++b) {
+        const int64_t lq = q_offsets[b + 1] - q_offsets[b], lk = kv_offsets[b + 1] - kv_offsets[b];
+        cost[b] = lq * lk + 64 * (lq + lk);
+    }
+    std::vector<int32_t> order(static_cast<size_t>(B));
+    for (int32_t b = 0; b < B; ++b) order[b] = b;
+    std::stable_sort(order.begin(), order.end(), [&](int32_t x, int32_t y) { return cost[x] > cost[y]; });
+    using Slot = std::pair<int64_t, int32_t>;  // (load, rank)
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+    for (int32_t r = 0; r < world; ++r) heap.push({0, r});
+    for (int32_t b : order) {
+        Slot s = heap.top();
+        heap.pop();
+        rank_of[b] = s.second;
+        heap.push({s.first + cost[b], s.second});
+    }
+    return JATTN_OK;
+}
+
 const char *jattn_status_str(jattn_status s) {
     switch (s) {
         case JATTN_OK: return "ok";
