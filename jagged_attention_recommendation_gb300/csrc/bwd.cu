@@ -508,7 +508,7 @@ template <int D, bool ACT, int BIAS>
 struct DkvCfg {
     static constexpr int BKV = 128, BQ = 64;
     static constexpr int NKB = D / 64;
-    static constexpr int NSQ = (D == 64) ? 5 : 3;   // Q / dO / lse / Delta ring
+    static constexpr int NSQ = (D == 64) ? 6 : 4;   // Q / dO / lse / Delta ring
     static constexpr uint32_t SUB_KV = BKV * 128;  // 16 KB
     static constexpr uint32_t SUB_Q = BQ * 128;    // 8 KB
     static constexpr uint32_t KV_BYTES = BKV * D * 2;
