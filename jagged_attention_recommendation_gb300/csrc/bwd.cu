@@ -19,18 +19,24 @@
 // Both passes share one layout, 16 warps (four warpgroups):
 //   warpgroup 0  warp 0: TMA producer of the looped-over blocks (K / V, or
 //                Q / dO with lse and Delta); warp 1: TMEM allocation and the
-//                single MMA-issuing thread; warp 2: TMA producer of the tile's
-//                own rows (Q / dO, or K / V); warp 3 idle.
+//                thread that issues the accumulating products (dQ, or dV and
+//                dK); warp 2: TMA producer of the tile's own rows (Q / dO, or
+//                K / V); warp 3: the thread that issues the two score-side
+//                products of every block (S and dP, or S^T and dP^T).
 //   warpgroups 1, 2  two compute groups; the CTA numbers its blocks n across
 //                tile boundaries and group g takes the blocks with n % 2 == g,
 //                one thread per tile row (TMEM lane), 32 columns at a time.
 //   warpgroup 3  output group: reads the accumulators and writes the rows.
 // A block's two products land in its group's TMEM columns; the compute group
 // overwrites them in place with bf16 dS (and P^T) and the accumulating product
-// reads that operand from TMEM.  The issuer orders
-//   SdP_0, SdP_1, acc_0, SdP_2, acc_1, SdP_3, ...
-// and tcgen05.mma operations of one thread execute in issue order, so SdP_{n+2}
-// overwrites block n's operands only after acc_n has read them.
+// reads that operand from TMEM.  Two issuing threads, because any wait of the
+// issuing thread (an mbarrier, a shared-memory load, a named barrier) holds it
+// until its queued MMAs have drained, which leaves the tensor pipe idle; with
+// two, one thread's products run while the other waits.  Block n + 2 reuses
+// block n's columns, so the score-side issuer waits for block n's accumulating
+// product to finish (an mbarrier committed by the other thread) before it
+// issues block n + 2; the accumulators have a single issuer, so their
+// summation order is fixed and results are reproducible.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -86,8 +92,8 @@ struct DqCfg {
     static constexpr uint32_t OFF_V = OFF_K + NSK * KV_BYTES;
     static constexpr uint32_t OFF_BAR = OFF_V + NSV * KV_BYTES;
     // qd_full[2], qd_empty[2], k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV],
-    // s_full[2], ds_full[2], dq_full[2], dq_empty[2], drain
-    static constexpr int NBAR = 4 + 2 * NSK + 2 * NSV + 8 + 1;
+    // s_full[2], ds_full[2], dq_full[2], dq_empty[2], dq_done[2], drain[2]
+    static constexpr int NBAR = 4 + 2 * NSK + 2 * NSV + 8 + 2 + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
@@ -123,7 +129,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *ds_full = s_full + 2;       // [2] per compute group
     uint64_t *dq_full = ds_full + 2;      // [2] per dQ buffer
     uint64_t *dq_empty = dq_full + 2;     // [2] per dQ buffer
-    uint64_t *drain = dq_empty + 2;
+    uint64_t *dq_done = dq_empty + 2;     // [2] per compute group: its block's dQ product finished
+    uint64_t *drain = dq_done + 2;        // [2] per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
@@ -140,6 +147,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&ds_full[s], 4);
             mbar_init(&dq_full[s], 1);
             mbar_init(&dq_empty[s], 4);
+            mbar_init(&dq_done[s], 1);
+            mbar_init(&drain[s], 1);
         }
         for (int s = 0; s < C::NSK; ++s) {
             mbar_init(&k_full[s], 1);
@@ -149,7 +158,6 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -235,125 +243,97 @@ __global__ void __launch_bounds__(512, 1)
                 for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
                     mbar_drain(&qd_full[i & 1], (i >> 1) & 1);
             }
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
-            // S / dP run two blocks ahead of dQ, across tile boundaries.
-            const uint32_t idesc_dq = idesc_bf16(128, D, false, true);
+        } else if (warp == 3 && lane == 0) {
+            // -------------------------------------------------------- S / dP issuer
+            // Two issuing threads keep the tensor pipe fed (a thread's own waits
+            // stall its queued MMAs): this one issues every S = Q K^T and
+            // dP = dO V^T, the other every dQ product.  Block n (the CTA's blocks
+            // in order, across tiles) reuses the TMEM columns of block n - 2, its
+            // compute group's previous block, once that block's dQ product is done.
             bool ok = true;
-            uint32_t d_cnt[2] = {0, 0};  // dS blocks consumed per compute group
-
             TileStream tsa(g, tbeg, tend);
             Tile ta;
-            int ja = 0, na = 0;
             uint32_t ta_n = 0, ns = 0;
-            // next tile with keys; a tile without keys only hands back its Q / dO slot
-            auto a_next = [&]() -> bool {
-                while (tsa.next(ta)) {
-                    if (!check_tile(g, ta, err, false)) continue;
-                    na = cdiv(ta.kv_len, C::BN);
-                    ja = 0;
-                    if (na > 0) return true;
-                    if (!(ok = mbar_wait(&qd_full[ta_n & 1], (ta_n >> 1) & 1, err))) return false;
-                    mma_commit(&qd_empty[ta_n & 1]);
-                    ++ta_n;
-                }
-                return false;
-            };
-            bool a_has = a_next();
-            // S_ns = Q K^T and dP_ns = dO V^T into the columns of group ns & 1
-            auto issue_SdP = [&]() {
+            while (ok && tsa.next(ta)) {
+                if (!check_tile(g, ta, err, false)) continue;
+                const int na = cdiv(ta.kv_len, C::BN);
                 const uint32_t qs = ta_n & 1;
-                if (ja == 0 && !(ok = mbar_wait(&qd_full[qs], (ta_n >> 1) & 1, err))) return;
-                const uint32_t ks = ns % C::NSK, vs = ns % C::NSV;
-                if (!(ok = mbar_wait(&k_full[ks], (ns / C::NSK) & 1, err))) return;
-                if (!(ok = mbar_wait(&v_full[vs], (ns / C::NSV) & 1, err))) return;
-                tc_fence_after();
-                const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
-                const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                if (!(ok = mbar_wait(&qd_full[qs], (ta_n >> 1) & 1, err))) break;
                 const uint32_t qb = sQ + qs * 2 * C::Q_BYTES;
                 const uint64_t dq0 = sdesc_sw128(qb, 16, 1024), ddo0 = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
-                const uint64_t dk0 = sdesc_sw128(sK + ks * C::KV_BYTES, 16, 1024);
-                const uint64_t dv0 = sdesc_sw128(sV + vs * C::KV_BYTES, 16, 1024);
-                const uint32_t dS = tmem + (ns & 1) * 128, dDP = dS + 64;
+                for (int ja = 0; ja < na; ++ja, ++ns) {
+                    const uint32_t grp = ns & 1;
+                    if (ns >= 2 && !(ok = mbar_wait(&dq_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t ks = ns % C::NSK, vs = ns % C::NSV;
+                    if (!(ok = mbar_wait(&k_full[ks], (ns / C::NSK) & 1, err))) break;
+                    if (!(ok = mbar_wait(&v_full[vs], (ns / C::NSV) & 1, err))) break;
+                    tc_fence_after();
+                    const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
+                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                    const uint64_t dk0 = sdesc_sw128(sK + ks * C::KV_BYTES, 16, 1024);
+                    const uint64_t dv0 = sdesc_sw128(sV + vs * C::KV_BYTES, 16, 1024);
+                    const uint32_t dS = tmem + grp * 128, dDP = dS + 64;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t ao = (k >> 2) * C::SUB_Q + (k & 3) * 32;
-                    const uint32_t bo = (k >> 2) * C::SUB_KV + (k & 3) * 32;
-                    mma_bf16_ss(dS, sdesc_add(dq0, ao), sdesc_add(dk0, bo), idesc, k > 0);
-                    mma_bf16_ss(dDP, sdesc_add(ddo0, ao), sdesc_add(dv0, bo), idesc, k > 0);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t ao = (k >> 2) * C::SUB_Q + (k & 3) * 32;
+                        const uint32_t bo = (k >> 2) * C::SUB_KV + (k & 3) * 32;
+                        mma_bf16_ss(dS, sdesc_add(dq0, ao), sdesc_add(dk0, bo), idesc, k > 0);
+                        mma_bf16_ss(dDP, sdesc_add(ddo0, ao), sdesc_add(dv0, bo), idesc, k > 0);
+                    }
+                    mma_commit(&s_full[grp]);
+                    mma_commit(&v_empty[vs]);  // dP was the V slot's only reader
                 }
-                mma_commit(&s_full[ns & 1]);
-                mma_commit(&v_empty[vs]);
-                ++ns;
-                if (++ja == na) {
-                    mma_commit(&qd_empty[qs]);  // the last reads of this Q / dO slot are in flight
-                    ++ta_n;
-                    a_has = a_next();
-                }
-            };
-
+                if (!ok) break;
+                mma_commit(&qd_empty[qs]);  // the last reads of this Q / dO slot are in flight
+                ++ta_n;
+            }
+            // every MMA this thread issued is done before TMEM is released
+            mma_commit(&drain[0]);
+            mbar_drain(&drain[0], 0);
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- dQ issuer
+            // dQ += dS K, dS (bf16; activation: hi and lo parts) read from TMEM, into
+            // the tile's dQ buffer (two, so the output group reads one while the
+            // next tile accumulates); one thread, so the accumulation order is fixed.
+            const uint32_t idesc_dq = idesc_bf16(128, D, false, true);
+            bool ok = true;
             TileStream tsb(g, tbeg, tend);
             Tile tb;
-            int jb = 0, nbk = 0;
             uint32_t tb_n = 0, np = 0;
-            // dQ buffer tb_n & 1 must have been read out for tile tb_n - 2
-            auto wait_out = [&]() -> bool {
-                return mbar_wait(&dq_empty[tb_n & 1], ((tb_n >> 1) & 1) ^ 1, err);
-            };
-            // next tile with keys; a tile without keys is handed to the output group in order
-            auto b_next = [&]() -> bool {
-                while (tsb.next(tb)) {
-                    if (!check_tile(g, tb, err, false)) continue;
-                    nbk = cdiv(tb.kv_len, C::BN);
-                    jb = 0;
-                    if (nbk > 0) return true;
-                    if (!(ok = wait_out())) return false;
-                    mma_commit(&dq_full[tb_n & 1]);
-                    ++tb_n;
-                }
-                return false;
-            };
-            bool b_has = b_next();
-            // dQ += dS_np K_np, dS (bf16; activation: hi and lo parts) read from TMEM
-            auto issue_dQ = [&]() {
-                const int grp = np & 1;
-                if (!(ok = mbar_wait(&ds_full[grp], d_cnt[grp] & 1, err))) return;
-                ++d_cnt[grp];
-                if (jb == 0 && !(ok = wait_out())) return;
-                tc_fence_after();
-                const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
-                const uint32_t ks = np % C::NSK;
-                const uint64_t bd0 = sdesc_sw128(sK + ks * C::KV_BYTES, C::SUB_KV, 1024);
-                const uint32_t dq = tmem + C::COL_DQ + (tb_n & 1) * D;
-                const uint32_t aS = tmem + grp * 128;
-                for (int k = 0; k < ksteps; ++k) {
-                    const uint64_t bd = sdesc_add(bd0, k * 2048);
-                    const uint32_t acc = (jb > 0 || k > 0) ? 1u : 0u;
-                    if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
-                        mma_bf16_ts(dq, aS + k * 16, bd, idesc_dq, acc);
-                        mma_bf16_ts(dq, aS + k * 16 + 8, bd, idesc_dq, 1u);
-                    } else {
-                        mma_bf16_ts(dq, aS + k * 8, bd, idesc_dq, acc);
+            while (ok && tsb.next(tb)) {
+                if (!check_tile(g, tb, err, false)) continue;
+                const int nbk = cdiv(tb.kv_len, C::BN);
+                const uint32_t b = tb_n & 1;
+                // dQ buffer b must have been read out for tile tb_n - 2
+                if (!(ok = mbar_wait(&dq_empty[b], ((tb_n >> 1) & 1) ^ 1, err))) break;
+                const uint32_t dq = tmem + C::COL_DQ + b * D;
+                for (int jb = 0; jb < nbk; ++jb, ++np) {
+                    const uint32_t grp = np & 1;
+                    if (!(ok = mbar_wait(&ds_full[grp], (np >> 1) & 1, err))) break;
+                    tc_fence_after();
+                    const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
+                    const uint32_t ks = np % C::NSK;
+                    const uint64_t bd0 = sdesc_sw128(sK + ks * C::KV_BYTES, C::SUB_KV, 1024);
+                    const uint32_t aS = tmem + grp * 128;
+                    for (int k = 0; k < ksteps; ++k) {
+                        const uint64_t bd = sdesc_add(bd0, k * 2048);
+                        const uint32_t acc = (jb > 0 || k > 0) ? 1u : 0u;
+                        if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                            mma_bf16_ts(dq, aS + k * 16, bd, idesc_dq, acc);
+                            mma_bf16_ts(dq, aS + k * 16 + 8, bd, idesc_dq, 1u);
+                        } else {
+                            mma_bf16_ts(dq, aS + k * 8, bd, idesc_dq, acc);
+                        }
                     }
+                    mma_commit(&k_empty[ks]);     // S and dQ were the K slot's readers
+                    mma_commit(&dq_done[grp]);    // the group's columns may take block np + 2
                 }
-                mma_commit(&k_empty[ks]);
-                ++np;
-                if (++jb == nbk) {
-                    mma_commit(&dq_full[tb_n & 1]);
-                    ++tb_n;
-                    b_has = b_next();
-                }
-            };
-
-            if (ok && a_has) issue_SdP();
-            if (ok && a_has) issue_SdP();
-            while (ok && b_has) {
-                issue_dQ();
-                // SdP_{np+1} overwrites block np-1's dS: issued after its dQ, executed after it
-                if (ok && a_has) issue_SdP();
+                if (!ok) break;
+                mma_commit(&dq_full[b]);
+                ++tb_n;
             }
-            mma_commit(drain);
-            mbar_drain(drain, 0);
+            mma_commit(&drain[1]);
+            mbar_drain(&drain[1], 0);
         }
     } else if (wgi < 3) {
         regs_claim<kRegCompute>();
@@ -518,8 +498,9 @@ struct DkvCfg {
     static constexpr uint32_t OFF_Q = 2 * KV_BYTES;  // [NSQ][Q | dO]
     static constexpr uint32_t OFF_LD = OFF_Q + NSQ * 2 * Q_BYTES;  // [NSQ][-lse log2 e | -Delta][64] floats
     static constexpr uint32_t OFF_BAR = OFF_LD + NSQ * 2 * BQ * 4;
-    // kv_full, kv_empty, qs_full[NSQ], qs_empty[NSQ], st_full[2], p_full[2], acc_full, acc_empty, drain
-    static constexpr int NBAR = 2 + 2 * NSQ + 4 + 2 + 1;
+    // kv_full, kv_empty, qs_full[NSQ], qs_empty[NSQ], st_full[2], p_full[2], acc_full, acc_empty,
+    // acc_done[2], drain[2]
+    static constexpr int NBAR = 2 + 2 * NSQ + 4 + 2 + 2 + 2;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
@@ -554,7 +535,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *p_full = st_full + 2;         // [2] per compute group
     uint64_t *acc_full = p_full + 2;
     uint64_t *acc_empty = acc_full + 1;
-    uint64_t *drain = acc_empty + 1;
+    uint64_t *acc_done = acc_empty + 1;  // [2] per compute group: its block's dV / dK products finished
+    uint64_t *drain = acc_done + 2;      // [2] per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
@@ -577,7 +559,10 @@ __global__ void __launch_bounds__(512, 1)
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
-        mbar_init(drain, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_done[b], 1);
+            mbar_init(&drain[b], 1);
+        }
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -670,124 +655,97 @@ __global__ void __launch_bounds__(512, 1)
                 }
             }
             if (!ok && t_local > 0) mbar_drain(kv_full, (t_local - 1) & 1);
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
-            // S^T / dP^T run two blocks ahead of dV / dK, across tile boundaries.
-            const uint32_t idesc_acc = idesc_bf16(128, D, false, true);
+        } else if (warp == 3 && lane == 0) {
+            // -------------------------------------------------------- S^T / dP^T issuer
+            // Two issuing threads keep the tensor pipe fed: a thread's own waits
+            // (any shared-memory access) stall its queued MMAs, so this thread
+            // issues every S^T = K Q^T and dP^T = V dO^T and the other every
+            // dV / dK product.  Block n (the CTA's blocks in order, across tiles)
+            // reuses the TMEM columns of block n - 2, its compute group's previous
+            // block, once that block's dV / dK products have finished.
             bool ok = true;
-            uint32_t p_cnt[2] = {0, 0};  // P^T / dS^T blocks consumed per compute group
-
             TileStream tsa(g, tbeg, tend);
             Tile ta;
-            int ia = 0, na = 0;
             uint32_t ta_n = 0, ns = 0;
-            // next tile with queries; a tile without queries only hands back its K / V
-            auto a_next = [&]() -> bool {
-                while (tsa.next(ta)) {
-                    if (!check_tile(g, ta, err, false)) continue;
-                    na = cdiv(ta.q_len, C::BQ);
-                    ia = 0;
-                    if (na > 0) return true;
-                    if (!(ok = mbar_wait(kv_full, ta_n & 1, err))) return false;
-                    mma_commit(kv_empty);
-                    ++ta_n;
-                }
-                return false;
-            };
-            bool a_has = a_next();
-            // S^T_ns = K Q^T and dP^T_ns = V dO^T into the columns of group ns & 1
-            auto issue_SdPT = [&]() {
-                if (ia == 0 && !(ok = mbar_wait(kv_full, ta_n & 1, err))) return;
-                const uint32_t slot = ns % C::NSQ;
-                if (!(ok = mbar_wait(&qs_full[slot], (ns / C::NSQ) & 1, err))) return;
-                tc_fence_after();
-                const int ncols = round_up16(min(C::BQ, ta.q_len - ia * C::BQ));
-                const uint32_t idesc = idesc_bf16(128, ncols, false, false);
-                const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
-                const uint64_t dqq = sdesc_sw128(qb, 16, 1024), ddo = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
-                const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, 16, 1024);
-                const uint32_t dS = tmem + (ns & 1) * 128, dDP = dS + 64;
+            const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, 16, 1024);
+            while (ok && tsa.next(ta)) {
+                if (!check_tile(g, ta, err, false)) continue;
+                const int na = cdiv(ta.q_len, C::BQ);
+                if (!(ok = mbar_wait(kv_full, ta_n & 1, err))) break;
+                for (int ia = 0; ia < na; ++ia, ++ns) {
+                    const uint32_t grp = ns & 1;
+                    if (ns >= 2 && !(ok = mbar_wait(&acc_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t slot = ns % C::NSQ;
+                    if (!(ok = mbar_wait(&qs_full[slot], (ns / C::NSQ) & 1, err))) break;
+                    tc_fence_after();
+                    const int ncols = round_up16(min(C::BQ, ta.q_len - ia * C::BQ));
+                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                    const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
+                    const uint64_t dqq = sdesc_sw128(qb, 16, 1024), ddo = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
+                    const uint32_t dS = tmem + grp * 128, dDP = dS + 64;
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t ao = (k >> 2) * C::SUB_KV + (k & 3) * 32;
-                    const uint32_t bo = (k >> 2) * C::SUB_Q + (k & 3) * 32;
-                    mma_bf16_ss(dS, sdesc_add(dk0, ao), sdesc_add(dqq, bo), idesc, k > 0);
-                    mma_bf16_ss(dDP, sdesc_add(dv0, ao), sdesc_add(ddo, bo), idesc, k > 0);
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t ao = (k >> 2) * C::SUB_KV + (k & 3) * 32;
+                        const uint32_t bo = (k >> 2) * C::SUB_Q + (k & 3) * 32;
+                        mma_bf16_ss(dS, sdesc_add(dk0, ao), sdesc_add(dqq, bo), idesc, k > 0);
+                        mma_bf16_ss(dDP, sdesc_add(dv0, ao), sdesc_add(ddo, bo), idesc, k > 0);
+                    }
+                    mma_commit(&st_full[grp]);
                 }
-                mma_commit(&st_full[ns & 1]);
-                ++ns;
-                if (++ia == na) {
-                    mma_commit(kv_empty);  // the tile's last reads of K and V are in flight
-                    ++ta_n;
-                    a_has = a_next();
-                }
-            };
-
+                if (!ok) break;
+                mma_commit(kv_empty);  // the tile's last reads of K and V are in flight
+                ++ta_n;
+            }
+            // every MMA this thread issued is done before TMEM is released
+            mma_commit(&drain[0]);
+            mbar_drain(&drain[0], 0);
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- dV / dK issuer
+            // dV += P^T dO and dK += dS^T Q, P^T and dS^T (bf16; activation: hi and
+            // lo parts) read from TMEM; one thread, so the accumulation order is fixed.
+            const uint32_t idesc_acc = idesc_bf16(128, D, false, true);
+            bool ok = true;
             TileStream tsb(g, tbeg, tend);
             Tile tb;
-            int ib = 0, nbq = 0;
             uint32_t tb_n = 0, np = 0;
-            // dV / dK must have been read out for tile tb_n - 1
-            auto wait_out = [&]() -> bool {
-                return mbar_wait(acc_empty, (tb_n & 1) ^ 1, err);
-            };
-            auto b_next = [&]() -> bool {
-                while (tsb.next(tb)) {
-                    if (!check_tile(g, tb, err, false)) continue;
-                    nbq = cdiv(tb.q_len, C::BQ);
-                    ib = 0;
-                    if (nbq > 0) return true;
-                    if (!(ok = wait_out())) return false;
-                    mma_commit(acc_full);
-                    ++tb_n;
-                }
-                return false;
-            };
-            bool b_has = b_next();
-            // dV += P^T dO and dK += dS^T Q, P^T and dS^T (bf16; activation: hi and lo) from TMEM
-            auto issue_acc = [&]() {
-                const int grp = np & 1;
-                if (!(ok = mbar_wait(&p_full[grp], p_cnt[grp] & 1, err))) return;
-                ++p_cnt[grp];
-                if (ib == 0 && !(ok = wait_out())) return;
-                tc_fence_after();
-                const int ksteps = round_up16(min(C::BQ, tb.q_len - ib * C::BQ)) / 16;
-                const uint32_t slot = np % C::NSQ;
-                const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
-                const uint64_t bq0 = sdesc_sw128(qb, C::SUB_Q, 1024), bdo0 = sdesc_sw128(qb + C::Q_BYTES, C::SUB_Q, 1024);
-                const uint32_t aP = tmem + grp * 128, aDS = aP + 64;
-                for (int k = 0; k < ksteps; ++k) {
-                    const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
-                    const uint64_t bdo = sdesc_add(bdo0, k * 2048);
-                    const uint64_t bq = sdesc_add(bq0, k * 2048);
-                    if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
-                        mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
-                        mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
-                        mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
-                        mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
-                    } else {
-                        mma_bf16_ts(tmem + C::COL_DV, aP + k * 8, bdo, idesc_acc, acc);
-                        mma_bf16_ts(tmem + C::COL_DK, aDS + k * 8, bq, idesc_acc, acc);
+            while (ok && tsb.next(tb)) {
+                if (!check_tile(g, tb, err, false)) continue;
+                const int nbq = cdiv(tb.q_len, C::BQ);
+                // the output group must have read dV / dK of the previous tile
+                if (!(ok = mbar_wait(acc_empty, (tb_n & 1) ^ 1, err))) break;
+                for (int ib = 0; ib < nbq; ++ib, ++np) {
+                    const uint32_t grp = np & 1;
+                    if (!(ok = mbar_wait(&p_full[grp], (np >> 1) & 1, err))) break;
+                    tc_fence_after();
+                    const int ksteps = round_up16(min(C::BQ, tb.q_len - ib * C::BQ)) / 16;
+                    const uint32_t slot = np % C::NSQ;
+                    const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
+                    const uint64_t bq0 = sdesc_sw128(qb, C::SUB_Q, 1024);
+                    const uint64_t bdo0 = sdesc_sw128(qb + C::Q_BYTES, C::SUB_Q, 1024);
+                    const uint32_t aP = tmem + grp * 128, aDS = aP + 64;
+                    for (int k = 0; k < ksteps; ++k) {
+                        const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
+                        const uint64_t bdo = sdesc_add(bdo0, k * 2048);
+                        const uint64_t bq = sdesc_add(bq0, k * 2048);
+                        if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
+                        } else {
+                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 8, bdo, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 8, bq, idesc_acc, acc);
+                        }
                     }
+                    mma_commit(&qs_empty[slot]);  // last reads of the Q / dO slot
+                    mma_commit(&acc_done[grp]);   // the group's columns may take block np + 2
                 }
-                mma_commit(&qs_empty[slot]);
-                ++np;
-                if (++ib == nbq) {
-                    mma_commit(acc_full);
-                    ++tb_n;
-                    b_has = b_next();
-                }
-            };
-
-            if (ok && a_has) issue_SdPT();
-            if (ok && a_has) issue_SdPT();
-            while (ok && b_has) {
-                issue_acc();
-                // SdPT_{np+1} overwrites block np-1's operands: issued after its products
-                if (ok && a_has) issue_SdPT();
+                if (!ok) break;
+                mma_commit(acc_full);
+                ++tb_n;
             }
-            mma_commit(drain);
-            mbar_drain(drain, 0);
+            mma_commit(&drain[1]);
+            mbar_drain(&drain[1], 0);
         }
     } else if (wgi < 3) {
         regs_claim<kRegCompute>();
