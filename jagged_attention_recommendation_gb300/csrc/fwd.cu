@@ -14,10 +14,10 @@
 //   warp 0      TMA producer for K and V (128-row tiles) through NST-deep rings
 //               with separate release barriers: a K slot refills as soon as
 //               its S = Q K^T is done, a V slot once its P V is done.
-//   warp 1      allocates TMEM; one thread issues every tcgen05.mma.
+//   warp 1      allocates TMEM; one thread issues every P V product.
 //   warp 2      TMA producer for Q, double-buffered so the next tile's rows
 //               arrive while the current tile runs.
-//   warp 3      idle (its registers go to the softmax warpgroups).
+//   warp 3      one thread issues every S = Q K^T.
 //   warps 4-7   softmax group 0: blocks n = 0, 2, 4, ...
 //   warps 8-11  softmax group 1: blocks n = 1, 3, 5, ...
 //   warps 12-15 output group: merges the two groups' partial results of a
@@ -32,11 +32,13 @@
 // activation modes simply O_0 + O_1).
 // P never touches shared memory: the softmax writes it as bf16 over the
 // group's own score columns in TMEM and P V reads it from there (the A operand
-// of tcgen05.mma may live in TMEM).  The issuer orders
-//   S_0, S_1, PV_0, S_2, PV_1, S_3, ...
-// and tcgen05.mma operations of one thread execute in issue order, so S_{n+2}
-// overwrites P_n only after PV_n has read it, while S_{n+1} is computed during
-// the softmax of block n.
+// of tcgen05.mma may live in TMEM).  Two threads issue the products, because
+// any wait of an issuing thread (an mbarrier, a shared-memory load) holds it
+// until its queued MMAs have drained, which idles the tensor pipe; with two,
+// one thread's products run while the other waits.  S_{n+2} overwrites P_n, so
+// the S issuer waits for PV_n to finish (an mbarrier committed by the P V
+// issuer) before it issues S_{n+2}; S_{n+1} is computed during the softmax of
+// block n.
 // Rows past a sequence's end are loaded (they belong to the next sequence or
 // are zero-filled past the tensor end) but masked as keys and never stored as
 // queries; the last key block of a sequence runs a narrower MMA (N rounded up
@@ -70,8 +72,8 @@ struct FwdCfg {
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;
     // q_full[2], q_empty[2], k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
-    // s_full[2], p_full[2], o_full, o_empty[2], l_full[2], drain
-    static constexpr int NBAR = 4 + 4 * NST + 2 + 2 + 1 + 2 + 2 + 1;
+    // s_full[2], p_full[2], o_full, o_empty[2], l_full[2], pv_done[2], drain[2]
+    static constexpr int NBAR = 4 + 4 * NST + 2 + 2 + 1 + 2 + 2 + 2 + 2;
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
@@ -117,7 +119,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *o_full = p_full + 2;
     uint64_t *o_empty = o_full + 1;  // [2] per tile parity
     uint64_t *l_full = o_empty + 2;  // [2] per tile parity
-    uint64_t *drain = l_full + 2;
+    uint64_t *pv_done = l_full + 2;  // [2] per softmax group: its block's P V finished
+    uint64_t *drain = pv_done + 2;   // [2] per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
@@ -136,6 +139,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&p_full[s], 4);
             mbar_init(&o_empty[s], 4);
             mbar_init(&l_full[s], 8);
+            mbar_init(&pv_done[s], 1);
+            mbar_init(&drain[s], 1);
         }
         for (int s = 0; s < C::NST; ++s) {
             mbar_init(&k_full[s], 1);
@@ -144,7 +149,6 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&v_empty[s], 1);
         }
         mbar_init(o_full, 1);
-        mbar_init(drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -244,128 +248,93 @@ __global__ void __launch_bounds__(512, 1)
                 for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
                     mbar_drain(&q_full[i & 1], (i >> 1) & 1);
             }
-        } else if (warp == 1 && lane == 0) {
-            // -------------------------------------------------------- MMA issuer
-            // Two cursors over the CTA's blocks: S runs two blocks ahead of P V,
-            // across tile boundaries.
-            const uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+        } else if (warp == 3 && lane == 0) {
+            // -------------------------------------------------------- S issuer
+            // Two issuing threads keep the tensor pipe fed (a thread's own waits
+            // stall its queued MMAs): this one issues every S = Q K^T, the other
+            // every P V.  Block n (the CTA's blocks in order, across tiles) reuses
+            // the score columns of block n - 2, its group's previous block, once
+            // that block's P V has finished.  So when the softmax sees S_n, its
+            // group's O already holds all of the group's earlier blocks, and a
+            // rescale of O may touch it.
             bool ok = true;
-            uint32_t p_cnt[2] = {0, 0};  // P blocks consumed per softmax group
-
-            // S cursor: tile ta (the ta_n-th valid tile), block ja of na, global block ns
             TileStream tsa(g, tbeg, tend);
             Tile ta;
-            int ja = 0, na = 0;
             uint32_t ta_n = 0, ns = 0;
-            // moves to the next tile with keys; tiles without keys only hand back their Q slot
-            auto a_next = [&]() -> bool {
-                while (tsa.next(ta)) {
-                    if (!check_tile(g, ta, err, false)) continue;
-                    na = cdiv(ta.kv_len, C::BN);
-                    ja = 0;
-                    if (na > 0) return true;
-                    if (!(ok = mbar_wait(&q_full[ta_n & 1], (ta_n >> 1) & 1, err))) return false;
-                    mma_commit(&q_empty[ta_n & 1]);
-                    ++ta_n;
-                }
-                return false;
-            };
-            bool a_has = a_next();
-            // S_ns = Q K^T into the score columns of group ns & 1
-            auto issue_S = [&]() {
+            while (ok && tsa.next(ta)) {
+                if (!check_tile(g, ta, err, false)) continue;
+                const int na = cdiv(ta.kv_len, C::BN);
                 const uint32_t qs = ta_n & 1;
-                if (ja == 0) {
-                    if (!(ok = mbar_wait(&q_full[qs], (ta_n >> 1) & 1, err))) return;
-                }
-                const uint32_t slot = ns % C::NST, use = ns / C::NST;
-                if (!(ok = mbar_wait(&k_full[slot], use & 1, err))) return;
-                tc_fence_after();
-                const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
-                const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                if (!(ok = mbar_wait(&q_full[qs], (ta_n >> 1) & 1, err))) break;
                 const uint64_t ad0 = sdesc_sw128(sQ + qs * C::Q_BYTES, 16, 1024);
-                const uint64_t bd0 = sdesc_sw128(sK + slot * C::KV_BYTES, 16, 1024);
-                const uint32_t dS = tmem + C::COL_S + (ns & 1) * C::BN;
+                for (int ja = 0; ja < na; ++ja, ++ns) {
+                    const uint32_t grp = ns & 1;
+                    if (ns >= 2 && !(ok = mbar_wait(&pv_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t slot = ns % C::NST, use = ns / C::NST;
+                    if (!(ok = mbar_wait(&k_full[slot], use & 1, err))) break;
+                    tc_fence_after();
+                    const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
+                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                    const uint64_t bd0 = sdesc_sw128(sK + slot * C::KV_BYTES, 16, 1024);
+                    const uint32_t dS = tmem + C::COL_S + grp * C::BN;
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    mma_bf16_ss(dS, sdesc_add(ad0, (ks >> 2) * C::SUB_Q + (ks & 3) * 32),
-                                sdesc_add(bd0, (ks >> 2) * C::SUB_KV + (ks & 3) * 32), idesc, ks > 0);
-                mma_commit(&s_full[ns & 1]);
-                mma_commit(&k_empty[slot]);
-                ++ns;
-                if (++ja == na) {
-                    mma_commit(&q_empty[qs]);  // the last read of this Q slot is in flight
-                    ++ta_n;
-                    a_has = a_next();
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_bf16_ss(dS, sdesc_add(ad0, (ks >> 2) * C::SUB_Q + (ks & 3) * 32),
+                                    sdesc_add(bd0, (ks >> 2) * C::SUB_KV + (ks & 3) * 32), idesc, ks > 0);
+                    mma_commit(&s_full[grp]);
+                    mma_commit(&k_empty[slot]);
                 }
-            };
-
-            // P V cursor: tile tb (the tb_n-th valid tile), block jb of nbk, global block np
+                if (!ok) break;
+                mma_commit(&q_empty[qs]);  // the last read of this Q slot is in flight
+                ++ta_n;
+            }
+            // every MMA this thread issued is done before TMEM is released
+            mma_commit(&drain[0]);
+            mbar_drain(&drain[0], 0);
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- P V issuer
+            // O_g (+)= P V for group g's blocks, P (bf16; activation: hi and lo
+            // parts) read from TMEM; one thread, so the accumulation order is fixed.
+            const uint32_t idesc_pv = idesc_bf16(128, D, false, true);
+            bool ok = true;
             TileStream tsb(g, tbeg, tend);
             Tile tb;
-            int jb = 0, nbk = 0;
             uint32_t tb_n = 0, np = 0;
-            // the output group must have read tile tb_n - 1 before O_0 / O_1 are reused
-            auto wait_out = [&]() -> bool {
-                if (tb_n == 0) return true;
-                return mbar_wait(&o_empty[(tb_n - 1) & 1], ((tb_n - 1) >> 1) & 1, err);
-            };
-            // moves to the next tile with keys; tiles without keys are handed to the
-            // output group (all-zero rows) in order
-            auto b_next = [&]() -> bool {
-                while (tsb.next(tb)) {
-                    if (!check_tile(g, tb, err, false)) continue;
-                    nbk = cdiv(tb.kv_len, C::BN);
-                    jb = 0;
-                    if (nbk > 0) return true;
-                    if (!(ok = wait_out())) return false;
-                    mma_commit(o_full);
-                    ++tb_n;
-                }
-                return false;
-            };
-            bool b_has = b_next();
-            // O_{np & 1} (+)= P_np V_np, P (bf16; activation: hi and lo parts) read from TMEM
-            auto issue_PV = [&]() {
-                const int grp = np & 1;
-                if (!(ok = mbar_wait(&p_full[grp], p_cnt[grp] & 1, err))) return;
-                ++p_cnt[grp];
-                if (jb == 0 && !(ok = wait_out())) return;
-                const uint32_t slot = np % C::NST, use = np / C::NST;
-                if (!(ok = mbar_wait(&v_full[slot], use & 1, err))) return;
-                tc_fence_after();
-                const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
-                const uint64_t bd0 = sdesc_sw128(sV + slot * C::KV_BYTES, C::SUB_KV, 1024);
-                const uint32_t dO = tmem + C::COL_O + grp * D;
-                const uint32_t aP = tmem + C::COL_S + grp * C::BN;
-                // the first two blocks of a tile start their group's accumulator
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    const uint64_t bd = sdesc_add(bd0, ks * 2048);
-                    if (ACT) {  // hi at columns 16 ks .. +7, lo at 16 ks + 8 .. +15
-                        mma_bf16_ts(dO, aP + ks * 16, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
-                        mma_bf16_ts(dO, aP + ks * 16 + 8, bd, idesc_pv, 1u);
-                    } else {
-                        mma_bf16_ts(dO, aP + ks * 8, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
+            while (ok && tsb.next(tb)) {
+                if (!check_tile(g, tb, err, false)) continue;
+                const int nbk = cdiv(tb.kv_len, C::BN);
+                // the output group must have read tile tb_n - 1 before O_0 / O_1 are
+                // reused (a tile without keys hands over all-zero rows in order)
+                if (tb_n > 0 && !(ok = mbar_wait(&o_empty[(tb_n - 1) & 1], ((tb_n - 1) >> 1) & 1, err))) break;
+                for (int jb = 0; jb < nbk; ++jb, ++np) {
+                    const uint32_t grp = np & 1;
+                    if (!(ok = mbar_wait(&p_full[grp], (np >> 1) & 1, err))) break;
+                    const uint32_t slot = np % C::NST, use = np / C::NST;
+                    if (!(ok = mbar_wait(&v_full[slot], use & 1, err))) break;
+                    tc_fence_after();
+                    const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
+                    const uint64_t bd0 = sdesc_sw128(sV + slot * C::KV_BYTES, C::SUB_KV, 1024);
+                    const uint32_t dO = tmem + C::COL_O + grp * D;
+                    const uint32_t aP = tmem + C::COL_S + grp * C::BN;
+                    // the first two blocks of a tile start their group's accumulator
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const uint64_t bd = sdesc_add(bd0, ks * 2048);
+                        if (ACT) {  // hi at columns 16 ks .. +7, lo at 16 ks + 8 .. +15
+                            mma_bf16_ts(dO, aP + ks * 16, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
+                            mma_bf16_ts(dO, aP + ks * 16 + 8, bd, idesc_pv, 1u);
+                        } else {
+                            mma_bf16_ts(dO, aP + ks * 8, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
+                        }
                     }
+                    mma_commit(&v_empty[slot]);
+                    mma_commit(&pv_done[grp]);  // the group's score columns may take block np + 2
                 }
-                mma_commit(&v_empty[slot]);
-                ++np;
-                if (++jb == nbk) {
-                    mma_commit(o_full);
-                    ++tb_n;
-                    b_has = b_next();
-                }
-            };
-
-            if (ok && a_has) issue_S();
-            if (ok && a_has) issue_S();
-            while (ok && b_has) {
-                issue_PV();
-                // S_{np+1} overwrites P_{np-1}: issued after that P V, executed after it
-                if (ok && a_has) issue_S();
+                if (!ok) break;
+                mma_commit(o_full);
+                ++tb_n;
             }
-            // wait for every MMA this thread issued before TMEM is released
-            mma_commit(drain);
-            mbar_drain(drain, 0);
+            mma_commit(&drain[1]);
+            mbar_drain(&drain[1], 0);
         }
         // warp 3 and the other lanes: idle
     } else if (wgi < 3) {
