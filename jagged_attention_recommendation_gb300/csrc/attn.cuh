@@ -117,6 +117,37 @@ __device__ __forceinline__ void st_row32_zero(uint32_t tile, uint32_t sub_bytes,
     for (int k = 0; k < 4; ++k) st_shared_v4(base + sw128_offset(row, k0 + k), 0u, 0u, 0u, 0u);
 }
 
+// Row-contiguous output through shared memory.  With one thread per result
+// row, a direct 16-byte store per thread touches 32 rows per instruction; a
+// warp instead stages W columns of its 32 rows as bf16 in a buffer of 32 x W
+// values (the 16-byte chunks of a row XOR-swizzled by row, so that neither the
+// per-row writes nor the row-contiguous reads have bank conflicts) and then
+// writes W-column row pieces, W / 8 lanes per row.
+template <int W>
+__device__ __forceinline__ void stage_row32_bf16(uint32_t stg, int lane, int c0, const uint32_t (&w)[16]) {
+    static_assert(W == 64 || W == 128, "staged width");
+    const uint32_t rowb = stg + static_cast<uint32_t>(lane) * (W * 2);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t ch = static_cast<uint32_t>((c0 >> 3) + k) ^ static_cast<uint32_t>(lane & 7);
+        st_shared_v4(rowb + ch * 16, w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+    }
+}
+// Rows 0..nrows-1 of the staged block to base + r * ld (bf16 elements); call
+// after a __syncwarp that follows the last stage_row32_bf16 of the block.
+template <int W>
+__device__ __forceinline__ void store_rows_bf16(uint32_t stg, int lane, __nv_bfloat16 *base, int64_t ld, int nrows) {
+    constexpr int CPR = W / 8;     // 16-byte chunks per row
+    constexpr int RPI = 32 / CPR;  // rows per instruction
+    const int ch = lane % CPR, rsub = lane / CPR;
+#pragma unroll
+    for (int it = 0; it < 32 / RPI; ++it) {
+        const int r = it * RPI + rsub;
+        const uint4 v = ld_shared_v4(stg + static_cast<uint32_t>(r * (W * 2) + ((ch ^ (r & 7)) * 16)));
+        if (r < nrows) *reinterpret_cast<uint4 *>(base + r * ld + ch * 8) = v;
+    }
+}
+
 // Store columns c0..c0+31 (times `mul`) of result row `row`, head h.
 __device__ __forceinline__ void store_out32(const OutDesc &o, int64_t row, int h, int c0, const float (&v)[32],
                                             float mul) {

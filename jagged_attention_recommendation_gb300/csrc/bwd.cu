@@ -504,7 +504,10 @@ struct DkvCfg {
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
-    static constexpr uint32_t SMEM = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
+    // per output warp: 32 rows x 64 bf16 staging for row-contiguous stores
+    static constexpr int STG_W = 64;
+    static constexpr uint32_t OFF_STG = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
+    static constexpr uint32_t SMEM = OFF_STG + 4 * 32 * STG_W * 2;
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     // group g: S^T at 128 g (P^T over it), dP^T at 128 g + 64 (dS^T over it); dV, dK
@@ -850,11 +853,18 @@ __global__ void __launch_bounds__(512, 1)
     } else {
         regs_release<kRegOut>();
         // ------------------------------------------------------------ output
-        // One thread per key row: dV and dK (times the score scale) from TMEM ->
-        // the rows of dv and dk (whole 64-byte pieces per thread).
+        // One thread per key row reads dV and dK (times the score scale) from
+        // TMEM.  bf16 outputs go out row-contiguous through the warp's staging
+        // buffer: dV is staged and dK packed into registers before the
+        // accumulators are handed back, so the next tile's products wait only
+        // for the TMEM reads, not for the stores.
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tDV = tmem + lane_base + C::COL_DV, tDK = tmem + lane_base + C::COL_DK;
+        constexpr int W = C::STG_W;
+        const uint32_t stg = smem_u32(smem + C::OFF_STG) + static_cast<uint32_t>(quad) * (32 * W * 2);
+        const bool staged = !a.dv.f32 && !a.dk.f32 && a.dv.cols == D && a.dk.cols == D;
         uint32_t t_local = 0;
         bool ok = true;
         TileStream ts(g, tbeg, tend);
@@ -870,13 +880,67 @@ __global__ void __launch_bounds__(512, 1)
                 continue;
             }
             tc_fence_after();
+            if (staged) {
+                const int nrows = min(32, t.kv_len - quad * 32);
+                const int64_t r0 = static_cast<int64_t>(t.kv_start) + quad * 32;
+                __nv_bfloat16 *dv0 = static_cast<__nv_bfloat16 *>(a.dv.ptr) + r0 * a.dv.ld + t.h * D;
+                __nv_bfloat16 *dk0 = static_cast<__nv_bfloat16 *>(a.dk.ptr) + r0 * a.dk.ld + t.h * D;
+                // dV: W columns at a time through the staging buffer
+#pragma unroll
+                for (int h0 = 0; h0 < D; h0 += W) {
+#pragma unroll
+                    for (int c = 0; c < W / 32; ++c) {
+                        float v[32];
+                        uint32_t w[16];
+                        if (nq > 0) {
+                            tmem_ld32(tDV + h0 + 32 * c, v);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        }
+                        pack16(v, w);
+                        stage_row32_bf16<W>(stg, lane, 32 * c, w);
+                    }
+                    __syncwarp();
+                    store_rows_bf16<W>(stg, lane, dv0 + h0, a.dv.ld, nrows);
+                    __syncwarp();
+                }
+                // dK (times the score scale) packed into registers
+                uint32_t kw[D / 32][16];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
+                    if (nq > 0) {
+                        tmem_ld32(tDK + 32 * c, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) mul2(v[i], v[i + 1], g.scale, g.scale);
+                    pack16(v, kw[c]);
+                }
+                // every TMEM read of this tile is done
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+#pragma unroll
+                for (int h0 = 0; h0 < D; h0 += W) {
+#pragma unroll
+                    for (int c = 0; c < W / 32; ++c) stage_row32_bf16<W>(stg, lane, 32 * c, kw[h0 / 32 + c]);
+                    __syncwarp();
+                    store_rows_bf16<W>(stg, lane, dk0 + h0, a.dk.ld, nrows);
+                    __syncwarp();
+                }
+                continue;
+            }
             const bool row_ok = row < t.kv_len;
             const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
 #pragma unroll 1
             for (int col = 0; col < D; col += 32) {
                 float ov[32], ok_[32];
                 if (nq > 0) {
-                    tmem_ld32x2(tmem + lane_base + C::COL_DV + col, tmem + lane_base + C::COL_DK + col, ov, ok_);
+                    tmem_ld32x2(tDV + col, tDK + col, ov, ok_);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) ov[i] = ok_[i] = 0.0f;
