@@ -506,7 +506,7 @@ struct DkvCfg {
     static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
     // per output warp: 32 rows x 64 bf16 staging for row-contiguous stores
     static constexpr int STG_W = 64;
-    static constexpr uint32_t OFF_STG = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
+    static constexpr uint32_t OFF_STG = (OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0) + 127) & ~127u;
     static constexpr uint32_t SMEM = OFF_STG + 4 * 32 * STG_W * 2;
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -515,6 +515,7 @@ struct DkvCfg {
     static constexpr uint32_t COL_DK = 256 + D;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "operand alignment");
+    static_assert(OFF_STG % 16 == 0, "16-byte shared-memory vectors");
     static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
 };
 
