@@ -196,6 +196,50 @@ jattn_status jattn_bwd_noalloc(const jattn_plan *plan, const void *dout, const v
                                const float *bias, const void *out, const float *lse, void *dq, void *dk, void *dv,
                                float *dbias, void *stream);
 
+/*
+ * One training step whose tensors live in host memory ("Training GEM at LLM
+ * scale", "Jagged Sequence Flash Attention": forward and backward of the jagged
+ * batch). The call re-plans the plan for the batch given by the host offsets,
+ * as jattn_plan_update does. It copies q, k, v, dout (and bias) host -> device,
+ * runs jattn_fwd and jattn_bwd, and copies out, dq, dk, dv (and lse)
+ * device -> host.
+ *
+ * Layouts and dtypes are those of jattn_fwd / jattn_bwd, all tensors on the
+ * host: q, dout, out, dq [Tq, H, D]; k, v, dk, dv [Tk, H, D] with Tq =
+ * q_offsets[B], Tk = kv_offsets[B]; bias [H, NB] fp32 (NULL iff the plan has no
+ * bias); lse [H, Tq] fp32 or NULL (not returned; softmax only).
+ *
+ * Asynchronous and pipelined: the call enqueues its work and returns. The plan
+ * owns two device staging sets and three streams for this (upload, compute,
+ * download). Consecutive calls therefore overlap: call n's uploads run during
+ * call n-1's kernels, and call n-1's downloads during call n's kernels. The work
+ * of a call starts after the work already queued on `stream` (the caller's
+ * stream, NULL = legacy default stream). The host buffers of a call belong to
+ * the library until jattn_step_host_join's wait has passed; they must not be
+ * modified or freed before. Page-locked (pinned) host memory gives full
+ * overlap; pageable memory is accepted, but its copies do not overlap.
+ *
+ * Errors: JATTN_ERR_INVALID_ARG for a NULL plan or required pointer, bad
+ * offsets or a bias that does not match the plan; JATTN_ERR_NO_DEVICE for a
+ * host-only plan; JATTN_ERR_CUDA when a CUDA call fails (details in
+ * jattn_last_cuda_error); errors of the enqueued kernels surface through
+ * jattn_check_device_status. The first call, and any call whose batch is larger
+ * than every earlier one, allocates the staging sets (after waiting for the
+ * calls that still use them).
+ */
+jattn_status jattn_step_host(jattn_plan *plan, const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B,
+                             const void *q, const void *k, const void *v, const void *dout, const float *bias,
+                             void *out, float *lse, void *dq, void *dk, void *dv, void *stream);
+
+/*
+ * Makes `stream` (NULL = legacy default stream) wait until every
+ * jattn_step_host call issued on the plan so far has finished, its downloads
+ * included. Once the stream passes that point, the calls' host buffers may be
+ * read and reused. Returns JATTN_ERR_INVALID_ARG for a NULL plan, JATTN_OK when
+ * no call was issued, JATTN_ERR_CUDA when the wait cannot be enqueued.
+ */
+jattn_status jattn_step_host_join(jattn_plan *plan, void *stream);
+
 /* Synchronises `stream`, then returns and clears the plan's device status word. */
 jattn_status jattn_check_device_status(const jattn_plan *plan, void *stream);
 

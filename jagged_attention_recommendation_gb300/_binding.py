@@ -24,7 +24,7 @@ TILES_Q, TILES_KV = 0, 1
 EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd_workspace_bytes",
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
             "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
-            "jattn_shard")
+            "jattn_shard", "jattn_step_host", "jattn_step_host_join")
 
 
 class JattnError(RuntimeError):
@@ -68,6 +68,10 @@ def load():
     lib.jattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
     lib.jattn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.jattn_bwd_noalloc.restype = i32
+    lib.jattn_step_host.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P, P, P]
+    lib.jattn_step_host.restype = i32
+    lib.jattn_step_host_join.argtypes = [P, P]
+    lib.jattn_step_host_join.restype = i32
     lib.jattn_check_device_status.argtypes = [P, P]
     lib.jattn_plan_set_events.argtypes = [P, P, i32]
     lib.jattn_plan_set_events.restype = i32
@@ -217,6 +221,31 @@ class Plan:
                                         _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _stream(stream)),
                "jattn_bwd_noalloc")
         return dq, dk, dv
+
+    def step_host(self, q_off, kv_off, q, k, v, dout, out, dq, dk, dv, bias=None, lse=None, stream=None):
+        """One training step on host tensors (pinned memory overlaps the copies): re-plan
+        for the batch, upload q, k, v, dout (bias), forward, backward, download into
+        out, dq, dk, dv (lse).  Asynchronous and pipelined with the previous call; the
+        host tensors must stay untouched until step_host_join's wait has passed."""
+        qo, ko = _i32(q_off), _i32(kv_off)
+        Tq, Tk = int(qo[-1]), int(ko[-1])
+        nq, nk = Tq * self.H * self.D, Tk * self.H * self.D
+        for name, t, n in (("q", q, nq), ("k", k, nk), ("v", v, nk), ("dout", dout, nq), ("out", out, nq),
+                           ("dq", dq, nq), ("dk", dk, nk), ("dv", dv, nk)):
+            if t.is_cuda or not t.is_contiguous() or t.numel() != n or t.dtype != self._tdtype():
+                raise ValueError("step_host: %s must be a contiguous %s host tensor of %d elements"
+                                 % (name, self._tdtype(), n))
+        for name, t, n in (("bias", bias, self.H * self.bias_buckets), ("lse", lse, self.H * Tq)):
+            if t is not None and (t.is_cuda or not t.is_contiguous() or t.numel() != n or t.dtype != torch.float32):
+                raise ValueError("step_host: %s must be a contiguous float32 host tensor of %d elements" % (name, n))
+        _check(load().jattn_step_host(self._h, qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p),
+                                      len(qo) - 1, _ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(bias), _ptr(out),
+                                      _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)), "jattn_step_host")
+        self.Tq, self.Tk = Tq, Tk
+
+    def step_host_join(self, stream=None):
+        """Makes `stream` wait for every step_host call issued so far."""
+        _check(load().jattn_step_host_join(self._h, _stream(stream)), "jattn_step_host_join")
 
     def set_events(self, events):
         """Record torch.cuda.Event objects around each kernel of later fwd / bwd calls (None: off)."""

@@ -60,6 +60,19 @@ struct jattn_plan {
     mutable std::vector<cudaEvent_t> prof_events;
     mutable int prof_next = 0;
     mutable int64_t launches = 0;
+    // jattn_step_host: two device staging sets and the upload / compute /
+    // download streams that overlap consecutive calls
+    struct HostStep {
+        bool init = false;
+        cudaStream_t s_up = nullptr, s_comp = nullptr, s_down = nullptr;
+        cudaEvent_t ev_start = nullptr;
+        cudaEvent_t up_done[2] = {nullptr, nullptr}, comp_done[2] = {nullptr, nullptr},
+                    down_done[2] = {nullptr, nullptr};
+        bool used[2] = {false, false};
+        uint8_t *dev[2] = {nullptr, nullptr};
+        size_t cap[2] = {0, 0};
+        int next = 0, last = -1;
+    } hs;
 };
 
 namespace {
@@ -456,6 +469,17 @@ void jattn_plan_destroy(jattn_plan *p) {
             if (p->h_pin[k]) cudaFreeHost(p->h_pin[k]);
             if (p->ev[k]) cudaEventDestroy(p->ev[k]);
         }
+        jattn_plan::HostStep &h = p->hs;
+        for (int k = 0; k < 2; ++k) {
+            if (h.dev[k]) cudaFree(h.dev[k]);
+            if (h.up_done[k]) cudaEventDestroy(h.up_done[k]);
+            if (h.comp_done[k]) cudaEventDestroy(h.comp_done[k]);
+            if (h.down_done[k]) cudaEventDestroy(h.down_done[k]);
+        }
+        if (h.ev_start) cudaEventDestroy(h.ev_start);
+        if (h.s_up) cudaStreamDestroy(h.s_up);
+        if (h.s_comp) cudaStreamDestroy(h.s_comp);
+        if (h.s_down) cudaStreamDestroy(h.s_down);
     }
     delete p;
 }
@@ -587,6 +611,112 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
     a.g.bias = bias;
     return cuda_status(log.done(launch_bwd_dkdv(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_KV), st)),
                        "jattn_bwd: dK/dV kernel launch");
+}
+
+jattn_status jattn_step_host(jattn_plan *p, const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B,
+                             const void *q, const void *k, const void *v, const void *dout, const float *bias,
+                             void *out, float *lse, void *dq, void *dk, void *dv, void *stream) {
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    if (!q || !k || !v || !dout || !out || !dq || !dk || !dv) return JATTN_ERR_INVALID_ARG;
+    if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;
+    jattn_status st = check_offsets(q_offsets, kv_offsets, B, p->mode.block != 0);
+    if (st != JATTN_OK) return st;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return note_error("jattn_step_host: cudaSetDevice failed");
+    (void)cudaGetLastError();
+    jattn_plan::HostStep &h = p->hs;
+    if (!h.init) {
+        CUDA_TRY(cudaStreamCreateWithFlags(&h.s_up, cudaStreamNonBlocking));
+        CUDA_TRY(cudaStreamCreateWithFlags(&h.s_comp, cudaStreamNonBlocking));
+        CUDA_TRY(cudaStreamCreateWithFlags(&h.s_down, cudaStreamNonBlocking));
+        CUDA_TRY(cudaEventCreateWithFlags(&h.ev_start, cudaEventDisableTiming));
+        for (int i = 0; i < 2; ++i) {
+            CUDA_TRY(cudaEventCreateWithFlags(&h.up_done[i], cudaEventDisableTiming));
+            CUDA_TRY(cudaEventCreateWithFlags(&h.comp_done[i], cudaEventDisableTiming));
+            CUDA_TRY(cudaEventCreateWithFlags(&h.down_done[i], cudaEventDisableTiming));
+        }
+        h.init = true;
+    }
+    const int i = h.next;
+    // host side of the re-plan; the tile lists reach the device on the compute
+    // stream, after the previous call's kernels
+    set_batch(p, q_offsets, kv_offsets, B);
+
+    // staging set i: q, k, v, dout, bias, out, lse, dq, dk, dv, workspaces
+    const size_t es = p->mode.dtype == JATTN_FP32 ? 4 : 2;
+    const size_t nq = static_cast<size_t>(p->Tq) * p->H * p->D * es;
+    const size_t nk = static_cast<size_t>(p->Tk) * p->H * p->D * es;
+    const size_t nb = bias ? static_cast<size_t>(p->H) * p->mode.bias_buckets * 4 : 0;
+    const size_t nl = p->mode.act == JATTN_SOFTMAX ? static_cast<size_t>(p->H) * p->Tq * 4 : 0;
+    const size_t nfw = jattn_fwd_workspace_bytes(p), nbw = jattn_bwd_workspace_bytes(p);
+    const size_t sizes[12] = {nq, nk, nk, nq, nb, nq, nl, nq, nk, nk, nfw, nbw};
+    size_t offs[12], total = 0;
+    for (int j = 0; j < 12; ++j) {
+        offs[j] = total;
+        total += align_up(sizes[j], kAlign);
+    }
+    if (total > h.cap[i]) {
+        if (h.used[i]) CUDA_TRY(cudaEventSynchronize(h.down_done[i]));  // its last use
+        if (h.dev[i]) cudaFree(h.dev[i]);
+        h.dev[i] = nullptr;
+        h.cap[i] = 0;
+        const size_t cap = total + total / 4;
+        CUDA_TRY(cudaMalloc(&h.dev[i], cap));
+        h.cap[i] = cap;
+    }
+    uint8_t *d = h.dev[i];
+    void *dq_in = d + offs[0], *dk_in = d + offs[1], *dv_in = d + offs[2], *ddo = d + offs[3];
+    float *dbias = nb ? reinterpret_cast<float *>(d + offs[4]) : nullptr;
+    void *dout_ = d + offs[5];
+    float *dlse = nl ? reinterpret_cast<float *>(d + offs[6]) : nullptr;
+    void *ddq = d + offs[7], *ddk = d + offs[8], *ddv = d + offs[9];
+    void *fws = nfw ? d + offs[10] : nullptr, *bws = nbw ? d + offs[11] : nullptr;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    CUDA_TRY(cudaEventRecord(h.ev_start, cs));
+    // uploads: after the caller's queued work and after set i's inputs were last read
+    CUDA_TRY(cudaStreamWaitEvent(h.s_up, h.ev_start, 0));
+    if (h.used[i]) CUDA_TRY(cudaStreamWaitEvent(h.s_up, h.comp_done[i], 0));
+    CUDA_TRY(cudaMemcpyAsync(dq_in, q, nq, cudaMemcpyHostToDevice, h.s_up));
+    CUDA_TRY(cudaMemcpyAsync(dk_in, k, nk, cudaMemcpyHostToDevice, h.s_up));
+    CUDA_TRY(cudaMemcpyAsync(dv_in, v, nk, cudaMemcpyHostToDevice, h.s_up));
+    CUDA_TRY(cudaMemcpyAsync(ddo, dout, nq, cudaMemcpyHostToDevice, h.s_up));
+    if (nb) CUDA_TRY(cudaMemcpyAsync(dbias, bias, nb, cudaMemcpyHostToDevice, h.s_up));
+    CUDA_TRY(cudaEventRecord(h.up_done[i], h.s_up));
+    // kernels: after the uploads and after set i's outputs were last read back
+    CUDA_TRY(cudaStreamWaitEvent(h.s_comp, h.ev_start, 0));
+    CUDA_TRY(cudaStreamWaitEvent(h.s_comp, h.up_done[i], 0));
+    if (h.used[i]) CUDA_TRY(cudaStreamWaitEvent(h.s_comp, h.down_done[i], 0));
+    st = upload(p, h.s_comp);
+    if (st != JATTN_OK) return st;
+    st = jattn_fwd(p, dq_in, dk_in, dv_in, dbias, dout_, dlse, fws, nfw, h.s_comp);
+    if (st != JATTN_OK) return st;
+    st = jattn_bwd(p, ddo, dq_in, dk_in, dv_in, dbias, dout_, dlse, ddq, ddk, ddv, nullptr, bws, nbw, h.s_comp);
+    if (st != JATTN_OK) return st;
+    CUDA_TRY(cudaEventRecord(h.comp_done[i], h.s_comp));
+    // downloads
+    CUDA_TRY(cudaStreamWaitEvent(h.s_down, h.comp_done[i], 0));
+    CUDA_TRY(cudaMemcpyAsync(out, dout_, nq, cudaMemcpyDeviceToHost, h.s_down));
+    if (lse && nl) CUDA_TRY(cudaMemcpyAsync(lse, dlse, nl, cudaMemcpyDeviceToHost, h.s_down));
+    CUDA_TRY(cudaMemcpyAsync(dq, ddq, nq, cudaMemcpyDeviceToHost, h.s_down));
+    CUDA_TRY(cudaMemcpyAsync(dk, ddk, nk, cudaMemcpyDeviceToHost, h.s_down));
+    CUDA_TRY(cudaMemcpyAsync(dv, ddv, nk, cudaMemcpyDeviceToHost, h.s_down));
+    CUDA_TRY(cudaEventRecord(h.down_done[i], h.s_down));
+    h.used[i] = true;
+    h.last = i;
+    h.next = i ^ 1;
+    return JATTN_OK;
+}
+
+jattn_status jattn_step_host_join(jattn_plan *p, void *stream) {
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0 || p->hs.last < 0) return JATTN_OK;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return note_error("jattn_step_host_join: cudaSetDevice failed");
+    // downloads run in call order on one stream: the last call's event covers all
+    CUDA_TRY(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), p->hs.down_done[p->hs.last], 0));
+    return JATTN_OK;
 }
 
 jattn_status jattn_plan_set_events(jattn_plan *p, void *const *events, int32_t n_events) {
