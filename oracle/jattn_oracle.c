@@ -19,6 +19,9 @@
  *               O_i = sum_j P_ij v_j,          lse_i = m_i + ln l_i
  *     act:      O_i = sum_j act(s_ij) v_j      (SiLU or tanh-GELU, no normalisation)
  *     block:    j restricted to the 64-block of i (floor(j/64) == floor(i/64))
+ *     window W: j restricted to |i - j| < W (sliding-window attention, section
+ *               "BlockAttention": each token attends only to nearby events;
+ *               the band is symmetric, like the relative-position bias)
  *
  *   backward (chain rule of the above):
  *     dP_ij = <dO_i, v_j>
@@ -49,7 +52,7 @@
 enum { ACT_SOFTMAX = 0, ACT_SILU = 1, ACT_GELU_TANH = 2 };
 
 typedef struct {
-    int act, block, B, H, D, nb;
+    int act, block, window, B, H, D, nb;
     const int32_t *q_off, *kv_off;
     const double *q, *k, *v, *bias, *dout;
     double scale;
@@ -101,6 +104,11 @@ static void key_range(const job_t *J, int i, int Lk, int *j0, int *j1) {
         *j0 = blk * J->block;
         *j1 = (blk + 1) * J->block < Lk ? (blk + 1) * J->block : Lk;
         if (*j0 > Lk) *j0 = Lk;
+    } else if (J->window > 0) {
+        int lo = i - J->window + 1, hi = i + J->window; /* |i - j| < W */
+        *j0 = lo > 0 ? lo : 0;
+        *j1 = hi < Lk ? hi : Lk;
+        if (*j0 > *j1) *j0 = *j1;
     } else {
         *j0 = 0;
         *j1 = Lk;
@@ -196,6 +204,7 @@ static void *worker(void *arg) {
 }
 
 static int run(job_t *J, int nthreads) {
+    if (J->window < 0 || (J->window > 0 && J->block > 0)) return 4;
     for (int b = 0; b < J->B; ++b) {
         if (J->q_off[b + 1] < J->q_off[b] || J->kv_off[b + 1] < J->kv_off[b]) return 2;
         if (J->block > 0 && (J->q_off[b + 1] - J->q_off[b]) != (J->kv_off[b + 1] - J->kv_off[b])) return 3;
@@ -214,25 +223,25 @@ static int run(job_t *J, int nthreads) {
     return J->err;
 }
 
-int jattn_oracle_fwd(int act, int block, int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
-                     const double *q, const double *k, const double *v, const double *bias, int nb,
-                     double scale, double *out, double *lse, int nthreads) {
+int jattn_oracle_fwd(int act, int block, int window, int B, int H, int D, const int32_t *q_off,
+                     const int32_t *kv_off, const double *q, const double *k, const double *v, const double *bias,
+                     int nb, double scale, double *out, double *lse, int nthreads) {
     job_t J;
     memset(&J, 0, sizeof(J));
-    J.act = act; J.block = block; J.B = B; J.H = H; J.D = D; J.nb = bias ? nb : 1;
+    J.act = act; J.block = block; J.window = window; J.B = B; J.H = H; J.D = D; J.nb = bias ? nb : 1;
     J.q_off = q_off; J.kv_off = kv_off; J.q = q; J.k = k; J.v = v; J.bias = bias;
     J.scale = scale; J.out = out; J.lse = lse; J.backward = 0;
     return run(&J, nthreads);
 }
 
 /* dq, dk, dv must be zero-filled by the caller; dbias (if given) is [H, nb]. */
-int jattn_oracle_bwd(int act, int block, int B, int H, int D, const int32_t *q_off, const int32_t *kv_off,
-                     const double *q, const double *k, const double *v, const double *bias, int nb,
-                     double scale, const double *dout, double *dq, double *dk, double *dv, double *dbias,
+int jattn_oracle_bwd(int act, int block, int window, int B, int H, int D, const int32_t *q_off,
+                     const int32_t *kv_off, const double *q, const double *k, const double *v, const double *bias,
+                     int nb, double scale, const double *dout, double *dq, double *dk, double *dv, double *dbias,
                      int nthreads) {
     job_t J;
     memset(&J, 0, sizeof(J));
-    J.act = act; J.block = block; J.B = B; J.H = H; J.D = D; J.nb = bias ? nb : 1;
+    J.act = act; J.block = block; J.window = window; J.B = B; J.H = H; J.D = D; J.nb = bias ? nb : 1;
     J.q_off = q_off; J.kv_off = kv_off; J.q = q; J.k = k; J.v = v; J.bias = bias;
     J.scale = scale; J.dout = dout; J.dq = dq; J.dk = dk; J.dv = dv; J.backward = 1;
     double *part = NULL;

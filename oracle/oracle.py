@@ -41,9 +41,9 @@ def _load():
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
         i, d = ctypes.c_int, ctypes.c_double
-        lib.jattn_oracle_fwd.argtypes = [i, i, i, i, i, P, P, P, P, P, P, i, d, P, P, i]
+        lib.jattn_oracle_fwd.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, i, d, P, P, i]
         lib.jattn_oracle_fwd.restype = i
-        lib.jattn_oracle_bwd.argtypes = [i, i, i, i, i, P, P, P, P, P, P, i, d, P, P, P, P, P, i]
+        lib.jattn_oracle_bwd.argtypes = [i, i, i, i, i, i, P, P, P, P, P, P, i, d, P, P, P, P, P, i]
         lib.jattn_oracle_bwd.restype = i
         lib.jattn_oracle_act.argtypes = [i, d]
         lib.jattn_oracle_act.restype = d
@@ -74,8 +74,9 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None):
-    """Returns (out [Tq,H,D] float64, lse [H,Tq] float64 or None)."""
+def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0):
+    """Returns (out [Tq,H,D] float64, lse [H,Tq] float64 or None).
+    window W > 0: row i attends only keys with |i - j| < W (sliding window)."""
     lib = _load()
     qo, ko = _i32(q_off), _i32(kv_off)
     q, k, v, bias = _f64(q), _f64(k), _f64(v), _f64(bias)
@@ -86,15 +87,15 @@ def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0,
     out = np.zeros((Tq, H, D), dtype=np.float64)
     lse = np.zeros((H, Tq), dtype=np.float64) if act == SOFTMAX else None
     nb = 0 if bias is None else bias.shape[1]
-    rc = lib.jattn_oracle_fwd(act, block, B, H, D, _ptr(qo), _ptr(ko), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
+    rc = lib.jattn_oracle_fwd(act, block, int(window), B, H, D, _ptr(qo), _ptr(ko), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
                               nb, float(scale), _ptr(out), _ptr(lse), nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle forward rejected its input (code %d)" % rc)
     return out, lse
 
 
-def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None):
-    """Returns (dq, dk, dv, dbias or None), all float64."""
+def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0):
+    """Returns (dq, dk, dv, dbias or None), all float64 (window as in forward)."""
     lib = _load()
     qo, ko = _i32(q_off), _i32(kv_off)
     q, k, v, dout, bias = _f64(q), _f64(k), _f64(v), _f64(dout), _f64(bias)
@@ -108,7 +109,7 @@ def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, b
     dv = np.zeros((Tk, H, D), dtype=np.float64)
     nb = 0 if bias is None else bias.shape[1]
     dbias = np.zeros((H, nb), dtype=np.float64) if bias is not None else None
-    rc = lib.jattn_oracle_bwd(act, block, B, H, D, _ptr(qo), _ptr(ko), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
+    rc = lib.jattn_oracle_bwd(act, block, int(window), B, H, D, _ptr(qo), _ptr(ko), _ptr(q), _ptr(k), _ptr(v), _ptr(bias),
                               nb, float(scale), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias),
                               nthreads or default_threads())
     if rc != 0:

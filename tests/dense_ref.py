@@ -24,7 +24,14 @@ def block_mask(L, block):
     return i == j
 
 
-def sdpa_forward(q_off, kv_off, q, k, v, bias=None, scale=None, block=0):
+def band_mask(Lq, Lk, window):
+    """True where |i - j| < window (sliding-window attention)."""
+    i = torch.arange(Lq).view(-1, 1)
+    j = torch.arange(Lk).view(1, -1)
+    return (i - j).abs() < window
+
+
+def sdpa_forward(q_off, kv_off, q, k, v, bias=None, scale=None, block=0, window=0):
     """Softmax attention per sequence with torch SDPA in float64."""
     q, k, v = (t.to(torch.float64) for t in (q, k, v))
     Tq, H, D = q.shape
@@ -43,12 +50,14 @@ def sdpa_forward(q_off, kv_off, q, k, v, bias=None, scale=None, block=0):
                 mask[h] = bias_matrix(bias[h].to(torch.float64), q1 - q0, k1 - k0)
         if block:
             mask = mask.masked_fill(~block_mask(q1 - q0, block), float("-inf"))
+        if window:
+            mask = mask.masked_fill(~band_mask(q1 - q0, k1 - k0, window), float("-inf"))
         o = F.scaled_dot_product_attention(qb, kb, vb, attn_mask=mask, scale=scale)
         out[q0:q1] = o.permute(1, 0, 2)
     return out
 
 
-def padded_dense(q_off, kv_off, q, k, v, dout=None, bias=None, scale=None, act=SOFTMAX, block=0):
+def padded_dense(q_off, kv_off, q, k, v, dout=None, bias=None, scale=None, act=SOFTMAX, block=0, window=0):
     """Pad the jagged batch to [B, H, Lmax, D], mask, and run attention densely.
 
     Softmax rows are masked with -inf; activation mode multiplies by a 0/1 mask
@@ -76,6 +85,8 @@ def padded_dense(q_off, kv_off, q, k, v, dout=None, bias=None, scale=None, act=S
         m[:lq[b], :lk[b]] = True
         if block:
             m[:lq[b], :lk[b]] &= block_mask(max(lq[b], lk[b]), block)[:lq[b], :lk[b]]
+        if window:
+            m[:lq[b], :lk[b]] &= band_mask(int(lq[b]), int(lk[b]), window)
         valid[b, 0] = m
     tbl = None
     if bias is not None:

@@ -289,3 +289,72 @@ def test_planted_mistakes_are_caught():
     assert np.abs(no_bias - ref).max() > 1e-3
     wrong_scale, _ = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], scale=1.0)
     assert np.abs(wrong_scale - ref).max() > 1e-3
+
+
+# --- sliding window (|i - j| < W) ------------------------------------------
+
+def test_window_matches_sdpa_with_band_mask():
+    """Window W: SDPA with -inf outside the band |i - j| < W, bias included."""
+    bt = batch(41, [9, 30, 1, 17], [9, 30, 1, 17], nb=6)
+    for w in (1, 3, 8):
+        out, _ = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], window=w)
+        ref = dense_ref.sdpa_forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"],
+                                     window=w).numpy()
+        np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU, GELU_TANH])
+def test_window_forward_backward_match_autograd(act):
+    """Window with cross-attention lengths (some rows see no key at all): forward,
+    lse and every gradient against masked dense attention under torch autograd."""
+    bt = batch(42, [12, 3, 25, 0], [5, 9, 30, 4], nb=5)
+    w = 4
+    out, lse = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], act=act,
+                              window=w)
+    dq, dk, dv, dt = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"],
+                                     bias=bt["bias"], act=act, window=w)
+    r_out, r_lse, r_dq, r_dk, r_dv, r_dt = dense_ref.padded_dense(bt["q_off"], bt["kv_off"], bt["q"], bt["k"],
+                                                                  bt["v"], dout=bt["dout"], bias=bt["bias"],
+                                                                  act=act, window=w)
+    np.testing.assert_allclose(out, r_out.numpy(), rtol=1e-11, atol=1e-11)
+    if act == SOFTMAX:
+        np.testing.assert_allclose(lse, r_lse.numpy(), rtol=1e-11, atol=1e-11)
+    for got, ref in ((dq, r_dq), (dk, r_dk), (dv, r_dv), (dt, r_dt)):
+        np.testing.assert_allclose(got, ref.detach().numpy(), rtol=1e-10, atol=1e-10)
+
+
+def test_window_one_is_the_diagonal():
+    """W = 1 keeps only j = i: O = V and lse = s_ii exactly; then P = 1, so
+    dS = dP - Delta = 0 gives dQ = dK = 0 and dV = dO."""
+    bt = batch(43, [7, 20, 1], [7, 20, 1], nb=0)
+    out, lse = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], window=1)
+    q, k, v, do = (bt[n].numpy() for n in ("q", "k", "v", "dout"))
+    assert np.array_equal(out, v)
+    D = q.shape[2]
+    np.testing.assert_allclose(lse, (np.einsum("thd,thd->ht", q, k) / math.sqrt(D)), rtol=1e-13, atol=1e-13)
+    dq, dk, dv, _ = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"], window=1)
+    assert np.array_equal(dq, np.zeros_like(dq)) and np.array_equal(dk, np.zeros_like(dk))
+    assert np.array_equal(dv, do)
+
+
+def test_window_wider_than_every_sequence_is_full_attention():
+    bt = batch(44, [13, 40, 2], [13, 40, 2], nb=4)
+    full, flse = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"])
+    win, wlse = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], window=40)
+    assert np.array_equal(full, win) and np.array_equal(flse, wlse)
+
+
+def test_window_band_is_symmetric_and_rejects_block():
+    """An off-by-one band (|i - j| <= W, or one-sided) changes row 0 against the
+    SDPA pin above; here: the W = 2 output of row i uses exactly keys i-1, i, i+1."""
+    bt = batch(45, [6], [6], nb=0)
+    out, _ = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], window=2)
+    q, k, v = (bt[n].numpy()[:, 0] for n in ("q", "k", "v"))
+    D = q.shape[1]
+    for i in range(6):
+        js = [j for j in (i - 1, i, i + 1) if 0 <= j < 6]
+        s = np.array([q[i] @ k[j] / math.sqrt(D) for j in js])
+        p = np.exp(s - s.max()) / np.exp(s - s.max()).sum()
+        np.testing.assert_allclose(out[i, 0], p @ v[js], rtol=1e-12, atol=1e-12)
+    with pytest.raises(ValueError):
+        oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], block=64, window=2)
