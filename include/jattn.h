@@ -72,6 +72,11 @@ typedef struct {
     float scale;          /* score scale; 0 selects 1/sqrt(D) */
     int32_t bias_buckets; /* 0 = no bias, else NB >= 1 with H * NB <= 256 */
     int32_t dtype;        /* jattn_dtype */
+    int32_t window;       /* sliding window W ("Training GEM at LLM scale", section
+                             "BlockAttention": each token attends only to nearby
+                             events): 0 = off; W > 0 restricts row i to keys j with
+                             |i - j| < W, local positions, and the planner skips the
+                             tiles outside that band; not combined with block */
 } jattn_mode;
 
 /* One unit of work: rows [q_start, q_start+q_len) of Q against rows

@@ -38,7 +38,7 @@ class JattnError(RuntimeError):
 
 class Mode(ctypes.Structure):
     _fields_ = [("act", ctypes.c_int32), ("block", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("bias_buckets", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("bias_buckets", ctypes.c_int32), ("dtype", ctypes.c_int32), ("window", ctypes.c_int32)]
 
 
 class TileRec(ctypes.Structure):
@@ -129,13 +129,14 @@ class Plan:
     """A planned jagged batch (tile lists + schedule) for one (H, D, mode)."""
 
     def __init__(self, q_off, kv_off, H: int, D: int, act: int = SOFTMAX, block: int = 0, scale: float = 0.0,
-                 bias_buckets: int = 0, dtype: str = "bf16", device: int = 0):
+                 bias_buckets: int = 0, dtype: str = "bf16", device: int = 0, window: int = 0):
         lib = load()
         qo, ko = _i32(q_off), _i32(kv_off)
         self.H, self.D, self.act, self.block, self.bias_buckets = H, D, act, block, bias_buckets
+        self.window = window
         self.dtype = dtype
         self.device = device
-        self.mode = Mode(act, block, float(scale), bias_buckets, FP32 if dtype == "fp32" else BF16)
+        self.mode = Mode(act, block, float(scale), bias_buckets, FP32 if dtype == "fp32" else BF16, window)
         self._h = ctypes.c_void_p()
         _check(lib.jattn_plan_create(qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p),
                                      len(qo) - 1, H, D, ctypes.byref(self.mode), device, ctypes.byref(self._h)),

@@ -141,6 +141,7 @@ void schedule(std::vector<jattn_tile> &list, std::vector<int32_t> &cta, int num_
 
 void build_lists(jattn_plan *p) {
     const bool block = p->mode.block != 0;
+    const int64_t win = p->mode.window;
     std::vector<jattn_tile> &tq = p->tiles[JATTN_TILES_Q];
     std::vector<jattn_tile> &tk = p->tiles[JATTN_TILES_KV];
     tq.clear();
@@ -150,12 +151,18 @@ void build_lists(jattn_plan *p) {
         const int32_t k0 = p->kv_off[b], Lk = p->kv_off[b + 1] - k0;
         for (int32_t s = 0; s < Lq; s += kTileRows) {
             const int32_t ql = std::min(kTileRows, Lq - s);
-            for (int32_t h = 0; h < p->H; ++h) {
-                if (block)
-                    tq.push_back({b, h, q0 + s, ql, k0 + s, ql});
-                else
-                    tq.push_back({b, h, q0 + s, ql, k0, Lk});
+            // keys the tile's rows may see: all, the same chunk (block), or the
+            // union of the rows' windows |i - j| < W (sliding window)
+            int32_t lo = 0, hi = Lk;
+            if (block) {
+                lo = s;
+                hi = s + ql;
+            } else if (win > 0) {
+                lo = static_cast<int32_t>(std::min<int64_t>(Lk, std::max<int64_t>(0, static_cast<int64_t>(s) - win + 1)));
+                hi = static_cast<int32_t>(std::min<int64_t>(Lk, static_cast<int64_t>(s) + ql + win - 1));
+                if (hi < lo) hi = lo;  // no key in reach: an empty range inside the sequence
             }
+            for (int32_t h = 0; h < p->H; ++h) tq.push_back({b, h, q0 + s, ql, k0 + lo, hi - lo});
         }
     }
     if (!block) {
@@ -164,7 +171,13 @@ void build_lists(jattn_plan *p) {
             const int32_t k0 = p->kv_off[b], Lk = p->kv_off[b + 1] - k0;
             for (int32_t s = 0; s < Lk; s += kTileRows) {
                 const int32_t kl = std::min(kTileRows, Lk - s);
-                for (int32_t h = 0; h < p->H; ++h) tk.push_back({b, h, q0, Lq, k0 + s, kl});
+                int32_t lo = 0, hi = Lq;  // queries whose window reaches the tile's keys
+                if (win > 0) {
+                    lo = static_cast<int32_t>(std::min<int64_t>(Lq, std::max<int64_t>(0, static_cast<int64_t>(s) - win + 1)));
+                    hi = static_cast<int32_t>(std::min<int64_t>(Lq, static_cast<int64_t>(s) + kl + win - 1));
+                    if (hi < lo) hi = lo;  // no query in reach: an empty range inside the sequence
+                }
+                for (int32_t h = 0; h < p->H; ++h) tk.push_back({b, h, q0 + lo, hi - lo, k0 + s, kl});
             }
         }
     }
@@ -320,6 +333,7 @@ Geom make_geom(const jattn_plan *p, int which) {
     g.Tk = static_cast<int32_t>(p->Tk);
     g.act = p->mode.act;
     g.block = p->mode.block;
+    g.window = std::min(p->mode.window, 1 << 30);  // wider than any sequence: same as no limit
     g.nb = p->mode.bias_buckets;
     g.scale = p->scale;
     g.bias = nullptr;
@@ -380,6 +394,7 @@ jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offse
     if (D != 32 && D != 64 && D != 128) return (D > 0) ? JATTN_ERR_UNSUPPORTED : JATTN_ERR_INVALID_ARG;
     if (mode->act < JATTN_SOFTMAX || mode->act > JATTN_GELU_TANH) return JATTN_ERR_INVALID_ARG;
     if (mode->block != 0 && mode->block != 64) return JATTN_ERR_UNSUPPORTED;
+    if (mode->window < 0 || (mode->window > 0 && mode->block != 0)) return JATTN_ERR_INVALID_ARG;
     if (mode->dtype != JATTN_BF16 && mode->dtype != JATTN_FP32) return JATTN_ERR_INVALID_ARG;
     if (mode->bias_buckets < 0) return JATTN_ERR_INVALID_ARG;
     if (mode->bias_buckets > 0 && H * mode->bias_buckets > kMaxBiasFloats) return JATTN_ERR_UNSUPPORTED;

@@ -117,6 +117,29 @@ __device__ __forceinline__ void st_row32_zero(uint32_t tile, uint32_t sub_bytes,
     for (int k = 0; k < 4; ++k) st_shared_v4(base + sw128_offset(row, k0 + k), 0u, 0u, 0u, 0u);
 }
 
+// Sliding window |p - o| < W on local positions: bit k is set when position
+// o0 + k of the other side is inside row p's band (all bits when W == 0).
+__device__ __forceinline__ uint32_t window_bits32(int W, int p, int o0) {
+    if (W <= 0) return 0xffffffffu;
+    const int lo = p - W + 1 - o0, hi = p + W - 1 - o0;  // allowed k in [lo, hi]
+    if (lo <= 0 && hi >= 31) return 0xffffffffu;
+    if (hi < 0 || lo > 31) return 0u;
+    const int a = lo < 0 ? 0 : lo, b = hi > 31 ? 31 : hi;
+    const uint32_t upto = b == 31 ? 0xffffffffu : ((1u << (b + 1)) - 1u);
+    return upto & ~((1u << a) - 1u);
+}
+// False when none of rows p0..p0+31 has o0..o0+31 in its band (a warp-uniform test).
+__device__ __forceinline__ bool window_chunk_live(int W, int p0, int o0) {
+    return W <= 0 || (o0 <= p0 + 31 + W - 1 && o0 + 31 >= p0 - W + 1);
+}
+// Entries of a 32-wide chunk outside the band take `fill`.
+__device__ __forceinline__ void window_fill32(float (&x)[32], uint32_t bits, float fill) {
+    if (bits == 0xffffffffu) return;
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+        if (!((bits >> k) & 1u)) x[k] = fill;
+}
+
 // Row-contiguous output through shared memory.  With one thread per result
 // row, a direct 16-byte store per thread touches 32 rows per instruction; a
 // warp instead stages W columns of its 32 rows as bf16 in a buffer of 32 x W

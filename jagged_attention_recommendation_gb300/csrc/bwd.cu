@@ -107,7 +107,8 @@ struct DqCfg {
     static_assert(COL_DQ + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D, bool ACT, int BIAS>
+// WIN: sliding window on (compile time, so kernels without one carry no band test)
+template <int D, bool ACT, int BIAS, bool WIN>
 __global__ void __launch_bounds__(512, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
@@ -402,6 +403,8 @@ __global__ void __launch_bounds__(512, 1)
                                 for (int i = 0; i < 32; ++i)
                                     if (c * 32 + i >= nvalid) x[i] = 0.0f;
                             }
+                            // keys outside the row's window
+                            if constexpr (WIN) window_fill32(x, window_bits32(g.window, q_loc, kvb + c * 32), 0.0f);
                             if constexpr (ACT) {
                                 uint32_t w[32];
                                 pack_hilo32(x, w);
@@ -519,7 +522,7 @@ struct DkvCfg {
     static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D, bool ACT, int BIAS>
+template <int D, bool ACT, int BIAS, bool WIN>
 __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
@@ -822,6 +825,11 @@ __global__ void __launch_bounds__(512, 1)
                                         dp[k] = 0.0f;
                                     }
                             }
+                            if constexpr (WIN) {  // queries whose window does not reach this key
+                                const uint32_t wb = window_bits32(g.window, kv_loc, qb + c * 32);
+                                window_fill32(x, wb, 0.0f);
+                                window_fill32(dp, wb, 0.0f);
+                            }
                             if constexpr (ACT) {
                                 uint32_t w[32];
                                 pack_hilo32(x, w);
@@ -970,24 +978,36 @@ __global__ void __launch_bounds__(512, 1)
 // ============================================================================
 // launchers
 // ============================================================================
-template <int D, bool ACT, int BIAS>
-static cudaError_t launch_dq_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+template <int D, bool ACT, int BIAS, bool WIN>
+static cudaError_t launch_dq_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = DqCfg<D, ACT, BIAS>;
     static bool done[64] = {};
-    cudaError_t e = ensure_smem(dq_kernel<D, ACT, BIAS>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(dq_kernel<D, ACT, BIAS, WIN>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    dq_kernel<D, ACT, BIAS><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    dq_kernel<D, ACT, BIAS, WIN><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    return cudaGetLastError();
+}
+
+template <int D, bool ACT, int BIAS, bool WIN>
+static cudaError_t launch_dkdv_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    using C = DkvCfg<D, ACT, BIAS>;
+    static bool done[64] = {};
+    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN>, C::SMEM_ALLOC, done);
+    if (e != cudaSuccess || n_ctas <= 0) return e;
+    dkdv_kernel<D, ACT, BIAS, WIN><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 
 template <int D, bool ACT, int BIAS>
+static cudaError_t launch_dq_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    return a.g.window > 0 ? launch_dq_w<D, ACT, BIAS, true>(tm, a, n_ctas, st)
+                          : launch_dq_w<D, ACT, BIAS, false>(tm, a, n_ctas, st);
+}
+
+template <int D, bool ACT, int BIAS>
 static cudaError_t launch_dkdv_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
-    using C = DkvCfg<D, ACT, BIAS>;
-    static bool done[64] = {};
-    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS>, C::SMEM_ALLOC, done);
-    if (e != cudaSuccess || n_ctas <= 0) return e;
-    dkdv_kernel<D, ACT, BIAS><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
-    return cudaGetLastError();
+    return a.g.window > 0 ? launch_dkdv_w<D, ACT, BIAS, true>(tm, a, n_ctas, st)
+                          : launch_dkdv_w<D, ACT, BIAS, false>(tm, a, n_ctas, st);
 }
 
 static int bias_form(const Geom &g) {

@@ -48,6 +48,7 @@ struct Geom {
     int32_t Tq, Tk;
     int32_t act;
     int32_t block;            // 0 or 64
+    int32_t window;           // 0, or W > 0: keys with |i - j| < W only (local positions)
     int32_t nb;               // bias buckets, 0 = none
     float scale;              // score scale
     const float *bias;        // [H, nb] or nullptr

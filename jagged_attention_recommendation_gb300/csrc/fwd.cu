@@ -96,11 +96,14 @@ struct FwdCfg {
     static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
-template <int D, bool ACT, int BIAS>
+// WIN: sliding window on (a compile-time switch, so that kernels without one
+// carry no band test in their softmax passes)
+template <int D, bool ACT, int BIAS, bool WIN>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
     using C = FwdCfg<D, ACT, BIAS>;
+    const int win = WIN ? a.g.window : 0;  // |i - j| < win, 0 = no window
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -383,9 +386,11 @@ __global__ void __launch_bounds__(512, 1)
                 // holds the scores between passes.
                 const int nvalid = min(C::BN, t.kv_len - j * C::BN);
                 const int kvb = t.kv_loc0 + j * C::BN;
-                // chunk c holds keys this row may see (block mode: its own 64-block)
+                // chunk c holds keys this row may see (block mode: its own 64-block;
+                // sliding window: some row of this warp has the chunk in its band)
                 auto live = [&](int c) {
-                    return c * 32 < nvalid && (g.block == 0 || ((c * 32) >> 6) == (row >> 6));
+                    return c * 32 < nvalid && (g.block == 0 || ((c * 32) >> 6) == (row >> 6)) &&
+                           window_chunk_live(win, t.q_loc0 + quad * 32, kvb + c * 32);
                 };
                 // scores of chunk c with scale, bias and key mask (softmax: log2 units;
                 // without a bias the scale waits for the exponent's FMA)
@@ -406,6 +411,8 @@ __global__ void __launch_bounds__(512, 1)
                         for (int i = 0; i < 32; ++i)
                             if (c * 32 + i >= nvalid) xc[i] = ACT ? 0.0f : -INFINITY;
                     }
+                    // keys outside the row's window (activation: act(0) = 0)
+                    if constexpr (WIN) window_fill32(xc, window_bits32(win, q_loc, kvb + c * 32), ACT ? 0.0f : -INFINITY);
                 };
 
                 if constexpr (!ACT) {
@@ -466,6 +473,7 @@ __global__ void __launch_bounds__(512, 1)
                                 for (int i = 0; i < 32; ++i)
                                     if (c * 32 + i >= nvalid) xc[i] = 0.0f;
                             }
+                            if constexpr (WIN && !scaled) window_fill32(xc, window_bits32(win, q_loc, kvb + c * 32), 0.0f);
                             rs += sum32(xc);
 #pragma unroll
                             for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(xc[2 * i], xc[2 * i + 1]);
@@ -633,15 +641,21 @@ __global__ void __launch_bounds__(512, 1)
     }
 }
 
-template <int D, bool ACT, int BIAS>
-static cudaError_t launch_fwd_t(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
+template <int D, bool ACT, int BIAS, bool WIN>
+static cudaError_t launch_fwd_w(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
     using C = FwdCfg<D, ACT, BIAS>;
-    auto kern = fwd_kernel<D, ACT, BIAS>;
+    auto kern = fwd_kernel<D, ACT, BIAS, WIN>;
     static bool done[64] = {};
     cudaError_t e = ensure_smem(kern, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
     kern<<<n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(tm.q, tm.k, tm.v, a);
     return cudaGetLastError();
+}
+
+template <int D, bool ACT, int BIAS>
+static cudaError_t launch_fwd_t(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
+    return a.g.window > 0 ? launch_fwd_w<D, ACT, BIAS, true>(tm, a, n_ctas, stream)
+                          : launch_fwd_w<D, ACT, BIAS, false>(tm, a, n_ctas, stream);
 }
 
 template <int D, bool ACT>

@@ -17,6 +17,11 @@ ones; the tile shape and record layout below are this library's reading:
     full attention : one record per 128-row key tile of every sequence with
                      Lk > 0, spanning all of that sequence's queries (q_len may be 0)
     block attention: empty (its backward runs on the query-major list)
+  sliding window W (section "BlockAttention": off-window tiles are skipped):
+    the same records, each one's other range cut to the band |i - j| < W of
+    its rows: a query tile [s, s + n) keeps keys [s - W + 1, s + n + W - 1)
+    clipped to the sequence, and a key tile keeps queries likewise (the range
+    may become empty; the record stays, so its rows are still written)
 """
 from __future__ import annotations
 
@@ -26,7 +31,14 @@ TILE_Q = 128
 TILE_KV = 128
 
 
-def q_major(q_off, kv_off, H: int, block: int = 0) -> np.ndarray:
+def _band(s: int, n: int, L: int, window: int):
+    """Positions of the other side within the window of rows [s, s + n)."""
+    lo = min(L, max(0, s - window + 1))
+    hi = min(L, s + n + window - 1)
+    return lo, max(hi, lo)  # empty when nothing is in reach, still inside the sequence
+
+
+def q_major(q_off, kv_off, H: int, block: int = 0, window: int = 0) -> np.ndarray:
     out = []
     B = len(q_off) - 1
     for b in range(B):
@@ -38,13 +50,16 @@ def q_major(q_off, kv_off, H: int, block: int = 0) -> np.ndarray:
             for h in range(H):
                 if block:
                     out.append((b, h, q0 + t * TILE_Q, ql, k0 + t * TILE_Q, ql))
+                elif window:
+                    lo, hi = _band(t * TILE_Q, ql, Lk, window)
+                    out.append((b, h, q0 + t * TILE_Q, ql, k0 + lo, hi - lo))
                 else:
                     out.append((b, h, q0 + t * TILE_Q, ql, k0, Lk))
             t += 1
     return np.array(out, dtype=np.int32).reshape(-1, 6)
 
 
-def kv_major(q_off, kv_off, H: int, block: int = 0) -> np.ndarray:
+def kv_major(q_off, kv_off, H: int, block: int = 0, window: int = 0) -> np.ndarray:
     out = []
     if block:
         return np.zeros((0, 6), dtype=np.int32)
@@ -56,16 +71,25 @@ def kv_major(q_off, kv_off, H: int, block: int = 0) -> np.ndarray:
         while t * TILE_KV < Lk:
             kl = min(TILE_KV, Lk - t * TILE_KV)
             for h in range(H):
-                out.append((b, h, q0, Lq, k0 + t * TILE_KV, kl))
+                if window:
+                    lo, hi = _band(t * TILE_KV, kl, Lq, window)
+                    out.append((b, h, q0 + lo, hi - lo, k0 + t * TILE_KV, kl))
+                else:
+                    out.append((b, h, q0, Lq, k0 + t * TILE_KV, kl))
             t += 1
     return np.array(out, dtype=np.int32).reshape(-1, 6)
 
 
-def covered_pairs(tiles: np.ndarray, block: int = 0) -> int:
-    """Number of valid (i, j) pairs the tiles cover, summed over heads."""
+def covered_pairs(tiles: np.ndarray, block: int = 0, window: int = 0, q_off=None, kv_off=None) -> int:
+    """Number of valid (i, j) pairs the tiles cover, summed over heads
+    (window: pairs inside the band, positions local via the offsets)."""
     total = 0
     for (b, h, qs, ql, ks, kl) in tiles.tolist():
-        if block:
+        if window:
+            i = np.arange(qs - int(q_off[b]), qs - int(q_off[b]) + ql).reshape(-1, 1)
+            j = np.arange(ks - int(kv_off[b]), ks - int(kv_off[b]) + kl).reshape(1, -1)
+            total += int((np.abs(i - j) < window).sum())
+        elif block:
             for base in range(0, ql, block):
                 n = min(block, ql - base)
                 total += n * n

@@ -45,11 +45,11 @@ def canonical(t):
     return t[np.lexsort((t[:, 1], t[:, 2], t[:, 4], t[:, 0]))] if len(t) else t
 
 
-def check_plan(qo, ko, H, D=128, block=0, act=0):
-    p = J.Plan(qo, ko, H, D, act=act, block=block, device=-1)
+def check_plan(qo, ko, H, D=128, block=0, act=0, window=0):
+    p = J.Plan(qo, ko, H, D, act=act, block=block, device=-1, window=window)
     for which, fn in ((J.TILES_Q, T.q_major), (J.TILES_KV, T.kv_major)):
         tiles, cta = p.tiles(which)
-        want = fn(qo, ko, H, block)
+        want = fn(qo, ko, H, block, window)
         assert tiles.dtype == np.int32 and tiles.shape == want.shape
         np.testing.assert_array_equal(canonical(tiles), canonical(want))
         # schedule: per-CTA contiguous ranges covering every tile once
@@ -68,6 +68,12 @@ def test_planner_matches_enumerator(lib, lens, H, block):
     lq, lk = lens
     lk = lq if lk is None else lk
     check_plan(W.offsets(np.array(lq)), W.offsets(np.array(lk)), H, block=block)
+
+
+@pytest.mark.parametrize("window", [1, 64, 257])
+def test_planner_matches_enumerator_with_window(lib, window):
+    lq, lk = [1, 128, 129, 0, 300, 900], [5, 0, 256, 7, 1, 900]
+    check_plan(W.offsets(np.array(lq)), W.offsets(np.array(lk)), 3, window=window)
 
 
 @pytest.mark.parametrize("wid", [2, 3, 4, 5])
@@ -96,10 +102,10 @@ def test_plan_update_replans(lib):
     np.testing.assert_array_equal(canonical(tiles), canonical(T.q_major(qo, qo, 2)))
 
 
-def create(lib, qo, ko, H=2, D=64, act=0, block=0, nb=0, dtype=0, scale=0.0, device=-1):
+def create(lib, qo, ko, H=2, D=64, act=0, block=0, nb=0, dtype=0, scale=0.0, device=-1, window=0):
     qo = np.ascontiguousarray(qo, dtype=np.int32)
     ko = np.ascontiguousarray(ko, dtype=np.int32)
-    m = J.Mode(act, block, scale, nb, dtype)
+    m = J.Mode(act, block, scale, nb, dtype, window)
     h = ctypes.c_void_p()
     rc = lib.jattn_plan_create(qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p), len(qo) - 1,
                                H, D, ctypes.byref(m), device, ctypes.byref(h))
@@ -124,6 +130,9 @@ def test_error_codes(lib):
     assert create(lib, ok, ok, H=8, nb=64) == J.ERR_UNSUPPORTED     # bias table larger than staged maximum
     assert create(lib, ok, ok, scale=-1.0) == J.ERR_INVALID_ARG
     assert create(lib, ok, ok, device=-2) == J.ERR_INVALID_ARG
+    assert create(lib, ok, ok, window=-1) == J.ERR_INVALID_ARG
+    assert create(lib, ok, ok, block=64, window=8) == J.ERR_INVALID_ARG   # window and block exclude each other
+    assert create(lib, ok, ok, window=8) == J.OK
 
 
 def test_host_only_plan_refuses_compute(lib):

@@ -53,6 +53,28 @@ def test_parity_small(case):
     PT.compare(gpu, ref)
 
 
+# sliding window W (|i - j| < W): (name, lq, lk, H, D, bias_buckets, act, W)
+WINDOW_CASES = [
+    ("win_self_d128", [1, 127, 128, 129, 300, 700], None, 2, 128, 0, SOFTMAX, 100),
+    ("win_self_bias", [45, 200, 129, 390], None, 4, 128, 64, SOFTMAX, 33),
+    ("win_one", [5, 130, 257], None, 2, 64, 0, SOFTMAX, 1),
+    ("win_cross_empty_rows", [200, 35, 129], [8, 64, 300], 2, 128, 0, SOFTMAX, 20),
+    ("win_silu", [300, 40], [500, 40], 2, 128, 0, SILU, 64),
+    ("win_gelu_d64_bias", [150, 300], [150, 300], 2, 64, 8, GELU, 128),
+    ("win_wider_than_all", [100, 300], None, 2, 128, 0, SOFTMAX, 5000),
+]
+
+
+@pytest.mark.parametrize("case", WINDOW_CASES, ids=[c[0] for c in WINDOW_CASES])
+def test_parity_window(case):
+    name, lq, lk, H, D, nb, act, win = case
+    lk = lq if lk is None else lk
+    bt = W.random_batch(zlib.crc32(name.encode()) % 10000, lq, lk, H, D, dtype=torch.bfloat16, bias_buckets=nb)
+    gpu = PT.run_library(bt, act=act, window=win)
+    ref = PT.run_oracle(bt, act=act, window=win)
+    PT.compare(gpu, ref)
+
+
 def test_tiny_workload_fp32():
     """The tiny fp32 workload, exactly as drawn (B=4, H=2, D=32)."""
     b = W.make_batch(1)

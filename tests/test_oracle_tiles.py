@@ -72,3 +72,28 @@ def test_total_pair_identity(wid):
     assert T.covered_pairs(T.q_major(qo, ko, w.H, w.block), w.block) == want
     if not w.block:
         assert T.covered_pairs(T.kv_major(qo, ko, w.H), 0) == want
+
+
+@pytest.mark.parametrize("window", [1, 50, 200])
+def test_window_tiles_cover_exactly_the_band(window):
+    """Sliding window: every in-band pair (|i - j| < W) is covered by exactly one
+    query-major and one key-major record, and the ranges are tight (the first
+    and last key of each query tile's range are inside some row's band)."""
+    lq, lk = [1, 128, 129, 300, 0, 700], [5, 130, 129, 300, 9, 40]
+    qo, ko = W.offsets(np.array(lq)), W.offsets(np.array(lk))
+    want = 0
+    for a, b in zip(lq, lk):
+        i, j = np.arange(a).reshape(-1, 1), np.arange(b).reshape(1, -1)
+        want += int((np.abs(i - j) < window).sum())
+    for fn in (T.q_major, T.kv_major):
+        tl = fn(qo, ko, 2, 0, window)
+        assert T.covered_pairs(tl, 0, window, qo, ko) == 2 * want
+        for (b, h, qs, ql, ks, kl) in tl.tolist():  # every range inside its own sequence
+            assert qo[b] <= qs and qs + ql <= qo[b + 1] and ko[b] <= ks and ks + kl <= ko[b + 1]
+    for (b, h, qs, ql, ks, kl) in T.q_major(qo, ko, 1, 0, window).tolist():
+        if kl == 0:
+            continue
+        i0, j0 = qs - qo[b], ks - ko[b]
+        assert i0 - j0 < window and (j0 + kl - 1) - (i0 + ql - 1) < window   # both ends in some row's band
+        assert j0 == 0 or i0 - (j0 - 1) >= window                            # one key earlier is out of band
+        assert j0 + kl == lk[b] or (j0 + kl) - (i0 + ql - 1) >= window        # one key later is out of band
