@@ -18,6 +18,7 @@ fp64 CPU oracle instead (rank 0 only), on a bounded sample of the same batch.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import subprocess
@@ -56,8 +57,9 @@ def dist_env():
 def workload_config(w: W.Workload, act: int, Bn: int, flush: bool, ws: int = 1, global_B=None) -> dict:
     return {"workload": "%s (B=%d, H=%d, D=%d, %s%s%s)" % (
         w.name, Bn, w.H, w.D, W.ACT_NAMES[act], ", rel-pos bias %d buckets" % w.bias_buckets if w.bias_buckets
-        else "", ", block %d" % w.block if w.block else ""),
+        else "", ", block %d" % w.block if w.block else "") + (", sliding window %d" % w.window if w.window else ""),
         "B": Bn, "H": w.H, "D": w.D, "act": W.ACT_NAMES[act], "block": w.block, "bias_buckets": w.bias_buckets,
+        "window": w.window,
         "input_dtype": w.dtype, "l2": "flushed between timed steps (256 MiB write)" if flush else "not flushed",
         "parallelism": ("single GPU" if ws == 1 else
                         "dp%d: %d sequences split across ranks by cost (jattn_shard), no collective" % (ws, global_B))}
@@ -148,14 +150,14 @@ def time_oracle(batch: W.Batch, frac: float, seed: int = 0):
     nthreads = oracle.default_threads()
     t0 = time.perf_counter()
     oracle.forward(qo, ko, q, k, v, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
-                   nthreads=nthreads)
+                   nthreads=nthreads, window=w.window)
     oracle.backward(qo, ko, q, k, v, dout, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
-                    nthreads=nthreads)
+                    nthreads=nthreads, window=w.window)
     dt = time.perf_counter() - t0
-    f, b = W.flops(qo, ko, w.H, w.D, w.block)
+    f, b = W.flops(qo, ko, w.H, w.D, w.block, w.window)
     desc = "%d of %d sequences (seeded), %.1f%% of the valid pairs" % (
-        len(seqs), batch.B, 100.0 * W.valid_pairs(qo, ko, w.block) / max(W.valid_pairs(batch.q_off, batch.kv_off,
-                                                                                          w.block), 1))
+        len(seqs), batch.B, 100.0 * W.valid_pairs(qo, ko, w.block, w.window) /
+        max(W.valid_pairs(batch.q_off, batch.kv_off, w.block, w.window), 1))
     return (f + b) / dt / 1e12, dt, nthreads, desc
 
 
@@ -218,7 +220,7 @@ KERNELS_BLOCK = ["fwd", "bwd_block"]
 def kernel_work(w, batch, name, pk):
     """Algorithmic (flops, bytes) of one launch of `name` over the batch."""
     H, D = w.H, w.D
-    p = W.valid_pairs(batch.q_off, batch.kv_off, w.block)
+    p = W.valid_pairs(batch.q_off, batch.kv_off, w.block, w.window)
     Tq, Tk = batch.Tq, batch.Tk
     e = H * D * 2
     if name == "fwd":
@@ -254,6 +256,7 @@ def run_ours(args, w, batch):
     q, k, v, dout = (t.to(dev) for t in (batch.q, batch.k, batch.v, batch.dout))
     bias = batch.bias.to(dev) if batch.bias is not None else None
     plan = J.Plan(batch.q_off, batch.kv_off, H, D, act=batch.act, block=w.block, bias_buckets=w.bias_buckets,
+                  window=w.window,
                   dtype="fp32" if f32 else "bf16", device=local)
     out = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
     lse = torch.empty(H, batch.Tq, dtype=torch.float32, device=dev) if batch.act == W.SOFTMAX else None
@@ -333,7 +336,7 @@ def run_ours(args, w, batch):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
 
-    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block)
+    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block, w.window)
     total_flops = args.global_flops if args.global_flops is not None else ws * (f_fwd + f_bwd)
     value = total_flops / (ms * 1e-3) / 1e12
     pk, pk_kind = peaks()
@@ -476,7 +479,7 @@ def run_e2e(args, w, batch, plan, dev, stream):
     if st != 0:
         raise RuntimeError("device status after the end-to-end steps: " + J.status_str(st))
     ms = e0.elapsed_time(e1) / n
-    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block)
+    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block, w.window)
     return {"value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
 
@@ -494,6 +497,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window W (keys with |i - j| < W) on the chosen workload; 0 = off")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -511,10 +516,14 @@ def main():
         qo, ko = W.offsets(lq), W.offsets(lk)
         mine = np.nonzero(J.shard(qo, ko, ws) == rank)[0]
         batch = W.make_batch(args.workload, act=act, lens=(lq[mine], lk[mine]))
-        args.global_flops = float(sum(W.flops(qo, ko, w.H, w.D, w.block)))
+        args.global_flops = float(sum(W.flops(qo, ko, w.H, w.D, w.block, args.window)))
         args.global_B = int(ws * w.B)
     else:
         batch = W.make_batch(args.workload, act=act)
+    if args.window:
+        if batch.w.block:
+            ap.error("--window does not combine with the block workload")
+        batch.w = dataclasses.replace(batch.w, window=args.window)
     if args.impl == "reference":
         run_reference(args, batch.w, batch)
     else:

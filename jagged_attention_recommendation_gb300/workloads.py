@@ -48,6 +48,7 @@ class Workload:
     block: int               # 0 = full attention, 64 = BlockAttention
     bias_buckets: int        # 0 = no bias, else the table width (64)
     q_rows_shared: int = 0   # >0: that many query rows shared by every sample
+    window: int = 0          # >0: sliding window, keys with |i - j| < window only
 
 
 WORKLOADS = {
@@ -182,18 +183,24 @@ def random_batch(seed: int, lq, lk, H: int, D: int, dtype=torch.bfloat16, bias_b
 # Work accounting (valid tokens only; padding and recompute are not counted)
 # ---------------------------------------------------------------------------
 
-def valid_pairs(q_off: np.ndarray, kv_off: np.ndarray, block: int = 0) -> int:
-    lq = np.diff(q_off.astype(np.int64))
-    lk = np.diff(kv_off.astype(np.int64))
+def valid_pairs(q_off: np.ndarray, kv_off: np.ndarray, block: int = 0, window: int = 0) -> int:
+    lq = np.diff(np.asarray(q_off).astype(np.int64))
+    lk = np.diff(np.asarray(kv_off).astype(np.int64))
+    if window:
+        total = 0
+        for a, b in zip(lq.tolist(), lk.tolist()):
+            i = np.arange(a, dtype=np.int64)
+            total += int(np.clip(np.minimum(b, i + window) - np.maximum(0, i - window + 1), 0, None).sum())
+        return total
     if block:
         full, rem = lq // block, lq % block
         return int((full * block * block + rem * rem).sum())
     return int((lq * lk).sum())
 
 
-def flops(q_off, kv_off, H: int, D: int, block: int = 0) -> tuple[float, float]:
+def flops(q_off, kv_off, H: int, D: int, block: int = 0, window: int = 0) -> tuple[float, float]:
     """(forward, backward) FLOPs: 4*D*H*pairs and 10*D*H*pairs."""
-    p = valid_pairs(q_off, kv_off, block)
+    p = valid_pairs(q_off, kv_off, block, window)
     return 4.0 * D * H * p, 10.0 * D * H * p
 
 
