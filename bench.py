@@ -191,8 +191,8 @@ def run_reference(args, w, batch):
 # record whose sources have changed since is reported as null.
 NCU_TRAFFIC = {
     (2, "fwd"): (269.32e6, ("fwd.cu",), "93875a3dd84160d7"),
-    (2, "bwd_dq"): (348.49e6, ("bwd.cu",), "c7446a8ff30d5974"),
-    (2, "bwd_dkdv"): (409.35e6, ("bwd.cu",), "c7446a8ff30d5974"),
+    (2, "bwd_dq"): (348.49e6, ("bwd.cu", "bwd_common.cuh"), "c7446a8ff30d5974"),
+    (2, "bwd_dkdv"): (409.35e6, ("bwd_dkdv.cu", "bwd_common.cuh"), "c7446a8ff30d5974"),
     (2, "bwd_delta"): (137.70e6, ("aux.cu",), "8a692c27b0da4f35"),
 }
 

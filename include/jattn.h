@@ -151,9 +151,14 @@ jattn_status jattn_fwd(const jattn_plan *plan, const void *q, const void *k, con
  * Backward.  dout, q, k, v, out: DEVICE inputs (out = the forward output);
  * lse: the forward's lse (required in full softmax mode, ignored otherwise);
  * dq, dk, dv: DEVICE outputs, fully overwritten (no accumulation, no atomics);
- * dbias: DEVICE float32 [H, NB] gradient of the bias table, written when non-NULL
- * (needs a bias); workspace: DEVICE scratch of jattn_bwd_workspace_bytes.
- * dq and dk include the score scale; dbias is the plain sum of dS per bucket.
+ * dbias: DEVICE float32 [H, NB] gradient of the bias table, overwritten when
+ * non-NULL (needs a bias; full attention and sliding window only: with block
+ * mode the call returns JATTN_ERR_UNSUPPORTED); workspace: DEVICE scratch of
+ * jattn_bwd_workspace_bytes.
+ * dq and dk include the score scale; dbias[h, n] is the plain sum of dS over
+ * the pairs of head h in bucket n = min(|i - j|, NB - 1). It is summed with
+ * floating-point atomic adds, so it is reproducible to rounding only (dq, dk
+ * and dv are bitwise reproducible).
  */
 jattn_status jattn_bwd(const jattn_plan *plan, const void *dout, const void *q, const void *k, const void *v,
                        const float *bias, const void *out, const float *lse, void *dq, void *dk, void *dv,

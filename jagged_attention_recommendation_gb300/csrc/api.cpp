@@ -550,7 +550,9 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
     if (!dout || !q || !k || !v || !out || !dq || !dk || !dv) return JATTN_ERR_INVALID_ARG;
     if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;
     if (softmax_full(p) && lse == nullptr) return JATTN_ERR_INVALID_ARG;
-    if (dbias != nullptr) return bias == nullptr ? JATTN_ERR_INVALID_ARG : JATTN_ERR_UNSUPPORTED;
+    if (dbias != nullptr && bias == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (dbias != nullptr && p->mode.block != 0) return JATTN_ERR_UNSUPPORTED;
+    if (dbias != nullptr && !aligned16(dbias)) return JATTN_ERR_ALIGNMENT;
     if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
         !aligned16(dk) || !aligned16(dv) || !aligned16(bias) || !aligned16(lse))
         return JATTN_ERR_ALIGNMENT;
@@ -591,6 +593,7 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
     a.dq = out_desc(p, dq);
     a.dk = out_desc(p, dk);
     a.dv = out_desc(p, dv);
+    a.dbias = dbias;
     TmapSet tm;
     if (p->mode.block != 0) {
         if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
@@ -613,6 +616,12 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
         return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
     a.g = make_geom(p, JATTN_TILES_Q);
     a.g.bias = bias;
+    if (dbias != nullptr) {  // the dQ pass adds every pair's dS into it
+        jattn_status e = cuda_status(
+            cudaMemsetAsync(dbias, 0, static_cast<size_t>(p->H) * p->mode.bias_buckets * sizeof(float), st),
+            "jattn_bwd: dbias zero fill");
+        if (e != JATTN_OK) return e;
+    }
     {
         jattn_status e = cuda_status(log.done(launch_bwd_dq(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
                                      "jattn_bwd: dQ kernel launch");

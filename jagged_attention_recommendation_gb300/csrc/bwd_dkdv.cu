@@ -1,0 +1,538 @@
+// bwd_dkdv.cu -- jagged attention backward, pass 2 (dK, dV over key-major
+// tiles); the layout, the roles and the reasoning behind them are described at
+// the top of bwd.cu (pass 1, dQ), which shares this file's helpers through
+// bwd_common.cuh.
+#include "bwd_common.cuh"
+
+namespace jattn {
+using namespace dev;
+namespace {
+// ============================================================================
+// pass 2: dK, dV
+// ============================================================================
+template <int D, bool ACT, int BIAS>
+struct DkvCfg {
+    static constexpr int BKV = 128, BQ = 64;
+    static constexpr int NKB = D / 64;
+    static constexpr int NSQ = (D == 64) ? 6 : 4;   // Q / dO / lse / Delta ring
+    static constexpr uint32_t SUB_KV = BKV * 128;  // 16 KB
+    static constexpr uint32_t SUB_Q = BQ * 128;    // 8 KB
+    static constexpr uint32_t KV_BYTES = BKV * D * 2;
+    static constexpr uint32_t Q_BYTES = BQ * D * 2;
+    static constexpr uint32_t OFF_K = 0;
+    static constexpr uint32_t OFF_V = KV_BYTES;
+    static constexpr uint32_t OFF_Q = 2 * KV_BYTES;  // [NSQ][Q | dO]
+    static constexpr uint32_t OFF_LD = OFF_Q + NSQ * 2 * Q_BYTES;  // [NSQ][-lse log2 e | -Delta][64] floats
+    static constexpr uint32_t OFF_BAR = OFF_LD + NSQ * 2 * BQ * 4;
+    // kv_full, kv_empty, qs_full[NSQ], qs_empty[NSQ], st_full[2], p_full[2], acc_full, acc_empty,
+    // acc_done[2], drain[2]
+    static constexpr int NBAR = 2 + 2 * NSQ + 4 + 2 + 2 + 2;
+    static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+    static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
+    static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
+    // per output warp: 32 rows x 64 bf16 staging for row-contiguous stores
+    static constexpr int STG_W = 64;
+    static constexpr uint32_t OFF_STG = (OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0) + 127) & ~127u;
+    static constexpr uint32_t SMEM = OFF_STG + 4 * 32 * STG_W * 2;
+    static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    // group g: S^T at 128 g (P^T over it), dP^T at 128 g + 64 (dS^T over it); dV, dK
+    static constexpr uint32_t COL_DV = 256;
+    static constexpr uint32_t COL_DK = 256 + D;
+    static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+    static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "operand alignment");
+    static_assert(OFF_STG % 16 == 0, "16-byte shared-memory vectors");
+    static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+};
+
+template <int D, bool ACT, int BIAS, bool WIN>
+__global__ void __launch_bounds__(512, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
+    using C = DkvCfg<D, ACT, BIAS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = align1024(smem_raw);
+    const Geom &g = a.g;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *kv_full = bars + 0;
+    uint64_t *kv_empty = bars + 1;
+    uint64_t *qs_full = bars + 2;
+    uint64_t *qs_empty = qs_full + C::NSQ;
+    uint64_t *st_full = qs_empty + C::NSQ;  // [2] per compute group
+    uint64_t *p_full = st_full + 2;         // [2] per compute group
+    uint64_t *acc_full = p_full + 2;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *acc_done = acc_empty + 1;  // [2] per compute group: its block's dV / dK products finished
+    uint64_t *drain = acc_done + 2;      // [2] per MMA-issuing thread
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+    float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
+    float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
+    float *sLD = reinterpret_cast<float *>(smem + C::OFF_LD);
+    const uint32_t sK = smem_u32(smem + C::OFF_K);
+    const uint32_t sV = smem_u32(smem + C::OFF_V);
+    const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+
+    if (threadIdx.x == 0) {
+        mbar_init(kv_full, 1);
+        mbar_init(kv_empty, 1);
+        for (int s = 0; s < C::NSQ; ++s) {
+            mbar_init(&qs_full[s], 1);
+            mbar_init(&qs_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&st_full[b], 1);
+            mbar_init(&p_full[b], 4);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&acc_done[b], 1);
+            mbar_init(&drain[b], 1);
+        }
+        *abort_flag = 0;
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (BIAS == kBiasTable) stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
+    if (BIAS == kBiasExt) stage_bias_ext(g, sext, ACT ? 1.0f : kLog2e);
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmDO);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const ErrCtx err{g.status, abort_flag};
+    const int tbeg = g.cta_begin[blockIdx.x];
+    const int tend = g.cta_begin[blockIdx.x + 1];
+
+    const int wgi = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 7, 0);
+    if (wgi == 0) {
+        regs_release<kRegCtrl>();
+        if (warp == 0) {
+            // -------------------------------------------------------- Q / dO producer
+            // lane 0 issues the copies; all lanes first write lse / Delta of the
+            // block's queries (negated, lse in log2 units) into the stage's slot.
+            uint32_t q_it = 0;
+            bool ok = true;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, lane == 0)) continue;
+                const int nq = cdiv(t.q_len, C::BQ);
+                for (int i = 0; i < nq; ++i, ++q_it) {
+                    const uint32_t slot = q_it % C::NSQ, use = q_it / C::NSQ;
+                    if (!(ok = mbar_wait_warp(&qs_empty[slot], (use & 1) ^ 1, err))) break;
+                    if (!ACT) {
+                        float *ld = sLD + slot * 2 * C::BQ;
+                        for (int k = lane; k < C::BQ; k += 32) {
+                            const int qi = i * C::BQ + k;
+                            float l2 = 0.0f, dl = 0.0f;
+                            if (qi < t.q_len) {
+                                const int64_t idx = static_cast<int64_t>(t.h) * g.Tq + t.q_start + qi;
+                                l2 = -a.lse[idx] * kLog2e;
+                                dl = -a.delta[idx];
+                            }
+                            ld[k] = l2;
+                            ld[C::BQ + k] = dl;
+                        }
+                        __syncwarp();
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&qs_full[slot], 2 * C::Q_BYTES);
+                        const int y = t.q_start + i * C::BQ;
+                        uint8_t *base = smem + C::OFF_Q + slot * 2 * C::Q_BYTES;
+                        for (int kb = 0; kb < C::NKB; ++kb) {
+                            tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qs_full[slot], t.h * D + kb * 64, y);
+                            tma_load_2d(base + C::Q_BYTES + kb * C::SUB_Q, &tmDO, &qs_full[slot], t.h * D + kb * 64,
+                                        y);
+                        }
+                    }
+                }
+            }
+            if (!ok && lane == 0) {
+                for (uint32_t s = 0; s < C::NSQ && s < q_it; ++s) {
+                    const uint32_t last = q_it - 1 - ((q_it - 1 - s) % C::NSQ);
+                    mbar_drain(&qs_full[last % C::NSQ], (last / C::NSQ) & 1);
+                }
+            }
+        } else if (warp == 2 && lane == 0) {
+            // -------------------------------------------------------- K / V producer
+            // one buffer: the tile's K and V are last read by its final S^T / dP^T,
+            // two blocks before the tile ends, so the next tile's rows load early
+            uint32_t t_local = 0;
+            bool ok = true;
+            TileStream ts(g, tbeg, tend);
+            Tile t;
+            while (ok && ts.next(t)) {
+                if (!check_tile(g, t, err, false)) continue;
+                if (!(ok = mbar_wait(kv_empty, (t_local & 1) ^ 1, err))) break;
+                ++t_local;
+                mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+                for (int kb = 0; kb < C::NKB; ++kb) {
+                    tma_load_2d(smem + C::OFF_K + kb * C::SUB_KV, &tmK, kv_full, t.h * D + kb * 64, t.kv_start);
+                    tma_load_2d(smem + C::OFF_V + kb * C::SUB_KV, &tmV, kv_full, t.h * D + kb * 64, t.kv_start);
+                }
+            }
+            if (!ok && t_local > 0) mbar_drain(kv_full, (t_local - 1) & 1);
+        } else if (warp == 3 && lane == 0) {
+            // -------------------------------------------------------- S^T / dP^T issuer
+            // Two issuing threads keep the tensor pipe fed: a thread's own waits
+            // (any shared-memory access) stall its queued MMAs, so this thread
+            // issues every S^T = K Q^T and dP^T = V dO^T and the other every
+            // dV / dK product.  Block n (the CTA's blocks in order, across tiles)
+            // reuses the TMEM columns of block n - 2, its compute group's previous
+            // block, once that block's dV / dK products have finished.
+            bool ok = true;
+            TileStream tsa(g, tbeg, tend);
+            Tile ta;
+            uint32_t ta_n = 0, ns = 0;
+            const uint64_t dk0 = sdesc_sw128(sK, 16, 1024), dv0 = sdesc_sw128(sV, 16, 1024);
+            while (ok && tsa.next(ta)) {
+                if (!check_tile(g, ta, err, false)) continue;
+                const int na = cdiv(ta.q_len, C::BQ);
+                if (!(ok = mbar_wait(kv_full, ta_n & 1, err))) break;
+                for (int ia = 0; ia < na; ++ia, ++ns) {
+                    const uint32_t grp = ns & 1;
+                    if (ns >= 2 && !(ok = mbar_wait(&acc_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t slot = ns % C::NSQ;
+                    if (!(ok = mbar_wait(&qs_full[slot], (ns / C::NSQ) & 1, err))) break;
+                    tc_fence_after();
+                    const int ncols = round_up16(min(C::BQ, ta.q_len - ia * C::BQ));
+                    const uint32_t idesc = idesc_bf16(128, ncols, false, false);
+                    const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
+                    const uint64_t dqq = sdesc_sw128(qb, 16, 1024), ddo = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
+                    const uint32_t dS = tmem + grp * 128, dDP = dS + 64;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t ao = (k >> 2) * C::SUB_KV + (k & 3) * 32;
+                        const uint32_t bo = (k >> 2) * C::SUB_Q + (k & 3) * 32;
+                        mma_bf16_ss(dS, sdesc_add(dk0, ao), sdesc_add(dqq, bo), idesc, k > 0);
+                        mma_bf16_ss(dDP, sdesc_add(dv0, ao), sdesc_add(ddo, bo), idesc, k > 0);
+                    }
+                    mma_commit(&st_full[grp]);
+                }
+                if (!ok) break;
+                mma_commit(kv_empty);  // the tile's last reads of K and V are in flight
+                ++ta_n;
+            }
+            // every MMA this thread issued is done before TMEM is released
+            mma_commit(&drain[0]);
+            mbar_drain(&drain[0], 0);
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------------- dV / dK issuer
+            // dV += P^T dO and dK += dS^T Q, P^T and dS^T (bf16; activation: hi and
+            // lo parts) read from TMEM; one thread, so the accumulation order is fixed.
+            const uint32_t idesc_acc = idesc_bf16(128, D, false, true);
+            bool ok = true;
+            TileStream tsb(g, tbeg, tend);
+            Tile tb;
+            uint32_t tb_n = 0, np = 0;
+            while (ok && tsb.next(tb)) {
+                if (!check_tile(g, tb, err, false)) continue;
+                const int nbq = cdiv(tb.q_len, C::BQ);
+                // the output group must have read dV / dK of the previous tile
+                if (!(ok = mbar_wait(acc_empty, (tb_n & 1) ^ 1, err))) break;
+                for (int ib = 0; ib < nbq; ++ib, ++np) {
+                    const uint32_t grp = np & 1;
+                    if (!(ok = mbar_wait(&p_full[grp], (np >> 1) & 1, err))) break;
+                    tc_fence_after();
+                    const int ksteps = round_up16(min(C::BQ, tb.q_len - ib * C::BQ)) / 16;
+                    const uint32_t slot = np % C::NSQ;
+                    const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
+                    const uint64_t bq0 = sdesc_sw128(qb, C::SUB_Q, 1024);
+                    const uint64_t bdo0 = sdesc_sw128(qb + C::Q_BYTES, C::SUB_Q, 1024);
+                    const uint32_t aP = tmem + grp * 128, aDS = aP + 64;
+                    for (int k = 0; k < ksteps; ++k) {
+                        const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
+                        const uint64_t bdo = sdesc_add(bdo0, k * 2048);
+                        const uint64_t bq = sdesc_add(bq0, k * 2048);
+                        if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
+                        } else {
+                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 8, bdo, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 8, bq, idesc_acc, acc);
+                        }
+                    }
+                    mma_commit(&qs_empty[slot]);  // last reads of the Q / dO slot
+                    mma_commit(&acc_done[grp]);   // the group's columns may take block np + 2
+                }
+                if (!ok) break;
+                mma_commit(acc_full);
+                ++tb_n;
+            }
+            mma_commit(&drain[1]);
+            mbar_drain(&drain[1], 0);
+        }
+    } else if (wgi < 3) {
+        regs_claim<kRegCompute>();
+        // ------------------------------------------------------------ compute groups
+        // One thread per key row (TMEM lane): P^T and dS^T of the group's query
+        // blocks, 32 queries at a time, written as bf16 over the block's S^T and
+        // dP^T columns (chunk c: columns 16c..16c+15, or 32c..32c+31 as hi / lo).
+        const int grp = wgi - 1;
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tS = tmem + lane_base + grp * 128, tDP = tS + 64;
+        const float sc = ACT ? g.scale : g.scale * kLog2e;
+        uint32_t s_it = 0, n0 = 0;
+        bool ok = true;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
+            const int nq = cdiv(t.q_len, C::BQ);
+            const float *bt = sbias + t.h * g.nb;
+            const float *ext_h = sext + t.h * ext_len(g.nb);
+            const int kv_loc = t.kv_loc0 + row;
+            const bool warp_live = quad * 32 < t.kv_len;
+            const int i0 = (grp - static_cast<int>(n0 & 1)) & 1;
+            auto blocks = [&](auto af) {
+                constexpr int AF = decltype(af)::value;
+                for (int i = i0; i < nq; i += 2) {
+                    if (!(ok = mbar_wait_warp(&st_full[grp], s_it & 1, err))) return;
+                    ++s_it;
+                    if (warp_live) {
+                        tc_fence_after();
+                        const int nvalid = min(C::BQ, t.q_len - i * C::BQ);
+                        const int qb = t.q_loc0 + i * C::BQ;
+                        // [-lse log2 e | -Delta] of the block's queries (shared by all rows)
+                        const float *ld = sLD + ((n0 + i) % C::NSQ) * 2 * C::BQ;
+#pragma unroll 1
+                        for (int c = 0; c < 2 && c * 32 < nvalid; ++c) {
+                            float x[32], dp[32];
+                            tmem_ld32x2(tS + 32 * c, tDP + 32 * c, x, dp);
+                            scale_bias_off32<BIAS>(x, sc, 0.0f, ext_h, bt, g.nb, kv_loc, qb + c * 32);
+                            if constexpr (ACT) {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) {
+                                    float pv;
+                                    dp[k] = act_bwd_t<AF>(x[k], pv) * dp[k];
+                                    x[k] = pv;
+                                }
+                            } else {
+                                const float4 *l4 = reinterpret_cast<const float4 *>(ld + c * 32);
+                                const float4 *d4 = reinterpret_cast<const float4 *>(ld + C::BQ + c * 32);
+#pragma unroll
+                                for (int k = 0; k < 8; ++k) {
+                                    const float4 lz = l4[k], dz = d4[k];
+                                    add2(x[4 * k], x[4 * k + 1], lz.x, lz.y);
+                                    add2(x[4 * k + 2], x[4 * k + 3], lz.z, lz.w);
+                                    add2(dp[4 * k], dp[4 * k + 1], dz.x, dz.y);
+                                    add2(dp[4 * k + 2], dp[4 * k + 3], dz.z, dz.w);
+                                }
+#pragma unroll
+                                for (int k = 0; k < 32; ++k) x[k] = ex2_approx(x[k]);
+#pragma unroll
+                                for (int k = 0; k < 32; k += 2) mul2(dp[k], dp[k + 1], x[k], x[k + 1]);
+                            }
+                            if (c * 32 + 32 > nvalid) {
+#pragma unroll
+                                for (int k = 0; k < 32; ++k)
+                                    if (c * 32 + k >= nvalid) {
+                                        x[k] = 0.0f;
+                                        dp[k] = 0.0f;
+                                    }
+                            }
+                            if constexpr (WIN) {  // queries whose window does not reach this key
+                                const uint32_t wb = window_bits32(g.window, kv_loc, qb + c * 32);
+                                window_fill32(x, wb, 0.0f);
+                                window_fill32(dp, wb, 0.0f);
+                            }
+                            if constexpr (ACT) {
+                                uint32_t w[32];
+                                pack_hilo32(x, w);
+                                tmem_st32_u32(tS + 32 * c, w);
+                                pack_hilo32(dp, w);
+                                tmem_st32_u32(tDP + 32 * c, w);
+                            } else {
+                                uint32_t w[16];
+                                pack16(x, w);
+                                tmem_st16_u32(tS + 16 * c, w);
+                                pack16(dp, w);
+                                tmem_st16_u32(tDP + 16 * c, w);
+                            }
+                        }
+                        tmem_wait_st();
+                        tc_fence_before();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&p_full[grp]);
+                }
+            };
+            if (!ACT || g.act == kSilu) {
+                blocks(std::integral_constant<int, kSilu>{});
+            } else {
+                blocks(std::integral_constant<int, kGeluTanh>{});
+            }
+            if (!ok) break;
+            n0 += nq;
+        }
+    } else {
+        regs_release<kRegOut>();
+        // ------------------------------------------------------------ output
+        // One thread per key row reads dV and dK (times the score scale) from
+        // TMEM.  bf16 outputs go out row-contiguous through the warp's staging
+        // buffer: dV is staged and dK packed into registers before the
+        // accumulators are handed back, so the next tile's products wait only
+        // for the TMEM reads, not for the stores.
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t tDV = tmem + lane_base + C::COL_DV, tDK = tmem + lane_base + C::COL_DK;
+        constexpr int W = C::STG_W;
+        const uint32_t stg = smem_u32(smem + C::OFF_STG) + static_cast<uint32_t>(quad) * (32 * W * 2);
+        const bool staged = !a.dv.f32 && !a.dk.f32 && a.dv.cols == D && a.dk.cols == D;
+        uint32_t t_local = 0;
+        bool ok = true;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
+            const int nq = cdiv(t.q_len, C::BQ);
+            if (!(ok = mbar_wait_warp(acc_full, t_local & 1, err))) break;
+            ++t_local;
+            if (quad * 32 >= t.kv_len) {  // no row of this warp is stored
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+                continue;
+            }
+            tc_fence_after();
+            if (staged) {
+                const int nrows = min(32, t.kv_len - quad * 32);
+                const int64_t r0 = static_cast<int64_t>(t.kv_start) + quad * 32;
+                __nv_bfloat16 *dv0 = static_cast<__nv_bfloat16 *>(a.dv.ptr) + r0 * a.dv.ld + t.h * D;
+                __nv_bfloat16 *dk0 = static_cast<__nv_bfloat16 *>(a.dk.ptr) + r0 * a.dk.ld + t.h * D;
+                // dV: W columns at a time through the staging buffer
+#pragma unroll
+                for (int h0 = 0; h0 < D; h0 += W) {
+#pragma unroll
+                    for (int c = 0; c < W / 32; ++c) {
+                        float v[32];
+                        uint32_t w[16];
+                        if (nq > 0) {
+                            tmem_ld32(tDV + h0 + 32 * c, v);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                        }
+                        pack16(v, w);
+                        stage_row32_bf16<W>(stg, lane, 32 * c, w);
+                    }
+                    __syncwarp();
+                    store_rows_bf16<W>(stg, lane, dv0 + h0, a.dv.ld, nrows);
+                    __syncwarp();
+                }
+                // dK (times the score scale) packed into registers
+                uint32_t kw[D / 32][16];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
+                    if (nq > 0) {
+                        tmem_ld32(tDK + 32 * c, v);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) mul2(v[i], v[i + 1], g.scale, g.scale);
+                    pack16(v, kw[c]);
+                }
+                // every TMEM read of this tile is done
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+#pragma unroll
+                for (int h0 = 0; h0 < D; h0 += W) {
+#pragma unroll
+                    for (int c = 0; c < W / 32; ++c) stage_row32_bf16<W>(stg, lane, 32 * c, kw[h0 / 32 + c]);
+                    __syncwarp();
+                    store_rows_bf16<W>(stg, lane, dk0 + h0, a.dk.ld, nrows);
+                    __syncwarp();
+                }
+                continue;
+            }
+            const bool row_ok = row < t.kv_len;
+            const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
+#pragma unroll 1
+            for (int col = 0; col < D; col += 32) {
+                float ov[32], ok_[32];
+                if (nq > 0) {
+                    tmem_ld32x2(tDV + col, tDK + col, ov, ok_);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) ov[i] = ok_[i] = 0.0f;
+                }
+                if (col + 32 >= D) {  // every TMEM read of this tile is done
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty);
+                }
+                if (row_ok) {
+                    store_out32(a.dv, krow, t.h, col, ov, 1.0f);
+                    store_out32(a.dk, krow, t.h, col, ok_, g.scale);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+}  // namespace
+
+// ============================================================================
+// launcher
+// ============================================================================
+template <int D, bool ACT, int BIAS, bool WIN>
+static cudaError_t launch_dkdv_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    using C = DkvCfg<D, ACT, BIAS>;
+    static bool done[64] = {};
+    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN>, C::SMEM_ALLOC, done);
+    if (e != cudaSuccess || n_ctas <= 0) return e;
+    dkdv_kernel<D, ACT, BIAS, WIN><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    return cudaGetLastError();
+}
+
+template <int D, bool ACT, int BIAS>
+static cudaError_t launch_dkdv_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    return a.g.window > 0 ? launch_dkdv_w<D, ACT, BIAS, true>(tm, a, n_ctas, st)
+                          : launch_dkdv_w<D, ACT, BIAS, false>(tm, a, n_ctas, st);
+}
+
+template <int D, bool ACT>
+static cudaError_t launch_dkdv_b(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    switch (bias_form(a.g)) {
+    case kBiasNone: return launch_dkdv_t<D, ACT, kBiasNone>(tm, a, n_ctas, st);
+    case kBiasExt: return launch_dkdv_t<D, ACT, kBiasExt>(tm, a, n_ctas, st);
+    default: return launch_dkdv_t<D, ACT, kBiasTable>(tm, a, n_ctas, st);
+    }
+}
+
+cudaError_t launch_bwd_dkdv(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    if (D == 128)
+        return act ? launch_dkdv_b<128, true>(tm, a, n_ctas, st) : launch_dkdv_b<128, false>(tm, a, n_ctas, st);
+    if (D == 64) return act ? launch_dkdv_b<64, true>(tm, a, n_ctas, st) : launch_dkdv_b<64, false>(tm, a, n_ctas, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace jattn

@@ -74,6 +74,7 @@ struct BwdArgs {
     const float *lse;    // [H, Tq] (full softmax)
     const float *delta;  // [H, Tq] (full softmax)
     OutDesc dq, dk, dv;
+    float *dbias;        // [H, nb] bias-table gradient (zeroed first, atomically summed) or nullptr
 };
 
 }  // namespace jattn

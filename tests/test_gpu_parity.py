@@ -133,3 +133,54 @@ def test_plan_update_between_batches():
     plan.update(bt2["q_off"], bt2["kv_off"])
     a = PT.run_library(bt2, plan=plan)
     PT.compare(a, PT.run_oracle(bt2))
+
+
+# bias-table gradient dT[h, n] = sum of dS over head h's pairs with min(|i - j|, NB - 1) = n
+DT_CASES = [
+    ("dt_self_d128", [45, 200, 129, 1, 390], None, 4, 128, 64, SOFTMAX, 0),
+    ("dt_self_d64", [70, 256, 3, 190], None, 2, 64, 16, SOFTMAX, 0),
+    ("dt_cross", [200, 35, 129, 511], [8, 64, 17, 40], 2, 128, 8, SOFTMAX, 0),
+    ("dt_silu_d64", [150, 3], [90, 400], 2, 64, 8, SILU, 0),
+    ("dt_gelu", [60, 300], [300, 60], 2, 128, 32, GELU, 0),
+    ("dt_window", [45, 700, 129], None, 2, 128, 64, SOFTMAX, 100),
+]
+
+
+@pytest.mark.parametrize("case", DT_CASES, ids=[c[0] for c in DT_CASES])
+def test_bias_gradient(case):
+    """dT is a sum over up to L^2 pairs whose softmax terms cancel (each row of dS
+    sums to zero), so its entries can be far smaller than the terms; the backward
+    tolerance is applied per head against the head's largest entry:
+    |dT - ref| <= 3e-2 * max|ref_h| + 3e-2 * |ref|."""
+    name, lq, lk, H, D, nb, act, win = case
+    lk = lq if lk is None else lk
+    bt = W.random_batch(zlib.crc32(name.encode()) % 10000, lq, lk, H, D, dtype=torch.bfloat16, bias_buckets=nb)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (bt[n].to(dev) for n in ("q", "k", "v", "dout"))
+    bias = bt["bias"].float().to(dev)
+    plan = J.Plan(bt["q_off"], bt["kv_off"], H, D, act=act, bias_buckets=nb, device=0, window=win)
+    out, lse = plan.fwd(q, k, v, bias=bias)
+    dbias = torch.full((H, nb), float("nan"), dtype=torch.float32, device=dev)
+    plan.bwd(do, q, k, v, out, lse=lse, bias=bias, dbias=dbias)
+    torch.cuda.synchronize()
+    assert plan.check_status() == 0
+    _, _, _, ref = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"],
+                                   bias=bt["bias"], scale=bt["scale"], act=act, window=win)
+    got = dbias.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    bound = 3e-2 * np.abs(ref).max(axis=1, keepdims=True) + 3e-2 * np.abs(ref)
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), (name, float((err / np.maximum(bound, 1e-30)).max()))
+    plan.close()
+
+
+def test_bias_gradient_rejected_in_block_mode():
+    bt = W.random_batch(7, [64, 100], [64, 100], 2, 64, dtype=torch.bfloat16, bias_buckets=4)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (bt[n].to(dev) for n in ("q", "k", "v", "dout"))
+    bias = bt["bias"].float().to(dev)
+    plan = J.Plan(bt["q_off"], bt["kv_off"], 2, 64, block=64, bias_buckets=4, device=0)
+    out, lse = plan.fwd(q, k, v, bias=bias)
+    with pytest.raises(J.JattnError):
+        plan.bwd(do, q, k, v, out, lse=lse, bias=bias, dbias=torch.zeros(2, 4, device=dev))
+    plan.close()
