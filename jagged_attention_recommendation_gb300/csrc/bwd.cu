@@ -23,13 +23,15 @@
 //                dK); warp 2: TMA producer of the tile's own rows (Q / dO, or
 //                K / V); warp 3: the thread that issues the two score-side
 //                products of every block (S and dP, or S^T and dP^T).
-//   warpgroups 1, 2  two compute groups; the CTA numbers its blocks n across
-//                tile boundaries and group g takes the blocks with n % 2 == g,
-//                one thread per tile row (TMEM lane), 32 columns at a time.
+//   warpgroups 1, 2  two compute groups, one thread per tile row (TMEM lane).
+//                The CTA numbers its blocks n across tile boundaries; block n
+//                uses TMEM buffer n % 2. In the dQ pass group g takes the blocks
+//                with n % 2 == g, 32 columns at a time; in the dK/dV pass both
+//                groups take every block, group g its 32-query half g.
 //   warpgroup 3  output group: reads the accumulators and writes the rows.
-// A block's two products land in its group's TMEM columns; the compute group
-// overwrites them in place with bf16 dS (and P^T) and the accumulating product
-// reads that operand from TMEM.  Two issuing threads, because any wait of the
+// A block's two products land in its buffer's TMEM columns; the compute groups
+// overwrite them in place with bf16 dS (and P^T), each 32-column chunk in its
+// own columns, and the accumulating product reads that operand from TMEM.  Two issuing threads, because any wait of the
 // issuing thread (an mbarrier, a shared-memory load, a named barrier) holds it
 // until its queued MMAs have drained, which leaves the tensor pipe idle; with
 // two, one thread's products run while the other waits.  Block n + 2 reuses

@@ -61,11 +61,11 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *kv_empty = bars + 1;
     uint64_t *qs_full = bars + 2;
     uint64_t *qs_empty = qs_full + C::NSQ;
-    uint64_t *st_full = qs_empty + C::NSQ;  // [2] per compute group
-    uint64_t *p_full = st_full + 2;         // [2] per compute group
+    uint64_t *st_full = qs_empty + C::NSQ;  // [2] per TMEM buffer (blocks alternate)
+    uint64_t *p_full = st_full + 2;         // [2] per TMEM buffer, both compute groups arrive
     uint64_t *acc_full = p_full + 2;
     uint64_t *acc_empty = acc_full + 1;
-    uint64_t *acc_done = acc_empty + 1;  // [2] per compute group: its block's dV / dK products finished
+    uint64_t *acc_done = acc_empty + 1;  // [2] per TMEM buffer: its block's dV / dK products finished
     uint64_t *drain = acc_done + 2;      // [2] per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st_full[b], 1);
-            mbar_init(&p_full[b], 4);
+            mbar_init(&p_full[b], 8);  // both compute groups' warps
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
@@ -203,8 +203,8 @@ __global__ void __launch_bounds__(512, 1)
                 const int na = cdiv(ta.q_len, C::BQ);
                 if (!(ok = mbar_wait(kv_full, ta_n & 1, err))) break;
                 for (int ia = 0; ia < na; ++ia, ++ns) {
-                    const uint32_t grp = ns & 1;
-                    if (ns >= 2 && !(ok = mbar_wait(&acc_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t buf = ns & 1;  // TMEM buffer of block ns
+                    if (ns >= 2 && !(ok = mbar_wait(&acc_done[buf], ((ns - 2) >> 1) & 1, err))) break;
                     const uint32_t slot = ns % C::NSQ;
                     if (!(ok = mbar_wait(&qs_full[slot], (ns / C::NSQ) & 1, err))) break;
                     tc_fence_after();
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t idesc = idesc_bf16(128, ncols, false, false);
                     const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
                     const uint64_t dqq = sdesc_sw128(qb, 16, 1024), ddo = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
-                    const uint32_t dS = tmem + grp * 128, dDP = dS + 64;
+                    const uint32_t dS = tmem + buf * 128, dDP = dS + 64;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t ao = (k >> 2) * C::SUB_KV + (k & 3) * 32;
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(512, 1)
                         mma_bf16_ss(dS, sdesc_add(dk0, ao), sdesc_add(dqq, bo), idesc, k > 0);
                         mma_bf16_ss(dDP, sdesc_add(dv0, ao), sdesc_add(ddo, bo), idesc, k > 0);
                     }
-                    mma_commit(&st_full[grp]);
+                    mma_commit(&st_full[buf]);
                 }
                 if (!ok) break;
                 mma_commit(kv_empty);  // the tile's last reads of K and V are in flight
@@ -244,15 +244,15 @@ __global__ void __launch_bounds__(512, 1)
                 // the output group must have read dV / dK of the previous tile
                 if (!(ok = mbar_wait(acc_empty, (tb_n & 1) ^ 1, err))) break;
                 for (int ib = 0; ib < nbq; ++ib, ++np) {
-                    const uint32_t grp = np & 1;
-                    if (!(ok = mbar_wait(&p_full[grp], (np >> 1) & 1, err))) break;
+                    const uint32_t buf = np & 1;
+                    if (!(ok = mbar_wait(&p_full[buf], (np >> 1) & 1, err))) break;
                     tc_fence_after();
                     const int ksteps = round_up16(min(C::BQ, tb.q_len - ib * C::BQ)) / 16;
                     const uint32_t slot = np % C::NSQ;
                     const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
                     const uint64_t bq0 = sdesc_sw128(qb, C::SUB_Q, 1024);
                     const uint64_t bdo0 = sdesc_sw128(qb + C::Q_BYTES, C::SUB_Q, 1024);
-                    const uint32_t aP = tmem + grp * 128, aDS = aP + 64;
+                    const uint32_t aP = tmem + buf * 128, aDS = aP + 64;
                     for (int k = 0; k < ksteps; ++k) {
                         const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
                         const uint64_t bdo = sdesc_add(bdo0, k * 2048);
@@ -263,12 +263,14 @@ __global__ void __launch_bounds__(512, 1)
                             mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
                             mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
                         } else {
-                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 8, bdo, idesc_acc, acc);
-                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 8, bq, idesc_acc, acc);
+                            // 32-query chunk k / 2 keeps its bf16 pairs in its own first 16 columns
+                            const uint32_t o = (k >> 1) * 32 + (k & 1) * 8;
+                            mma_bf16_ts(tmem + C::COL_DV, aP + o, bdo, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + o, bq, idesc_acc, acc);
                         }
                     }
                     mma_commit(&qs_empty[slot]);  // last reads of the Q / dO slot
-                    mma_commit(&acc_done[grp]);   // the group's columns may take block np + 2
+                    mma_commit(&acc_done[buf]);   // the buffer may take block np + 2
                 }
                 if (!ok) break;
                 mma_commit(acc_full);
@@ -287,9 +289,9 @@ __global__ void __launch_bounds__(512, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base + grp * 128, tDP = tS + 64;
+        const uint32_t tS0 = tmem + lane_base;  // buffer b of a block: S^T at 128 b, dP^T at 128 b + 64
         const float sc = ACT ? g.scale : g.scale * kLog2e;
-        uint32_t s_it = 0, n0 = 0;
+        uint32_t n0 = 0;
         bool ok = true;
         TileStream ts(g, tbeg, tend);
         Tile t;
@@ -300,20 +302,21 @@ __global__ void __launch_bounds__(512, 1)
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int kv_loc = t.kv_loc0 + row;
             const bool warp_live = quad * 32 < t.kv_len;
-            const int i0 = (grp - static_cast<int>(n0 & 1)) & 1;
             auto blocks = [&](auto af) {
                 constexpr int AF = decltype(af)::value;
-                for (int i = i0; i < nq; i += 2) {
-                    if (!(ok = mbar_wait_warp(&st_full[grp], s_it & 1, err))) return;
-                    ++s_it;
-                    if (warp_live) {
+                // every block of the tile; this group takes its 32-query chunk c = grp
+                for (int i = 0; i < nq; ++i) {
+                    const uint32_t n = n0 + i, b = n & 1;
+                    if (!(ok = mbar_wait_warp(&st_full[b], (n >> 1) & 1, err))) return;
+                    const int nvalid = min(C::BQ, t.q_len - i * C::BQ);
+                    const int c = grp;
+                    if (warp_live && c * 32 < nvalid) {
                         tc_fence_after();
-                        const int nvalid = min(C::BQ, t.q_len - i * C::BQ);
+                        const uint32_t tS = tS0 + b * 128, tDP = tS + 64;
                         const int qb = t.q_loc0 + i * C::BQ;
                         // [-lse log2 e | -Delta] of the block's queries (shared by all rows)
-                        const float *ld = sLD + ((n0 + i) % C::NSQ) * 2 * C::BQ;
-#pragma unroll 1
-                        for (int c = 0; c < 2 && c * 32 < nvalid; ++c) {
+                        const float *ld = sLD + (n % C::NSQ) * 2 * C::BQ;
+                        {
                             float x[32], dp[32];
                             tmem_ld32x2(tS + 32 * c, tDP + 32 * c, x, dp);
                             scale_bias_off32<BIAS>(x, sc, 0.0f, ext_h, bt, g.nb, kv_loc, qb + c * 32);
@@ -361,17 +364,17 @@ __global__ void __launch_bounds__(512, 1)
                                 tmem_st32_u32(tDP + 32 * c, w);
                             } else {
                                 uint32_t w[16];
-                                pack16(x, w);
-                                tmem_st16_u32(tS + 16 * c, w);
+                                pack16(x, w);  // over the chunk's own first 16 columns
+                                tmem_st16_u32(tS + 32 * c, w);
                                 pack16(dp, w);
-                                tmem_st16_u32(tDP + 16 * c, w);
+                                tmem_st16_u32(tDP + 32 * c, w);
                             }
                         }
                         tmem_wait_st();
                         tc_fence_before();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[grp]);
+                    if (lane == 0) mbar_arrive(&p_full[b]);
                 }
             };
             if (!ACT || g.act == kSilu) {
