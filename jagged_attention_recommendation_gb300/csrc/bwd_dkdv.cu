@@ -1,7 +1,10 @@
 // bwd_dkdv.cu -- jagged attention backward, pass 2 (dK, dV over key-major
 // tiles); the layout, the roles and the reasoning behind them are described at
 // the top of bwd.cu (pass 1, dQ), which shares this file's helpers through
-// bwd_common.cuh.
+// bwd_common.cuh. Here both compute groups work on every query block, group g
+// on its 32 queries 32 g .. 32 g + 31, so a block's P^T / dS^T take half the
+// time of one group doing all 64; the hand-off to the dV / dK issuer waits for
+// all eight compute warps.
 #include "bwd_common.cuh"
 
 namespace jattn {
