@@ -25,9 +25,9 @@
 //                products of every block (S and dP, or S^T and dP^T).
 //   warpgroups 1, 2  two compute groups, one thread per tile row (TMEM lane).
 //                The CTA numbers its blocks n across tile boundaries; block n
-//                uses TMEM buffer n % 2. In the dQ pass group g takes the blocks
-//                with n % 2 == g, 32 columns at a time; in the dK/dV pass both
-//                groups take every block, group g its 32-query half g.
+//                uses TMEM buffer n % 2. Both groups take every block, group g
+//                its 32-column half g (keys in the dQ pass, queries in the dK/dV
+//                pass); a block's hand-off waits for all eight compute warps.
 //   warpgroup 3  output group: reads the accumulators and writes the rows.
 // A block's two products land in its buffer's TMEM columns; the compute groups
 // overwrite them in place with bf16 dS (and P^T), each 32-column chunk in its
@@ -100,11 +100,11 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *k_empty = k_full + C::NSK;
     uint64_t *v_full = k_empty + C::NSK;
     uint64_t *v_empty = v_full + C::NSV;
-    uint64_t *s_full = v_empty + C::NSV;  // [2] per compute group
-    uint64_t *ds_full = s_full + 2;       // [2] per compute group
+    uint64_t *s_full = v_empty + C::NSV;  // [2] per TMEM buffer (blocks alternate)
+    uint64_t *ds_full = s_full + 2;       // [2] per TMEM buffer, both compute groups arrive
     uint64_t *dq_full = ds_full + 2;      // [2] per dQ buffer
     uint64_t *dq_empty = dq_full + 2;     // [2] per dQ buffer
-    uint64_t *dq_done = dq_empty + 2;     // [2] per compute group: its block's dQ product finished
+    uint64_t *dq_done = dq_empty + 2;     // [2] per TMEM buffer: its block's dQ product finished
     uint64_t *drain = dq_done + 2;        // [2] per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&qd_full[s], 1);
             mbar_init(&qd_empty[s], 1);
             mbar_init(&s_full[s], 1);
-            mbar_init(&ds_full[s], 4);
+            mbar_init(&ds_full[s], 8);  // both compute groups' warps
             mbar_init(&dq_full[s], 1);
             mbar_init(&dq_empty[s], 4);
             mbar_init(&dq_done[s], 1);
@@ -241,8 +241,8 @@ __global__ void __launch_bounds__(512, 1)
                 const uint32_t qb = sQ + qs * 2 * C::Q_BYTES;
                 const uint64_t dq0 = sdesc_sw128(qb, 16, 1024), ddo0 = sdesc_sw128(qb + C::Q_BYTES, 16, 1024);
                 for (int ja = 0; ja < na; ++ja, ++ns) {
-                    const uint32_t grp = ns & 1;
-                    if (ns >= 2 && !(ok = mbar_wait(&dq_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t buf = ns & 1;  // TMEM buffer of block ns
+                    if (ns >= 2 && !(ok = mbar_wait(&dq_done[buf], ((ns - 2) >> 1) & 1, err))) break;
                     const uint32_t ks = ns % C::NSK, vs = ns % C::NSV;
                     if (!(ok = mbar_wait(&k_full[ks], (ns / C::NSK) & 1, err))) break;
                     if (!(ok = mbar_wait(&v_full[vs], (ns / C::NSV) & 1, err))) break;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t idesc = idesc_bf16(128, ncols, false, false);
                     const uint64_t dk0 = sdesc_sw128(sK + ks * C::KV_BYTES, 16, 1024);
                     const uint64_t dv0 = sdesc_sw128(sV + vs * C::KV_BYTES, 16, 1024);
-                    const uint32_t dS = tmem + grp * 128, dDP = dS + 64;
+                    const uint32_t dS = tmem + buf * 128, dDP = dS + 64;
 #pragma unroll
                     for (int k = 0; k < D / 16; ++k) {
                         const uint32_t ao = (k >> 2) * C::SUB_Q + (k & 3) * 32;
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(512, 1)
                         mma_bf16_ss(dS, sdesc_add(dq0, ao), sdesc_add(dk0, bo), idesc, k > 0);
                         mma_bf16_ss(dDP, sdesc_add(ddo0, ao), sdesc_add(dv0, bo), idesc, k > 0);
                     }
-                    mma_commit(&s_full[grp]);
+                    mma_commit(&s_full[buf]);
                     mma_commit(&v_empty[vs]);  // dP was the V slot's only reader
                 }
                 if (!ok) break;
@@ -287,13 +287,13 @@ __global__ void __launch_bounds__(512, 1)
                 if (!(ok = mbar_wait(&dq_empty[b], ((tb_n >> 1) & 1) ^ 1, err))) break;
                 const uint32_t dq = tmem + C::COL_DQ + b * D;
                 for (int jb = 0; jb < nbk; ++jb, ++np) {
-                    const uint32_t grp = np & 1;
-                    if (!(ok = mbar_wait(&ds_full[grp], (np >> 1) & 1, err))) break;
+                    const uint32_t buf = np & 1;
+                    if (!(ok = mbar_wait(&ds_full[buf], (np >> 1) & 1, err))) break;
                     tc_fence_after();
                     const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
                     const uint32_t ks = np % C::NSK;
                     const uint64_t bd0 = sdesc_sw128(sK + ks * C::KV_BYTES, C::SUB_KV, 1024);
-                    const uint32_t aS = tmem + grp * 128;
+                    const uint32_t aS = tmem + buf * 128;
                     for (int k = 0; k < ksteps; ++k) {
                         const uint64_t bd = sdesc_add(bd0, k * 2048);
                         const uint32_t acc = (jb > 0 || k > 0) ? 1u : 0u;
@@ -301,11 +301,12 @@ __global__ void __launch_bounds__(512, 1)
                             mma_bf16_ts(dq, aS + k * 16, bd, idesc_dq, acc);
                             mma_bf16_ts(dq, aS + k * 16 + 8, bd, idesc_dq, 1u);
                         } else {
-                            mma_bf16_ts(dq, aS + k * 8, bd, idesc_dq, acc);
+                            // 32-key chunk k / 2 keeps its bf16 pairs in its own first 16 columns
+                            mma_bf16_ts(dq, aS + (k >> 1) * 32 + (k & 1) * 8, bd, idesc_dq, acc);
                         }
                     }
                     mma_commit(&k_empty[ks]);     // S and dQ were the K slot's readers
-                    mma_commit(&dq_done[grp]);    // the group's columns may take block np + 2
+                    mma_commit(&dq_done[buf]);    // the buffer may take block np + 2
                 }
                 if (!ok) break;
                 mma_commit(&dq_full[b]);
@@ -324,9 +325,9 @@ __global__ void __launch_bounds__(512, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base + grp * 128, tDP = tS + 64;
+        const uint32_t tS0 = tmem + lane_base;  // buffer b of a block: S at 128 b, dP at 128 b + 64
         const float sc = ACT ? g.scale : g.scale * kLog2e;
-        uint32_t s_it = 0, n0 = 0;
+        uint32_t n0 = 0;
         float dt_far = 0.0f;  // this row's dS in the last bias bucket, per tile
         bool ok = true;
         TileStream ts(g, tbeg, tend);
@@ -339,24 +340,25 @@ __global__ void __launch_bounds__(512, 1)
             const int q_loc = t.q_loc0 + row;
             const bool row_ok = row < t.q_len;
             const bool warp_live = quad * 32 < t.q_len;  // else its rows reach nothing that is stored
-            const int j0 = (grp - static_cast<int>(n0 & 1)) & 1;
             float lse2 = 0.0f, dlt = 0.0f;  // log2 units / Delta of this row
-            if (!ACT && row_ok && j0 < nkv) {
+            if (!ACT && row_ok && nkv > 0) {
                 const int64_t idx = static_cast<int64_t>(t.h) * g.Tq + t.q_start + row;
                 lse2 = a.lse[idx] * kLog2e;
                 dlt = a.delta[idx];
             }
             auto blocks = [&](auto af) {
                 constexpr int AF = decltype(af)::value;
-                for (int j = j0; j < nkv; j += 2) {
-                    if (!(ok = mbar_wait_warp(&s_full[grp], s_it & 1, err))) return;
-                    ++s_it;
-                    if (warp_live) {
+                // every block of the tile; this group takes its 32-key chunk c = grp
+                for (int j = 0; j < nkv; ++j) {
+                    const uint32_t n = n0 + j, b = n & 1;
+                    if (!(ok = mbar_wait_warp(&s_full[b], (n >> 1) & 1, err))) return;
+                    const int nvalid = min(C::BN, t.kv_len - j * C::BN);
+                    const int c = grp;
+                    if (warp_live && c * 32 < nvalid) {
                         tc_fence_after();
-                        const int nvalid = min(C::BN, t.kv_len - j * C::BN);
+                        const uint32_t tS = tS0 + b * 128, tDP = tS + 64;
                         const int kvb = t.kv_loc0 + j * C::BN;
-#pragma unroll 1
-                        for (int c = 0; c < 2 && c * 32 < nvalid; ++c) {
+                        {
                             float x[32], dp[32];
                             tmem_ld32x2(tS + 32 * c, tDP + 32 * c, x, dp);
                             // x = scale * s + bias (softmax: minus lse, log2 units)
@@ -411,14 +413,14 @@ __global__ void __launch_bounds__(512, 1)
                             } else {
                                 uint32_t w[16];
                                 pack16(x, w);
-                                tmem_st16_u32(tS + 16 * c, w);
+                                tmem_st16_u32(tS + 32 * c, w);  // over the chunk's own first 16 columns
                             }
                         }
                         tmem_wait_st();
                         tc_fence_before();
                     }
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&ds_full[grp]);
+                    if (lane == 0) mbar_arrive(&ds_full[b]);
                 }
             };
             if (!ACT || g.act == kSilu) {
