@@ -117,12 +117,12 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *k_empty = k_full + C::NST;
     uint64_t *v_full = k_empty + C::NST;
     uint64_t *v_empty = v_full + C::NST;
-    uint64_t *s_full = v_empty + C::NST;  // [2] per softmax group
-    uint64_t *p_full = s_full + 2;        // [2] per softmax group
+    uint64_t *s_full = v_empty + C::NST;  // [2] per score buffer (blocks alternate)
+    uint64_t *p_full = s_full + 2;        // [2] per score buffer, both softmax groups arrive
     uint64_t *o_full = p_full + 2;
     uint64_t *o_empty = o_full + 1;  // [2] per tile parity
     uint64_t *l_full = o_empty + 2;  // [2] per tile parity
-    uint64_t *pv_done = l_full + 2;  // [2] per softmax group: its block's P V finished
+    uint64_t *pv_done = l_full + 2;  // [2] per score buffer: its block's P V finished
     uint64_t *drain = pv_done + 2;   // [2] per MMA-issuing thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1);
             mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 4);
+            mbar_init(&p_full[s], 8);  // both softmax groups' warps
             mbar_init(&o_empty[s], 4);
             mbar_init(&l_full[s], 8);
             mbar_init(&pv_done[s], 1);
@@ -271,20 +271,20 @@ __global__ void __launch_bounds__(512, 1)
                 if (!(ok = mbar_wait(&q_full[qs], (ta_n >> 1) & 1, err))) break;
                 const uint64_t ad0 = sdesc_sw128(sQ + qs * C::Q_BYTES, 16, 1024);
                 for (int ja = 0; ja < na; ++ja, ++ns) {
-                    const uint32_t grp = ns & 1;
-                    if (ns >= 2 && !(ok = mbar_wait(&pv_done[grp], ((ns - 2) >> 1) & 1, err))) break;
+                    const uint32_t buf = ns & 1;  // score buffer of block ns
+                    if (ns >= 2 && !(ok = mbar_wait(&pv_done[buf], ((ns - 2) >> 1) & 1, err))) break;
                     const uint32_t slot = ns % C::NST, use = ns / C::NST;
                     if (!(ok = mbar_wait(&k_full[slot], use & 1, err))) break;
                     tc_fence_after();
                     const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
                     const uint32_t idesc = idesc_bf16(128, ncols, false, false);
                     const uint64_t bd0 = sdesc_sw128(sK + slot * C::KV_BYTES, 16, 1024);
-                    const uint32_t dS = tmem + C::COL_S + grp * C::BN;
+                    const uint32_t dS = tmem + C::COL_S + buf * C::BN;
 #pragma unroll
                     for (int ks = 0; ks < D / 16; ++ks)
                         mma_bf16_ss(dS, sdesc_add(ad0, (ks >> 2) * C::SUB_Q + (ks & 3) * 32),
                                     sdesc_add(bd0, (ks >> 2) * C::SUB_KV + (ks & 3) * 32), idesc, ks > 0);
-                    mma_commit(&s_full[grp]);
+                    mma_commit(&s_full[buf]);
                     mma_commit(&k_empty[slot]);
                 }
                 if (!ok) break;
@@ -296,8 +296,9 @@ __global__ void __launch_bounds__(512, 1)
             mbar_drain(&drain[0], 0);
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- P V issuer
-            // O_g (+)= P V for group g's blocks, P (bf16; activation: hi and lo
-            // parts) read from TMEM; one thread, so the accumulation order is fixed.
+            // O_g (+)= P_g V_g for softmax group g's 64 keys of every block, P
+            // (bf16; activation: hi and lo parts) read from TMEM; one thread, so
+            // the accumulation order is fixed.
             const uint32_t idesc_pv = idesc_bf16(128, D, false, true);
             bool ok = true;
             TileStream tsb(g, tbeg, tend);
@@ -310,27 +311,35 @@ __global__ void __launch_bounds__(512, 1)
                 // reused (a tile without keys hands over all-zero rows in order)
                 if (tb_n > 0 && !(ok = mbar_wait(&o_empty[(tb_n - 1) & 1], ((tb_n - 1) >> 1) & 1, err))) break;
                 for (int jb = 0; jb < nbk; ++jb, ++np) {
-                    const uint32_t grp = np & 1;
-                    if (!(ok = mbar_wait(&p_full[grp], (np >> 1) & 1, err))) break;
+                    const uint32_t buf = np & 1;
+                    if (!(ok = mbar_wait(&p_full[buf], (np >> 1) & 1, err))) break;
                     const uint32_t slot = np % C::NST, use = np / C::NST;
                     if (!(ok = mbar_wait(&v_full[slot], use & 1, err))) break;
                     tc_fence_after();
-                    const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
+                    const int nvalid = min(C::BN, tb.kv_len - jb * C::BN);
                     const uint64_t bd0 = sdesc_sw128(sV + slot * C::KV_BYTES, C::SUB_KV, 1024);
-                    const uint32_t dO = tmem + C::COL_O + grp * D;
-                    const uint32_t aP = tmem + C::COL_S + grp * C::BN;
-                    // the first two blocks of a tile start their group's accumulator
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint64_t bd = sdesc_add(bd0, ks * 2048);
-                        if (ACT) {  // hi at columns 16 ks .. +7, lo at 16 ks + 8 .. +15
-                            mma_bf16_ts(dO, aP + ks * 16, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
-                            mma_bf16_ts(dO, aP + ks * 16 + 8, bd, idesc_pv, 1u);
-                        } else {
-                            mma_bf16_ts(dO, aP + ks * 8, bd, idesc_pv, (jb >= 2 || ks > 0) ? 1u : 0u);
+                    const uint32_t aP = tmem + C::COL_S + buf * C::BN;
+#pragma unroll
+                    for (int grp = 0; grp < 2; ++grp) {
+                        // group grp's keys 64 grp .. of the block; its 16-key step ks is
+                        // block step 4 grp + ks, whose P sits in 32-key chunk (4 grp + ks) / 2
+                        const int keys = min(64, nvalid - 64 * grp);
+                        const int ksteps = keys > 0 ? round_up16(keys) / 16 : 0;
+                        const uint32_t dO = tmem + C::COL_O + grp * D;
+                        for (int ks = 0; ks < ksteps; ++ks) {
+                            const int st = 4 * grp + ks;
+                            const uint64_t bd = sdesc_add(bd0, st * 2048);
+                            const uint32_t acc = (jb > 0 || ks > 0) ? 1u : 0u;  // the tile's first block starts O_grp
+                            if (ACT) {  // hi at columns 16 st .. +7, lo at 16 st + 8 .. +15
+                                mma_bf16_ts(dO, aP + st * 16, bd, idesc_pv, acc);
+                                mma_bf16_ts(dO, aP + st * 16 + 8, bd, idesc_pv, 1u);
+                            } else {
+                                mma_bf16_ts(dO, aP + (st >> 1) * 32 + (st & 1) * 8, bd, idesc_pv, acc);
+                            }
                         }
                     }
                     mma_commit(&v_empty[slot]);
-                    mma_commit(&pv_done[grp]);  // the group's score columns may take block np + 2
+                    mma_commit(&pv_done[buf]);  // the buffer may take block np + 2; O_0 / O_1 hold block np
                 }
                 if (!ok) break;
                 mma_commit(o_full);
@@ -347,15 +356,15 @@ __global__ void __launch_bounds__(512, 1)
         // group's blocks: scores -> bias, mask, online softmax (or activation)
         // -> P as bf16 over the same TMEM columns; rare O rescales in TMEM; per
         // tile the row max and row sum go to the output group.
-        const int grp = wgi - 1;                   // blocks n with n % 2 == grp
+        const int grp = wgi - 1;                   // keys 64 grp .. 64 grp + 63 of every block
         const int quad = warp & 3;                 // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;          // query row within the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tS = tmem + lane_base + C::COL_S + grp * C::BN;  // S, then P over it
+        const uint32_t tS0 = tmem + lane_base + C::COL_S;  // buffer b of block n = n % 2 at b BN
         const uint32_t tO = tmem + lane_base + C::COL_O + grp * D;
         const float sc = ACT ? g.scale : g.scale * kLog2e;
         constexpr bool scaled = ACT || BIAS != kBiasNone;  // else the scale is folded into the exponent
-        uint32_t s_it = 0, t_local = 0, n0 = 0;  // n0: global number of the tile's first block
+        uint32_t t_local = 0, n0 = 0;  // n0: global number of the tile's first block
         bool ok = true;
         TileStream ts(g, tbeg, tend);
         Tile t;
@@ -365,19 +374,19 @@ __global__ void __launch_bounds__(512, 1)
             const float *bt = sbias + t.h * g.nb;
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int q_loc = t.q_loc0 + row;
-            const int j0 = (grp - static_cast<int>(n0 & 1)) & 1;  // this group's first block of the tile
             // A warp whose 32 rows all lie past the tile's end only keeps the hand-offs
             // going: rows are independent through both products, so whatever its TMEM
             // lanes hold reaches only output rows that are never stored.
             const bool warp_live = quad * 32 < t.q_len;
             float m = -INFINITY, l = 0.0f;
 
-            for (int j = j0; j < nkv; j += 2) {
-                if (!(ok = mbar_wait_warp(&s_full[grp], s_it & 1, err))) break;
-                ++s_it;
+            for (int j = 0; j < nkv; ++j) {
+                const uint32_t n = n0 + j, b = n & 1;
+                if (!(ok = mbar_wait_warp(&s_full[b], (n >> 1) & 1, err))) break;
+                const uint32_t tS = tS0 + b * C::BN;  // S, then P over it
                 if (!warp_live) {
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&p_full[grp]);
+                    if (lane == 0) mbar_arrive(&p_full[b]);
                     continue;
                 }
                 tc_fence_after();
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(512, 1)
                     // pass 1: row max of the block (biased scores written back in place)
                     float mloc = -INFINITY;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
                         if (!live(c)) continue;
                         float xc[32];
                         tmem_ld32(tS + 32 * c, xc);
@@ -438,20 +447,22 @@ __global__ void __launch_bounds__(512, 1)
                     // lazy rescale: keep the old max while it is within the threshold
                     float alpha = 1.0f;
                     bool resc = false;
-                    if (j == j0) {
+                    if (j == 0) {
                         m = m_new;
                     } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
-                        alpha = ex2_approx(m - m_new);
+                        // the test is warp-wide: a row of the warp that has seen no
+                        // key yet (m = m_new = -inf) keeps its zero l and O as they are
+                        alpha = m_new == -INFINITY ? 1.0f : ex2_approx(m - m_new);
                         resc = true;
                         l *= alpha;
                         m = m_new;
                     }
                     const float nm = (m == -INFINITY) ? 0.0f : -m;
-                    // pass 2: P = 2^(s - m) as bf16; chunk c goes to columns 16c..16c+15,
-                    // which hold scores already consumed
+                    // pass 2: P = 2^(s - m) as bf16; chunk c goes to its own first 16
+                    // columns 32c..32c+15, scores already consumed
                     float rs = 0.0f;
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
                         uint32_t pw[16];
                         if (!live(c)) {
 #pragma unroll
@@ -478,12 +489,16 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
                             for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(xc[2 * i], xc[2 * i + 1]);
                         }
-                        tmem_st16_u32(tS + 16 * c, pw);
+                        tmem_st16_u32(tS + 32 * c, pw);
                     }
                     l += rs;
                     if (resc) {
-                        // O_grp holds this group's earlier blocks of the tile (its last
-                        // P V finished before S_j did); bring it to the new max first
+                        // O_grp holds the tile's earlier blocks once P V of block n - 1 has
+                        // finished (block n - 2's finished before S_n was issued, so the
+                        // barrier is at most that one phase behind); then bring O_grp to
+                        // the new max before this block's P V adds on
+                        if (!(ok = mbar_wait_warp(&pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1, err))) break;
+                        tc_fence_after();
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
                             float o[32];
@@ -500,7 +515,7 @@ __global__ void __launch_bounds__(512, 1)
                     auto act_block = [&](auto af) {
                         constexpr int AF = decltype(af)::value;
 #pragma unroll 1
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
                             uint32_t w[32];
                             if (!live(c)) {
 #pragma unroll
@@ -532,7 +547,7 @@ __global__ void __launch_bounds__(512, 1)
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&p_full[grp]);
+                if (lane == 0) mbar_arrive(&p_full[b]);
             }
             if (!ok) break;
 
@@ -568,10 +583,9 @@ __global__ void __launch_bounds__(512, 1)
         while (ok && ts.next(t)) {
             if (!check_tile(g, t, err, false)) continue;
             const int nkv = cdiv(t.kv_len, C::BN);
-            // group g has blocks in this tile when there are two or more, or one
-            // that is its turn
-            const bool has0 = nkv >= 2 || (nkv == 1 && (n0 & 1) == 0);
-            const bool has1 = nkv >= 2 || (nkv == 1 && (n0 & 1) == 1);
+            // group g has keys in this tile when the tile has more than 64 g keys
+            const bool has0 = t.kv_len > 0;
+            const bool has1 = t.kv_len > 64;
             const uint32_t sl = t_local & 1;
             if (!(ok = mbar_wait_warp(o_full, t_local & 1, err))) break;
             float c0 = has0 ? 1.0f : 0.0f, c1 = has1 ? 1.0f : 0.0f, lse = -INFINITY;
