@@ -18,27 +18,26 @@
 //   warp 2      TMA producer for Q, double-buffered so the next tile's rows
 //               arrive while the current tile runs.
 //   warp 3      one thread issues every S = Q K^T.
-//   warps 4-7   softmax group 0: blocks n = 0, 2, 4, ...
-//   warps 8-11  softmax group 1: blocks n = 1, 3, 5, ...
+//   warps 4-7   softmax group 0: keys 0..63 of every key block.
+//   warps 8-11  softmax group 1: keys 64..127 of every key block.
 //   warps 12-15 output group: merges the two groups' partial results of a
 //               tile, O / l -> global, lse.
 // Each softmax group runs its own online softmax (row max m_g, row sum l_g)
-// over its blocks of a tile into its own TMEM accumulator O_g, so the groups
-// never wait for each other, their exp, scale and max phases interleave on
-// the SM sub-partitions, and at a tile boundary one group starts the next tile
-// while the other finishes the current one.  The output group combines
+// over its half of every block of a tile into its own TMEM accumulator O_g, so
+// the groups never wait for each other and both have work on every block but
+// a last one of at most 64 keys.  The output group combines
 //   O = (2^(m_0-m) O_0 + 2^(m_1-m) O_1) / (2^(m_0-m) l_0 + 2^(m_1-m) l_1),
-// m = max(m_0, m_1), over the groups that had blocks in the tile (in the
+// m = max(m_0, m_1), over the groups that saw keys in the tile (in the
 // activation modes simply O_0 + O_1).
 // P never touches shared memory: the softmax writes it as bf16 over the
 // group's own score columns in TMEM and P V reads it from there (the A operand
 // of tcgen05.mma may live in TMEM).  Two threads issue the products, because
 // any wait of an issuing thread (an mbarrier, a shared-memory load) holds it
 // until its queued MMAs have drained, which idles the tensor pipe; with two,
-// one thread's products run while the other waits.  S_{n+2} overwrites P_n, so
-// the S issuer waits for PV_n to finish (an mbarrier committed by the P V
-// issuer) before it issues S_{n+2}; S_{n+1} is computed during the softmax of
-// block n.
+// one thread's products run while the other waits.  The score columns are
+// double-buffered by block parity: S_{n+2} overwrites P_n, so the S issuer
+// waits for PV_n to finish (an mbarrier committed by the P V issuer) before it
+// issues S_{n+2}, and S_{n+1} is computed during the softmax of block n.
 // Rows past a sequence's end are loaded (they belong to the next sequence or
 // are zero-filled past the tensor end) but masked as keys and never stored as
 // queries; the last key block of a sequence runs a narrower MMA (N rounded up
@@ -352,8 +351,8 @@ __global__ void __launch_bounds__(512, 1)
     } else if (wgi < 3) {
         regs_claim<C::REG_SOFTMAX>();
         // ------------------------------------------------------------ softmax
-        // One thread per query row (TMEM lane) over all 128 columns of the
-        // group's blocks: scores -> bias, mask, online softmax (or activation)
+        // One thread per query row (TMEM lane) over the group's 64 columns of
+        // every block: scores -> bias, mask, online softmax (or activation)
         // -> P as bf16 over the same TMEM columns; rare O rescales in TMEM; per
         // tile the row max and row sum go to the output group.
         const int grp = wgi - 1;                   // keys 64 grp .. 64 grp + 63 of every block
