@@ -179,6 +179,26 @@ def random_batch(seed: int, lq, lk, H: int, D: int, dtype=torch.bfloat16, bias_b
     return dict(q_off=qo, kv_off=ko, q=q, k=k, v=v, bias=bias, dout=dout, scale=1.0 / math.sqrt(D))
 
 
+def rope_table(P: int, D: int, kind: str = "standard", base: float = 10000.0, seed: int = 0):
+    """Rotary-embedding tables (cos, sin), float32 [P, D/2], for positions 0..P-1.
+
+    kind "standard": angle p * base^(-2d/D) for feature pair d (the usual
+    frequency ladder); "random": seeded uniform angles in [-pi, pi), so that no
+    structure of the ladder can hide an indexing slip; "identity": angle 0.
+    """
+    half = D // 2
+    if kind == "standard":
+        inv = base ** (-2.0 * np.arange(half, dtype=np.float64) / D)
+        phi = np.arange(P, dtype=np.float64)[:, None] * inv[None, :]
+    elif kind == "random":
+        phi = np.random.default_rng(seed).uniform(-np.pi, np.pi, size=(P, half))
+    elif kind == "identity":
+        phi = np.zeros((P, half))
+    else:
+        raise ValueError(kind)
+    return (torch.from_numpy(np.cos(phi).astype(np.float32)), torch.from_numpy(np.sin(phi).astype(np.float32)))
+
+
 # ---------------------------------------------------------------------------
 # Work accounting (valid tokens only; padding and recompute are not counted)
 # ---------------------------------------------------------------------------

@@ -74,12 +74,47 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0):
+def rope_rotate(x, offsets, cos, sin, transpose=False) -> np.ndarray:
+    """Rotary position embedding of a jagged [T, H, D] tensor, in float64.
+
+    "Training GEM at LLM scale", section "BlockAttention": RoPE is applied to
+    the queries and keys before the attention, and its backward is fused into
+    the attention's epilogue.  The pages give no formula; this is the standard
+    rotary embedding with the half-split pairing.  Row t of sequence b sits at
+    local position p = t - offsets[b].  Each feature pair (d, d + D/2), d < D/2,
+    is turned by the angle whose cosine and sine are cos[p, d] and sin[p, d]:
+        y[d]       = x[d] cos - x[d + D/2] sin
+        y[d + D/2] = x[d + D/2] cos + x[d] sin
+    transpose=True applies the transposed rotation.  That maps a gradient with
+    respect to the rotated rows back to the unrotated ones.
+    """
+    x = _f64(x)
+    cos, sin = _f64(cos), _f64(sin)
+    off = np.asarray(offsets, dtype=np.int64)
+    T, _, D = x.shape
+    half = D // 2
+    pos = np.zeros(T, dtype=np.int64)
+    for b in range(len(off) - 1):
+        pos[off[b]:off[b + 1]] = np.arange(off[b + 1] - off[b])
+    c = cos[pos][:, None, :]  # [T, 1, D/2]
+    s = sin[pos][:, None, :]
+    if transpose:
+        s = -s
+    a, b_ = x[..., :half], x[..., half:]
+    return np.concatenate([a * c - b_ * s, b_ * c + a * s], axis=-1)
+
+
+def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0,
+            rope=None):
     """Returns (out [Tq,H,D] float64, lse [H,Tq] float64 or None).
-    window W > 0: row i attends only keys with |i - j| < W (sliding window)."""
+    window W > 0: row i attends only keys with |i - j| < W (sliding window).
+    rope = (cos, sin), tables [P, D/2]: Q and K are rotated first (rope_rotate)."""
     lib = _load()
     qo, ko = _i32(q_off), _i32(kv_off)
     q, k, v, bias = _f64(q), _f64(k), _f64(v), _f64(bias)
+    if rope is not None:
+        q = rope_rotate(q, qo, rope[0], rope[1])
+        k = rope_rotate(k, ko, rope[0], rope[1])
     Tq, H, D = q.shape
     B = len(qo) - 1
     if scale is None:
@@ -94,11 +129,16 @@ def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0,
     return out, lse
 
 
-def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0):
-    """Returns (dq, dk, dv, dbias or None), all float64 (window as in forward)."""
+def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0,
+             rope=None):
+    """Returns (dq, dk, dv, dbias or None), all float64 (window and rope as in
+    forward; with rope, dq and dk are the gradients of the unrotated Q and K)."""
     lib = _load()
     qo, ko = _i32(q_off), _i32(kv_off)
     q, k, v, dout, bias = _f64(q), _f64(k), _f64(v), _f64(dout), _f64(bias)
+    if rope is not None:
+        q = rope_rotate(q, qo, rope[0], rope[1])
+        k = rope_rotate(k, ko, rope[0], rope[1])
     Tq, H, D = q.shape
     Tk = k.shape[0]
     B = len(qo) - 1
@@ -114,6 +154,9 @@ def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, b
                               nthreads or default_threads())
     if rc != 0:
         raise ValueError("oracle backward rejected its input (code %d)" % rc)
+    if rope is not None:
+        dq = rope_rotate(dq, qo, rope[0], rope[1], transpose=True)
+        dk = rope_rotate(dk, ko, rope[0], rope[1], transpose=True)
     return dq, dk, dv, dbias
 
 

@@ -57,13 +57,27 @@ def sdpa_forward(q_off, kv_off, q, k, v, bias=None, scale=None, block=0, window=
     return out
 
 
-def padded_dense(q_off, kv_off, q, k, v, dout=None, bias=None, scale=None, act=SOFTMAX, block=0, window=0):
+def rotate_complex(x, phi):
+    """Rotary embedding as complex multiplication: the feature pair
+    (x[d], x[d + D/2]) is the complex number x[d] + i x[d + D/2], multiplied by
+    e^(i phi[p, d]) at padded position p (the row index of dimension -2)."""
+    half = x.shape[-1] // 2
+    z = torch.complex(x[..., :half], x[..., half:])
+    w = torch.polar(torch.ones_like(phi), phi)[: x.shape[-2]]
+    y = z * w
+    return torch.cat([y.real, y.imag], dim=-1)
+
+
+def padded_dense(q_off, kv_off, q, k, v, dout=None, bias=None, scale=None, act=SOFTMAX, block=0, window=0,
+                 rope_phi=None):
     """Pad the jagged batch to [B, H, Lmax, D], mask, and run attention densely.
 
     Softmax rows are masked with -inf; activation mode multiplies by a 0/1 mask
-    (a -inf score would give NaN through SiLU).  If ``dout`` is given the
-    gradients come from torch autograd.  Returns (out, lse, dq, dk, dv, dbias)
-    in the jagged layout, float64.
+    (a -inf score would give NaN through SiLU).  rope_phi [P, D/2] (float64
+    angles): the padded Q and K are rotated by ``rotate_complex`` first, inside
+    the autograd graph.  If ``dout`` is given the gradients come from torch
+    autograd.  Returns (out, lse, dq, dk, dv, dbias) in the jagged layout,
+    float64.
     """
     B = len(q_off) - 1
     Tq, H, D = q.shape
@@ -93,7 +107,11 @@ def padded_dense(q_off, kv_off, q, k, v, dout=None, bias=None, scale=None, act=S
         tbl = bias.to(torch.float64).clone().requires_grad_(dout is not None)
     for t in (qd, kd, vd):
         t.requires_grad_(dout is not None)
-    s = scale * qd @ kd.transpose(-1, -2)
+    qa, ka = qd, kd
+    if rope_phi is not None:
+        qa = rotate_complex(qd, rope_phi.to(torch.float64))
+        ka = rotate_complex(kd, rope_phi.to(torch.float64))
+    s = scale * qa @ ka.transpose(-1, -2)
     if tbl is not None:
         i = torch.arange(Mq).view(-1, 1)
         j = torch.arange(Mk).view(1, -1)

@@ -358,3 +358,115 @@ def test_window_band_is_symmetric_and_rejects_block():
         np.testing.assert_allclose(out[i, 0], p @ v[js], rtol=1e-12, atol=1e-12)
     with pytest.raises(ValueError):
         oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], block=64, window=2)
+
+
+# --- rotary position embedding (RoPE, then attention) -----------------------
+
+def test_rope_hand_rotation():
+    """Half-split pairing, sign and local position, worked by hand.
+
+    D = 4; the row under test is local position 1 of the second sequence (global
+    row 4).  Table row 1: cos = (0.6, 0), sin = (0.8, 1); x = (1, 2, 3, 4):
+      pair (0, 2): 1*0.6 - 3*0.8 = -1.8,  3*0.6 + 1*0.8 = 2.6
+      pair (1, 3): 2*0   - 4*1   = -4,    4*0   + 2*1   = 2
+    so y = (-1.8, -4, 2.6, 2).  Local position 0 (global row 3) takes table row
+    0, the identity.  Rows 3 and 4 of the table hold other angles, so global
+    indexing would give other values.
+    """
+    off = [0, 3, 5]
+    x = np.zeros((5, 1, 4))
+    x[3, 0] = x[4, 0] = [1.0, 2.0, 3.0, 4.0]
+    cos = np.array([[1.0, 1.0], [0.6, 0.0], [0.0, 0.0], [0.0, 1.0], [-1.0, 0.0]])
+    sin = np.array([[0.0, 0.0], [0.8, 1.0], [1.0, 1.0], [1.0, 0.0], [0.0, -1.0]])
+    y = oracle.rope_rotate(x, off, cos, sin)
+    np.testing.assert_allclose(y[4, 0], [-1.8, -4.0, 2.6, 2.0], rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(y[3, 0], [1.0, 2.0, 3.0, 4.0])
+    # cos^2 + sin^2 = 1 in both pairs: the transposed rotation undoes it
+    back = oracle.rope_rotate(y, off, cos, sin, transpose=True)
+    np.testing.assert_allclose(back[4, 0], [1.0, 2.0, 3.0, 4.0], rtol=0, atol=1e-15)
+
+
+def _phi(P, D, seed):
+    return torch.from_numpy(np.random.default_rng(seed).uniform(-np.pi, np.pi, size=(P, D // 2)))
+
+
+@pytest.mark.parametrize("act", [SOFTMAX, SILU])
+@pytest.mark.parametrize("block", [0, 64])
+def test_rope_matches_autograd_complex(act, block):
+    """Rotate-then-attend equals torch autograd through padded dense attention
+    whose Q and K are rotated by complex multiplication (x[d] + i x[d+D/2]) e^(i phi):
+    outputs and the gradients of the unrotated Q, K, V and the bias table."""
+    if block:
+        lq = lk = [70, 9, 130]
+    else:
+        lq, lk = [9, 3, 14, 1], [6, 11, 2, 8]
+    bt = batch(51, lq, lk, nb=6)
+    phi = _phi(140, 8, 52)
+    rope = (np.cos(phi.numpy()), np.sin(phi.numpy()))
+    out, _ = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], act=act,
+                            block=block, rope=rope)
+    dq, dk, dv, db = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"],
+                                     bias=bt["bias"], act=act, block=block, rope=rope)
+    rout, _, rdq, rdk, rdv, rdb = dense_ref.padded_dense(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"],
+                                                         dout=bt["dout"], bias=bt["bias"], act=act, block=block,
+                                                         rope_phi=phi)
+    np.testing.assert_allclose(out, rout.numpy(), rtol=1e-11, atol=1e-12)
+    for a, r in ((dq, rdq), (dk, rdk), (dv, rdv), (db, rdb)):
+        np.testing.assert_allclose(a, r.numpy(), rtol=1e-11, atol=1e-12)
+
+
+def test_rope_identity_table_is_no_rope():
+    """Angle 0 everywhere: outputs and gradients equal the unrotated oracle exactly."""
+    bt = batch(53, [70, 9, 130], [70, 9, 130], nb=4)
+    cos, sin = W.rope_table(130, 8, "identity")
+    for block in (0, 64):
+        a = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], block=block,
+                           rope=(cos, sin))[0]
+        b = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], block=block)[0]
+        np.testing.assert_array_equal(a, b)
+        ga = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"], bias=bt["bias"],
+                             block=block, rope=(cos, sin))
+        gb = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"], bias=bt["bias"],
+                             block=block)
+        for x, y in zip(ga[:3], gb[:3]):
+            np.testing.assert_array_equal(x, y)
+
+
+def _ladder(P, D, shift=0):
+    inv = 10000.0 ** (-2.0 * np.arange(D // 2) / D)
+    phi = (np.arange(P)[:, None] + shift) * inv[None, :]
+    return np.cos(phi), np.sin(phi)
+
+
+@pytest.mark.parametrize("block", [0, 64])
+def test_rope_scores_depend_on_offset_only(block):
+    """With angles linear in the position, <R_i q, R_j k> depends on i - j only:
+    starting every sequence at position 37 instead of 0 leaves O (and dV)
+    unchanged.  Rotating K the wrong way (angle -phi) breaks this."""
+    bt = batch(54, [70, 9, 130], [70, 9, 130], nb=4)
+    r0, r37 = _ladder(130, 8), _ladder(130, 8, shift=37)
+    o0 = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], block=block, rope=r0)[0]
+    o37 = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt["bias"], block=block,
+                         rope=r37)[0]
+    np.testing.assert_allclose(o0, o37, rtol=1e-11, atol=1e-12)
+    g0 = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"], bias=bt["bias"],
+                         block=block, rope=r0)
+    g37 = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"], bias=bt["bias"],
+                          block=block, rope=r37)
+    np.testing.assert_allclose(g0[2], g37[2], rtol=1e-11, atol=1e-12)
+
+    def planted(rope):  # a slip planted on the CPU: K rotated by -phi
+        q = oracle.rope_rotate(bt["q"], bt["q_off"], rope[0], rope[1])
+        k = oracle.rope_rotate(bt["k"], bt["kv_off"], rope[0], rope[1], transpose=True)
+        return oracle.forward(bt["q_off"], bt["kv_off"], q, k, bt["v"], bias=bt["bias"], block=block)[0]
+
+    assert np.abs(planted(r0) - planted(r37)).max() > 1e-3
+
+
+def test_rope_preserves_norms_and_transpose_inverts():
+    bt = batch(55, [40, 17], [40, 17], D=16)
+    cos, sin = _ladder(40, 16)
+    y = oracle.rope_rotate(bt["q"], bt["q_off"], cos, sin)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(bt["q"].numpy(), axis=-1), rtol=1e-13)
+    np.testing.assert_allclose(oracle.rope_rotate(y, bt["q_off"], cos, sin, transpose=True), bt["q"].numpy(),
+                               rtol=0, atol=1e-13)
