@@ -141,7 +141,13 @@ def sample_sequences(q_off, kv_off, frac: float, seed: int = 0):
     return sorted(picked)
 
 
-def time_oracle(batch: W.Batch, frac: float, seed: int = 0):
+def rope_tables(batch: W.Batch, w: W.Workload):
+    """Standard rotary tables (cos, sin) covering the batch's longest sequence."""
+    longest = int(max(np.diff(batch.q_off.astype(np.int64)).max(), np.diff(batch.kv_off.astype(np.int64)).max()))
+    return W.rope_table(longest, w.D, "standard")
+
+
+def time_oracle(batch: W.Batch, frac: float, seed: int = 0, rope=None):
     from oracle import oracle
     w = batch.w
     seqs = sample_sequences(batch.q_off, batch.kv_off, frac, seed)
@@ -150,9 +156,9 @@ def time_oracle(batch: W.Batch, frac: float, seed: int = 0):
     nthreads = oracle.default_threads()
     t0 = time.perf_counter()
     oracle.forward(qo, ko, q, k, v, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
-                   nthreads=nthreads, window=w.window)
+                   nthreads=nthreads, window=w.window, rope=rope)
     oracle.backward(qo, ko, q, k, v, dout, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
-                    nthreads=nthreads, window=w.window)
+                    nthreads=nthreads, window=w.window, rope=rope)
     dt = time.perf_counter() - t0
     f, b = W.flops(qo, ko, w.H, w.D, w.block, w.window)
     desc = "%d of %d sequences (seeded), %.1f%% of the valid pairs" % (
@@ -162,14 +168,15 @@ def time_oracle(batch: W.Batch, frac: float, seed: int = 0):
 
 
 def run_reference(args, w, batch):
+    rope = rope_tables(batch, w) if args.rope else None
     ws, rank, _ = dist_env()
     if rank != 0:
         return
     for _ in range(args.warmup):
-        time_oracle(batch, args.ref_frac, seed=1)
+        time_oracle(batch, args.ref_frac, seed=1, rope=rope)
     vals, times = [], []
     for s in range(args.steps):
-        v, dt, cores, desc = time_oracle(batch, args.ref_frac, seed=2 + s)
+        v, dt, cores, desc = time_oracle(batch, args.ref_frac, seed=2 + s, rope=rope)
         vals.append(v)
         times.append(dt)
     value = float(np.mean(vals))
@@ -266,11 +273,14 @@ def run_ours(args, w, batch):
     fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
     bws = torch.empty(max(plan.bwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    rope = rope_tables(batch, w) if args.rope else None
+    rp = None if rope is None else tuple(t.to(dev) for t in rope)
 
     def step():
         plan.update(batch.q_off, batch.kv_off, stream)
-        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
-        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream,
+                 rope=rp)
 
     for _ in range(args.warmup):
         step()
@@ -311,9 +321,10 @@ def run_ours(args, w, batch):
         plan.update(batch.q_off, batch.kv_off, stream)
         starts[s].record(stream)
         plan.set_events(kev[s][0:n_fwd + 1])
-        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
         plan.set_events(kev[s][n_fwd:])
-        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream,
+                 rope=rp)
         ends[s].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -368,9 +379,10 @@ def run_ours(args, w, batch):
         cap = torch.cuda.Stream(device=dev)
         cap.wait_stream(stream)
         with torch.cuda.graph(g_f, stream=cap):
-            plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=cap)
+            plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=cap, rope=rp)
         with torch.cuda.graph(g_b, stream=cap):
-            plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=cap)
+            plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=cap,
+                     rope=rp)
         stream.wait_stream(cap)
         gev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
         with torch.cuda.stream(stream):
@@ -401,8 +413,9 @@ def run_ours(args, w, batch):
                  "note": "fwd and bwd launches replayed from CUDA graphs; plan update not included"}
         del g_f, g_b
 
-    # end to end through the public API with host buffers
-    e2e = run_e2e(args, w, batch, plan, dev, stream) if not args.no_e2e else None
+    # end to end through the public API with host buffers (the host-buffer step
+    # has no rotary-embedding form)
+    e2e = run_e2e(args, w, batch, plan, dev, stream) if not (args.no_e2e or args.rope) else None
     if ws > 1 and e2e is not None:
         t = torch.tensor([e2e["ms_per_step"]], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -412,7 +425,9 @@ def run_ours(args, w, batch):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, batch.act, batch.B, True, ws, args.global_B),
+            "config": dict(workload_config(w, batch.act, batch.B, True, ws, args.global_B),
+                           **({"rope": "Q and K rotated in the kernels, standard table (base 10000)"}
+                              if args.rope else {})),
             "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
             "pct_of_bf16_peak_sustained": 100.0 * value / ws / pk["bf16_tflops_sustained"],
             "per_kernel_ms": per_kernel, "gpu_launches": int(launches),
@@ -428,7 +443,7 @@ def run_ours(args, w, batch):
         line["e2e"] = {k2: e2e[k2] for k2 in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
         line["e2e"]["ms_per_step"] = e2e["ms_per_step"]
     if rank == 0 and ws == 1 and not args.no_cpu:
-        v_cpu, dt, cores, desc = time_oracle(batch, args.cpu_frac, seed=0)
+        v_cpu, dt, cores, desc = time_oracle(batch, args.cpu_frac, seed=0, rope=rope)
         line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     if ws > 1:
@@ -497,6 +512,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--rope", action="store_true",
+                    help="rotary position embedding of Q and K (standard frequency table; block workload only)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window W (keys with |i - j| < W) on the chosen workload; 0 = off")
     args = ap.parse_args()
@@ -520,6 +537,8 @@ def main():
         args.global_B = int(ws * w.B)
     else:
         batch = W.make_batch(args.workload, act=act)
+    if args.rope and not batch.w.block:
+        ap.error("--rope runs on the BlockAttention workload (--workload 5)")
     if args.window:
         if batch.w.block:
             ap.error("--window does not combine with the block workload")

@@ -165,6 +165,46 @@ jattn_status jattn_bwd(const jattn_plan *plan, const void *dout, const void *q, 
                        float *dbias, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * Rotary position embedding (RoPE) on the BlockAttention path ("Training GEM at
+ * LLM scale", section "BlockAttention": RoPE, with its backward fused into the
+ * attention epilogue).  The angle tables are the caller's.
+ */
+typedef struct {
+    const float *cos; /* DEVICE float32 [rows, D/2], row p = position p: cos of the angle of feature pair d */
+    const float *sin; /* DEVICE float32 [rows, D/2]: sin of the same angles */
+    int32_t rows;     /* positions 0 .. rows-1; must cover the longest sequence of the batch */
+} jattn_rope;
+
+/*
+ * jattn_fwd with Q and K rotated before the scores.  Row i of a sequence sits at
+ * local position p = i; each feature pair (d, d + D/2), d < D/2, is turned:
+ *   q'[d] = q[d] c - q[d + D/2] s,   q'[d + D/2] = q[d + D/2] c + q[d] s,
+ * with c = cos[p * D/2 + d] and s = sin[p * D/2 + d]; K likewise.  The kernel
+ * rotates each Q and K tile in shared memory as it arrives (in float32, rounded
+ * to bf16 for the tensor cores); no rotated copy of Q or K is written.
+ * rope = NULL: exactly jattn_fwd.  Otherwise the plan must be BlockAttention
+ * (mode.block = 64) on bf16 data with D in {64, 128}, else
+ * JATTN_ERR_UNSUPPORTED.  cos or sin NULL, or rows below the longest sequence:
+ * JATTN_ERR_INVALID_ARG.  cos or sin not 16-byte aligned: JATTN_ERR_ALIGNMENT.
+ * The tables are read, never written, and must stay valid until the kernel ends.
+ */
+jattn_status jattn_fwd_rope(const jattn_plan *plan, const void *q, const void *k, const void *v, const float *bias,
+                            const jattn_rope *rope, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream);
+
+/*
+ * jattn_bwd for a forward made by jattn_fwd_rope with the same tables.  q and k
+ * are the unrotated inputs; dq and dk are the gradients of the unrotated Q and
+ * K.  The kernel rotates the loaded Q and K tiles again.  Its epilogue applies
+ * the transposed rotation to dQ and dK in float32, before the bf16 store:
+ *   dq[d] = c g[d] + s g[d + D/2],   dq[d + D/2] = c g[d + D/2] - s g[d],
+ * where g is the gradient of the rotated rows.  Errors: as jattn_fwd_rope.
+ */
+jattn_status jattn_bwd_rope(const jattn_plan *plan, const void *dout, const void *q, const void *k, const void *v,
+                            const float *bias, const jattn_rope *rope, const void *out, const float *lse, void *dq,
+                            void *dk, void *dv, float *dbias, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Profiling hook (optional).  After this call every jattn_fwd / jattn_bwd on
  * the plan records events[0] on its stream before its first kernel and
  * events[i] right after its i-th kernel (i < n_events), so elapsed times

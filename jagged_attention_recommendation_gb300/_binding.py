@@ -24,7 +24,7 @@ TILES_Q, TILES_KV = 0, 1
 EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd_workspace_bytes",
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
             "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
-            "jattn_shard", "jattn_step_host", "jattn_step_host_join")
+            "jattn_shard", "jattn_step_host", "jattn_step_host_join", "jattn_fwd_rope", "jattn_bwd_rope")
 
 
 class JattnError(RuntimeError):
@@ -39,6 +39,23 @@ class JattnError(RuntimeError):
 class Mode(ctypes.Structure):
     _fields_ = [("act", ctypes.c_int32), ("block", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("bias_buckets", ctypes.c_int32), ("dtype", ctypes.c_int32), ("window", ctypes.c_int32)]
+
+
+class Rope(ctypes.Structure):
+    _fields_ = [("cos", ctypes.c_void_p), ("sin", ctypes.c_void_p), ("rows", ctypes.c_int32)]
+
+
+def _rope(rope):
+    """(cos, sin) float32 device tensors [P, D/2] -> a jattn_rope (kept alive by
+    the caller's tensors for the call), or None."""
+    if rope is None:
+        return None
+    cos, sin = rope
+    if cos.shape != sin.shape or cos.dim() != 2:
+        raise ValueError("rope tables: cos and sin must both be [P, D/2]")
+    if cos.dtype != torch.float32 or sin.dtype != torch.float32 or not cos.is_contiguous() or not sin.is_contiguous():
+        raise ValueError("rope tables: contiguous float32 tensors expected")
+    return Rope(cos.data_ptr(), sin.data_ptr(), int(cos.shape[0]))
 
 
 class TileRec(ctypes.Structure):
@@ -66,6 +83,10 @@ def load():
     lib.jattn_plan_destroy.restype = None
     lib.jattn_fwd.argtypes = [P, P, P, P, P, P, P, P, sz, P]
     lib.jattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.jattn_fwd_rope.argtypes = [P, P, P, P, P, ctypes.POINTER(Rope), P, P, P, sz, P]
+    lib.jattn_fwd_rope.restype = i32
+    lib.jattn_bwd_rope.argtypes = [P, P, P, P, P, P, ctypes.POINTER(Rope), P, P, P, P, P, P, P, sz, P]
+    lib.jattn_bwd_rope.restype = i32
     lib.jattn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.jattn_bwd_noalloc.restype = i32
     lib.jattn_step_host.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P, P, P]
@@ -184,27 +205,40 @@ class Plan:
             ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda:%d" % self.device)
         return ws
 
-    def fwd(self, q, k, v, bias=None, out=None, lse=None, want_lse=True, workspace=None, stream=None):
-        """Forward.  Returns (out, lse or None)."""
+    def fwd(self, q, k, v, bias=None, out=None, lse=None, want_lse=True, workspace=None, stream=None, rope=None):
+        """Forward.  Returns (out, lse or None).  rope = (cos, sin): rotary
+        position embedding of Q and K (jattn_fwd_rope)."""
         if out is None:
             out = torch.empty(self.Tq, self.H, self.D, dtype=self._tdtype(), device=q.device)
         if lse is None and want_lse and self.act == SOFTMAX:
             lse = torch.empty(self.H, self.Tq, dtype=torch.float32, device=q.device)
         ws = self._ws(self.fwd_workspace_bytes, workspace)
         nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+        if rope is not None:
+            r = _rope(rope)
+            _check(load().jattn_fwd_rope(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(bias), ctypes.byref(r), _ptr(out),
+                                         _ptr(lse), _ptr(ws), nbytes, _stream(stream)), "jattn_fwd_rope")
+            return out, lse
         _check(load().jattn_fwd(self._h, _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse), _ptr(ws),
                                 nbytes, _stream(stream)), "jattn_fwd")
         return out, lse
 
     def bwd(self, dout, q, k, v, out, lse=None, bias=None, dq=None, dk=None, dv=None, dbias=None, workspace=None,
-            stream=None):
-        """Backward.  Returns (dq, dk, dv)."""
+            stream=None, rope=None):
+        """Backward.  Returns (dq, dk, dv).  rope = (cos, sin) as in fwd: dq and
+        dk are then the gradients of the unrotated Q and K (jattn_bwd_rope)."""
         dt = self._tdtype()
         dq = torch.empty(self.Tq, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
         dk = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dk is None else dk
         dv = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dv is None else dv
         ws = self._ws(self.bwd_workspace_bytes, workspace)
         nbytes = 0 if ws is None else ws.numel() * ws.element_size()
+        if rope is not None:
+            r = _rope(rope)
+            _check(load().jattn_bwd_rope(self._h, _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), ctypes.byref(r),
+                                         _ptr(out), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(ws),
+                                         nbytes, _stream(stream)), "jattn_bwd_rope")
+            return dq, dk, dv
         _check(load().jattn_bwd(self._h, _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out), _ptr(lse),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(ws), nbytes, _stream(stream)),
                "jattn_bwd")

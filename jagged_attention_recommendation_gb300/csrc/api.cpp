@@ -352,6 +352,25 @@ OutDesc out_desc(const jattn_plan *p, void *ptr) {
 
 int n_ctas(const jattn_plan *p, int which) { return static_cast<int>(p->cta[which].size()) - 1; }
 
+// Rotary embedding: BlockAttention plans on bf16 data with D in {64, 128};
+// the tables must cover the longest sequence of the batch.
+jattn_status check_rope(const jattn_plan *p, const jattn_rope *r) {
+    if (r == nullptr) return JATTN_OK;
+    if (p->mode.block == 0 || p->staged || (p->D != 64 && p->D != 128)) return JATTN_ERR_UNSUPPORTED;
+    if (r->cos == nullptr || r->sin == nullptr || r->rows < 1) return JATTN_ERR_INVALID_ARG;
+    if (!aligned16(r->cos) || !aligned16(r->sin)) return JATTN_ERR_ALIGNMENT;
+    int32_t longest = 0;
+    for (int32_t b = 0; b < p->B; ++b)
+        longest = std::max({longest, p->q_off[b + 1] - p->q_off[b], p->kv_off[b + 1] - p->kv_off[b]});
+    return r->rows < longest ? JATTN_ERR_INVALID_ARG : JATTN_OK;
+}
+
+void set_rope(Geom &g, const jattn_rope *r) {
+    g.rope_cos = r ? r->cos : nullptr;
+    g.rope_sin = r ? r->sin : nullptr;
+    g.rope_rows = r ? r->rows : 0;
+}
+
 // Per-call launch bookkeeping: records the profiling events (if any) and counts kernels.
 struct LaunchLog {
     const jattn_plan *p;
@@ -501,9 +520,19 @@ void jattn_plan_destroy(jattn_plan *p) {
 
 jattn_status jattn_fwd(const jattn_plan *p, const void *q, const void *k, const void *v, const float *bias, void *out,
                        float *lse, void *workspace, size_t workspace_bytes, void *stream) {
+    return jattn_fwd_rope(p, q, k, v, bias, nullptr, out, lse, workspace, workspace_bytes, stream);
+}
+
+jattn_status jattn_fwd_rope(const jattn_plan *p, const void *q, const void *k, const void *v, const float *bias,
+                            const jattn_rope *rope, void *out, float *lse, void *workspace, size_t workspace_bytes,
+                            void *stream) {
     if (p == nullptr) return JATTN_ERR_INVALID_ARG;
     if (p->device < 0) return JATTN_ERR_NO_DEVICE;
     if (!q || !k || !v || !out) return JATTN_ERR_INVALID_ARG;
+    {
+        const jattn_status e = check_rope(p, rope);
+        if (e != JATTN_OK) return e;
+    }
     if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;
     if (lse != nullptr && p->mode.act != JATTN_SOFTMAX) return JATTN_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse) || !aligned16(bias))
@@ -538,16 +567,30 @@ jattn_status jattn_fwd(const jattn_plan *p, const void *q, const void *k, const 
     a.g.bias = bias;
     a.out = out_desc(p, out);
     a.lse = lse;
-    return cuda_status(log.done(launch_fwd(p->Dp, p->mode.act != JATTN_SOFTMAX, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
+    set_rope(a.g, rope);
+    const bool act = p->mode.act != JATTN_SOFTMAX;
+    return cuda_status(log.done(rope ? launch_fwd_rope(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)
+                                     : launch_fwd(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
                        "jattn_fwd: forward kernel launch");
 }
 
 jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, const void *k, const void *v,
                        const float *bias, const void *out, const float *lse, void *dq, void *dk, void *dv,
                        float *dbias, void *workspace, size_t workspace_bytes, void *stream) {
+    return jattn_bwd_rope(p, dout, q, k, v, bias, nullptr, out, lse, dq, dk, dv, dbias, workspace, workspace_bytes,
+                          stream);
+}
+
+jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q, const void *k, const void *v,
+                            const float *bias, const jattn_rope *rope, const void *out, const float *lse, void *dq,
+                            void *dk, void *dv, float *dbias, void *workspace, size_t workspace_bytes, void *stream) {
     if (p == nullptr) return JATTN_ERR_INVALID_ARG;
     if (p->device < 0) return JATTN_ERR_NO_DEVICE;
     if (!dout || !q || !k || !v || !out || !dq || !dk || !dv) return JATTN_ERR_INVALID_ARG;
+    {
+        const jattn_status e = check_rope(p, rope);
+        if (e != JATTN_OK) return e;
+    }
     if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;
     if (softmax_full(p) && lse == nullptr) return JATTN_ERR_INVALID_ARG;
     if (dbias != nullptr && bias == nullptr) return JATTN_ERR_INVALID_ARG;
@@ -601,6 +644,7 @@ jattn_status jattn_bwd(const jattn_plan *p, const void *dout, const void *q, con
             return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
         a.g = make_geom(p, JATTN_TILES_Q);
         a.g.bias = bias;
+        set_rope(a.g, rope);
         return cuda_status(log.done(launch_bwd_block(p->Dp, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
                            "jattn_bwd: block kernel launch");
     }

@@ -25,7 +25,9 @@ __device__ __forceinline__ bool check_tile(const Geom &g, const Tile &t, const E
     bool ok = t.b >= 0 && t.b < g.B && t.h >= 0 && t.h < g.H && t.q_len >= 0 && t.q_len <= g.max_q_len &&
               t.kv_len >= 0 && t.kv_len <= g.max_kv_len && t.q_start >= 0 && t.kv_start >= 0 &&
               t.q_loc0 >= 0 && t.kv_loc0 >= 0 && static_cast<int64_t>(t.q_start) + t.q_len <= g.Tq &&
-              static_cast<int64_t>(t.kv_start) + t.kv_len <= g.Tk;
+              static_cast<int64_t>(t.kv_start) + t.kv_len <= g.Tk &&
+              (g.rope_cos == nullptr ||
+               (t.q_loc0 + t.q_len <= g.rope_rows && t.kv_loc0 + t.kv_len <= g.rope_rows));
     if (!ok && report) raise_error(e, kStatusDeviceCheck);
     return ok;
 }
@@ -115,6 +117,79 @@ __device__ __forceinline__ void st_row32_zero(uint32_t tile, uint32_t sub_bytes,
     const uint32_t k0 = (c0 & 63u) >> 3;
 #pragma unroll
     for (int k = 0; k < 4; ++k) st_shared_v4(base + sw128_offset(row, k0 + k), 0u, 0u, 0u, 0u);
+}
+
+// Rotary position embedding, in place, of rows [0, nrows) of one or two
+// [128, D] bf16 operand tiles in 128B-swizzled shared memory (D/64 sub-tiles of
+// 128 rows x 64 columns, sub_bytes apart; tile2 = 0: one tile).  Row r of
+// both tiles sits at the same position, whose cos and sin rows (D/2 floats
+// each) start at tc + r * D/2 and ts + r * D/2 (generic pointers: shared or
+// global memory).  Feature pair (d, d + D/2), d < D/2, with c = cos, s = sin:
+//   x[d] <- x[d] c - x[d + D/2] s,   x[d + D/2] <- x[d + D/2] c + x[d] s,
+// in float32 with a fixed operation order, rounded to bf16.  One warp: lane l
+// takes 16-byte chunk pair l % (D/16) (8 feature pairs) of every (32 / (D/16))-th
+// row from row l / (D/16).
+__device__ __forceinline__ void rope_pair8(uint32_t alo, uint32_t ahi, const float4 *pc, const float4 *ps) {
+    uint4 x = ld_shared_v4(alo), y = ld_shared_v4(ahi);
+    uint32_t *xw = reinterpret_cast<uint32_t *>(&x), *yw = reinterpret_cast<uint32_t *>(&y);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {  // four feature pairs per table load
+        const float4 c4 = pc[h], s4 = ps[h];
+        const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+            const int e = 2 * h + e2;
+            const float x0 = __uint_as_float(xw[e] << 16), x1 = __uint_as_float(xw[e] & 0xffff0000u);
+            const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xffff0000u);
+            const float a0 = __fmaf_rn(x0, c[2 * e2], __fmul_rn(-y0, sn[2 * e2]));
+            const float a1 = __fmaf_rn(x1, c[2 * e2 + 1], __fmul_rn(-y1, sn[2 * e2 + 1]));
+            const float b0 = __fmaf_rn(y0, c[2 * e2], __fmul_rn(x0, sn[2 * e2]));
+            const float b1 = __fmaf_rn(y1, c[2 * e2 + 1], __fmul_rn(x1, sn[2 * e2 + 1]));
+            xw[e] = pack_bf16x2(a0, a1);
+            yw[e] = pack_bf16x2(b0, b1);
+        }
+    }
+    st_shared_v4(alo, x.x, x.y, x.z, x.w);
+    st_shared_v4(ahi, y.x, y.y, y.z, y.w);
+}
+
+template <int D>
+__device__ __forceinline__ void rope_tile(uint32_t tile, uint32_t tile2, uint32_t sub_bytes, int nrows,
+                                          const float *tc, const float *ts, int lane) {
+    constexpr int NCP = D / 16;      // 16-byte chunk pairs per row
+    constexpr int RSTEP = 32 / NCP;  // rows per pass of the warp
+    const int cp = lane % NCP;
+    const uint32_t lo_col = cp * 8, hi_col = cp * 8 + D / 2;
+    const uint32_t lo_off = (lo_col >> 6) * sub_bytes, hi_off = (hi_col >> 6) * sub_bytes;
+    const uint32_t lo_chunk = (lo_col & 63u) >> 3, hi_chunk = (hi_col & 63u) >> 3;
+#pragma unroll 1
+    for (int r = lane / NCP; r < nrows; r += RSTEP) {
+        const float4 *pc = reinterpret_cast<const float4 *>(tc + r * (D / 2) + cp * 8);
+        const float4 *ps = reinterpret_cast<const float4 *>(ts + r * (D / 2) + cp * 8);
+        const uint32_t olo = lo_off + sw128_offset(r, lo_chunk), ohi = hi_off + sw128_offset(r, hi_chunk);
+        rope_pair8(tile + olo, tile + ohi, pc, ps);
+        if (tile2 != 0u) rope_pair8(tile2 + olo, tile2 + ohi, pc, ps);
+    }
+}
+
+// The transposed rotation of 32 + 32 float32 values of one row (features
+// d0..d0+31 in lo, d0+D/2.. in hi), which carries a gradient with respect to
+// the rotated row back to the unrotated one:
+//   g[d] = c x[d] + s x[d + D/2],   g[d + D/2] = c x[d + D/2] - s x[d].
+// tc, ts: the row's cos and sin from feature d0 on (global memory).
+__device__ __forceinline__ void rope_grad32(float (&lo)[32], float (&hi)[32], const float *tc, const float *ts) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 c = *reinterpret_cast<const float4 *>(tc + i);
+        const float4 s = *reinterpret_cast<const float4 *>(ts + i);
+        const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x = lo[i + e], y = hi[i + e];
+            lo[i + e] = __fmaf_rn(x, cc[e], __fmul_rn(y, ss[e]));
+            hi[i + e] = __fmaf_rn(y, cc[e], __fmul_rn(-x, ss[e]));
+        }
+    }
 }
 
 // Sliding window |p - o| < W on local positions: bit k is set when position

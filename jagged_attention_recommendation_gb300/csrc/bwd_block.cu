@@ -15,6 +15,12 @@
 // the diagonal blocks) and read by the tensor cores both as K-major and as
 // MN-major operands, so no transpose is ever materialised.  In activation mode
 // dS is unnormalised and also gets its bf16 remainder plane (hi + lo).
+// With rotary position embedding (ROPE; same section: RoPE's backward fused
+// into the attention epilogue) a seventh warp rotates each chunk's Q and K rows
+// in shared memory as they arrive, the products run on the rotated operands,
+// and the epilogue applies the transposed rotation to dQ and dK in float32,
+// before the bf16 store, so the gradients leave for the unrotated inputs and
+// no separate rotary kernel reads or writes them.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -38,8 +44,8 @@ struct BlkCfg {
     static constexpr uint32_t OFF_DS = OFF_P + M_BYTES;
     static constexpr uint32_t OFF_DSLO = OFF_DS + M_BYTES;  // bf16 remainder of dS (activation mode)
     static constexpr uint32_t OFF_BAR = OFF_DSLO + M_BYTES;
-    // in_full[NBUF], in_empty[NBUF], s_full, pd_full, acc_full, acc_empty, drain
-    static constexpr int NBAR = 2 * NBUF + 5;
+    // in_full[NBUF], in_empty[NBUF], s_full, pd_full, acc_full, acc_empty, drain, rot_full[NBUF]
+    static constexpr int NBAR = 3 * NBUF + 5;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
@@ -54,8 +60,8 @@ struct BlkCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
-template <int D>
-__global__ void __launch_bounds__(192, 1)
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
     bwd_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const BwdArgs a) {
@@ -74,6 +80,7 @@ __global__ void __launch_bounds__(192, 1)
     uint64_t *acc_full = pd_full + 1;
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *drain = acc_empty + 1;
+    uint64_t *rot_full = drain + 1;  // [NBUF] RoPE: the buffer's Q and K rows are rotated
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
@@ -93,6 +100,7 @@ __global__ void __launch_bounds__(192, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         mbar_init(drain, 1);
+        for (int b = 0; b < C::NBUF; ++b) mbar_init(&rot_full[b], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -154,7 +162,7 @@ __global__ void __launch_bounds__(192, 1)
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, false)) continue;
                 const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
-                if (!(ok = mbar_wait(&in_full[buf], use & 1, err))) break;
+                if (!(ok = mbar_wait(ROPE ? &rot_full[buf] : &in_full[buf], use & 1, err))) break;
                 if (!(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
                 tc_fence_after();
                 const uint32_t base = sIn + buf * C::IN_BYTES;
@@ -197,7 +205,26 @@ __global__ void __launch_bounds__(192, 1)
             mma_commit(drain);
             mbar_drain(drain, 0);
         }
-    } else {
+    } else if (ROPE && warp == 6) {
+        // RoPE: rotate the chunk's Q and K rows (the same positions) in place as
+        // soon as they land; the products wait for rot_full.
+        uint32_t t_local = 0;
+        bool ok = true;
+        TileStream ts(g, tbeg, tend);
+        Tile t;
+        while (ok && ts.next(t)) {
+            if (!check_tile(g, t, err, false)) continue;
+            const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
+            if (!(ok = mbar_wait_warp(&in_full[buf], use & 1, err))) break;
+            const uint32_t base = sIn + buf * C::IN_BYTES;
+            const int64_t r0 = static_cast<int64_t>(t.q_loc0) * (D / 2);
+            rope_tile<D>(base + C::IQ, base + C::IK, C::SUB, t.q_len, g.rope_cos + r0, g.rope_sin + r0, lane);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rot_full[buf]);
+            ++t_local;
+        }
+    } else if (warp >= 2 && warp < 6) {
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const int half = row >> 6;  // which 64-block of the chunk this row belongs to
@@ -327,19 +354,66 @@ __global__ void __launch_bounds__(192, 1)
                 for (int pass = 0; pass < 3; ++pass) {
                     const uint32_t col = pass == 0 ? C::COL_S : (pass == 1 ? C::COL_DK : C::COL_DV);
                     const float mul = pass == 2 ? 1.0f : g.scale;
+                    if (ROPE && pass < 2) {
+                        // dQ / dK of the rotated rows -> of the unrotated ones: the
+                        // transposed rotation at the row's position, in float32
+                        const int64_t pr = static_cast<int64_t>((pass == 0 ? t.q_loc0 : t.kv_loc0) + (row_ok ? row : 0));
+                        const float *tc = g.rope_cos + pr * (D / 2), *tsn = g.rope_sin + pr * (D / 2);
+#pragma unroll 1
+                        for (int cp = 0; cp < D / 64; ++cp) {
+                            float lo[32], hi[32];
+                            tmem_ld32x2(tmem + lane_base + col + cp * 32, tmem + lane_base + col + D / 2 + cp * 32,
+                                        lo, hi);
 #pragma unroll
-                    for (int hc = 0; hc < D / 64; ++hc) {
-                        float oa[64];
-                        tmem_ld64(tmem + lane_base + col + hc * 64, oa);
+                            for (int i = 0; i < 32; i += 2) {
+                                mul2(lo[i], lo[i + 1], mul, mul);
+                                mul2(hi[i], hi[i + 1], mul, mul);
+                            }
+                            rope_grad32(lo, hi, tc + cp * 32, tsn + cp * 32);
+                            st_row32_bf16(sP, C::SUB, row, cp * 32, lo);
+                            st_row32_bf16(sP, C::SUB, row, D / 2 + cp * 32, hi);
+                        }
+                    } else {
 #pragma unroll
-                        for (int i = 0; i < 64; i += 2) mul2(oa[i], oa[i + 1], mul, mul);
-                        st_row32_bf16(sP, C::SUB, row, hc * 64, sub32(oa, 0));
-                        st_row32_bf16(sP, C::SUB, row, hc * 64 + 32, sub32(oa, 1));
+                        for (int hc = 0; hc < D / 64; ++hc) {
+                            float oa[64];
+                            tmem_ld64(tmem + lane_base + col + hc * 64, oa);
+#pragma unroll
+                            for (int i = 0; i < 64; i += 2) mul2(oa[i], oa[i + 1], mul, mul);
+                            st_row32_bf16(sP, C::SUB, row, hc * 64, sub32(oa, 0));
+                            st_row32_bf16(sP, C::SUB, row, hc * 64 + 32, sub32(oa, 1));
+                        }
                     }
                     __syncwarp();
                     copy_rows_out<D>(sP, C::SUB, quad * 32, len, pass == 0 ? a.dq : (pass == 1 ? a.dk : a.dv),
                                      pass == 0 ? t.q_start : t.kv_start, t.h, lane);
                     __syncwarp();
+                }
+            } else if (ROPE) {
+                // the same with direct stores (bf16 data with D in {64, 128}
+                // takes the staged path above; this keeps the kernel whole)
+                for (int pass = 0; pass < 2; ++pass) {
+                    const uint32_t col = pass == 0 ? C::COL_S : C::COL_DK;
+                    const int64_t pr = static_cast<int64_t>((pass == 0 ? t.q_loc0 : t.kv_loc0) + (row_ok ? row : 0));
+                    const float *tc = g.rope_cos + pr * (D / 2), *tsn = g.rope_sin + pr * (D / 2);
+#pragma unroll 1
+                    for (int cp = 0; cp < D / 64; ++cp) {
+                        float lo[32], hi[32];
+                        tmem_ld32x2(tmem + lane_base + col + cp * 32, tmem + lane_base + col + D / 2 + cp * 32, lo,
+                                    hi);
+                        rope_grad32(lo, hi, tc + cp * 32, tsn + cp * 32);
+                        if (row_ok) {
+                            store_out32(pass == 0 ? a.dq : a.dk, pass == 0 ? qrow : krow, t.h, cp * 32, lo, g.scale);
+                            store_out32(pass == 0 ? a.dq : a.dk, pass == 0 ? qrow : krow, t.h, D / 2 + cp * 32, hi,
+                                        g.scale);
+                        }
+                    }
+                }
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + C::COL_DV + c * 32, o);
+                    if (row_ok) store_out32(a.dv, krow, t.h, c * 32, o, 1.0f);
                 }
             } else {
 #pragma unroll
@@ -368,19 +442,21 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
-template <int D>
+template <int D, bool ROPE>
 static cudaError_t launch_block_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = BlkCfg<D>;
     static bool done[64] = {};
-    cudaError_t e = ensure_smem(bwd_block_kernel<D>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(bwd_block_kernel<D, ROPE>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    bwd_block_kernel<D><<<n_ctas, 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    bwd_block_kernel<D, ROPE><<<n_ctas, ROPE ? 224 : 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
-    if (D == 128) return launch_block_t<128>(tm, a, n_ctas, st);
-    if (D == 64) return launch_block_t<64>(tm, a, n_ctas, st);
+    const bool rope = a.g.rope_cos != nullptr;
+    if (rope && a.g.rope_sin == nullptr) return cudaErrorInvalidValue;
+    if (D == 128) return rope ? launch_block_t<128, true>(tm, a, n_ctas, st) : launch_block_t<128, false>(tm, a, n_ctas, st);
+    if (D == 64) return rope ? launch_block_t<64, true>(tm, a, n_ctas, st) : launch_block_t<64, false>(tm, a, n_ctas, st);
     return cudaErrorInvalidValue;
 }
 

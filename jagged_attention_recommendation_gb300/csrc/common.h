@@ -53,6 +53,9 @@ struct Geom {
     float scale;              // score scale
     const float *bias;        // [H, nb] or nullptr
     int *status;              // device status word
+    const float *rope_cos;    // rotary embedding: cos [rope_rows, D/2] float32, or nullptr (off)
+    const float *rope_sin;    // ... and sin
+    int32_t rope_rows;        // table positions 0 .. rope_rows - 1
 };
 
 // Where a [T, H, D] result goes: element (t, h, c) at ptr[t*ld + h*cols + c] for c < cols.

@@ -28,11 +28,15 @@ struct TmapSet {
 // forward: D in {64, 128}; act selects the GDPA activation path
 cudaError_t launch_fwd(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream);
 
+// forward with rotary position embedding of Q and K (a.g.rope_cos / rope_sin set, no window)
+cudaError_t launch_fwd_rope(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream);
+
 // backward, full attention: dQ pass (query-major tiles) and dK/dV pass (key-major tiles)
 cudaError_t launch_bwd_dq(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
 
-// backward, BlockAttention: one fused pass over query-major tiles
+// backward, BlockAttention: one fused pass over query-major tiles (with
+// rotary position embedding when a.g.rope_cos is set)
 cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
 
 // Delta_i = <dO_i, O_i> (fp32) for every row and head: delta[h * Tq + t]

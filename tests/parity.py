@@ -19,19 +19,21 @@ def to_dev(t):
     return None if t is None else t.to("cuda:0").contiguous()
 
 
-def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, window=0):
-    """Forward (+ backward) of batch dict ``bt`` on cuda:0; returns float64 numpy arrays."""
+def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, window=0, rope=None):
+    """Forward (+ backward) of batch dict ``bt`` on cuda:0; returns float64 numpy arrays.
+    rope = (cos, sin) host float32 tables: rotary embedding of Q and K."""
     q, k, v, dout = (to_dev(bt[n]) for n in ("q", "k", "v", "dout"))
     bias = to_dev(bt["bias"].float()) if bt.get("bias") is not None else None
+    rp = None if rope is None else tuple(to_dev(t.float().contiguous()) for t in rope)
     H, D = q.shape[1], q.shape[2]
     nb = 0 if bias is None else bias.shape[1]
     if plan is None:
         plan = J.Plan(bt["q_off"], bt["kv_off"], H, D, act=act, block=block, bias_buckets=nb, dtype=dtype, device=0,
                       window=window)
-    out, lse = plan.fwd(q, k, v, bias=bias)
+    out, lse = plan.fwd(q, k, v, bias=bias, rope=rp)
     res = {"out": out, "lse": lse}
     if backward:
-        dq, dk, dv = plan.bwd(dout, q, k, v, out, lse=lse, bias=bias)
+        dq, dk, dv = plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, rope=rp)
         res.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     status = plan.check_status()
@@ -39,13 +41,14 @@ def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, wind
     return {n: (None if t is None else t.double().cpu().numpy()) for n, t in res.items()}
 
 
-def run_oracle(bt, act=0, block=0, backward=True, window=0):
+def run_oracle(bt, act=0, block=0, backward=True, window=0, rope=None):
     out, lse = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt.get("bias"),
-                              scale=bt["scale"], act=act, block=block, window=window)
+                              scale=bt["scale"], act=act, block=block, window=window, rope=rope)
     res = {"out": out, "lse": lse}
     if backward:
         dq, dk, dv, _ = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"],
-                                        bias=bt.get("bias"), scale=bt["scale"], act=act, block=block, window=window)
+                                        bias=bt.get("bias"), scale=bt["scale"], act=act, block=block, window=window,
+                                        rope=rope)
         res.update(dq=dq, dk=dk, dv=dv)
     return res
 
