@@ -40,10 +40,16 @@ def _case(case):
 
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_rope_parity(case):
+    """Against the oracle with the rotated Q and K rounded to bf16 (what the
+    tensor cores take; the same as rotating, casting and attending); softmax
+    cases also against the exact rotation.  Activation mode sums up to 64
+    unnormalised terms, so the bf16 rounding of the rotated operands alone moves
+    its outputs by up to ~0.1 from the exact rotation, beyond 1e-2 + 1e-2 |ref|."""
     bt, act, rope = _case(case)
     gpu = PT.run_library(bt, act=act, block=64, rope=rope)
-    ref = PT.run_oracle(bt, act=act, block=64, rope=rope)
-    PT.compare(gpu, ref)
+    PT.compare(gpu, PT.run_oracle(bt, act=act, block=64, rope=rope, rope_bf16=True))
+    if act == SOFTMAX:
+        PT.compare(gpu, PT.run_oracle(bt, act=act, block=64, rope=rope))
 
 
 def test_rope_identity_table_is_plain_path():
@@ -126,7 +132,7 @@ def test_rope_full_size_block_workload_sampled():
     qo, ko, (q, dout), (k, v), qidx, kidx = oracle.sub_batch(b.q_off, b.kv_off, seqs, b.q, b.dout,
                                                              tensors_kv=(b.k, b.v))
     sub = dict(q_off=qo, kv_off=ko, q=q, k=k, v=v, bias=b.bias, dout=dout, scale=b.scale)
-    ref = PT.run_oracle(sub, block=w.block, rope=rope)
+    ref = PT.run_oracle(sub, block=w.block, rope=rope, rope_bf16=True)
     PT.assert_close(gpu["out"][qidx], ref["out"], PT.FWD_TOL, "out")
     PT.assert_close(gpu["dq"][qidx], ref["dq"], PT.BWD_TOL, "dq")
     PT.assert_close(gpu["dk"][kidx], ref["dk"], PT.BWD_TOL, "dk")
