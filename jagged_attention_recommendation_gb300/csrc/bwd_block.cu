@@ -14,7 +14,9 @@
 // P and dS are written once to shared memory as 128x128 bf16 tiles (zeros off
 // the diagonal blocks) and read by the tensor cores both as K-major and as
 // MN-major operands, so no transpose is ever materialised.  In activation mode
-// dS is unnormalised and also gets its bf16 remainder plane (hi + lo).
+// P and dS are unnormalised and both get a bf16 remainder (hi + lo) in one
+// shared lo plane: P's first, read by the dV products, then dS's, read by the
+// dK and dQ products (a second hand-off, lo_free / dslo_full).
 // With rotary position embedding (ROPE; same section: RoPE's backward fused
 // into the attention epilogue) a seventh warp rotates each chunk's Q and K rows
 // in shared memory as they arrive, the products run on the rotated operands,
@@ -44,8 +46,9 @@ struct BlkCfg {
     static constexpr uint32_t OFF_DS = OFF_P + M_BYTES;
     static constexpr uint32_t OFF_DSLO = OFF_DS + M_BYTES;  // bf16 remainder of dS (activation mode)
     static constexpr uint32_t OFF_BAR = OFF_DSLO + M_BYTES;
-    // in_full[NBUF], in_empty[NBUF], s_full, pd_full, acc_full, acc_empty, drain, rot_full[NBUF]
-    static constexpr int NBAR = 3 * NBUF + 5;
+    // in_full[NBUF], in_empty[NBUF], s_full, pd_full, acc_full, acc_empty, drain, rot_full[NBUF],
+    // lo_free, dslo_full
+    static constexpr int NBAR = 3 * NBUF + 7;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
@@ -81,6 +84,8 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
     uint64_t *acc_empty = acc_full + 1;
     uint64_t *drain = acc_empty + 1;
     uint64_t *rot_full = drain + 1;  // [NBUF] RoPE: the buffer's Q and K rows are rotated
+    uint64_t *lo_free = rot_full + C::NBUF;  // activation: the dV products are done with P's lo plane
+    uint64_t *dslo_full = lo_free + 1;       // activation: dS's lo plane is written
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
@@ -101,6 +106,8 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
         mbar_init(acc_empty, 4);
         mbar_init(drain, 1);
         for (int b = 0; b < C::NBUF; ++b) mbar_init(&rot_full[b], 1);
+        mbar_init(lo_free, 1);
+        mbar_init(dslo_full, 4);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -185,12 +192,20 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
                     const uint32_t acc = ks > 0 ? 1u : 0u;
                     mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sP + ks * 2048, C::SUB, 1024),
                                 sdesc_sw128(base + C::IDO + ks * 2048, C::SUB, 1024), idesc_mn, acc);
+                    if (ACT)  // unnormalised P: its bf16 remainder, in the lo plane for now
+                        mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sDSlo + ks * 2048, C::SUB, 1024),
+                                    sdesc_sw128(base + C::IDO + ks * 2048, C::SUB, 1024), idesc_mn, 1u);
                     mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDS + ks * 2048, C::SUB, 1024),
                                 sdesc_sw128(base + C::IQ + ks * 2048, C::SUB, 1024), idesc_mn, acc);
                     // dQ += dS K: reduction over key rows ks*16..+15
                     mma_bf16_ss(tmem + C::COL_S, sdesc_sw128(sDS + (ks >> 2) * C::SUB + (ks & 3) * 32, 16, 1024),
                                 sdesc_sw128(base + C::IK + ks * 2048, C::SUB, 1024), idesc_kmn, acc);
-                    if (ACT) {  // unnormalised dS: add its bf16 remainder to dK and dQ
+                }
+                if (ACT) {  // unnormalised dS: add its bf16 remainder to dK and dQ
+                    mma_commit(lo_free);
+                    if (!(ok = mbar_wait(dslo_full, t_local & 1, err))) break;
+                    tc_fence_after();
+                    for (int ks = 0; ks < ksteps; ++ks) {
                         mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDSlo + ks * 2048, C::SUB, 1024),
                                     sdesc_sw128(base + C::IQ + ks * 2048, C::SUB, 1024), idesc_mn, 1u);
                         mma_bf16_ss(tmem + C::COL_S,
@@ -320,15 +335,16 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
                     }
             }
             // P and dS rows: this row's block gets values, the other block zeros
+            // (activation: the lo plane takes P's remainder first)
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 const uint32_t col = half * 64 + c * 32;
                 if (live[c] && row_valid) {
-                    st_row32_bf16(sP, C::SUB, row, col, sub32(s, c));
                     if (ACT)
-                        st_row32_bf16_hilo(sDS, sDSlo, C::SUB, row, col, sub32(dp, c));
+                        st_row32_bf16_hilo(sP, sDSlo, C::SUB, row, col, sub32(s, c));
                     else
-                        st_row32_bf16(sDS, C::SUB, row, col, sub32(dp, c));
+                        st_row32_bf16(sP, C::SUB, row, col, sub32(s, c));
+                    st_row32_bf16(sDS, C::SUB, row, col, sub32(dp, c));
                 } else {
                     st_row32_zero(sP, C::SUB, row, col);
                     st_row32_zero(sDS, C::SUB, row, col);
@@ -343,6 +359,29 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pd_full);
+            if (ACT) {
+                // once the dV products are done with P's remainder, the lo plane
+                // takes dS's (hi was rounded from the same values above); the rest
+                // of the plane is still zero from P's
+                if (!(ok = mbar_wait_warp(lo_free, t_local & 1, err))) break;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    if (live[c] && row_valid) {
+                        float lo[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float x = dp[c * 32 + i];
+                            lo[i] = x - __bfloat162float(__float2bfloat16_rn(x));
+                        }
+                        st_row32_bf16(sDSlo, C::SUB, row, half * 64 + c * 32, lo);
+                    }
+                }
+                fence_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dslo_full);
+            }
 
             if (!(ok = mbar_wait_warp(acc_full, t_local & 1, err))) break;
             tc_fence_after();
