@@ -119,79 +119,6 @@ __device__ __forceinline__ void st_row32_zero(uint32_t tile, uint32_t sub_bytes,
     for (int k = 0; k < 4; ++k) st_shared_v4(base + sw128_offset(row, k0 + k), 0u, 0u, 0u, 0u);
 }
 
-// Rotary position embedding, in place, of rows [0, nrows) of one or two
-// [128, D] bf16 operand tiles in 128B-swizzled shared memory (D/64 sub-tiles of
-// 128 rows x 64 columns, sub_bytes apart; tile2 = 0: one tile).  Row r of
-// both tiles sits at the same position, whose cos and sin rows (D/2 floats
-// each) start at tc + r * D/2 and ts + r * D/2 (generic pointers: shared or
-// global memory).  Feature pair (d, d + D/2), d < D/2, with c = cos, s = sin:
-//   x[d] <- x[d] c - x[d + D/2] s,   x[d + D/2] <- x[d + D/2] c + x[d] s,
-// in float32 with a fixed operation order, rounded to bf16.  One warp: lane l
-// takes 16-byte chunk pair l % (D/16) (8 feature pairs) of every (32 / (D/16))-th
-// row from row l / (D/16).
-__device__ __forceinline__ void rope_pair8(uint32_t alo, uint32_t ahi, const float4 *pc, const float4 *ps) {
-    uint4 x = ld_shared_v4(alo), y = ld_shared_v4(ahi);
-    uint32_t *xw = reinterpret_cast<uint32_t *>(&x), *yw = reinterpret_cast<uint32_t *>(&y);
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {  // four feature pairs per table load
-        const float4 c4 = pc[h], s4 = ps[h];
-        const float c[4] = {c4.x, c4.y, c4.z, c4.w}, sn[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-            const int e = 2 * h + e2;
-            const float x0 = __uint_as_float(xw[e] << 16), x1 = __uint_as_float(xw[e] & 0xffff0000u);
-            const float y0 = __uint_as_float(yw[e] << 16), y1 = __uint_as_float(yw[e] & 0xffff0000u);
-            const float a0 = __fmaf_rn(x0, c[2 * e2], __fmul_rn(-y0, sn[2 * e2]));
-            const float a1 = __fmaf_rn(x1, c[2 * e2 + 1], __fmul_rn(-y1, sn[2 * e2 + 1]));
-            const float b0 = __fmaf_rn(y0, c[2 * e2], __fmul_rn(x0, sn[2 * e2]));
-            const float b1 = __fmaf_rn(y1, c[2 * e2 + 1], __fmul_rn(x1, sn[2 * e2 + 1]));
-            xw[e] = pack_bf16x2(a0, a1);
-            yw[e] = pack_bf16x2(b0, b1);
-        }
-    }
-    st_shared_v4(alo, x.x, x.y, x.z, x.w);
-    st_shared_v4(ahi, y.x, y.y, y.z, y.w);
-}
-
-template <int D>
-__device__ __forceinline__ void rope_tile(uint32_t tile, uint32_t tile2, uint32_t sub_bytes, int nrows,
-                                          const float *tc, const float *ts, int lane) {
-    constexpr int NCP = D / 16;      // 16-byte chunk pairs per row
-    constexpr int RSTEP = 32 / NCP;  // rows per pass of the warp
-    const int cp = lane % NCP;
-    const uint32_t lo_col = cp * 8, hi_col = cp * 8 + D / 2;
-    const uint32_t lo_off = (lo_col >> 6) * sub_bytes, hi_off = (hi_col >> 6) * sub_bytes;
-    const uint32_t lo_chunk = (lo_col & 63u) >> 3, hi_chunk = (hi_col & 63u) >> 3;
-#pragma unroll 1
-    for (int r = lane / NCP; r < nrows; r += RSTEP) {
-        const float4 *pc = reinterpret_cast<const float4 *>(tc + r * (D / 2) + cp * 8);
-        const float4 *ps = reinterpret_cast<const float4 *>(ts + r * (D / 2) + cp * 8);
-        const uint32_t olo = lo_off + sw128_offset(r, lo_chunk), ohi = hi_off + sw128_offset(r, hi_chunk);
-        rope_pair8(tile + olo, tile + ohi, pc, ps);
-        if (tile2 != 0u) rope_pair8(tile2 + olo, tile2 + ohi, pc, ps);
-    }
-}
-
-// The transposed rotation of 32 + 32 float32 values of one row (features
-// d0..d0+31 in lo, d0+D/2.. in hi), which carries a gradient with respect to
-// the rotated row back to the unrotated one:
-//   g[d] = c x[d] + s x[d + D/2],   g[d + D/2] = c x[d + D/2] - s x[d].
-// tc, ts: the row's cos and sin from feature d0 on (global memory).
-__device__ __forceinline__ void rope_grad32(float (&lo)[32], float (&hi)[32], const float *tc, const float *ts) {
-#pragma unroll
-    for (int i = 0; i < 32; i += 4) {
-        const float4 c = *reinterpret_cast<const float4 *>(tc + i);
-        const float4 s = *reinterpret_cast<const float4 *>(ts + i);
-        const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float x = lo[i + e], y = hi[i + e];
-            lo[i + e] = __fmaf_rn(x, cc[e], __fmul_rn(y, ss[e]));
-            hi[i + e] = __fmaf_rn(y, cc[e], __fmul_rn(-x, ss[e]));
-        }
-    }
-}
-
 // Sliding window |p - o| < W on local positions: bit k is set when position
 // o0 + k of the other side is inside row p's band (all bits when W == 0).
 __device__ __forceinline__ uint32_t window_bits32(int W, int p, int o0) {
@@ -573,6 +500,107 @@ __device__ __forceinline__ float (&sub64(float (&a)[N], int c))[64] {
 template <int N>
 __device__ __forceinline__ float (&sub32(float (&a)[N], int c))[32] {
     return *reinterpret_cast<float(*)[32]>(&a[32 * c]);
+}
+
+// Rotary position embedding, in place, of rows [0, nrows) of one or two
+// [128, D] bf16 operand tiles in 128B-swizzled shared memory (D/64 sub-tiles of
+// 128 rows x 64 columns, sub_bytes apart; tile2 = 0: one tile).  Row r of
+// both tiles sits at the same position, whose cos and sin rows (D/2 floats
+// each) start at tc + r * D/2 and ts + r * D/2 (generic pointers: shared or
+// global memory).  Feature pair (d, d + D/2), d < D/2, with c = cos, s = sin:
+//   x[d] <- x[d] c - x[d + D/2] s,   x[d + D/2] <- x[d + D/2] c + x[d] s,
+// each product rounded to float32, then one fused multiply-add, then bf16.
+// One warp: a lane takes four feature pairs (16 bytes of table row, 8 of each
+// bf16 half) of one row per pass; D/8 lanes cover a row.  With D = 64 a pass
+// covers rows {0, 4, 1, 5} or {2, 6, 3, 7} of an 8-row band, so that both the
+// swizzled 8-byte tile accesses and the 16-byte table accesses of a warp spread
+// evenly over the shared-memory banks.
+__device__ __forceinline__ void rope_pairs4(uint32_t alo, uint32_t ahi, const float4 &c, const float4 &s) {
+    const uint2 x = ld_shared_v2(alo), y = ld_shared_v2(ahi);
+    float x0 = __uint_as_float(x.x << 16), x1 = __uint_as_float(x.x & 0xffff0000u);
+    float x2 = __uint_as_float(x.y << 16), x3 = __uint_as_float(x.y & 0xffff0000u);
+    float y0 = __uint_as_float(y.x << 16), y1 = __uint_as_float(y.x & 0xffff0000u);
+    float y2 = __uint_as_float(y.y << 16), y3 = __uint_as_float(y.y & 0xffff0000u);
+    // t = -y s, u = x s (rounded), then a = x c + t, b = y c + u
+    float t0 = y0, t1 = y1, t2 = y2, t3 = y3, u0 = x0, u1 = x1, u2 = x2, u3 = x3;
+    mul2(t0, t1, -s.x, -s.y);
+    mul2(t2, t3, -s.z, -s.w);
+    mul2(u0, u1, s.x, s.y);
+    mul2(u2, u3, s.z, s.w);
+    fma2(x0, x1, c.x, c.y, t0, t1);
+    fma2(x2, x3, c.z, c.w, t2, t3);
+    fma2(y0, y1, c.x, c.y, u0, u1);
+    fma2(y2, y3, c.z, c.w, u2, u3);
+    st_shared_v2(alo, pack_bf16x2(x0, x1), pack_bf16x2(x2, x3));
+    st_shared_v2(ahi, pack_bf16x2(y0, y1), pack_bf16x2(y2, y3));
+}
+
+template <int D, int UNROLL>
+__device__ __forceinline__ int rope_row(int k, int grp) {
+    constexpr int RP = 32 / (D / 8);  // rows per pass
+    if (RP == 4) {
+        const int i = (k & 1) * 4 + grp;                 // 0..7
+        return (k >> 1) * 8 + ((i >> 1) | ((i & 1) << 2));  // rows 0, 4, 1, 5 | 2, 6, 3, 7 of the band
+    }
+    return k * RP + grp;
+}
+
+// UNROLL passes at a time: their table loads are all issued before the first
+// rotation touches shared memory, so their latencies overlap.
+template <int D, int UNROLL>
+__device__ __forceinline__ void rope_tile(uint32_t tile, uint32_t tile2, uint32_t sub_bytes, int nrows,
+                                          const float *tc, const float *ts, int lane) {
+    constexpr int PPR = D / 8;       // lanes per row (four feature pairs each)
+    constexpr int RP = 32 / PPR;     // rows per pass
+    const int piece = lane % PPR, grp = lane / PPR;
+    const uint32_t lo_col = piece * 4, hi_col = piece * 4 + D / 2;
+    const uint32_t lo_off = (lo_col >> 6) * sub_bytes + (piece & 1) * 8u;
+    const uint32_t hi_off = (hi_col >> 6) * sub_bytes + (piece & 1) * 8u;
+    const uint32_t lo_chunk = (lo_col & 63u) >> 3, hi_chunk = (hi_col & 63u) >> 3;
+    // passes that reach row nrows - 1 (with RP = 4, two passes cover an 8-row band);
+    // rows at or past nrows in the last batch are skipped
+    const int npass = RP == 4 ? 2 * ((nrows + 7) / 8) : (nrows + RP - 1) / RP;
+#pragma unroll 1
+    for (int k0 = 0; k0 < npass; k0 += UNROLL) {
+        float4 c[UNROLL], s[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int r = rope_row<D, UNROLL>(k0 + u, grp);
+            if (r < nrows) {
+                c[u] = *reinterpret_cast<const float4 *>(tc + r * (D / 2) + piece * 4);
+                s[u] = *reinterpret_cast<const float4 *>(ts + r * (D / 2) + piece * 4);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int r = rope_row<D, UNROLL>(k0 + u, grp);
+            if (r < nrows) {
+                const uint32_t olo = lo_off + sw128_offset(r, lo_chunk), ohi = hi_off + sw128_offset(r, hi_chunk);
+                rope_pairs4(tile + olo, tile + ohi, c[u], s[u]);
+                if (tile2 != 0u) rope_pairs4(tile2 + olo, tile2 + ohi, c[u], s[u]);
+            }
+        }
+    }
+}
+
+// The transposed rotation of 32 + 32 float32 values of one row (features
+// d0..d0+31 in lo, d0+D/2.. in hi), which carries a gradient with respect to
+// the rotated row back to the unrotated one:
+//   g[d] = c x[d] + s x[d + D/2],   g[d + D/2] = c x[d + D/2] - s x[d].
+// tc, ts: the row's cos and sin from feature d0 on (global memory).
+__device__ __forceinline__ void rope_grad32(float (&lo)[32], float (&hi)[32], const float *tc, const float *ts) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 4) {
+        const float4 c = *reinterpret_cast<const float4 *>(tc + i);
+        const float4 s = *reinterpret_cast<const float4 *>(ts + i);
+        const float cc[4] = {c.x, c.y, c.z, c.w}, ss[4] = {s.x, s.y, s.z, s.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float x = lo[i + e], y = hi[i + e];
+            lo[i + e] = __fmaf_rn(x, cc[e], __fmul_rn(y, ss[e]));
+            hi[i + e] = __fmaf_rn(y, cc[e], __fmul_rn(-x, ss[e]));
+        }
+    }
 }
 
 }  // namespace dev

@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
             if (!(ok = mbar_wait_warp(&in_full[buf], use & 1, err))) break;
             const uint32_t base = sIn + buf * C::IN_BYTES;
             const int64_t r0 = static_cast<int64_t>(t.q_loc0) * (D / 2);
-            rope_tile<D>(base + C::IQ, base + C::IK, C::SUB, t.q_len, g.rope_cos + r0, g.rope_sin + r0, lane);
+            rope_tile<D, 8>(base + C::IQ, base + C::IK, C::SUB, t.q_len, g.rope_cos + r0, g.rope_sin + r0, lane);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&rot_full[buf]);

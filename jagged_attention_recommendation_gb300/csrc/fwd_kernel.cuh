@@ -99,8 +99,7 @@ struct FwdCfg {
     static constexpr uint32_t COL_S = 0;    // S_g / P_g: BN columns per group
     static constexpr uint32_t COL_O = 256;  // O_g: D columns per group
     // registers per thread after the split (launch: 512 threads x 128)
-    // (RoPE: the rotation warp needs more, the output warpgroup gives them)
-    static constexpr uint32_t REG_CTRL = ROPE ? 72 : 56, REG_SOFTMAX = ROPE ? 168 : 176, REG_OUT = ROPE ? 96 : 104;
+    static constexpr uint32_t REG_CTRL = 56, REG_SOFTMAX = 176, REG_OUT = 104;
     static_assert(REG_CTRL * 128 + REG_SOFTMAX * 256 + REG_OUT * 128 <= 128 * 512, "register split");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "operand alignment");
@@ -110,9 +109,9 @@ struct FwdCfg {
 // WIN: sliding window on (a compile-time switch, so that kernels without one
 // carry no band test in their softmax passes).  ROPE: rotary position
 // embedding of Q and K ("Training GEM at LLM scale", section "BlockAttention")
-// in shared memory as the tiles arrive: warp 0 then loads Q as well as K and
-// V, and warp 2 rotates every Q tile and K block before the S issuer may use
-// it (q_rot / k_rot).
+// in shared memory as the tiles arrive: the output warpgroup rotates each
+// BlockAttention tile's Q rows and its one K block two tiles ahead, before the
+// S issuer may use them (q_rot / k_rot).
 template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -168,9 +167,9 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        if (ROPE) {
-            for (int s = 0; s < 2; ++s) mbar_init(&q_rot[s], 1);
-            for (int s = 0; s < C::NST; ++s) mbar_init(&k_rot[s], 1);
+        if (ROPE) {  // the output warpgroup's four warps
+            for (int s = 0; s < 2; ++s) mbar_init(&q_rot[s], 4);
+            for (int s = 0; s < C::NST; ++s) mbar_init(&k_rot[s], 4);
         }
         mbar_init(o_full, 1);
         *abort_flag = 0;
@@ -220,27 +219,10 @@ __global__ void __launch_bounds__(512, 1)
                 v_pending = false;
                 return true;
             };
-            uint32_t q_it = 0;  // RoPE: Q tiles loaded here
             TileStream ts(g, tbeg, tend);
             Tile t;
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, true)) continue;
-                if (ROPE) {  // Q (and, with D = 64, its rotation table rows) ahead of the tile's keys
-                    const uint32_t s = q_it & 1, use = q_it >> 1;
-                    if (!(ok = mbar_wait(&q_empty[s], (use & 1) ^ 1, err))) break;
-                    const uint32_t tab = static_cast<uint32_t>(t.q_len) * (D / 2) * 4;  // bytes of one table
-                    mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES + (C::TAB ? 2 * tab : 0));
-                    for (int kb = 0; kb < C::NKB; ++kb)
-                        tma_load_2d(smem + C::OFF_Q + s * C::Q_BYTES + kb * C::SUB_Q, &tmQ, &q_full[s],
-                                    t.h * D + kb * 64, t.q_start);
-                    if (C::TAB) {
-                        const int64_t r0 = static_cast<int64_t>(t.q_loc0) * (D / 2);
-                        uint8_t *dst = smem + C::OFF_TAB + s * C::TAB_BYTES;
-                        bulk_load(dst, g.rope_cos + r0, tab, &q_full[s]);
-                        bulk_load(dst + C::TAB_BYTES / 2, g.rope_sin + r0, tab, &q_full[s]);
-                    }
-                    ++q_it;
-                }
                 const int nkv = cdiv(t.kv_len, C::BN);
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t slot = k_it % C::NST, use = k_it / C::NST;
@@ -268,49 +250,8 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t last = v_it - 1 - ((v_it - 1 - s) % C::NST);
                     mbar_drain(&v_full[last % C::NST], (last / C::NST) & 1);
                 }
-                for (uint32_t i = (q_it > 2 ? q_it - 2 : 0); i < q_it; ++i) mbar_drain(&q_full[i & 1], (i >> 1) & 1);
             }
-        } else if (ROPE && warp == 2) {
-            // -------------------------------------------------------- RoPE
-            // The whole warp rotates each Q tile, then the tile's K blocks, in the
-            // order the S issuer takes them; it waits only for copies to land.
-            // A K block at the Q tile's positions (BlockAttention) reuses the
-            // table rows staged with Q.
-            uint32_t t_local = 0, k_it = 0;
-            bool ok = true;
-            TileStream ts(g, tbeg, tend);
-            Tile t;
-            while (ok && ts.next(t)) {
-                if (!check_tile(g, t, err, false)) continue;
-                const uint32_t qs = t_local & 1;
-                if (!(ok = mbar_wait_warp(&q_full[qs], (t_local >> 1) & 1, err))) break;
-                const float *qc = g.rope_cos + static_cast<int64_t>(t.q_loc0) * (D / 2);
-                const float *qsn = g.rope_sin + static_cast<int64_t>(t.q_loc0) * (D / 2);
-                if (C::TAB) {
-                    qc = reinterpret_cast<const float *>(smem + C::OFF_TAB + qs * C::TAB_BYTES);
-                    qsn = qc + C::BM * (D / 2);
-                }
-                rope_tile<D>(sQ + qs * C::Q_BYTES, 0u, C::SUB_Q, t.q_len, qc, qsn, lane);
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&q_rot[qs]);
-                const int nkv = cdiv(t.kv_len, C::BN);
-                for (int j = 0; j < nkv && ok; ++j, ++k_it) {
-                    const uint32_t slot = k_it % C::NST, use = k_it / C::NST;
-                    if (!(ok = mbar_wait_warp(&k_full[slot], use & 1, err))) break;
-                    const int p0 = t.kv_loc0 + j * C::BN;
-                    const int rows = min(C::BN, t.kv_len - j * C::BN);
-                    const bool same = p0 == t.q_loc0 && rows <= t.q_len;
-                    const float *kc = same ? qc : g.rope_cos + static_cast<int64_t>(p0) * (D / 2);
-                    const float *ksn = same ? qsn : g.rope_sin + static_cast<int64_t>(p0) * (D / 2);
-                    rope_tile<D>(sK + slot * C::KV_BYTES, 0u, C::SUB_KV, rows, kc, ksn, lane);
-                    fence_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&k_rot[slot]);
-                }
-                ++t_local;
-            }
-        } else if (!ROPE && warp == 2 && lane == 0) {
+        } else if (warp == 2 && lane == 0) {
             // -------------------------------------------------------- Q producer
             uint32_t t_local = 0;
             bool ok = true;
@@ -320,10 +261,19 @@ __global__ void __launch_bounds__(512, 1)
                 if (!check_tile(g, t, err, false)) continue;
                 const uint32_t s = t_local & 1, use = t_local >> 1;
                 if (!(ok = mbar_wait(&q_empty[s], (use & 1) ^ 1, err))) break;
-                mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES);
+                // RoPE with D = 64: the cos / sin rows of the tile's query positions
+                // travel with Q
+                const uint32_t tab = C::TAB ? static_cast<uint32_t>(t.q_len) * (D / 2) * 4 : 0u;
+                mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES + 2 * tab);
                 for (int kb = 0; kb < C::NKB; ++kb)
                     tma_load_2d(smem + C::OFF_Q + s * C::Q_BYTES + kb * C::SUB_Q, &tmQ, &q_full[s],
                                 t.h * D + kb * 64, t.q_start);
+                if (C::TAB) {
+                    const int64_t r0 = static_cast<int64_t>(t.q_loc0) * (D / 2);
+                    uint8_t *dst = smem + C::OFF_TAB + s * C::TAB_BYTES;
+                    bulk_load(dst, g.rope_cos + r0, tab, &q_full[s]);
+                    bulk_load(dst + C::TAB_BYTES / 2, g.rope_sin + r0, tab, &q_full[s]);
+                }
                 ++t_local;
             }
             if (!ok) {
@@ -657,10 +607,51 @@ __global__ void __launch_bounds__(512, 1)
         const uint32_t tO0 = tmem + lane_base + C::COL_O, tO1 = tO0 + D;
         uint32_t t_local = 0, n0 = 0;
         bool ok = true;
+        // RoPE: this warpgroup rotates Q and K two tiles ahead of the one whose
+        // output it writes (each warp its 32 rows), so the rotation of tile
+        // t + 2, which only needs S_t done, never waits for this group's output
+        // of tile t, and S_{t+2} finds it done.  Only BlockAttention tiles (one
+        // K block at the Q rows' positions) are rotated here; any other tile
+        // is a device error.
+        TileStream rs(g, tbeg, tend);
+        uint32_t r_local = 0, rk_it = 0;
+        auto rotate_next = [&]() -> bool {
+            Tile rt;
+            bool found = false;
+            while (!found && rs.next(rt)) found = check_tile(g, rt, err, false);
+            if (!found) return true;
+            const uint32_t qs = r_local & 1, slot = rk_it % C::NST;
+            const bool joint = rt.kv_len == rt.q_len && rt.kv_loc0 == rt.q_loc0 && rt.kv_len <= C::BN;
+            if (!joint) {
+                if (lane == 0) raise_error(err, kStatusDeviceCheck);
+                return false;
+            }
+            if (!mbar_wait_warp(&q_full[qs], (r_local >> 1) & 1, err)) return false;
+            if (!mbar_wait_warp(&k_full[slot], (rk_it / C::NST) & 1, err)) return false;
+            const int r0 = quad * 32, nrows = min(32, rt.q_len - r0);
+            if (nrows > 0) {
+                const float *qc = C::TAB ? reinterpret_cast<const float *>(smem + C::OFF_TAB + qs * C::TAB_BYTES)
+                                         : g.rope_cos + static_cast<int64_t>(rt.q_loc0) * (D / 2);
+                const float *qsn = C::TAB ? qc + C::BM * (D / 2) : g.rope_sin + static_cast<int64_t>(rt.q_loc0) * (D / 2);
+                rope_tile<D, 1>(sQ + qs * C::Q_BYTES + r0 * 128, sK + slot * C::KV_BYTES + r0 * 128, C::SUB_Q, nrows,
+                                qc + r0 * (D / 2), qsn + r0 * (D / 2), lane);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&q_rot[qs]);
+                mbar_arrive(&k_rot[slot]);
+            }
+            ++r_local;
+            ++rk_it;
+            return true;
+        };
+        if (ROPE) ok = rotate_next() && rotate_next();
         TileStream ts(g, tbeg, tend);
         Tile t;
         while (ok && ts.next(t)) {
             if (!check_tile(g, t, err, false)) continue;
+            if (ROPE && !(ok = rotate_next())) break;
             const int nkv = cdiv(t.kv_len, C::BN);
             // group g has keys in this tile when the tile has more than 64 g keys
             const bool has0 = t.kv_len > 0;
