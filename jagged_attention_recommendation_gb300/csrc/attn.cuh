@@ -583,6 +583,17 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, uint32_t tile2, uint32_
     }
 }
 
+// rope_grad32 on values i0..i0+15 with their cos and sin in registers.
+__device__ __forceinline__ void rope_grad16_regs(float (&lo)[32], float (&hi)[32], int i0, const float (&c)[16],
+                                                 const float (&s)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float x = lo[i0 + i], y = hi[i0 + i];
+        lo[i0 + i] = __fmaf_rn(x, c[i], __fmul_rn(y, s[i]));
+        hi[i0 + i] = __fmaf_rn(y, c[i], __fmul_rn(-x, s[i]));
+    }
+}
+
 // The transposed rotation of 32 + 32 float32 values of one row (features
 // d0..d0+31 in lo, d0+D/2.. in hi), which carries a gradient with respect to
 // the rotated row back to the unrotated one:

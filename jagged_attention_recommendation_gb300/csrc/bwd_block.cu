@@ -18,7 +18,7 @@
 // shared lo plane: P's first, read by the dV products, then dS's, read by the
 // dK and dQ products (a second hand-off, lo_free / dslo_full).
 // With rotary position embedding (ROPE; same section: RoPE's backward fused
-// into the attention epilogue) a seventh warp rotates each chunk's Q and K rows
+// into the attention epilogue) two more warps rotate each chunk's Q and K rows
 // in shared memory as they arrive, the products run on the rotated operands,
 // and the epilogue applies the transposed rotation to dQ and dK in float32,
 // before the bf16 store, so the gradients leave for the unrotated inputs and
@@ -58,13 +58,15 @@ struct BlkCfg {
     static constexpr uint32_t COL_DP = 128;
     static constexpr uint32_t COL_DK = 256;
     static constexpr uint32_t COL_DV = 256 + D;
+    // RoPE, D = 64: the epilogue's cos / sin row per lane (columns past dV)
+    static constexpr uint32_t COL_TAB = D == 64 ? 256 + 2 * D : 0;
     // operand offsets inside one input buffer
     static constexpr uint32_t IQ = 0, IK = T_BYTES, IV = 2 * T_BYTES, IDO = 3 * T_BYTES;
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
 template <int D, bool ROPE>
-__global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
+__global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     bwd_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const BwdArgs a) {
@@ -105,7 +107,7 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         mbar_init(drain, 1);
-        for (int b = 0; b < C::NBUF; ++b) mbar_init(&rot_full[b], 1);
+        for (int b = 0; b < C::NBUF; ++b) mbar_init(&rot_full[b], 2);  // the two rotation warps
         mbar_init(lo_free, 1);
         mbar_init(dslo_full, 4);
         *abort_flag = 0;
@@ -220,9 +222,11 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
             mma_commit(drain);
             mbar_drain(drain, 0);
         }
-    } else if (ROPE && warp == 6) {
+    } else if (ROPE && warp >= 6) {
         // RoPE: rotate the chunk's Q and K rows (the same positions) in place as
-        // soon as they land; the products wait for rot_full.
+        // soon as they land, warp 6 rows 0..63 and warp 7 rows 64..127 (two
+        // sub-partitions share the extra issue load); the products wait for
+        // rot_full.
         uint32_t t_local = 0;
         bool ok = true;
         TileStream ts(g, tbeg, tend);
@@ -231,9 +235,12 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
             if (!check_tile(g, t, err, false)) continue;
             const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
             if (!(ok = mbar_wait_warp(&in_full[buf], use & 1, err))) break;
-            const uint32_t base = sIn + buf * C::IN_BYTES;
-            const int64_t r0 = static_cast<int64_t>(t.q_loc0) * (D / 2);
-            rope_tile<D, 8>(base + C::IQ, base + C::IK, C::SUB, t.q_len, g.rope_cos + r0, g.rope_sin + r0, lane);
+            const int h0 = (warp - 6) * 64, nrows = min(64, t.q_len - h0);
+            if (nrows > 0) {
+                const uint32_t base = sIn + buf * C::IN_BYTES + h0 * 128;
+                const int64_t r0 = static_cast<int64_t>(t.q_loc0 + h0) * (D / 2);
+                rope_tile<D, 8>(base + C::IQ, base + C::IK, C::SUB, nrows, g.rope_cos + r0, g.rope_sin + r0, lane);
+            }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&rot_full[buf]);
@@ -383,14 +390,35 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
                 if (lane == 0) mbar_arrive(dslo_full);
             }
 
+            // RoPE, D = 64: this row's cos / sin (its query and its key share the
+            // position) go to free TMEM columns while the products run, so the
+            // epilogue reads them without a global-memory wait
+            const bool tab_tmem = ROPE && C::COL_TAB > 0 && t.q_loc0 == t.kv_loc0;
+            if (tab_tmem) {
+                const int64_t pr = static_cast<int64_t>(t.q_loc0 + (row < len ? row : 0)) * (D / 2);
+#pragma unroll 1
+                for (int part = 0; part < 2; ++part) {
+                    const float *src = (part == 0 ? g.rope_cos : g.rope_sin) + pr;
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(src + i);
+                        v[i] = x.x, v[i + 1] = x.y, v[i + 2] = x.z, v[i + 3] = x.w;
+                    }
+                    tmem_st32(tmem + lane_base + C::COL_TAB + part * 32, v);
+                }
+                tmem_wait_st();
+            }
             if (!(ok = mbar_wait_warp(acc_full, t_local & 1, err))) break;
             tc_fence_after();
             const bool row_ok = row < len;
             const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
             const int64_t krow = static_cast<int64_t>(t.kv_start) + row;
             if (rows_fast<D>(a.dq)) {
-                // stage dQ, dK, dV in turn in this warp's rows of the P tile (every MMA is done)
-                for (int pass = 0; pass < 3; ++pass) {
+                // stage dV, dQ, dK in turn in this warp's rows of the P tile (every MMA is done)
+#pragma unroll 1
+                for (int pp = 0; pp < 3; ++pp) {
+                    const int pass = pp == 0 ? 2 : pp - 1;
                     const uint32_t col = pass == 0 ? C::COL_S : (pass == 1 ? C::COL_DK : C::COL_DV);
                     const float mul = pass == 2 ? 1.0f : g.scale;
                     if (ROPE && pass < 2) {
@@ -408,7 +436,17 @@ __global__ void __launch_bounds__(ROPE ? 224 : 192, 1)
                                 mul2(lo[i], lo[i + 1], mul, mul);
                                 mul2(hi[i], hi[i + 1], mul, mul);
                             }
-                            rope_grad32(lo, hi, tc + cp * 32, tsn + cp * 32);
+                            if (tab_tmem) {
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {  // 16 cos and 16 sin at a time
+                                    float c[16], sn[16];
+                                    tmem_ld16x2(tmem + lane_base + C::COL_TAB + h * 16,
+                                                tmem + lane_base + C::COL_TAB + 32 + h * 16, c, sn);
+                                    rope_grad16_regs(lo, hi, h * 16, c, sn);
+                                }
+                            } else {
+                                rope_grad32(lo, hi, tc + cp * 32, tsn + cp * 32);
+                            }
                             st_row32_bf16(sP, C::SUB, row, cp * 32, lo);
                             st_row32_bf16(sP, C::SUB, row, D / 2 + cp * 32, hi);
                         }
@@ -487,7 +525,7 @@ static cudaError_t launch_block_t(const TmapSet &tm, const BwdArgs &a, int n_cta
     static bool done[64] = {};
     cudaError_t e = ensure_smem(bwd_block_kernel<D, ROPE>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    bwd_block_kernel<D, ROPE><<<n_ctas, ROPE ? 224 : 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    bwd_block_kernel<D, ROPE><<<n_ctas, ROPE ? 256 : 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 

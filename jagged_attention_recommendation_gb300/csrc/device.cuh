@@ -147,6 +147,11 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
+// Pull the 128-byte line holding p into L1 (a hint; no register, no wait).
+__device__ __forceinline__ void prefetch_l1(const void *p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 // Order this thread's generic-proxy shared memory writes before later
 // async-proxy (tensor core / TMA) reads of the same bytes.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -284,6 +289,22 @@ __device__ __forceinline__ void tmem_ld64x2(uint32_t ta, uint32_t tb, float (&v0
 }
 
 // Two 32-column loads (e.g. matching chunks of two accumulators) behind one wait.
+// Two 16-column loads (columns ta.. and tb.. of this warp's 32 lanes), one wait.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t ta, uint32_t tb, float (&v0)[16], float (&v1)[16]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%32];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%33];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta), "r"(tb)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v0[i] = __uint_as_float(r[i]);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v1[i] = __uint_as_float(r[16 + i]);
+}
+
 __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&v0)[32], float (&v1)[32]) {
     uint32_t r[64];
     asm volatile(

@@ -68,9 +68,9 @@ template <int D, bool ACT, int BIAS, bool ROPE = false>
 struct FwdCfg {
     static constexpr int BM = 128, BN = 128;
     static constexpr int NKB = D / 64;  // 64-column sub-tiles along D
-    // depth of the K ring and of the V ring (D = 64 with RoPE: 2, to make room
+    // depth of the K ring and of the V ring (D = 64 with RoPE: 3, to make room
     // for the staged rotation tables)
-    static constexpr int NST = (D == 64 && !ROPE) ? 4 : 2;
+    static constexpr int NST = D == 64 ? (ROPE ? 3 : 4) : 2;
     // RoPE with D = 64: the cos / sin rows of a tile's query positions travel
     // with its Q (one slot per Q buffer); D = 128 reads them from global memory
     static constexpr bool TAB = ROPE && D == 64;
