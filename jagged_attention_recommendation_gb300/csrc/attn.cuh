@@ -583,6 +583,45 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, uint32_t tile2, uint32_
     }
 }
 
+// rope_tile with the table rows in shared memory (tc, ts: shared addresses).
+template <int D, int UNROLL>
+__device__ __forceinline__ void rope_tile_s(uint32_t tile, uint32_t tile2, uint32_t sub_bytes, int nrows, uint32_t tc,
+                                            uint32_t ts, int lane) {
+    constexpr int PPR = D / 8;
+    constexpr int RP = 32 / PPR;
+    const int piece = lane % PPR, grp = lane / PPR;
+    const uint32_t lo_col = piece * 4, hi_col = piece * 4 + D / 2;
+    const uint32_t lo_off = (lo_col >> 6) * sub_bytes + (piece & 1) * 8u;
+    const uint32_t hi_off = (hi_col >> 6) * sub_bytes + (piece & 1) * 8u;
+    const uint32_t lo_chunk = (lo_col & 63u) >> 3, hi_chunk = (hi_col & 63u) >> 3;
+    const int npass = RP == 4 ? 2 * ((nrows + 7) / 8) : (nrows + RP - 1) / RP;
+#pragma unroll 1
+    for (int k0 = 0; k0 < npass; k0 += UNROLL) {
+        float4 c[UNROLL], s[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int r = rope_row<D, UNROLL>(k0 + u, grp);
+            if (r < nrows) {
+                const uint32_t o = (r * (D / 2) + piece * 4) * 4;
+                const uint4 cv = ld_shared_v4(tc + o), sv = ld_shared_v4(ts + o);
+                c[u] = make_float4(__uint_as_float(cv.x), __uint_as_float(cv.y), __uint_as_float(cv.z),
+                                   __uint_as_float(cv.w));
+                s[u] = make_float4(__uint_as_float(sv.x), __uint_as_float(sv.y), __uint_as_float(sv.z),
+                                   __uint_as_float(sv.w));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int r = rope_row<D, UNROLL>(k0 + u, grp);
+            if (r < nrows) {
+                const uint32_t olo = lo_off + sw128_offset(r, lo_chunk), ohi = hi_off + sw128_offset(r, hi_chunk);
+                rope_pairs4(tile + olo, tile + ohi, c[u], s[u]);
+                if (tile2 != 0u) rope_pairs4(tile2 + olo, tile2 + ohi, c[u], s[u]);
+            }
+        }
+    }
+}
+
 // rope_grad32 on values i0..i0+15 with their cos and sin in registers.
 __device__ __forceinline__ void rope_grad16_regs(float (&lo)[32], float (&hi)[32], int i0, const float (&c)[16],
                                                  const float (&s)[16]) {

@@ -68,9 +68,9 @@ template <int D, bool ACT, int BIAS, bool ROPE = false>
 struct FwdCfg {
     static constexpr int BM = 128, BN = 128;
     static constexpr int NKB = D / 64;  // 64-column sub-tiles along D
-    // depth of the K ring and of the V ring (D = 64 with RoPE: 3, to make room
+    // depth of the K ring and of the V ring (D = 64 with RoPE: 2, to make room
     // for the staged rotation tables)
-    static constexpr int NST = D == 64 ? (ROPE ? 3 : 4) : 2;
+    static constexpr int NST = (D == 64 && !ROPE) ? 4 : 2;
     // RoPE with D = 64: the cos / sin rows of a tile's query positions travel
     // with its Q (one slot per Q buffer); D = 128 reads them from global memory
     static constexpr bool TAB = ROPE && D == 64;
@@ -633,8 +633,12 @@ __global__ void __launch_bounds__(512, 1)
                 const float *qc = C::TAB ? reinterpret_cast<const float *>(smem + C::OFF_TAB + qs * C::TAB_BYTES)
                                          : g.rope_cos + static_cast<int64_t>(rt.q_loc0) * (D / 2);
                 const float *qsn = C::TAB ? qc + C::BM * (D / 2) : g.rope_sin + static_cast<int64_t>(rt.q_loc0) * (D / 2);
-                rope_tile<D, 1>(sQ + qs * C::Q_BYTES + r0 * 128, sK + slot * C::KV_BYTES + r0 * 128, C::SUB_Q, nrows,
-                                qc + r0 * (D / 2), qsn + r0 * (D / 2), lane);
+                if (C::TAB)
+                    rope_tile_s<D, 1>(sQ + qs * C::Q_BYTES + r0 * 128, sK + slot * C::KV_BYTES + r0 * 128, C::SUB_Q,
+                                      nrows, smem_u32(qc + r0 * (D / 2)), smem_u32(qsn + r0 * (D / 2)), lane);
+                else
+                    rope_tile<D, 1>(sQ + qs * C::Q_BYTES + r0 * 128, sK + slot * C::KV_BYTES + r0 * 128, C::SUB_Q,
+                                    nrows, qc + r0 * (D / 2), qsn + r0 * (D / 2), lane);
             }
             fence_async_smem();
             __syncwarp();
