@@ -275,9 +275,17 @@ def run_ours(args, w, batch):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     rope = rope_tables(batch, w) if args.rope else None
     rp = None if rope is None else tuple(t.to(dev) for t in rope)
+    d_qo = torch.from_numpy(batch.q_off.astype(np.int32)).to(dev)
+    d_ko = torch.from_numpy(batch.kv_off.astype(np.int32)).to(dev)
+
+    def replan():
+        if args.device_plan:  # tile lists built on the GPU from the device offsets
+            plan.update_device(d_qo, d_ko, batch.Tq, batch.Tk, stream)
+        else:
+            plan.update(batch.q_off, batch.kv_off, stream)
 
     def step():
-        plan.update(batch.q_off, batch.kv_off, stream)
+        replan()
         plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
         plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream,
                  rope=rp)
@@ -290,12 +298,17 @@ def run_ours(args, w, batch):
         raise RuntimeError("device status after warm-up: " + J.status_str(st))
 
     # planner host time on an idle stream (no wait on earlier uploads)
-    plan_host_ms = []
+    plan_host_ms, plan_dev_ms = [], []
     for _ in range(max(args.steps, 5)):
         torch.cuda.synchronize()
         t_p = time.perf_counter()
-        plan.update(batch.q_off, batch.kv_off, stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        replan()
         plan_host_ms.append((time.perf_counter() - t_p) * 1e3)
+        e1.record(stream)
+        e1.synchronize()
+        plan_dev_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
 
     names = KERNELS_BLOCK if w.block else [n for n in KERNELS_FULL if n != "bwd_delta" or batch.act == W.SOFTMAX]
@@ -318,7 +331,7 @@ def run_ours(args, w, batch):
         flush.fill_(s & 0xFF)
         # the planner's host work (tile lists, schedule, upload enqueue) is reported
         # on its own (planner_host_ms), not inside the device-timed step
-        plan.update(batch.q_off, batch.kv_off, stream)
+        replan()
         starts[s].record(stream)
         plan.set_events(kev[s][0:n_fwd + 1])
         plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
@@ -436,6 +449,8 @@ def run_ours(args, w, batch):
             "roofline": roof, "clocks": clocks,
             "workload_intensity_flop_per_byte": intensity,
             "planner_host_ms": float(np.median(plan_host_ms)),
+            "planner_stream_ms": float(np.median(plan_dev_ms)),
+            "planner": "device (jattn_plan_update_device)" if args.device_plan else "host (jattn_plan_update)",
             "timed_wall_s": t_wall}
     if graph is not None:
         line["graph"] = graph
@@ -512,6 +527,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--device-plan", action="store_true",
+                    help="re-plan every step on the GPU from device offsets (jattn_plan_update_device)")
     ap.add_argument("--rope", action="store_true",
                     help="rotary position embedding of Q and K (standard frequency table; block workload only)")
     ap.add_argument("--window", type=int, default=0,

@@ -122,9 +122,38 @@ jattn_status jattn_plan_update(jattn_plan *plan, const int32_t *q_offsets, const
                                void *stream);
 
 /*
+ * Re-plan on the device from offsets already in DEVICE memory ("Training GEM
+ * at LLM scale", section "Generalized Dot-Product Attention (GDPA)": the valid
+ * tiles are precomputed and spread over the SMs in a zigzag).  One kernel on
+ * `stream` builds the same tile records as jattn_plan_update and a zigzag
+ * schedule: sequences sorted by tile cost, tiles dealt over the SMs in the order
+ * 0..C-1, C-1..0, ...  The host reads no offsets and builds nothing, and later
+ * calls on `stream` use the new lists.  Results equal those of a host plan bit
+ * for bit.
+ *   q_offsets, kv_offsets : DEVICE int32 [B+1], 4-byte aligned; read by the
+ *                           kernel, so they must stay valid until it has run
+ *   B in [1, 8192]        : more sequences return JATTN_ERR_UNSUPPORTED
+ *   Tq, Tk                : the last entries of the offsets (the caller's tensor
+ *                           lengths; they size the workspaces and tensor maps)
+ * Offsets that do not start at 0, decrease, end elsewhere than Tq / Tk, or
+ * (BlockAttention) give a sequence different query and key lengths are found
+ * by the kernel: it plans no tile and sets JATTN_ERR_DEVICE_CHECK on the
+ * device status word (jattn_check_device_status).  With a device plan,
+ * jattn_fwd_rope / jattn_bwd_rope leave the table-length check to the kernels,
+ * which report a short table as JATTN_ERR_DEVICE_CHECK.  The device buffer
+ * grows, stream-synchronising, when the batch needs more room than any before.
+ */
+jattn_status jattn_plan_update_device(jattn_plan *plan, const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B,
+                                      int64_t Tq, int64_t Tk, void *stream);
+
+/*
  * Host view of a scheduled tile list, for inspection and tests.  The records are
  * grouped by CTA: CTA c runs tiles[cta_begin[c] .. cta_begin[c+1]) in order.
- * The pointers stay valid until the next jattn_plan_update or jattn_plan_destroy.
+ * After jattn_plan_update_device the call first synchronises the plan's device
+ * and downloads the device lists (CTA count = the SM count; CTAs past the last
+ * tile have empty ranges).
+ * The pointers stay valid until the next jattn_plan_update(_device) or
+ * jattn_plan_destroy.
  */
 jattn_status jattn_plan_tiles(const jattn_plan *plan, int32_t which, const jattn_tile **tiles, int64_t *n_tiles,
                               const int32_t **cta_begin, int32_t *n_ctas);

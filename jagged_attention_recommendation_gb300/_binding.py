@@ -24,7 +24,8 @@ TILES_Q, TILES_KV = 0, 1
 EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn_fwd_workspace_bytes",
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
             "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
-            "jattn_shard", "jattn_step_host", "jattn_step_host_join", "jattn_fwd_rope", "jattn_bwd_rope")
+            "jattn_shard", "jattn_step_host", "jattn_step_host_join", "jattn_fwd_rope", "jattn_bwd_rope",
+            "jattn_plan_update_device")
 
 
 class JattnError(RuntimeError):
@@ -83,6 +84,8 @@ def load():
     lib.jattn_plan_destroy.restype = None
     lib.jattn_fwd.argtypes = [P, P, P, P, P, P, P, P, sz, P]
     lib.jattn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P, sz, P]
+    lib.jattn_plan_update_device.argtypes = [P, P, P, i32, i64, i64, P]
+    lib.jattn_plan_update_device.restype = i32
     lib.jattn_fwd_rope.argtypes = [P, P, P, P, P, ctypes.POINTER(Rope), P, P, P, sz, P]
     lib.jattn_fwd_rope.restype = i32
     lib.jattn_bwd_rope.argtypes = [P, P, P, P, P, P, ctypes.POINTER(Rope), P, P, P, P, P, P, P, sz, P]
@@ -170,6 +173,17 @@ class Plan:
         _check(load().jattn_plan_update(self._h, qo.ctypes.data_as(ctypes.c_void_p),
                                         ko.ctypes.data_as(ctypes.c_void_p), len(qo) - 1, st), "jattn_plan_update")
         self.Tq, self.Tk = int(qo[-1]), int(ko[-1])
+
+    def update_device(self, q_off, kv_off, Tq: int, Tk: int, stream=None):
+        """Re-plan on the device (jattn_plan_update_device): q_off, kv_off are
+        int32 CUDA tensors [B+1]; Tq, Tk their last entries."""
+        if q_off.dtype != torch.int32 or kv_off.dtype != torch.int32 or not q_off.is_cuda or not kv_off.is_cuda:
+            raise ValueError("update_device: int32 CUDA offset tensors expected")
+        if q_off.numel() != kv_off.numel():
+            raise ValueError("update_device: offsets of different lengths")
+        _check(load().jattn_plan_update_device(self._h, q_off.data_ptr(), kv_off.data_ptr(), q_off.numel() - 1,
+                                               int(Tq), int(Tk), _stream(stream)), "jattn_plan_update_device")
+        self.Tq, self.Tk = int(Tq), int(Tk)
 
     def tiles(self, which: int = TILES_Q):
         """(tiles int32 [n, 6] in schedule order, cta_begin int32 [n_ctas + 1])."""

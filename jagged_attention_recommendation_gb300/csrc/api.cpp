@@ -41,6 +41,9 @@ struct jattn_plan {
     int32_t device = -1;
     int32_t num_sms = kDefaultSms;
     bool staged = false;  // inputs are copied to bf16 [T, H, Dp] first (fp32 data or D = 32)
+    // planned on the device (jattn_plan_update_device): the host tile lists and
+    // offsets are stale until jattn_plan_tiles downloads them
+    bool dev_planned = false;
     int64_t Tq = 0, Tk = 0;
     std::vector<int32_t> q_off, kv_off;
     std::vector<jattn_tile> tiles[2];
@@ -266,6 +269,7 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
 jattn_status set_batch(jattn_plan *p, const int32_t *qo, const int32_t *ko, int32_t B) {
     jattn_status st = check_offsets(qo, ko, B, p->mode.block != 0);
     if (st != JATTN_OK) return st;
+    p->dev_planned = false;
     p->B = B;
     p->q_off.assign(qo, qo + B + 1);
     p->kv_off.assign(ko, ko + B + 1);
@@ -311,6 +315,7 @@ bool make_tmap(CUtensorMap *m, const void *ptr, int64_t T, int H, int Dp, int bo
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 size_t stage_bytes(const jattn_plan *p, int64_t rows) {
     return align_up(static_cast<size_t>(rows) * p->H * p->Dp * 2, kAlign);
@@ -359,6 +364,7 @@ jattn_status check_rope(const jattn_plan *p, const jattn_rope *r) {
     if (p->mode.block == 0 || p->staged || (p->D != 64 && p->D != 128)) return JATTN_ERR_UNSUPPORTED;
     if (r->cos == nullptr || r->sin == nullptr || r->rows < 1) return JATTN_ERR_INVALID_ARG;
     if (!aligned16(r->cos) || !aligned16(r->sin)) return JATTN_ERR_ALIGNMENT;
+    if (p->dev_planned) return JATTN_OK;  // lengths unknown on the host: the kernels check the table bounds
     int32_t longest = 0;
     for (int32_t b = 0; b < p->B; ++b)
         longest = std::max({longest, p->q_off[b + 1] - p->q_off[b], p->kv_off[b + 1] - p->kv_off[b]});
@@ -470,9 +476,112 @@ jattn_status jattn_plan_update(jattn_plan *plan, const int32_t *q_offsets, const
     return upload(plan, static_cast<cudaStream_t>(stream));
 }
 
+jattn_status jattn_plan_update_device(jattn_plan *p, const int32_t *q_offsets, const int32_t *kv_offsets, int32_t B,
+                                      int64_t Tq, int64_t Tk, void *stream) {
+    if (p == nullptr || q_offsets == nullptr || kv_offsets == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    if (B < 1 || Tq < 0 || Tk < 0 || Tq >= INT32_MAX || Tk >= INT32_MAX) return JATTN_ERR_INVALID_ARG;
+    if (p->mode.block != 0 && Tq != Tk) return JATTN_ERR_INVALID_ARG;
+    if (B > kDevPlanMaxSeqs) return JATTN_ERR_UNSUPPORTED;
+    if (!aligned4(q_offsets) || !aligned4(kv_offsets)) return JATTN_ERR_ALIGNMENT;
+    const int64_t H = p->H;
+    const int64_t cap_q = H * ((Tq + kTileRows - 1) / kTileRows + B);
+    const int64_t cap_kv = p->mode.block != 0 ? 0 : H * ((Tk + kTileRows - 1) / kTileRows + B);
+    if (cap_q >= INT32_MAX || cap_kv >= INT32_MAX) return JATTN_ERR_INVALID_ARG;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return note_error("jattn_plan_update_device: cudaSetDevice failed");
+    (void)cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int C = std::max(p->num_sms, 1);
+    size_t off = 0;
+    p->off_tiles[0] = off;
+    off = align_up(off + static_cast<size_t>(cap_q) * sizeof(Tile), 16);
+    p->off_tiles[1] = off;
+    off = align_up(off + static_cast<size_t>(cap_kv) * sizeof(Tile), 16);
+    for (int w = 0; w < 2; ++w) {
+        p->off_cta[w] = off;
+        off = align_up(off + static_cast<size_t>(C + 1) * sizeof(int32_t), 16);
+    }
+    p->off_qoff = off;
+    off = align_up(off + static_cast<size_t>(B + 1) * sizeof(int32_t), 16);
+    p->off_kvoff = off;
+    off = align_up(off + static_cast<size_t>(B + 1) * sizeof(int32_t), 16);
+    if (off > p->d_cap) {
+        CUDA_TRY(cudaStreamSynchronize(st));  // earlier launches may still read the old buffer
+        if (p->d_buf) cudaFree(p->d_buf);
+        p->d_buf = nullptr;
+        p->d_cap = 0;
+        const size_t cap = std::max(off + off / 2, static_cast<size_t>(4096));
+        CUDA_TRY(cudaMalloc(&p->d_buf, cap));
+        p->d_cap = cap;
+    }
+    // the offsets are kept with the lists (for jattn_plan_tiles)
+    CUDA_TRY(cudaMemcpyAsync(p->d_buf + p->off_qoff, q_offsets, (B + 1) * sizeof(int32_t), cudaMemcpyDeviceToDevice, st));
+    CUDA_TRY(cudaMemcpyAsync(p->d_buf + p->off_kvoff, kv_offsets, (B + 1) * sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                             st));
+    DevPlanArgs a{};
+    a.q_off = q_offsets;
+    a.kv_off = kv_offsets;
+    a.B = B;
+    a.H = p->H;
+    a.block = p->mode.block;
+    a.window = std::min(p->mode.window, 1 << 30);
+    a.n_ctas = C;
+    a.Tq = static_cast<int32_t>(Tq);
+    a.Tk = static_cast<int32_t>(Tk);
+    a.tiles_q = reinterpret_cast<Tile *>(p->d_buf + p->off_tiles[0]);
+    a.tiles_kv = reinterpret_cast<Tile *>(p->d_buf + p->off_tiles[1]);
+    a.cta_q = reinterpret_cast<int32_t *>(p->d_buf + p->off_cta[0]);
+    a.cta_kv = reinterpret_cast<int32_t *>(p->d_buf + p->off_cta[1]);
+    a.cap_q = static_cast<int32_t>(cap_q);
+    a.cap_kv = static_cast<int32_t>(cap_kv);
+    a.status = p->d_status;
+    a.sort_len = 2;
+    while (a.sort_len < B) a.sort_len <<= 1;
+    CUDA_TRY(launch_plan_device(a, st));
+    ++p->launches;
+    p->B = B;
+    p->Tq = Tq;
+    p->Tk = Tk;
+    p->dev_planned = true;
+    for (int w = 0; w < 2; ++w) {
+        p->tiles[w].clear();
+        p->cta[w].assign(static_cast<size_t>(C) + 1, 0);
+    }
+    p->q_off.assign(static_cast<size_t>(B) + 1, 0);
+    p->kv_off.assign(static_cast<size_t>(B) + 1, 0);
+    return JATTN_OK;
+}
+
 jattn_status jattn_plan_tiles(const jattn_plan *plan, int32_t which, const jattn_tile **tiles, int64_t *n_tiles,
                               const int32_t **cta_begin, int32_t *n_ctas_out) {
     if (plan == nullptr || (which != JATTN_TILES_Q && which != JATTN_TILES_KV)) return JATTN_ERR_INVALID_ARG;
+    if (plan->dev_planned) {
+        // a device plan: wait for it and bring the lists, ranges and offsets to the host
+        jattn_plan *p = const_cast<jattn_plan *>(plan);
+        DeviceGuard guard(p->device);
+        if (!guard.ok) return note_error("jattn_plan_tiles: cudaSetDevice failed");
+        CUDA_TRY(cudaDeviceSynchronize());
+        for (int w = 0; w < 2; ++w) {
+            CUDA_TRY(cudaMemcpy(p->cta[w].data(), p->d_buf + p->off_cta[w], p->cta[w].size() * sizeof(int32_t),
+                                cudaMemcpyDeviceToHost));
+        }
+        CUDA_TRY(cudaMemcpy(p->q_off.data(), p->d_buf + p->off_qoff, p->q_off.size() * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost));
+        CUDA_TRY(cudaMemcpy(p->kv_off.data(), p->d_buf + p->off_kvoff, p->kv_off.size() * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost));
+        for (int w = 0; w < 2; ++w) {
+            const size_t n = static_cast<size_t>(std::max(p->cta[w].back(), 0));
+            std::vector<Tile> dev(n);
+            if (n > 0)
+                CUDA_TRY(cudaMemcpy(dev.data(), p->d_buf + p->off_tiles[w], n * sizeof(Tile), cudaMemcpyDeviceToHost));
+            p->tiles[w].resize(n);
+            for (size_t i = 0; i < n; ++i)
+                p->tiles[w][i] = jattn_tile{dev[i].b, dev[i].h, dev[i].q_start, dev[i].q_len, dev[i].kv_start,
+                                            dev[i].kv_len};
+        }
+        p->dev_planned = false;
+    }
     if (tiles) *tiles = plan->tiles[which].data();
     if (n_tiles) *n_tiles = static_cast<int64_t>(plan->tiles[which].size());
     if (cta_begin) *cta_begin = plan->cta[which].data();

@@ -46,4 +46,19 @@ cudaError_t launch_delta(const void *out, const void *dout, int f32, int64_t Tq,
 // src [rows, D] (bf16 or fp32) -> dst [rows, Dp] bf16, zero-padded columns D..Dp-1
 cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, void *dst, cudaStream_t stream);
 
+// device-side planner: tile lists and zigzag schedule from device offsets
+constexpr int kDevPlanMaxSeqs = 8192;  // sequences per batch the one-CTA sort takes
+struct DevPlanArgs {
+    const int32_t *q_off, *kv_off;  // DEVICE [B + 1]
+    int32_t B, H, block, window;
+    int32_t n_ctas;                 // CTAs the kernels launch (each list gets n_ctas + 1 range entries)
+    int32_t Tq, Tk;                 // expected last offsets
+    Tile *tiles_q, *tiles_kv;
+    int32_t *cta_q, *cta_kv;
+    int32_t cap_q, cap_kv;          // capacities in tiles
+    int *status;                    // device status word (bad offsets or capacity: kStatusDeviceCheck)
+    int32_t sort_len;               // power of two >= B, <= kDevPlanMaxSeqs
+};
+cudaError_t launch_plan_device(const DevPlanArgs &a, cudaStream_t stream);
+
 }  // namespace jattn
