@@ -236,6 +236,8 @@ def kernel_work(w, batch, name, pk):
         return 10.0 * D * H * p, W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)[1]
     if name == "bwd_delta":
         return 0.0, 2.0 * Tq * e + 4.0 * H * Tq
+    if name == "bwd_dq_reduce":  # fp32 per-sequence dQ rows in, the shared rows' bf16 sum out
+        return 0.0, 4.0 * Tq * H * D + 2.0 * w.q_rows_shared * H * D
     if name == "bwd_dq":  # dQ GEMM; its S and dP recompute is not counted
         lse = 8.0 * H * Tq if batch.act == W.SOFTMAX else 0.0
         return 2.0 * D * H * p, 2.0 * Tq * e + 2.0 * Tk * e + Tq * e + lse
@@ -264,10 +266,12 @@ def run_ours(args, w, batch):
     bias = batch.bias.to(dev) if batch.bias is not None else None
     plan = J.Plan(batch.q_off, batch.kv_off, H, D, act=batch.act, block=w.block, bias_buckets=w.bias_buckets,
                   window=w.window,
-                  dtype="fp32" if f32 else "bf16", device=local)
+                  dtype="fp32" if f32 else "bf16", device=local, broadcast_q=args.broadcast_q)
+    if args.broadcast_q:  # the shared query rows once, not one copy per sequence
+        q = q[:w.q_rows_shared].contiguous()
     out = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
     lse = torch.empty(H, batch.Tq, dtype=torch.float32, device=dev) if batch.act == W.SOFTMAX else None
-    dq = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
+    dq = torch.empty(plan.q_rows, H, D, dtype=tdt, device=dev)
     dk = torch.empty(batch.Tk, H, D, dtype=tdt, device=dev)
     dv = torch.empty(batch.Tk, H, D, dtype=tdt, device=dev)
     fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
@@ -312,6 +316,8 @@ def run_ours(args, w, batch):
     torch.cuda.synchronize()
 
     names = KERNELS_BLOCK if w.block else [n for n in KERNELS_FULL if n != "bwd_delta" or batch.act == W.SOFTMAX]
+    if args.broadcast_q:  # the dQ pass's per-sequence rows are summed by one more kernel
+        names.insert(names.index("bwd_dq") + 1, "bwd_dq_reduce")
     n_fwd, n_bwd = 1, len(names) - 1
     if f32 or D == 32:
         raise SystemExit("bench: staged (fp32 / D=32) workloads are parity cases, not bench lines")
@@ -428,7 +434,7 @@ def run_ours(args, w, batch):
 
     # end to end through the public API with host buffers (the host-buffer step
     # has no rotary-embedding form)
-    e2e = run_e2e(args, w, batch, plan, dev, stream) if not (args.no_e2e or args.rope) else None
+    e2e = run_e2e(args, w, batch, plan, dev, stream) if not (args.no_e2e or args.rope or args.broadcast_q) else None
     if ws > 1 and e2e is not None:
         t = torch.tensor([e2e["ms_per_step"]], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -440,7 +446,9 @@ def run_ours(args, w, batch):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(workload_config(w, batch.act, batch.B, True, ws, args.global_B),
                            **({"rope": "Q and K rotated in the kernels, standard table (base 10000)"}
-                              if args.rope else {})),
+                              if args.rope else {}),
+                           **({"broadcast_q": "%d shared query rows, dQ summed over the sequences" % w.q_rows_shared}
+                              if args.broadcast_q else {})),
             "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
             "pct_of_bf16_peak_sustained": 100.0 * value / ws / pk["bf16_tflops_sustained"],
             "per_kernel_ms": per_kernel, "gpu_launches": int(launches),
@@ -527,6 +535,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--broadcast-q", action="store_true",
+                    help="pooled-attention workload: one shared Q read by every sequence, dQ summed (--workload 4)")
     ap.add_argument("--device-plan", action="store_true",
                     help="re-plan every step on the GPU from device offsets (jattn_plan_update_device)")
     ap.add_argument("--rope", action="store_true",
@@ -554,6 +564,8 @@ def main():
         args.global_B = int(ws * w.B)
     else:
         batch = W.make_batch(args.workload, act=act)
+    if args.broadcast_q and not batch.w.q_rows_shared:
+        ap.error("--broadcast-q runs on the pooled-attention workload (--workload 4)")
     if args.rope and not batch.w.block:
         ap.error("--rope runs on the BlockAttention workload (--workload 5)")
     if args.window:

@@ -77,6 +77,16 @@ typedef struct {
                              events): 0 = off; W > 0 restricts row i to keys j with
                              |i - j| < W, local positions, and the planner skips the
                              tiles outside that band; not combined with block */
+    int32_t broadcast_q;  /* 1: the queries are shared by every sequence ("Training GEM at LLM
+                             scale", section "Generalized Dot-Product Attention (GDPA)": pooled
+                             attention with learned query rows).  Every sequence has the same
+                             Lq = n query rows, which are the rows 0..n-1 of one DEVICE Q
+                             [n, H, D] (not materialised per sequence); O, dO and lse keep one
+                             row per sequence and query ([B*n, ...]); jattn_bwd returns dq
+                             [n, H, D] = the sum over the sequences of their query gradients,
+                             reduced in a fixed order (bitwise reproducible).  Needs full
+                             attention (no block), bf16 data and D in {64, 128}; jattn_step_host
+                             does not take it.  0 = off. */
 } jattn_mode;
 
 /* One unit of work: rows [q_start, q_start+q_len) of Q against rows

@@ -39,7 +39,8 @@ class JattnError(RuntimeError):
 
 class Mode(ctypes.Structure):
     _fields_ = [("act", ctypes.c_int32), ("block", ctypes.c_int32), ("scale", ctypes.c_float),
-                ("bias_buckets", ctypes.c_int32), ("dtype", ctypes.c_int32), ("window", ctypes.c_int32)]
+                ("bias_buckets", ctypes.c_int32), ("dtype", ctypes.c_int32), ("window", ctypes.c_int32),
+                ("broadcast_q", ctypes.c_int32)]
 
 
 class Rope(ctypes.Structure):
@@ -153,19 +154,26 @@ class Plan:
     """A planned jagged batch (tile lists + schedule) for one (H, D, mode)."""
 
     def __init__(self, q_off, kv_off, H: int, D: int, act: int = SOFTMAX, block: int = 0, scale: float = 0.0,
-                 bias_buckets: int = 0, dtype: str = "bf16", device: int = 0, window: int = 0):
+                 bias_buckets: int = 0, dtype: str = "bf16", device: int = 0, window: int = 0,
+                 broadcast_q: bool = False):
+        """broadcast_q: every sequence's queries are the rows of one shared Q
+        [n, H, D] (n = each sequence's Lq); bwd then returns dq [n, H, D], the
+        sum over the sequences."""
         lib = load()
         qo, ko = _i32(q_off), _i32(kv_off)
         self.H, self.D, self.act, self.block, self.bias_buckets = H, D, act, block, bias_buckets
         self.window = window
         self.dtype = dtype
         self.device = device
-        self.mode = Mode(act, block, float(scale), bias_buckets, FP32 if dtype == "fp32" else BF16, window)
+        self.broadcast_q = bool(broadcast_q)
+        self.mode = Mode(act, block, float(scale), bias_buckets, FP32 if dtype == "fp32" else BF16, window,
+                         1 if broadcast_q else 0)
         self._h = ctypes.c_void_p()
         _check(lib.jattn_plan_create(qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p),
                                      len(qo) - 1, H, D, ctypes.byref(self.mode), device, ctypes.byref(self._h)),
                "jattn_plan_create")
         self.Tq, self.Tk = int(qo[-1]), int(ko[-1])
+        self.q_rows = int(qo[1] - qo[0]) if broadcast_q else self.Tq
 
     def update(self, q_off, kv_off, stream=None):
         qo, ko = _i32(q_off), _i32(kv_off)
@@ -173,6 +181,7 @@ class Plan:
         _check(load().jattn_plan_update(self._h, qo.ctypes.data_as(ctypes.c_void_p),
                                         ko.ctypes.data_as(ctypes.c_void_p), len(qo) - 1, st), "jattn_plan_update")
         self.Tq, self.Tk = int(qo[-1]), int(ko[-1])
+        self.q_rows = int(qo[1] - qo[0]) if self.broadcast_q else self.Tq
 
     def update_device(self, q_off, kv_off, Tq: int, Tk: int, stream=None):
         """Re-plan on the device (jattn_plan_update_device): q_off, kv_off are
@@ -184,6 +193,7 @@ class Plan:
         _check(load().jattn_plan_update_device(self._h, q_off.data_ptr(), kv_off.data_ptr(), q_off.numel() - 1,
                                                int(Tq), int(Tk), _stream(stream)), "jattn_plan_update_device")
         self.Tq, self.Tk = int(Tq), int(Tk)
+        self.q_rows = self.Tq // (q_off.numel() - 1) if self.broadcast_q else self.Tq
 
     def tiles(self, which: int = TILES_Q):
         """(tiles int32 [n, 6] in schedule order, cta_begin int32 [n_ctas + 1])."""
@@ -242,7 +252,7 @@ class Plan:
         """Backward.  Returns (dq, dk, dv).  rope = (cos, sin) as in fwd: dq and
         dk are then the gradients of the unrotated Q and K (jattn_bwd_rope)."""
         dt = self._tdtype()
-        dq = torch.empty(self.Tq, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
+        dq = torch.empty(self.q_rows, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
         dk = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dk is None else dk
         dv = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dv is None else dv
         ws = self._ws(self.bwd_workspace_bytes, workspace)
@@ -263,7 +273,7 @@ class Plan:
         """Backward with the library's fixed device scratch instead of a workspace.
         Returns (dq, dk, dv); the output tensors are allocated here unless given."""
         dt = self._tdtype()
-        dq = torch.empty(self.Tq, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
+        dq = torch.empty(self.q_rows, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
         dk = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dk is None else dk
         dv = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dv is None else dv
         _check(load().jattn_bwd_noalloc(self._h, _ptr(dout), _ptr(q), _ptr(k), _ptr(v), _ptr(bias), _ptr(out),

@@ -44,6 +44,7 @@ struct jattn_plan {
     // planned on the device (jattn_plan_update_device): the host tile lists and
     // offsets are stale until jattn_plan_tiles downloads them
     bool dev_planned = false;
+    int32_t bcast_n = 0;  // broadcast Q: rows of the shared Q (every sequence's Lq)
     int64_t Tq = 0, Tk = 0;
     std::vector<int32_t> q_off, kv_off;
     std::vector<jattn_tile> tiles[2];
@@ -269,6 +270,12 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
 jattn_status set_batch(jattn_plan *p, const int32_t *qo, const int32_t *ko, int32_t B) {
     jattn_status st = check_offsets(qo, ko, B, p->mode.block != 0);
     if (st != JATTN_OK) return st;
+    if (p->mode.broadcast_q) {  // every sequence has the shared Q's rows
+        for (int32_t b = 1; b < B; ++b)
+            if (qo[b + 1] - qo[b] != qo[1] - qo[0]) return JATTN_ERR_INVALID_ARG;
+        if (qo[1] - qo[0] < 1) return JATTN_ERR_INVALID_ARG;
+        p->bcast_n = qo[1] - qo[0];
+    }
     p->dev_planned = false;
     p->B = B;
     p->q_off.assign(qo, qo + B + 1);
@@ -323,6 +330,14 @@ size_t stage_bytes(const jattn_plan *p, int64_t rows) {
 
 bool softmax_full(const jattn_plan *p) { return p->mode.act == JATTN_SOFTMAX && p->mode.block == 0; }
 
+// rows of the Q tensor a call reads: the shared rows with broadcast Q, else Tq
+int64_t q_rows(const jattn_plan *p) { return p->mode.broadcast_q ? p->bcast_n : p->Tq; }
+
+// broadcast Q: the dQ pass's per-sequence float32 rows, summed afterwards
+size_t bcast_ws_bytes(const jattn_plan *p) {
+    return p->mode.broadcast_q ? align_up(static_cast<size_t>(p->Tq) * p->H * p->D * 4, kAlign) : 0;
+}
+
 Geom make_geom(const jattn_plan *p, int which) {
     Geom g{};
     g.tiles = reinterpret_cast<const Tile *>(p->d_buf + p->off_tiles[which]);
@@ -339,6 +354,7 @@ Geom make_geom(const jattn_plan *p, int which) {
     g.act = p->mode.act;
     g.block = p->mode.block;
     g.window = std::min(p->mode.window, 1 << 30);  // wider than any sequence: same as no limit
+    g.q_bcast = p->mode.broadcast_q;
     g.nb = p->mode.bias_buckets;
     g.scale = p->scale;
     g.bias = nullptr;
@@ -420,6 +436,9 @@ jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offse
     if (mode->act < JATTN_SOFTMAX || mode->act > JATTN_GELU_TANH) return JATTN_ERR_INVALID_ARG;
     if (mode->block != 0 && mode->block != 64) return JATTN_ERR_UNSUPPORTED;
     if (mode->window < 0 || (mode->window > 0 && mode->block != 0)) return JATTN_ERR_INVALID_ARG;
+    if (mode->broadcast_q != 0 && mode->broadcast_q != 1) return JATTN_ERR_INVALID_ARG;
+    if (mode->broadcast_q && (mode->block != 0 || mode->dtype != JATTN_BF16 || D < 64))
+        return JATTN_ERR_UNSUPPORTED;
     if (mode->dtype != JATTN_BF16 && mode->dtype != JATTN_FP32) return JATTN_ERR_INVALID_ARG;
     if (mode->bias_buckets < 0) return JATTN_ERR_INVALID_ARG;
     if (mode->bias_buckets > 0 && H * mode->bias_buckets > kMaxBiasFloats) return JATTN_ERR_UNSUPPORTED;
@@ -469,7 +488,8 @@ jattn_status jattn_plan_update(jattn_plan *plan, const int32_t *q_offsets, const
     if (plan == nullptr) return JATTN_ERR_INVALID_ARG;
     jattn_status st = check_offsets(q_offsets, kv_offsets, B, plan->mode.block != 0);
     if (st != JATTN_OK) return st;
-    set_batch(plan, q_offsets, kv_offsets, B);
+    st = set_batch(plan, q_offsets, kv_offsets, B);
+    if (st != JATTN_OK) return st;
     if (plan->device < 0) return JATTN_OK;
     DeviceGuard g(plan->device);
     if (!g.ok) return note_error("jattn_plan_update: cudaSetDevice failed");
@@ -484,6 +504,7 @@ jattn_status jattn_plan_update_device(jattn_plan *p, const int32_t *q_offsets, c
     if (p->mode.block != 0 && Tq != Tk) return JATTN_ERR_INVALID_ARG;
     if (B > kDevPlanMaxSeqs) return JATTN_ERR_UNSUPPORTED;
     if (!aligned4(q_offsets) || !aligned4(kv_offsets)) return JATTN_ERR_ALIGNMENT;
+    if (p->mode.broadcast_q && (Tq % B != 0 || Tq == 0)) return JATTN_ERR_INVALID_ARG;
     const int64_t H = p->H;
     const int64_t cap_q = H * ((Tq + kTileRows - 1) / kTileRows + B);
     const int64_t cap_kv = p->mode.block != 0 ? 0 : H * ((Tk + kTileRows - 1) / kTileRows + B);
@@ -538,12 +559,14 @@ jattn_status jattn_plan_update_device(jattn_plan *p, const int32_t *q_offsets, c
     a.status = p->d_status;
     a.sort_len = 2;
     while (a.sort_len < B) a.sort_len <<= 1;
+    a.bcast_n = p->mode.broadcast_q ? static_cast<int32_t>(Tq / B) : 0;
     CUDA_TRY(launch_plan_device(a, st));
     ++p->launches;
     p->B = B;
     p->Tq = Tq;
     p->Tk = Tk;
     p->dev_planned = true;
+    if (p->mode.broadcast_q) p->bcast_n = static_cast<int32_t>(Tq / B);
     for (int w = 0; w < 2; ++w) {
         p->tiles[w].clear();
         p->cta[w].assign(static_cast<size_t>(C) + 1, 0);
@@ -598,7 +621,7 @@ size_t jattn_bwd_workspace_bytes(const jattn_plan *p) {
     if (p == nullptr) return 0;
     size_t n = softmax_full(p) ? align_up(static_cast<size_t>(p->H) * p->Tq * 4, kAlign) : 0;
     if (p->staged) n += 2 * stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
-    return n;
+    return n + bcast_ws_bytes(p);
 }
 
 void jattn_plan_destroy(jattn_plan *p) {
@@ -667,7 +690,7 @@ jattn_status jattn_fwd_rope(const jattn_plan *p, const void *q, const void *k, c
         vv = vs;
     }
     TmapSet tm;
-    if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
+    if (!make_tmap(&tm.q, qq, q_rows(p), p->H, p->Dp, 128) || !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) ||
         !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
         return note_error("jattn_fwd: cuTensorMapEncodeTiled failed");
     tm.dout = tm.q;
@@ -739,10 +762,16 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
         kk = ks;
         vv = vs;
     }
+    float *dq_rows = nullptr;  // broadcast Q: per-sequence float32 dQ rows, at the workspace's end
+    if (p->mode.broadcast_q) dq_rows = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + need - bcast_ws_bytes(p));
     BwdArgs a;
     a.lse = lse;
     a.delta = delta;
     a.dq = out_desc(p, dq);
+    if (dq_rows != nullptr) {
+        a.dq.ptr = dq_rows;
+        a.dq.f32 = 1;
+    }
     a.dk = out_desc(p, dk);
     a.dv = out_desc(p, dv);
     a.dbias = dbias;
@@ -764,7 +793,7 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
     }
     const bool act = p->mode.act != JATTN_SOFTMAX;
     // pass 1: dQ over query-major tiles (128 query rows, keys in blocks of 64)
-    if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128) ||
+    if (!make_tmap(&tm.q, qq, q_rows(p), p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128) ||
         !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 64) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 64))
         return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
     a.g = make_geom(p, JATTN_TILES_Q);
@@ -780,8 +809,14 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
                                      "jattn_bwd: dQ kernel launch");
         if (e != JATTN_OK) return e;
     }
+    if (dq_rows != nullptr) {  // the shared queries' gradient: the sum over the sequences
+        jattn_status e = cuda_status(
+            log.done(launch_bcast_reduce(dq_rows, p->B, p->bcast_n, static_cast<int64_t>(p->H) * p->D, dq, st)),
+            "jattn_bwd: dQ reduction launch");
+        if (e != JATTN_OK) return e;
+    }
     // pass 2: dK, dV over key-major tiles (128 key rows, queries in blocks of 64)
-    if (!make_tmap(&tm.q, qq, p->Tq, p->H, p->Dp, 64) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 64) ||
+    if (!make_tmap(&tm.q, qq, q_rows(p), p->H, p->Dp, 64) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 64) ||
         !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
         return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
     a.g = make_geom(p, JATTN_TILES_KV);
@@ -794,6 +829,7 @@ jattn_status jattn_step_host(jattn_plan *p, const int32_t *q_offsets, const int3
                              const void *q, const void *k, const void *v, const void *dout, const float *bias,
                              void *out, float *lse, void *dq, void *dk, void *dv, void *stream) {
     if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->mode.broadcast_q) return JATTN_ERR_UNSUPPORTED;
     if (p->device < 0) return JATTN_ERR_NO_DEVICE;
     if (!q || !k || !v || !dout || !out || !dq || !dk || !dv) return JATTN_ERR_INVALID_ARG;
     if ((p->mode.bias_buckets > 0) != (bias != nullptr)) return JATTN_ERR_INVALID_ARG;

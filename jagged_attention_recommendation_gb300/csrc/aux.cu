@@ -1,5 +1,7 @@
 // aux.cu -- small memory-bound helpers of the attention passes.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -111,6 +113,31 @@ cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, 
     else
         stage_kernel<__nv_bfloat16><<<grid, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(src), rows, D, Dp,
                                                                static_cast<__nv_bfloat16 *>(dst));
+    return cudaGetLastError();
+}
+
+// Broadcast Q: dq[i, c] = sum over b of ws[b * n + i, c], b in order (fp32
+// sums, one thread per element, so the result is reproducible bit for bit),
+// stored as bf16.  ws: [B * n, HD] float32; dq: [n, HD] bf16.
+__global__ void bcast_reduce_kernel(const float *__restrict__ ws, int B, int n, int64_t HD,
+                                    __nv_bfloat16 *__restrict__ dq) {
+    const int64_t total = static_cast<int64_t>(n) * HD;
+    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
+         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float acc = 0.0f;
+        for (int b = 0; b < B; ++b) acc += ws[static_cast<int64_t>(b) * total + e];
+        dq[e] = __float2bfloat16_rn(acc);
+    }
+}
+
+cudaError_t launch_bcast_reduce(const float *ws, int B, int n, int64_t HD, void *dq, cudaStream_t stream) {
+    const int64_t total = static_cast<int64_t>(n) * HD;
+    if (total <= 0 || B <= 0) return cudaSuccess;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int64_t want = (total + 255) / 256;
+    const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
+    bcast_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, B, n, HD, static_cast<__nv_bfloat16 *>(dq));
     return cudaGetLastError();
 }
 

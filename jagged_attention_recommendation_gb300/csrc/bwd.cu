@@ -212,8 +212,9 @@ __global__ void __launch_bounds__(512, 1)
                 if (!(ok = mbar_wait(&qd_empty[s], (use & 1) ^ 1, err))) break;
                 mbar_arrive_expect_tx(&qd_full[s], 2 * C::Q_BYTES);
                 uint8_t *base = smem + C::OFF_Q + s * 2 * C::Q_BYTES;
+                const int qrow = g.q_bcast ? t.q_loc0 : t.q_start;  // shared Q: the local row
                 for (int kb = 0; kb < C::NKB; ++kb) {
-                    tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qd_full[s], t.h * D + kb * 64, t.q_start);
+                    tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qd_full[s], t.h * D + kb * 64, qrow);
                     tma_load_2d(base + C::Q_BYTES + kb * C::SUB_Q, &tmDO, &qd_full[s], t.h * D + kb * 64, t.q_start);
                 }
                 ++t_local;

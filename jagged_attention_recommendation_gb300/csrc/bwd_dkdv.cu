@@ -154,9 +154,10 @@ __global__ void __launch_bounds__(512, 1)
                     if (lane == 0) {
                         mbar_arrive_expect_tx(&qs_full[slot], 2 * C::Q_BYTES);
                         const int y = t.q_start + i * C::BQ;
+                        const int yq = (g.q_bcast ? t.q_loc0 : t.q_start) + i * C::BQ;  // shared Q: the local row
                         uint8_t *base = smem + C::OFF_Q + slot * 2 * C::Q_BYTES;
                         for (int kb = 0; kb < C::NKB; ++kb) {
-                            tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qs_full[slot], t.h * D + kb * 64, y);
+                            tma_load_2d(base + kb * C::SUB_Q, &tmQ, &qs_full[slot], t.h * D + kb * 64, yq);
                             tma_load_2d(base + C::Q_BYTES + kb * C::SUB_Q, &tmDO, &qs_full[slot], t.h * D + kb * 64,
                                         y);
                         }

@@ -56,6 +56,8 @@ struct Geom {
     const float *rope_cos;    // rotary embedding: cos [rope_rows, D/2] float32, or nullptr (off)
     const float *rope_sin;    // ... and sin
     int32_t rope_rows;        // table positions 0 .. rope_rows - 1
+    int32_t q_bcast;          // 1: every sequence's queries are the rows 0 .. Lq-1 of one shared Q
+                              // (Q is read at the local row, O / dO / lse at the sequence's rows)
 };
 
 // Where a [T, H, D] result goes: element (t, h, c) at ptr[t*ld + h*cols + c] for c < cols.

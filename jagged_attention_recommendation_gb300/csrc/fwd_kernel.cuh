@@ -265,9 +265,10 @@ __global__ void __launch_bounds__(512, 1)
                 // travel with Q
                 const uint32_t tab = C::TAB ? static_cast<uint32_t>(t.q_len) * (D / 2) * 4 : 0u;
                 mbar_arrive_expect_tx(&q_full[s], C::Q_BYTES + 2 * tab);
+                const int qrow = g.q_bcast ? t.q_loc0 : t.q_start;  // shared Q: the local row
                 for (int kb = 0; kb < C::NKB; ++kb)
                     tma_load_2d(smem + C::OFF_Q + s * C::Q_BYTES + kb * C::SUB_Q, &tmQ, &q_full[s],
-                                t.h * D + kb * 64, t.q_start);
+                                t.h * D + kb * 64, qrow);
                 if (C::TAB) {
                     const int64_t r0 = static_cast<int64_t>(t.q_loc0) * (D / 2);
                     uint8_t *dst = smem + C::OFF_TAB + s * C::TAB_BYTES;

@@ -46,6 +46,9 @@ cudaError_t launch_delta(const void *out, const void *dout, int f32, int64_t Tq,
 // src [rows, D] (bf16 or fp32) -> dst [rows, Dp] bf16, zero-padded columns D..Dp-1
 cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, void *dst, cudaStream_t stream);
 
+// broadcast Q: dq [n, HD] bf16 = sum over the B samples of ws [B * n, HD] float32, in order
+cudaError_t launch_bcast_reduce(const float *ws, int B, int n, int64_t HD, void *dq, cudaStream_t stream);
+
 // device-side planner: tile lists and zigzag schedule from device offsets
 constexpr int kDevPlanMaxSeqs = 8192;  // sequences per batch the one-CTA sort takes
 struct DevPlanArgs {
@@ -58,6 +61,7 @@ struct DevPlanArgs {
     int32_t cap_q, cap_kv;          // capacities in tiles
     int *status;                    // device status word (bad offsets or capacity: kStatusDeviceCheck)
     int32_t sort_len;               // power of two >= B, <= kDevPlanMaxSeqs
+    int32_t bcast_n;                // broadcast Q: every sequence must have this many queries (0: off)
 };
 cudaError_t launch_plan_device(const DevPlanArgs &a, cudaStream_t stream);
 

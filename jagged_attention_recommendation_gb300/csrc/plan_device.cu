@@ -118,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) plan_kernel(const DevPlanArgs a) 
         if (b == 0) ok = ok && q0 == 0 && k0 == 0;
         if (b == B - 1) ok = ok && q1 == a.Tq && k1 == a.Tk;
         if (a.block) ok = ok && (q1 - q0) == (k1 - k0);
+        if (a.bcast_n > 0) ok = ok && (q1 - q0) == a.bcast_n;
         if (!ok) bad = 1;
     }
     __syncthreads();

@@ -172,3 +172,28 @@ def test_set_events_rejects_null_handles(lib):
     assert lib.jattn_plan_set_events(p._h, None, 3) == J.ERR_INVALID_ARG
     assert lib.jattn_plan_launch_count(p._h) == 0
     assert lib.jattn_last_cuda_error() == b""
+
+
+def test_broadcast_q_plan_checks():
+    """Broadcast Q: every sequence must have the shared rows' count; no block
+    mode, fp32 data or D = 32."""
+    ko = np.array([0, 50, 60, 200], np.int32)
+    qo = np.array([0, 32, 64, 96], np.int32)
+    p = J.Plan(qo, ko, 2, 128, device=-1, broadcast_q=True)
+    assert p.q_rows == 32
+    p.close()
+    with pytest.raises(J.JattnError) as e:
+        J.Plan(np.array([0, 32, 63, 95], np.int32), ko, 2, 128, device=-1, broadcast_q=True)
+    assert e.value.code == J.ERR_INVALID_ARG
+    for kw in (dict(block=64), dict(dtype="fp32")):
+        with pytest.raises(J.JattnError) as e:
+            J.Plan(qo, qo, 2, 128, device=-1, broadcast_q=True, **kw)
+        assert e.value.code == J.ERR_UNSUPPORTED
+    with pytest.raises(J.JattnError) as e:
+        J.Plan(qo, ko, 2, 32, device=-1, broadcast_q=True)
+    assert e.value.code == J.ERR_UNSUPPORTED
+    p = J.Plan(qo, ko, 2, 128, device=-1, broadcast_q=True)
+    with pytest.raises(J.JattnError) as e:  # a re-plan keeps the rule
+        p.update(np.array([0, 32, 60, 96], np.int32), ko)
+    assert e.value.code == J.ERR_INVALID_ARG
+    p.close()
