@@ -147,11 +147,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
                  : "memory");
 }
 
-// Pull the 128-byte line holding p into L1 (a hint; no register, no wait).
-__device__ __forceinline__ void prefetch_l1(const void *p) {
-    asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
-}
-
 // Order this thread's generic-proxy shared memory writes before later
 // async-proxy (tensor core / TMA) reads of the same bytes.
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
