@@ -1,0 +1,132 @@
+"""Pins of the MXFP8 attention reference (oracle/mxfp8.py) against things other
+than itself: torch's float8_e4m3fn decoding and rounding, the round-to-even and
+saturation rules of the format, the block-exponent rule, the transpose
+invariance of 32 x 32 blocks that the pages state, closed forms, and the fp64
+oracle's plain attention on the quantised inputs (with the P-quantisation error
+bound)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import mxfp8 as M
+from oracle import oracle
+from jagged_attention_recommendation_gb300 import workloads as W
+
+f8 = getattr(torch, "float8_e4m3fn", None)
+
+
+def test_e4m3_grid_decoding():
+    g = M.e4m3_values()
+    assert len(g) == 253  # 254 finite codes, +0 and -0 equal
+    assert g.max() == 448.0 and g.min() == -448.0
+    pos = g[g > 0]
+    assert pos.min() == 2.0 ** -9          # smallest subnormal
+    assert 2.0 ** -6 in pos and 1.0 in pos and 1.125 in pos and 1.0625 not in pos
+    np.testing.assert_array_equal(g, -g[::-1])
+
+
+@pytest.mark.skipif(f8 is None, reason="torch without float8_e4m3fn")
+def test_e4m3_grid_matches_torch():
+    codes = torch.arange(256, dtype=torch.uint8).view(f8).to(torch.float64).numpy()
+    finite = np.unique(codes[np.isfinite(codes)])
+    np.testing.assert_array_equal(finite, M.e4m3_values())
+
+
+@pytest.mark.skipif(f8 is None, reason="torch without float8_e4m3fn")
+def test_e4m3_rounding_matches_torch_in_range():
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.uniform(-448, 448, 20000), rng.normal(0, 1, 20000), rng.normal(0, 0.01, 5000),
+                        (M.e4m3_values()[1:] + M.e4m3_values()[:-1]) / 2])  # every midpoint
+    ref = torch.from_numpy(x).to(f8).to(torch.float64).numpy()
+    np.testing.assert_array_equal(M.quantize_e4m3(x), ref)
+
+
+def test_e4m3_ties_to_even_and_saturation():
+    q = M.quantize_e4m3(np.array([1.0625, 1.1875, -1.0625, 500.0, -1e9, 448.0, 0.0, 2.0 ** -10, 3 * 2.0 ** -10]))
+    # 1.0625: between 1.0 (code 0x38) and 1.125 (0x39) -> 1.0; 1.1875 -> 1.25 (0x3A);
+    # beyond 448 -> 448; 2^-10 is half the smallest subnormal -> 0 (even); 3*2^-10 -> 2^-8 (code 2)
+    np.testing.assert_array_equal(q, [1.0, 1.25, -1.0, 448.0, -448.0, 448.0, 0.0, 0.0, 2.0 ** -8])
+
+
+def test_block_exponent_rule():
+    np.testing.assert_array_equal(M.block_exponent(np.array([448.0, 256.0, 511.9, 1.0, 0.75, 2.0 ** -130, 0.0])),
+                                  [0, 0, 0, -8, -9, -127, -127])
+    # amax / 2^e lies in [256, 512): the largest element lands at the top of E4M3's range
+    rng = np.random.default_rng(1)
+    a = np.exp(rng.uniform(-20, 20, 1000))
+    r = a / 2.0 ** M.block_exponent(a)
+    assert np.all((r >= 256) & (r < 512))
+
+
+def test_qdq_error_bound_and_fixed_points():
+    rng = np.random.default_rng(2)
+    for s in (1e-3, 1.0, 37.0):
+        x = rng.normal(0, s, (64, 96))
+        y = M.qdq_rows_cols(x, 32, 32)
+        for r in range(0, 64, 32):
+            for c in range(0, 96, 32):
+                xb, yb = x[r:r + 32, c:c + 32], y[r:r + 32, c:c + 32]
+                sc = 2.0 ** M.block_exponent(np.abs(xb).max())
+                sat = np.abs(xb) > 448 * sc
+                bound = np.maximum(2.0 ** -4 * np.abs(xb), 2.0 ** -10 * sc)
+                assert np.all(np.abs(xb - yb)[~sat] <= bound[~sat])
+                assert np.all(np.abs(yb[sat]) == 448 * sc)
+                np.testing.assert_array_equal(M.qdq_rows_cols(yb, 32, 32), yb)  # already representable
+
+
+def test_square_blocks_are_transpose_invariant():
+    """The pages' reason for 32 x 32 blocks: quantising X^T gives (quantised X)^T."""
+    x = np.random.default_rng(3).normal(0, 1, (100, 70))
+    np.testing.assert_array_equal(M.qdq_rows_cols(x, 32, 32).T, M.qdq_rows_cols(x.T, 32, 32))
+    # row blocks of 1 x 32 (how P is quantised) are not
+    assert not np.array_equal(M.qdq_rows_cols(x, 1, 32).T, M.qdq_rows_cols(x.T, 1, 32))
+
+
+def test_jagged_blocks_start_at_each_sequence():
+    """Blocks restart at every sequence's first row: a batch quantises like its
+    sequences quantised alone."""
+    bt = W.random_batch(4, [40, 7, 70], [40, 7, 70], 2, 64, dtype=torch.float64)
+    whole = M.qdq_jagged(bt["q"].numpy(), bt["q_off"])
+    off = bt["q_off"]
+    for b in range(3):
+        alone = M.qdq_jagged(bt["q"][off[b]:off[b + 1]].numpy(), [0, off[b + 1] - off[b]])
+        np.testing.assert_array_equal(whole[off[b]:off[b + 1]], alone)
+
+
+def test_single_key_closed_form():
+    """One key: P = [1], which MXFP8 holds exactly, so O = the quantised v_0."""
+    bt = W.random_batch(5, [3, 40], [1, 1], 2, 64, dtype=torch.float64)
+    out, lse = M.forward(bt["q_off"], bt["kv_off"], bt["q"].numpy(), bt["k"].numpy(), bt["v"].numpy())
+    vq = M.qdq_jagged(bt["v"].numpy(), bt["kv_off"])
+    for b, (q0, q1) in enumerate(((0, 3), (3, 43))):
+        np.testing.assert_array_equal(out[q0:q1], np.broadcast_to(vq[b], out[q0:q1].shape))
+
+
+def test_against_plain_attention_on_quantised_inputs():
+    """On the quantised Q, K, V the fp64 oracle's plain softmax attention gives
+    the same lse exactly (up to fp64 rounding) and an O that differs only by the
+    quantisation of P: |O_mx - O| <= sum_j |P_j - Pq_j| |v_j| / l, with
+    |P - Pq| <= max(2^-4 P, 2^-10 * block scale) per element."""
+    bt = W.random_batch(6, [45, 200, 3], [130, 64, 300], 2, 64, dtype=torch.float64)
+    q, k, v = (bt[n].numpy() for n in ("q", "k", "v"))
+    out, lse = M.forward(bt["q_off"], bt["kv_off"], q, k, v)
+    qq, kq, vq = (M.qdq_jagged(t, o) for t, o in ((q, bt["q_off"]), (k, bt["kv_off"]), (v, bt["kv_off"])))
+    ref, ref_lse = oracle.forward(bt["q_off"], bt["kv_off"], qq, kq, vq)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+    # element-wise bound, computed per row from the unquantised P
+    scale = 1.0 / np.sqrt(64)
+    for b in range(3):
+        q0, q1 = bt["q_off"][b], bt["q_off"][b + 1]
+        k0, k1 = bt["kv_off"][b], bt["kv_off"][b + 1]
+        for h in range(2):
+            s = scale * qq[q0:q1, h] @ kq[k0:k1, h].T
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            l = p.sum(axis=1, keepdims=True)
+            blk_amax = np.maximum.reduceat(p, np.arange(0, p.shape[1], 32), axis=1)
+            sc = 2.0 ** M.block_exponent(blk_amax)
+            sc = np.repeat(sc, 32, axis=1)[:, :p.shape[1]]
+            dp = np.maximum(2.0 ** -4 * p, 2.0 ** -10 * sc)
+            bound = (dp @ np.abs(vq[k0:k1, h])) / l
+            err = np.abs(out[q0:q1, h] - ref[q0:q1, h])
+            assert np.all(err <= bound + 1e-12)
+            assert err.max() > 0  # P's quantisation is visible
