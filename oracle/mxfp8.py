@@ -1,4 +1,4 @@
-"""MXFP8 attention reference (forward) -- TEST INFRASTRUCTURE ONLY.
+"""MXFP8 attention reference (forward and backward) -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/`` may import this module.  Plain numpy in float64; nothing is
 shared with the CUDA path.
@@ -33,6 +33,14 @@ The readings of the pages taken here:
   * The row sum l is accumulated from the unquantised P, as the softmax warps
     hold it in float32 before the conversion.
   * O = (P_q V_q) / l, with lse = m + ln l.
+  * Backward: dO is quantised like Q (32 x 32 blocks).  P and dS each feed
+    two products with different K dimensions (P: dV = P^T dO; dS: dQ = dS K
+    and dK = dS^T Q), so in the backward they are quantised in 32 x 32 blocks,
+    which serve a matrix and its transpose alike.  The backward P is exp(s - lse)
+    (normalised), and Delta_i = <dO_i, O_i> uses the unquantised dO and O (the
+    Delta pre-pass).  dS = P (dP - Delta) uses the unquantised P and
+    dP = dO_q V_q^T; then dV = P_q^T dO_q, dQ = scale dS_q K_q,
+    dK = scale dS_q^T Q_q.
 """
 from __future__ import annotations
 
@@ -140,3 +148,31 @@ def forward(q_off, kv_off, q, k, v, scale=None):
             out[q0:q1, h] = (pq @ vq[k0:k1, h]) / l
             lse[h, q0:q1] = (m + np.log(l))[:, 0]
     return out, lse
+
+
+def backward(q_off, kv_off, q, k, v, dout, scale=None):
+    """MXFP8 softmax attention backward: returns (dq, dk, dv) in float64."""
+    q, k, v, dout = (np.asarray(t, dtype=np.float64) for t in (q, k, v, dout))
+    Tq, H, D = q.shape
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    out, lse = forward(q_off, kv_off, q, k, v, scale)
+    qq, kq, vq = qdq_jagged(q, q_off), qdq_jagged(k, kv_off), qdq_jagged(v, kv_off)
+    dq_ = qdq_jagged(dout, q_off)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    qo = np.asarray(q_off, dtype=np.int64)
+    ko = np.asarray(kv_off, dtype=np.int64)
+    for b in range(len(qo) - 1):
+        q0, q1, k0, k1 = qo[b], qo[b + 1], ko[b], ko[b + 1]
+        if q1 == q0 or k1 == k0:
+            continue
+        for h in range(H):
+            s = scale * qq[q0:q1, h] @ kq[k0:k1, h].T
+            p = np.exp(s - lse[h, q0:q1, None])
+            delta = np.sum(dout[q0:q1, h] * out[q0:q1, h], axis=1, keepdims=True)
+            dp = dq_[q0:q1, h] @ vq[k0:k1, h].T
+            ds = p * (dp - delta)
+            pq, dsq = qdq_rows_cols(p, 32, 32), qdq_rows_cols(ds, 32, 32)
+            dv[k0:k1, h] = pq.T @ dq_[q0:q1, h]
+            dq[q0:q1, h] = scale * dsq @ kq[k0:k1, h]
+            dk[k0:k1, h] = scale * dsq.T @ qq[q0:q1, h]
+    return dq, dk, dv

@@ -130,3 +130,68 @@ def test_against_plain_attention_on_quantised_inputs():
             err = np.abs(out[q0:q1, h] - ref[q0:q1, h])
             assert np.all(err <= bound + 1e-12)
             assert err.max() > 0  # P's quantisation is visible
+
+
+def test_backward_against_plain_gradients_on_quantised_inputs():
+    """Backward vs the fp64 oracle's plain gradients on the quantised Q, K, V, dO:
+    they differ only by the quantisation of P (in dV) and dS (in dQ, dK), within
+    the bounds that per-element errors of max(2^-4 |x|, 2^-10 * block scale)
+    give; with P and dS exactly representable they would agree."""
+    bt = W.random_batch(7, [45, 70], [130, 33], 2, 64, dtype=torch.float64)
+    q, k, v, do = (bt[n].numpy() for n in ("q", "k", "v", "dout"))
+    dq, dk, dv = M.backward(bt["q_off"], bt["kv_off"], q, k, v, do)
+    qq, kq, vq, dq_ = (M.qdq_jagged(t, o) for t, o in ((q, bt["q_off"]), (k, bt["kv_off"]), (v, bt["kv_off"]),
+                                                      (do, bt["q_off"])))
+    out_mx, _ = M.forward(bt["q_off"], bt["kv_off"], q, k, v)
+    scale = 1.0 / np.sqrt(64)
+
+    def err_bound(x):  # per element, 32 x 32 blocks
+        out = np.empty_like(x)
+        for r in range(0, x.shape[0], 32):
+            for c in range(0, x.shape[1], 32):
+                xb = x[r:r + 32, c:c + 32]
+                sc = 2.0 ** M.block_exponent(np.abs(xb).max())
+                out[r:r + 32, c:c + 32] = np.maximum(2.0 ** -4 * np.abs(xb), 2.0 ** -10 * sc)
+        return out
+
+    for b in range(2):
+        q0, q1 = bt["q_off"][b], bt["q_off"][b + 1]
+        k0, k1 = bt["kv_off"][b], bt["kv_off"][b + 1]
+        for h in range(2):
+            s = scale * qq[q0:q1, h] @ kq[k0:k1, h].T
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            delta = np.sum(do[q0:q1, h] * out_mx[q0:q1, h], axis=1, keepdims=True)
+            ds = p * (dq_[q0:q1, h] @ vq[k0:k1, h].T - delta)
+            # plain products of the unquantised P and dS
+            dv_p = p.T @ dq_[q0:q1, h]
+            dq_p = scale * ds @ kq[k0:k1, h]
+            dk_p = scale * ds.T @ qq[q0:q1, h]
+            ep, eds = err_bound(p), err_bound(ds)
+            assert np.all(np.abs(dv[k0:k1, h] - dv_p) <= ep.T @ np.abs(dq_[q0:q1, h]) + 1e-12)
+            assert np.all(np.abs(dq[q0:q1, h] - dq_p) <= scale * eds @ np.abs(kq[k0:k1, h]) + 1e-12)
+            assert np.all(np.abs(dk[k0:k1, h] - dk_p) <= scale * eds.T @ np.abs(qq[q0:q1, h]) + 1e-12)
+
+
+def test_backward_single_key_closed_form():
+    """One key: P = 1 exactly (forward and backward), so dV is the sum of the
+    quantised dO rows.  dS_i = dP_i - Delta_i = (dO_q,i - dO_i) . v_q, the
+    residue of dO's quantisation (Delta comes from the unquantised dO and O =
+    v_q); dQ_i = scale * dS_q,i k_q and dK = scale * sum_i dS_q,i q_q,i with dS
+    quantised in 32 x 32 blocks (here 32 x 1)."""
+    bt = W.random_batch(8, [5, 40], [1, 1], 2, 64, dtype=torch.float64)
+    q, k, v, do = (bt[n].numpy() for n in ("q", "k", "v", "dout"))
+    dq, dk, dv = M.backward(bt["q_off"], bt["kv_off"], q, k, v, do)
+    qq = M.qdq_jagged(q, bt["q_off"])
+    kq, vq = M.qdq_jagged(k, bt["kv_off"]), M.qdq_jagged(v, bt["kv_off"])
+    doq = M.qdq_jagged(do, bt["q_off"])
+    scale = 1.0 / 8.0
+    for b, (q0, q1) in enumerate(((0, 5), (5, 45))):
+        for h in range(2):
+            ds = (doq[q0:q1, h] - do[q0:q1, h]) @ vq[b, h]          # [Lq]
+            dsq = M.qdq_rows_cols(ds[:, None], 32, 32)[:, 0]
+            np.testing.assert_allclose(dv[b, h], doq[q0:q1, h].sum(axis=0), rtol=1e-13, atol=1e-13)
+            np.testing.assert_allclose(dq[q0:q1, h], scale * dsq[:, None] * kq[b, h][None, :], rtol=1e-12,
+                                       atol=1e-15)
+            np.testing.assert_allclose(dk[b, h], scale * dsq @ qq[q0:q1, h], rtol=1e-12, atol=1e-15)
+            assert np.abs(ds).max() > 0 and np.abs(ds).max() < 0.1 * np.abs(doq[q0:q1, h] @ vq[b, h]).max()
