@@ -141,6 +141,16 @@ def sample_sequences(q_off, kv_off, frac: float, seed: int = 0):
     return sorted(picked)
 
 
+def variant_keys(args, w: W.Workload) -> dict:
+    """Config entries of the optional variants (the same on both arms)."""
+    out = {}
+    if args.rope:
+        out["rope"] = "Q and K rotated in the kernels, standard table (base 10000)"
+    if args.broadcast_q:
+        out["broadcast_q"] = "%d shared query rows, dQ summed over the sequences" % w.q_rows_shared
+    return out
+
+
 def rope_tables(batch: W.Batch, w: W.Workload):
     """Standard rotary tables (cos, sin) covering the batch's longest sequence."""
     longest = int(max(np.diff(batch.q_off.astype(np.int64)).max(), np.diff(batch.kv_off.astype(np.int64)).max()))
@@ -183,7 +193,7 @@ def run_reference(args, w, batch):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * float(np.mean(times)), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(w, batch.act, batch.B, False),
+            "config": dict(workload_config(w, batch.act, batch.B, False), **variant_keys(args, w)),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": "per step: " + desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -444,11 +454,7 @@ def run_ours(args, w, batch):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": dict(workload_config(w, batch.act, batch.B, True, ws, args.global_B),
-                           **({"rope": "Q and K rotated in the kernels, standard table (base 10000)"}
-                              if args.rope else {}),
-                           **({"broadcast_q": "%d shared query rows, dQ summed over the sequences" % w.q_rows_shared}
-                              if args.broadcast_q else {})),
+            "config": dict(workload_config(w, batch.act, batch.B, True, ws, args.global_B), **variant_keys(args, w)),
             "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
             "pct_of_bf16_peak_sustained": 100.0 * value / ws / pk["bf16_tflops_sustained"],
             "per_kernel_ms": per_kernel, "gpu_launches": int(launches),
