@@ -154,3 +154,34 @@ def _dp_worker(rank: int, world: int, port: int, case: str):
 @pytest.mark.parametrize("case", sorted(CASES))
 def test_two_rank_shards_reproduce_the_whole_batch(case):
     mp.spawn(_dp_worker, args=(2, _free_port(), case), nprocs=2, join=True)
+
+
+def _bcast_worker(rank: int, world: int, port: int):
+    """Broadcast Q across data-parallel ranks: each rank sums its shard's
+    per-sequence query gradients (what jattn_bwd returns for a broadcast-Q
+    plan); one all-reduce of that [n, H, D] sum gives the whole batch's."""
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        n, lk = 8, [50, 3, 31, 80, 66, 9]
+        b = W.random_batch(8, [n] * len(lk), lk, 2, 16, dtype=torch.float64)
+        shared = b["q"][:n].clone()
+        b["q"] = shared.repeat(len(lk), 1, 1)
+        qo, ko = b["q_off"], b["kv_off"]
+        r = J.shard(qo, ko, world)
+        seqs, lqo, lko, qrows, krows = J.local_rows(qo, ko, r, rank)
+        qi, ki = torch.from_numpy(qrows), torch.from_numpy(krows)
+        dq, _, _, _ = O.backward(lqo, lko, b["q"][qi], b["k"][ki], b["v"][ki], b["dout"][qi], act=W.SILU, nthreads=2)
+        local = torch.from_numpy(dq.reshape(len(seqs), n, 2, 16).sum(axis=0) if len(seqs) else np.zeros((n, 2, 16)))
+        dist.all_reduce(local)
+        f_dq, _, _, _ = O.backward(qo, ko, b["q"], b["k"], b["v"], b["dout"], act=W.SILU, nthreads=2)
+        want = f_dq.reshape(len(lk), n, 2, 16).sum(axis=0)
+        np.testing.assert_allclose(local.numpy(), want, rtol=1e-12, atol=1e-13)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_rank_broadcast_q_gradient_all_reduce():
+    mp.spawn(_bcast_worker, args=(2, _free_port()), nprocs=2, join=True)
