@@ -536,7 +536,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", type=int, default=2, help="1..5 (default 2: jagged self-attention + bias)")
     ap.add_argument("--act", choices=["softmax", "silu", "gelu_tanh"], default=None)
-    ap.add_argument("--cpu-frac", type=float, default=0.25, help="share of the batch's pairs the CPU baseline runs")
+    ap.add_argument("--cpu-frac", type=float, default=1.0, help="share of the batch's pairs the CPU baseline runs")
     ap.add_argument("--ref-frac", type=float, default=1.0 / 32, help="share of the batch per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
