@@ -197,3 +197,18 @@ def test_broadcast_q_plan_checks():
         p.update(np.array([0, 32, 60, 96], np.int32), ko)
     assert e.value.code == J.ERR_INVALID_ARG
     p.close()
+
+
+def test_device_update_argument_checks_on_host():
+    """jattn_plan_update_device: NULL offsets are an argument error, and a
+    host-only plan has no device to plan on (both decided before any pointer is
+    read)."""
+    import ctypes
+    qo = np.array([0, 10, 30], np.int32)
+    p = J.Plan(qo, qo, 2, 64, device=-1)
+    lib = J.load()
+    fake = ctypes.c_void_p(16)  # never dereferenced: the call returns first
+    assert lib.jattn_plan_update_device(p._h, None, fake, 2, 30, 30, None) == J.ERR_INVALID_ARG
+    assert lib.jattn_plan_update_device(p._h, fake, fake, 2, 30, 30, None) == J.ERR_NO_DEVICE
+    assert lib.jattn_plan_update_device(None, fake, fake, 2, 30, 30, None) == J.ERR_INVALID_ARG
+    p.close()
