@@ -24,7 +24,11 @@
  *   lse              : float32 [H, Tq] (softmax only)
  *   element type     : bfloat16 (JATTN_BF16) or float32 (JATTN_FP32) for q, k, v,
  *                      out, dout, dq, dk, dv alike; all arithmetic runs in bf16
- *                      tensor-core products with fp32 accumulation.
+ *                      tensor-core products with fp32 accumulation.  float32
+ *                      data are rounded to bf16 on entry, which keeps softmax
+ *                      results inside the tolerances but not the unnormalised
+ *                      activation sums: float32 plans take softmax only
+ *                      (JATTN_ERR_UNSUPPORTED otherwise).
  * Device pointers must be 16-byte aligned.  D is 32, 64 or 128.  Positions i, j
  * are local to the sequence (also in cross-attention).  A sequence with Lk = 0
  * yields O_i = 0 and lse_i = -inf; a sequence with Lq = 0 yields dk = dv = 0.
@@ -221,9 +225,11 @@ typedef struct {
  * with c = cos[p * D/2 + d] and s = sin[p * D/2 + d]; K likewise.  The kernel
  * rotates each Q and K tile in shared memory as it arrives (in float32, rounded
  * to bf16 for the tensor cores); no rotated copy of Q or K is written.
- * rope = NULL: exactly jattn_fwd.  Otherwise the plan must be BlockAttention
- * (mode.block = 64) on bf16 data with D in {64, 128}, else
- * JATTN_ERR_UNSUPPORTED.  cos or sin NULL, or rows below the longest sequence:
+ * rope = NULL: exactly jattn_fwd.  Otherwise the plan must be softmax
+ * BlockAttention (mode.act = JATTN_SOFTMAX, mode.block = 64) on bf16 data with
+ * D in {64, 128}, else JATTN_ERR_UNSUPPORTED.  (The rotated rows reach the
+ * tensor cores as bf16; a normalised softmax row keeps that rounding inside
+ * the tolerances, the unnormalised activation sums do not.)  cos or sin NULL, or rows below the longest sequence:
  * JATTN_ERR_INVALID_ARG.  cos or sin not 16-byte aligned: JATTN_ERR_ALIGNMENT.
  * The tables are read, never written, and must stay valid until the kernel ends.
  */
@@ -275,8 +281,11 @@ int64_t jattn_plan_launch_count(const jattn_plan *plan);
  * allocating library routine is called.
  *
  * The first call on a device looks up the array's device address with that
- * device current (cudaGetSymbolAddress, once per device); make that first call
- * before any stream capture.  All calls share the one array and each call
+ * device current (cudaGetSymbolAddress, once per device) and keeps it for the
+ * life of the process; make that first call before any stream capture.  A
+ * device reset (cudaDeviceReset, or the primary context torn down and made
+ * again) unloads the library's module on that device and leaves the kept
+ * address stale: do not call this entry point on a device after resetting it.  All calls share the one array and each call
  * overwrites the part it uses (nothing in it has to start at zero), so calls
  * whose work overlaps on the GPU (different streams, or different host threads
  * without ordering) race on it: order them.
@@ -328,6 +337,23 @@ jattn_status jattn_step_host(jattn_plan *plan, const int32_t *q_offsets, const i
  * no call was issued, JATTN_ERR_CUDA when the wait cannot be enqueued.
  */
 jattn_status jattn_step_host_join(jattn_plan *plan, void *stream);
+
+/*
+ * Test hook: the error path of a bounded wait on a real launch.  The paper has
+ * no counterpart.  Launches a test build of the forward kernel whose
+ * score-issuing thread first waits on a barrier that nothing completes; after
+ * wait_ns nanoseconds (100 us .. 2 s; the library's own kernels wait 2 s) that
+ * wait gives up, writes JATTN_ERR_DEVICE_TIMEOUT to the plan's status word and
+ * raises the CTA's abort flag; every other role of the CTA leaves its loop, the
+ * copies in flight are drained, TMEM is freed and the kernel returns.  Nothing
+ * traps; the device stays usable.  out and lse receive no defined values.  The
+ * plan must be full softmax attention on bf16 data without bias, window or
+ * broadcast Q, D in {64, 128} (else JATTN_ERR_UNSUPPORTED); the tensors are
+ * those of jattn_fwd, lse required.  The status is read with
+ * jattn_check_device_status.
+ */
+jattn_status jattn_test_fwd_stall(const jattn_plan *plan, const void *q, const void *k, const void *v, void *out,
+                                  float *lse, uint64_t wait_ns, void *stream);
 
 /* Synchronises `stream`, then returns and clears the plan's device status word. */
 jattn_status jattn_check_device_status(const jattn_plan *plan, void *stream);

@@ -359,6 +359,7 @@ Geom make_geom(const jattn_plan *p, int which) {
     g.scale = p->scale;
     g.bias = nullptr;
     g.status = p->d_status;
+    g.wait_ns = kWaitTimeoutNs;
     return g;
 }
 
@@ -373,11 +374,16 @@ OutDesc out_desc(const jattn_plan *p, void *ptr) {
 
 int n_ctas(const jattn_plan *p, int which) { return static_cast<int>(p->cta[which].size()) - 1; }
 
-// Rotary embedding: BlockAttention plans on bf16 data with D in {64, 128};
-// the tables must cover the longest sequence of the batch.
+// Rotary embedding: softmax BlockAttention plans on bf16 data with D in
+// {64, 128}; the tables must cover the longest sequence of the batch.  The
+// tensor cores take the rotated Q and K as bf16.  A softmax row is normalised,
+// so that rounding stays inside the forward tolerance; an activation-mode row
+// sums up to 64 unnormalised terms, which the rounding alone can move beyond
+// it, so activation mode is not offered with the rotation.
 jattn_status check_rope(const jattn_plan *p, const jattn_rope *r) {
     if (r == nullptr) return JATTN_OK;
-    if (p->mode.block == 0 || p->staged || (p->D != 64 && p->D != 128)) return JATTN_ERR_UNSUPPORTED;
+    if (p->mode.block == 0 || p->staged || (p->D != 64 && p->D != 128) || p->mode.act != JATTN_SOFTMAX)
+        return JATTN_ERR_UNSUPPORTED;
     if (r->cos == nullptr || r->sin == nullptr || r->rows < 1) return JATTN_ERR_INVALID_ARG;
     if (!aligned16(r->cos) || !aligned16(r->sin)) return JATTN_ERR_ALIGNMENT;
     if (p->dev_planned) return JATTN_OK;  // lengths unknown on the host: the kernels check the table bounds
@@ -440,6 +446,10 @@ jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offse
     if (mode->broadcast_q && (mode->block != 0 || mode->dtype != JATTN_BF16 || D < 64))
         return JATTN_ERR_UNSUPPORTED;
     if (mode->dtype != JATTN_BF16 && mode->dtype != JATTN_FP32) return JATTN_ERR_INVALID_ARG;
+    // float32 data enter the tensor cores rounded to bf16.  Normalised softmax
+    // rows keep that rounding inside the tolerances; unnormalised activation
+    // sums over many keys do not, so float32 is offered with softmax only.
+    if (mode->dtype == JATTN_FP32 && mode->act != JATTN_SOFTMAX) return JATTN_ERR_UNSUPPORTED;
     if (mode->bias_buckets < 0) return JATTN_ERR_INVALID_ARG;
     if (mode->bias_buckets > 0 && H * mode->bias_buckets > kMaxBiasFloats) return JATTN_ERR_UNSUPPORTED;
     if (!(mode->scale >= 0.0f) || std::isinf(mode->scale)) return JATTN_ERR_INVALID_ARG;
@@ -942,6 +952,37 @@ jattn_status jattn_plan_set_events(jattn_plan *p, void *const *events, int32_t n
 }
 
 int64_t jattn_plan_launch_count(const jattn_plan *p) { return p == nullptr ? 0 : p->launches; }
+
+jattn_status jattn_test_fwd_stall(const jattn_plan *p, const void *q, const void *k, const void *v, void *out,
+                                  float *lse, uint64_t wait_ns, void *stream) {
+    if (p == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    if (!q || !k || !v || !out || !lse) return JATTN_ERR_INVALID_ARG;
+    if (wait_ns < 100000ull || wait_ns > kWaitTimeoutNs) return JATTN_ERR_INVALID_ARG;
+    if (p->mode.act != JATTN_SOFTMAX || p->mode.bias_buckets > 0 || p->mode.window > 0 || p->mode.block != 0 ||
+        p->mode.broadcast_q || p->staged)
+        return JATTN_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return JATTN_ERR_ALIGNMENT;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return note_error("jattn_test_fwd_stall: cudaSetDevice failed");
+    (void)cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    TmapSet tm;
+    if (!make_tmap(&tm.q, q, q_rows(p), p->H, p->Dp, 128) || !make_tmap(&tm.k, k, p->Tk, p->H, p->Dp, 128) ||
+        !make_tmap(&tm.v, v, p->Tk, p->H, p->Dp, 128))
+        return note_error("jattn_test_fwd_stall: cuTensorMapEncodeTiled failed");
+    tm.dout = tm.q;
+    FwdArgs a;
+    a.g = make_geom(p, JATTN_TILES_Q);
+    a.g.wait_ns = wait_ns;
+    a.out = out_desc(p, out);
+    a.lse = lse;
+    set_rope(a.g, nullptr);
+    LaunchLog log(p, st);
+    return cuda_status(log.done(launch_fwd_stall(p->Dp, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
+                       "jattn_test_fwd_stall: kernel launch");
+}
 
 jattn_status jattn_check_device_status(const jattn_plan *p, void *stream) {
     if (p == nullptr) return JATTN_ERR_INVALID_ARG;

@@ -10,7 +10,7 @@ template <int D, bool ACT, int BIAS>
 static cudaError_t launch_rope_t(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
     using C = FwdCfg<D, ACT, BIAS, true>;
     auto kern = fwd_kernel<D, ACT, BIAS, false, true>;
-    static bool done[64] = {};
+    static SmemOnce done;
     cudaError_t e = ensure_smem(kern, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
     kern<<<n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(tm.q, tm.k, tm.v, a);
@@ -24,12 +24,11 @@ static cudaError_t launch_rope_b(const TmapSet &tm, const FwdArgs &a, int n_ctas
     return launch_rope_t<D, ACT, kBiasTable>(tm, a, n_ctas, stream);
 }
 
+// softmax only (the host rejects activation mode with the rotation)
 cudaError_t launch_fwd_rope(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
-    if (a.g.rope_cos == nullptr || a.g.rope_sin == nullptr || a.g.window > 0) return cudaErrorInvalidValue;
-    if (D == 128)
-        return act ? launch_rope_b<128, true>(tm, a, n_ctas, stream) : launch_rope_b<128, false>(tm, a, n_ctas, stream);
-    if (D == 64)
-        return act ? launch_rope_b<64, true>(tm, a, n_ctas, stream) : launch_rope_b<64, false>(tm, a, n_ctas, stream);
+    if (a.g.rope_cos == nullptr || a.g.rope_sin == nullptr || a.g.window > 0 || act) return cudaErrorInvalidValue;
+    if (D == 128) return launch_rope_b<128, false>(tm, a, n_ctas, stream);
+    if (D == 64) return launch_rope_b<64, false>(tm, a, n_ctas, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -74,12 +74,7 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
-def round_bf16(x: np.ndarray) -> np.ndarray:
-    """Round float64 values to the nearest bfloat16 (ties to even), as float64."""
-    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).to(torch.float64).numpy()
-
-
-def rope_rotate(x, offsets, cos, sin, transpose=False, to_bf16=False) -> np.ndarray:
+def rope_rotate(x, offsets, cos, sin, transpose=False) -> np.ndarray:
     """Rotary position embedding of a jagged [T, H, D] tensor, in float64.
 
     "Training GEM at LLM scale", section "BlockAttention": RoPE is applied to
@@ -91,9 +86,7 @@ def rope_rotate(x, offsets, cos, sin, transpose=False, to_bf16=False) -> np.ndar
         y[d]       = x[d] cos - x[d + D/2] sin
         y[d + D/2] = x[d + D/2] cos + x[d] sin
     transpose=True applies the transposed rotation.  That maps a gradient with
-    respect to the rotated rows back to the unrotated ones.  to_bf16=True rounds
-    the rotated rows to bfloat16: the rotated Q and K are then the bf16 tensors
-    a bf16 pipeline feeds the attention (rotate, cast, attend).
+    respect to the rotated rows back to the unrotated ones.
     """
     x = _f64(x)
     cos, sin = _f64(cos), _f64(sin)
@@ -109,21 +102,21 @@ def rope_rotate(x, offsets, cos, sin, transpose=False, to_bf16=False) -> np.ndar
         s = -s
     a, b_ = x[..., :half], x[..., half:]
     y = np.concatenate([a * c - b_ * s, b_ * c + a * s], axis=-1)
-    return round_bf16(y) if to_bf16 else y
+    return y
 
 
 def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0,
-            rope=None, rope_bf16=False):
+            rope=None):
     """Returns (out [Tq,H,D] float64, lse [H,Tq] float64 or None).
     window W > 0: row i attends only keys with |i - j| < W (sliding window).
-    rope = (cos, sin), tables [P, D/2]: Q and K are rotated first (rope_rotate;
-    rope_bf16: the rotated Q and K rounded to bfloat16)."""
+    rope = (cos, sin), tables [P, D/2]: Q and K are rotated first (rope_rotate),
+    exactly, in float64."""
     lib = _load()
     qo, ko = _i32(q_off), _i32(kv_off)
     q, k, v, bias = _f64(q), _f64(k), _f64(v), _f64(bias)
     if rope is not None:
-        q = rope_rotate(q, qo, rope[0], rope[1], to_bf16=rope_bf16)
-        k = rope_rotate(k, ko, rope[0], rope[1], to_bf16=rope_bf16)
+        q = rope_rotate(q, qo, rope[0], rope[1])
+        k = rope_rotate(k, ko, rope[0], rope[1])
     Tq, H, D = q.shape
     B = len(qo) - 1
     if scale is None:
@@ -139,16 +132,15 @@ def forward(q_off, kv_off, q, k, v, bias=None, scale=None, act=SOFTMAX, block=0,
 
 
 def backward(q_off, kv_off, q, k, v, dout, bias=None, scale=None, act=SOFTMAX, block=0, nthreads=None, window=0,
-             rope=None, rope_bf16=False):
+             rope=None):
     """Returns (dq, dk, dv, dbias or None), all float64 (window and rope as in
-    forward; with rope, dq and dk are the gradients of the unrotated Q and K,
-    the bf16 rounding of rope_bf16 passing gradients through unchanged)."""
+    forward; with rope, dq and dk are the gradients of the unrotated Q and K)."""
     lib = _load()
     qo, ko = _i32(q_off), _i32(kv_off)
     q, k, v, dout, bias = _f64(q), _f64(k), _f64(v), _f64(dout), _f64(bias)
     if rope is not None:
-        q = rope_rotate(q, qo, rope[0], rope[1], to_bf16=rope_bf16)
-        k = rope_rotate(k, ko, rope[0], rope[1], to_bf16=rope_bf16)
+        q = rope_rotate(q, qo, rope[0], rope[1])
+        k = rope_rotate(k, ko, rope[0], rope[1])
     Tq, H, D = q.shape
     Tk = k.shape[0]
     B = len(qo) - 1

@@ -41,14 +41,14 @@ def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, wind
     return {n: (None if t is None else t.double().cpu().numpy()) for n, t in res.items()}
 
 
-def run_oracle(bt, act=0, block=0, backward=True, window=0, rope=None, rope_bf16=False):
+def run_oracle(bt, act=0, block=0, backward=True, window=0, rope=None):
     out, lse = oracle.forward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bias=bt.get("bias"),
-                              scale=bt["scale"], act=act, block=block, window=window, rope=rope, rope_bf16=rope_bf16)
+                              scale=bt["scale"], act=act, block=block, window=window, rope=rope)
     res = {"out": out, "lse": lse}
     if backward:
         dq, dk, dv, _ = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"],
                                         bias=bt.get("bias"), scale=bt["scale"], act=act, block=block, window=window,
-                                        rope=rope, rope_bf16=rope_bf16)
+                                        rope=rope)
         res.update(dq=dq, dk=dk, dv=dv)
     return res
 

@@ -133,6 +133,11 @@ def test_error_codes(lib):
     assert create(lib, ok, ok, window=-1) == J.ERR_INVALID_ARG
     assert create(lib, ok, ok, block=64, window=8) == J.ERR_INVALID_ARG   # window and block exclude each other
     assert create(lib, ok, ok, window=8) == J.OK
+    # float32 data: softmax only (their bf16 rounding on entry would exceed the
+    # tolerances of the unnormalised activation sums)
+    assert create(lib, ok, ok, dtype=1) == J.OK
+    assert create(lib, ok, ok, dtype=1, act=1) == J.ERR_UNSUPPORTED
+    assert create(lib, ok, ok, dtype=1, act=2) == J.ERR_UNSUPPORTED
 
 
 def test_host_only_plan_refuses_compute(lib):

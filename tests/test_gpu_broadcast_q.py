@@ -98,10 +98,13 @@ def test_broadcast_q_device_plan_and_determinism():
 
 def test_broadcast_q_full_size_pooled_workload():
     """The full pooled-attention workload (B=256, 32 shared rows, keys up to 8000,
-    SiLU): O, dK, dV equal the materialised path bit for bit.  dQ equals the sum
-    over the sequences of the materialised path's per-sequence dQ, taken from
-    its float32-output form (the same bf16 kernels, unrounded results), summed in
-    float64; the sum of 256 bf16-rounded rows would carry 256 roundings."""
+    SiLU), in the launch configuration the bench times: O, dK and dV equal the
+    materialised path bit for bit (that path is checked against the oracle on
+    sampled sequences of this workload), and the summed dQ of the shared rows
+    is checked element by element against the oracle: its per-sequence
+    gradients on the materialised batch, summed over all 256 sequences in
+    float64."""
+    from oracle import oracle
     b = W.make_batch(4, act=SILU)
     w = b.w
     bt = dict(q_off=b.q_off, kv_off=b.kv_off, q=b.q, k=b.k, v=b.v, bias=b.bias, dout=b.dout, scale=b.scale)
@@ -111,6 +114,5 @@ def test_broadcast_q_full_size_pooled_workload():
     mat = PT.run_library(bt, act=SILU)
     for name in ("out", "dk", "dv"):
         np.testing.assert_array_equal(got[name], mat[name], err_msg=name)
-    bt32 = dict(bt, **{n: bt[n].float() for n in ("q", "k", "v", "dout")})
-    mat32 = PT.run_library(bt32, act=SILU, dtype="fp32")
-    PT.assert_close(got["dq"], _dq_sum(mat32["dq"], b.B, w.q_rows_shared), PT.FWD_TOL, "dq")
+    ref_dq, _, _, _ = oracle.backward(b.q_off, b.kv_off, b.q, b.k, b.v, b.dout, scale=b.scale, act=SILU)
+    PT.assert_close(got["dq"], _dq_sum(ref_dq, b.B, w.q_rows_shared), PT.BWD_TOL, "dq (sum over 256 sequences)")

@@ -470,18 +470,3 @@ def test_rope_preserves_norms_and_transpose_inverts():
     np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(bt["q"].numpy(), axis=-1), rtol=1e-13)
     np.testing.assert_allclose(oracle.rope_rotate(y, bt["q_off"], cos, sin, transpose=True), bt["q"].numpy(),
                                rtol=0, atol=1e-13)
-
-
-def test_rope_bf16_rounding():
-    """rope_bf16: the rotated rows are the nearest bfloat16 values of the exact
-    rotation (torch's float32 -> bfloat16 cast of an exactly representable
-    float32 agrees), and bf16 rows rotated by the identity stay as they are."""
-    bt = batch(56, [40, 17], [40, 17], D=16, dtype=torch.bfloat16)
-    cos, sin = _ladder(40, 16)
-    exact = oracle.rope_rotate(bt["q"], bt["q_off"], cos, sin)
-    r = oracle.rope_rotate(bt["q"], bt["q_off"], cos, sin, to_bf16=True)
-    assert np.all(np.abs(r - exact) <= 2.0 ** -8 * np.abs(exact))
-    np.testing.assert_array_equal(r, torch.from_numpy(r).to(torch.bfloat16).double().numpy())
-    one, zero = np.ones((40, 8)), np.zeros((40, 8))
-    np.testing.assert_array_equal(oracle.rope_rotate(bt["q"], bt["q_off"], one, zero, to_bf16=True),
-                                  bt["q"].double().numpy())
