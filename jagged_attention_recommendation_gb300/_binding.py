@@ -25,7 +25,7 @@ EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
             "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
             "jattn_shard", "jattn_step_host", "jattn_step_host_join", "jattn_fwd_rope", "jattn_bwd_rope",
-            "jattn_plan_update_device")
+            "jattn_plan_update_device", "jattn_test_fwd_stall")
 
 
 class JattnError(RuntimeError):
@@ -93,6 +93,8 @@ def load():
     lib.jattn_bwd_rope.restype = i32
     lib.jattn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.jattn_bwd_noalloc.restype = i32
+    lib.jattn_test_fwd_stall.argtypes = [P, P, P, P, P, P, ctypes.c_uint64, P]
+    lib.jattn_test_fwd_stall.restype = i32
     lib.jattn_step_host.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P, P, P]
     lib.jattn_step_host.restype = i32
     lib.jattn_step_host_join.argtypes = [P, P]

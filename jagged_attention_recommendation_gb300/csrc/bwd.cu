@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const ErrCtx err{g.status, abort_flag};
+    const ErrCtx err{g.status, abort_flag, g.wait_ns};
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
@@ -190,7 +190,7 @@ __global__ void __launch_bounds__(512, 1)
                     ++v_it;
                 }
             }
-            if (!ok) {
+            {  // the last copy into every slot has landed before the CTA leaves (also after an abort)
                 for (uint32_t s = 0; s < C::NSK && s < k_it; ++s) {
                     const uint32_t last = k_it - 1 - ((k_it - 1 - s) % C::NSK);
                     mbar_drain(&k_full[last % C::NSK], (last / C::NSK) & 1);
@@ -219,10 +219,9 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 ++t_local;
             }
-            if (!ok) {
-                for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
-                    mbar_drain(&qd_full[i & 1], (i >> 1) & 1);
-            }
+            // the last copy into each slot has landed before the CTA leaves
+            for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
+                mbar_drain(&qd_full[i & 1], (i >> 1) & 1);
         } else if (warp == 3 && lane == 0) {
             // -------------------------------------------------------- S / dP issuer
             // Two issuing threads keep the tensor pipe fed (a thread's own waits
@@ -507,7 +506,7 @@ __global__ void __launch_bounds__(512, 1)
 template <int D, bool ACT, int BIAS, bool WIN, bool DT>
 static cudaError_t launch_dq_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = DqCfg<D, ACT, BIAS>;
-    static bool done[64] = {};
+    static SmemOnce done;
     cudaError_t e = ensure_smem(dq_kernel<D, ACT, BIAS, WIN, DT>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
     dq_kernel<D, ACT, BIAS, WIN, DT><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);

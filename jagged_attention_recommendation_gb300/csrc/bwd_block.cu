@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const ErrCtx err{g.status, abort_flag};
+    const ErrCtx err{g.status, abort_flag, g.wait_ns};
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                     tma_load_2d(base + C::IDO + kb * C::SUB, &tmDO, &in_full[buf], x, t.q_start);
                 }
             }
-            if (!ok) {
+            {  // the last copy into every buffer has landed before the CTA leaves (also after an abort)
                 for (uint32_t b = 0; b < C::NBUF && b < t_local; ++b) {
                     const uint32_t last = t_local - 1 - ((t_local - 1 - b) % C::NBUF);
                     mbar_drain(&in_full[last % C::NBUF], (last / C::NBUF) & 1);
@@ -522,7 +522,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
 template <int D, bool ROPE>
 static cudaError_t launch_block_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = BlkCfg<D>;
-    static bool done[64] = {};
+    static SmemOnce done;
     cudaError_t e = ensure_smem(bwd_block_kernel<D, ROPE>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
     bwd_block_kernel<D, ROPE><<<n_ctas, ROPE ? 256 : 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
@@ -531,7 +531,8 @@ static cudaError_t launch_block_t(const TmapSet &tm, const BwdArgs &a, int n_cta
 
 cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     const bool rope = a.g.rope_cos != nullptr;
-    if (rope && a.g.rope_sin == nullptr) return cudaErrorInvalidValue;
+    // the rotation is offered with softmax only (checked by the host first)
+    if (rope && (a.g.rope_sin == nullptr || a.g.act != kSoftmax)) return cudaErrorInvalidValue;
     if (D == 128) return rope ? launch_block_t<128, true>(tm, a, n_ctas, st) : launch_block_t<128, false>(tm, a, n_ctas, st);
     if (D == 64) return rope ? launch_block_t<64, true>(tm, a, n_ctas, st) : launch_block_t<64, false>(tm, a, n_ctas, st);
     return cudaErrorInvalidValue;

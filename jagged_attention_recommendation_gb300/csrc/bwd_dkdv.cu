@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const ErrCtx err{g.status, abort_flag};
+    const ErrCtx err{g.status, abort_flag, g.wait_ns};
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(512, 1)
                     }
                 }
             }
-            if (!ok && lane == 0) {
+            if (lane == 0) {  // the last copy into every slot has landed before the CTA leaves
                 for (uint32_t s = 0; s < C::NSQ && s < q_it; ++s) {
                     const uint32_t last = q_it - 1 - ((q_it - 1 - s) % C::NSQ);
                     mbar_drain(&qs_full[last % C::NSQ], (last / C::NSQ) & 1);
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(512, 1)
                     tma_load_2d(smem + C::OFF_V + kb * C::SUB_KV, &tmV, kv_full, t.h * D + kb * 64, t.kv_start);
                 }
             }
-            if (!ok && t_local > 0) mbar_drain(kv_full, (t_local - 1) & 1);
+            if (t_local > 0) mbar_drain(kv_full, (t_local - 1) & 1);  // also after an abort
         } else if (warp == 3 && lane == 0) {
             // -------------------------------------------------------- S^T / dP^T issuer
             // Two issuing threads keep the tensor pipe fed: a thread's own waits
@@ -513,7 +513,7 @@ __global__ void __launch_bounds__(512, 1)
 template <int D, bool ACT, int BIAS, bool WIN>
 static cudaError_t launch_dkdv_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = DkvCfg<D, ACT, BIAS>;
-    static bool done[64] = {};
+    static SmemOnce done;
     cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
     dkdv_kernel<D, ACT, BIAS, WIN><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);

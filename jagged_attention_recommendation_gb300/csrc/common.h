@@ -13,7 +13,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kStatusDeviceTimeout = 6;
 constexpr int kStatusDeviceCheck = 7;
 
-// a bounded wait gives up after this much wall time
+// a bounded wait gives up after this much wall time (the kernels take the
+// limit from Geom::wait_ns, which the library sets to this value; only the
+// stall test build of the forward shortens it)
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
 
 // largest bias table (H * NB floats) the kernels stage in shared memory
@@ -58,6 +60,7 @@ struct Geom {
     int32_t rope_rows;        // table positions 0 .. rope_rows - 1
     int32_t q_bcast;          // 1: every sequence's queries are the rows 0 .. Lq-1 of one shared Q
                               // (Q is read at the local row, O / dO / lse at the sequence's rows)
+    unsigned long long wait_ns;  // limit of every bounded wait (kWaitTimeoutNs)
 };
 
 // Where a [T, H, D] result goes: element (t, h, c) at ptr[t*ld + h*cols + c] for c < cols.

@@ -41,8 +41,9 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 // role of a CTA leave its loop once any role has given up waiting.
 // ---------------------------------------------------------------------------
 struct ErrCtx {
-    int *gstatus;          // device status word (global)
-    volatile int *abort;   // shared-memory abort flag of this CTA
+    int *gstatus;                // device status word (global)
+    volatile int *abort;         // shared-memory abort flag of this CTA
+    unsigned long long limit_ns; // a wait gives up after this much wall time
 };
 
 __device__ __forceinline__ void raise_error(const ErrCtx &e, int code) {
@@ -83,7 +84,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Gives up after
-// kWaitTimeoutNs of wall time (or at once when another role has aborted),
+// e.limit_ns of wall time (or at once when another role has aborted),
 // records JATTN_ERR_DEVICE_TIMEOUT and returns false.  Kernels that move
 // registers between warpgroups (setmaxnreg) define JATTN_INLINE_WAITS before
 // including this header: ptxas cannot share one out-of-line function between
@@ -98,7 +99,7 @@ static __device__ JATTN_WAIT_LINKAGE bool mbar_wait_slow(uint64_t *bar, uint32_t
     for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*e.abort) return false;
-        if ((it & 255u) == 255u && global_timer_ns() - t0 > kWaitTimeoutNs) {
+        if ((it & 255u) == 255u && global_timer_ns() - t0 > e.limit_ns) {
             raise_error(e, kStatusDeviceTimeout);
             return false;
         }
@@ -119,7 +120,7 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t *bar, uint32_t parity, c
 // Bounded wait used while draining after an abort: ignores the abort flag.
 __device__ __forceinline__ void mbar_drain(uint64_t *bar, uint32_t parity) {
     int zero = 0;
-    const ErrCtx quiet{nullptr, &zero};
+    const ErrCtx quiet{nullptr, &zero, kWaitTimeoutNs};
     mbar_wait(bar, parity, quiet);
 }
 

@@ -8,7 +8,7 @@ template <int D, bool ACT, int BIAS, bool WIN>
 static cudaError_t launch_fwd_w(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
     using C = FwdCfg<D, ACT, BIAS>;
     auto kern = fwd_kernel<D, ACT, BIAS, WIN>;
-    static bool done[64] = {};
+    static SmemOnce done;
     cudaError_t e = ensure_smem(kern, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
     kern<<<n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(tm.q, tm.k, tm.v, a);

@@ -111,8 +111,12 @@ struct FwdCfg {
 // embedding of Q and K ("Training GEM at LLM scale", section "BlockAttention")
 // in shared memory as the tiles arrive: the output warpgroup rotates each
 // BlockAttention tile's Q rows and its one K block two tiles ahead, before the
-// S issuer may use them (q_rot / k_rot).
-template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false>
+// S issuer may use them (q_rot / k_rot).  STALL: a test build only (one
+// instantiation, launched by jattn_test_fwd_stall): before its first product
+// the S issuer waits on a barrier that nothing completes at that point, so
+// the bounded wait runs out and the kernel takes its error path (status word,
+// abort flag, drained copies, TMEM freed) on a real launch.
+template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false, bool STALL = false>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
@@ -191,7 +195,7 @@ __global__ void __launch_bounds__(512, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const ErrCtx err{g.status, abort_flag};
+    const ErrCtx err{g.status, abort_flag, g.wait_ns};
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
@@ -240,8 +244,11 @@ __global__ void __launch_bounds__(512, 1)
                 }
             }
             if (ok && v_pending) ok = load_v();
-            // Do not leave the CTA with copies still landing in shared memory.
-            if (!ok) {
+            // Do not leave the CTA with copies still landing in shared memory:
+            // wait for the last copy into every slot.  In a normal run the
+            // consumers have waited for them all; after an abort (here or in
+            // another role) nobody else may.
+            {
                 for (uint32_t s = 0; s < C::NST && s < k_it; ++s) {
                     const uint32_t last = k_it - 1 - ((k_it - 1 - s) % C::NST);  // last load into slot s
                     mbar_drain(&k_full[last % C::NST], (last / C::NST) & 1);
@@ -277,10 +284,9 @@ __global__ void __launch_bounds__(512, 1)
                 }
                 ++t_local;
             }
-            if (!ok) {
-                for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
-                    mbar_drain(&q_full[i & 1], (i >> 1) & 1);
-            }
+            // the last copy into each slot has landed before the CTA leaves
+            for (uint32_t i = (t_local > 2 ? t_local - 2 : 0); i < t_local; ++i)
+                mbar_drain(&q_full[i & 1], (i >> 1) & 1);
         } else if (warp == 3 && lane == 0) {
             // -------------------------------------------------------- S issuer
             // Two issuing threads keep the tensor pipe fed (a thread's own waits
@@ -291,6 +297,9 @@ __global__ void __launch_bounds__(512, 1)
             // group's O already holds all of the group's earlier blocks, and a
             // rescale of O may touch it.
             bool ok = true;
+            // test build: drain[0] completes only when this thread commits to it
+            // after its loop, so this wait runs out (bounded by g.wait_ns)
+            if constexpr (STALL) ok = mbar_wait(&drain[0], 0, err);
             TileStream tsa(g, tbeg, tend);
             Tile ta;
             uint32_t ta_n = 0, ns = 0;

@@ -4,19 +4,32 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "common.h"
 
 namespace jattn {
 
+// Per-device record of a kernel's shared-memory opt-in.  Atomic, because host
+// threads driving different plans may launch the same kernel for the first
+// time at once; the opt-in itself is idempotent, so two threads that both find
+// it unset both make it, and either result stands.
+struct SmemOnce {
+    std::atomic<bool> done[64];
+    SmemOnce() {
+        for (auto &d : done) d.store(false, std::memory_order_relaxed);
+    }
+};
+
 // Opt a kernel into `bytes` of dynamic shared memory, once per device.
 template <typename K>
-inline cudaError_t ensure_smem(K kern, uint32_t bytes, bool (&done)[64]) {
+inline cudaError_t ensure_smem(K kern, uint32_t bytes, SmemOnce &once) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) dev = 0;
     const bool cacheable = dev >= 0 && dev < 64;
-    if (cacheable && done[dev]) return cudaSuccess;
+    if (cacheable && once.done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess && cacheable) done[dev] = true;
+    if (e == cudaSuccess && cacheable) once.done[dev].store(true, std::memory_order_release);
     return e;
 }
 
@@ -27,6 +40,10 @@ struct TmapSet {
 
 // forward: D in {64, 128}; act selects the GDPA activation path
 cudaError_t launch_fwd(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream);
+
+// test build of the forward whose first bounded wait runs out after a.g.wait_ns
+// (softmax, no bias, no window, D in {64, 128})
+cudaError_t launch_fwd_stall(int D, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream);
 
 // forward with rotary position embedding of Q and K (a.g.rope_cos / rope_sin set, no window)
 cudaError_t launch_fwd_rope(int D, bool act, const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream);

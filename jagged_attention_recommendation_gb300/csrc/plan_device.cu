@@ -238,7 +238,7 @@ cudaError_t launch_plan_device(const DevPlanArgs &a, cudaStream_t stream) {
         a.n_ctas < 1)
         return cudaErrorInvalidValue;
     const size_t smem = plan_device_smem(a.sort_len);
-    static bool done[64] = {};
+    static SmemOnce done;
     cudaError_t e = ensure_smem(plan_kernel, static_cast<uint32_t>(plan_device_smem(kDevPlanMaxSeqs)), done);
     if (e != cudaSuccess) return e;
     plan_kernel<<<1, kThreads, smem, stream>>>(a);
