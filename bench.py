@@ -337,11 +337,21 @@ def run_ours(args, w, batch):
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     phys = int(visible[local]) if local < len(visible) and visible[local].strip().isdigit() else local
     sampler = ClockSampler(phys)
+    sampler.start()
+    # Load soak: the same step, back to back, for --soak seconds right before the
+    # timed region, so that the clock sampler (and any outside one) sees the GPU
+    # under this load and the timed steps run at its loaded clocks.
+    soak_steps = 0
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < args.soak:
+        for _ in range(16):
+            step()
+        soak_steps += 16
+        torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = plan.launch_count
-    sampler.start()
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         flush.fill_(s & 0xFF)
@@ -361,6 +371,8 @@ def run_ours(args, w, batch):
         dist.barrier()
     torch.cuda.synchronize()
     clocks = sampler.stop()
+    clocks["window"] = "sampled every 50 ms over a %.1f s load soak (%d steps) and the timed steps" % (
+        args.soak, soak_steps)
     plan.set_events(None)
     launches = plan.launch_count - launches0
     st = plan.check_status()
@@ -382,23 +394,9 @@ def run_ours(args, w, batch):
     pk, pk_kind = peaks()
 
     # roofline of the dominant kernel (largest share of the step's kernel time)
-    dom = max(per_kernel, key=per_kernel.get)
-    fl, by = kernel_work(w, batch, dom, pk)
-    t_dom = per_kernel[dom] * 1e-3
     bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
     intensity = (f_fwd + f_bwd) / (bf + bb)
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if fl > 0 and fl / by >= ridge * 0.5:
-        roof = {"bound": "tensor", "achieved": fl / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
-    else:
-        roof = {"bound": "hbm", "achieved": by / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
-    roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.wid, dom)
-    roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
-    roof["kernel"] = dom
-    roof["peak_source"] = pk_kind + " (burst)"
-    roof["algorithmic_flops_per_launch"] = fl
-    roof["algorithmic_bytes_per_launch"] = by
+    roof = roofline_of(w, batch, per_kernel, pk, pk_kind)
 
     # the same forward and backward launches captured once as two CUDA graphs and
     # replayed (no host launch work); L2 flushed between steps as above
@@ -471,6 +469,18 @@ def run_ours(args, w, batch):
     if e2e is not None:
         line["e2e"] = {k2: e2e[k2] for k2 in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
         line["e2e"]["ms_per_step"] = e2e["ms_per_step"]
+    plain = not (args.rope or args.broadcast_q or args.window or args.device_plan or args.act is not None)
+    if rank == 0 and ws == 1 and w.wid == 2 and plain and not args.no_others:
+        # the other workloads' step throughput and dominant-kernel roofline
+        # fractions, measured in this run beside the self-attention line
+        del q, k, v, dout, out, dq, dk, dv, fws, bws
+        torch.cuda.empty_cache()
+        others = {}
+        for wid, act in OTHER_WORKLOADS:
+            key = "%d_%s" % (wid, W.ACT_NAMES[act])
+            others[key] = measure_other(wid, act, dev, stream, max(10, min(args.steps, 30)), flush)
+            torch.cuda.empty_cache()
+        line["others"] = others
     if rank == 0 and ws == 1 and not args.no_cpu:
         v_cpu, dt, cores, desc = time_oracle(batch, args.cpu_frac, seed=0, rope=rope)
         line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -480,6 +490,86 @@ def run_ours(args, w, batch):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+# the other workloads measured beside the self-attention line (the tiny fp32
+# workload is a parity case only)
+OTHER_WORKLOADS = [(3, W.SOFTMAX), (4, W.SILU), (4, W.GELU_TANH), (5, W.SOFTMAX)]
+
+
+def roofline_of(w, batch, per_kernel, pk, pk_kind):
+    """Roofline record of the kernel with the largest share of the step."""
+    dom = max(per_kernel, key=per_kernel.get)
+    fl, by = kernel_work(w, batch, dom, pk)
+    t_dom = per_kernel[dom] * 1e-3
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
+    if fl > 0 and fl / by >= ridge * 0.5:
+        roof = {"bound": "tensor", "achieved": fl / t_dom / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": by / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = measured_traffic(w.wid, dom)
+    roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
+    roof["kernel"] = dom
+    roof["peak_source"] = pk_kind + " (burst)"
+    roof["algorithmic_flops_per_launch"] = fl
+    roof["algorithmic_bytes_per_launch"] = by
+    return roof
+
+
+def measure_other(wid, act, dev, stream, steps, flush):
+    """One other workload at full size: device-timed steps (plan update queued
+    first, L2 flushed between steps), per-kernel times from the library's event
+    hook, valid-token TFLOP/s and the dominant kernel's roofline fraction."""
+    import jagged_attention_recommendation_gb300 as J
+    batch = W.make_batch(wid, act=act)
+    w = batch.w
+    H, D = w.H, w.D
+    q, k, v, dout = (t.to(dev) for t in (batch.q, batch.k, batch.v, batch.dout))
+    bias = batch.bias.to(dev) if batch.bias is not None else None
+    plan = J.Plan(batch.q_off, batch.kv_off, H, D, act=batch.act, block=w.block, bias_buckets=w.bias_buckets,
+                  device=dev.index)
+    out = torch.empty(batch.Tq, H, D, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(H, batch.Tq, dtype=torch.float32, device=dev) if batch.act == W.SOFTMAX else None
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    bws = torch.empty(max(plan.bwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
+    names = KERNELS_BLOCK if w.block else [n for n in KERNELS_FULL if n != "bwd_delta" or batch.act == W.SOFTMAX]
+
+    def step(evs=None):
+        plan.update(batch.q_off, batch.kv_off, stream)
+        if evs is not None:
+            plan.set_events(evs[0:2])
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
+        if evs is not None:
+            plan.set_events(evs[1:])
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(steps)]
+    for s_ in range(steps):
+        flush.fill_(s_ & 0xFF)
+        step(kev[s_])
+    torch.cuda.synchronize()
+    plan.set_events(None)
+    st = plan.check_status()
+    if st != 0:
+        raise RuntimeError("device status, workload %d: %s" % (wid, J.status_str(st)))
+    per_kernel = {n: float(np.mean([kev[s_][i].elapsed_time(kev[s_][i + 1]) for s_ in range(steps)]))
+                  for i, n in enumerate(names)}
+    ms = float(np.mean([kev[s_][0].elapsed_time(kev[s_][-1]) for s_ in range(steps)]))
+    f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block, w.window)
+    bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
+    pk, pk_kind = peaks()
+    roof = roofline_of(w, batch, per_kernel, pk, pk_kind)
+    plan.close()
+    return {"workload": workload_config(w, batch.act, batch.B, True)["workload"], "steps": steps,
+            "value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "per_kernel_ms": per_kernel,
+            "step_hbm_frac": (bf + bb) / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "roofline": roof}
 
 
 def run_e2e(args, w, batch, plan, dev, stream):
@@ -549,6 +639,10 @@ def main():
                     help="rotary position embedding of Q and K (standard frequency table; block workload only)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window W (keys with |i - j| < W) on the chosen workload; 0 = off")
+    ap.add_argument("--soak", type=float, default=1.5,
+                    help="seconds of back-to-back steps right before the timed region (clocks under load)")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the other workloads' lines (others) in the self-attention run")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

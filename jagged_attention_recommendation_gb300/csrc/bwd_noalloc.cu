@@ -26,7 +26,9 @@ void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_bwd_scratch on `dev`, looked up once per device with that
 // device current.  In host code the array's name is only a host-side stand-in;
-// kernels must be given this address.
+// kernels must be given this address.  The caller's current device is put back
+// afterwards; if that fails, the call fails too (and caches nothing), so a
+// success never leaves the caller on another device.
 cudaError_t scratch_address(int dev, void **addr) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_scratch_addr[dev] == nullptr) {
@@ -36,7 +38,10 @@ cudaError_t scratch_address(int dev, void **addr) {
         if (prev != dev && (e = cudaSetDevice(dev)) != cudaSuccess) return e;
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-        if (prev != dev) cudaSetDevice(prev);
+        if (prev != dev) {
+            const cudaError_t r = cudaSetDevice(prev);
+            if (e == cudaSuccess) e = r;
+        }
         if (e != cudaSuccess) return e;
         g_scratch_addr[dev] = p;
     }
