@@ -230,12 +230,27 @@ def measured_traffic(wid: int, kernel: str):
     return rec[0]
 
 
-KERNELS_FULL = ["fwd", "bwd_delta", "bwd_dq", "bwd_dkdv"]
+KERNELS_FULL = ["fwd", "bwd_delta", "bwd_dq", "bwd_dkdv"]       # backward with the recomputing dQ pass
+KERNELS_FULL_DS = ["fwd", "bwd_delta", "bwd_dkdv", "bwd_dq_gemm"]  # backward with dS chunks (full workspace)
 KERNELS_BLOCK = ["fwd", "bwd_block"]
 
 
-def kernel_work(w, batch, name, pk):
-    """Algorithmic (flops, bytes) of one launch of `name` over the batch."""
+def kernel_names(w, act, device_plan=False, broadcast_q=False):
+    """The kernels one step launches, in order (the library takes the dS-chunk
+    backward for full attention on a host plan without a window, given the full
+    workspace as the bench does)."""
+    if w.block:
+        return list(KERNELS_BLOCK)
+    ds = not w.window and not device_plan
+    names = [n for n in (KERNELS_FULL_DS if ds else KERNELS_FULL) if n != "bwd_delta" or act == W.SOFTMAX]
+    if broadcast_q:  # the per-sequence dQ rows are summed by one more kernel
+        names.insert(names.index("bwd_dq_gemm" if ds else "bwd_dq") + 1, "bwd_dq_reduce")
+    return names
+
+
+def kernel_work(w, batch, name, pk, ds=True):
+    """Algorithmic (flops, bytes) of one launch of `name` over the batch (ds:
+    the backward writes dS chunks, i.e. full workspace on a host plan)."""
     H, D = w.H, w.D
     p = W.valid_pairs(batch.q_off, batch.kv_off, w.block, w.window)
     Tq, Tk = batch.Tq, batch.Tk
@@ -248,12 +263,17 @@ def kernel_work(w, batch, name, pk):
         return 0.0, 2.0 * Tq * e + 4.0 * H * Tq
     if name == "bwd_dq_reduce":  # fp32 per-sequence dQ rows in, the shared rows' bf16 sum out
         return 0.0, 4.0 * Tq * H * D + 2.0 * w.q_rows_shared * H * D
+    # the dS chunks (bf16 per valid pair and head; activation modes: hi and lo)
+    ds_bytes = 2.0 * H * p * (1 if batch.act == W.SOFTMAX else 2)
     if name == "bwd_dq":  # dQ GEMM; its S and dP recompute is not counted
         lse = 8.0 * H * Tq if batch.act == W.SOFTMAX else 0.0
         return 2.0 * D * H * p, 2.0 * Tq * e + 2.0 * Tk * e + Tq * e + lse
-    if name == "bwd_dkdv":  # S, dP, dV, dK
+    if name == "bwd_dq_gemm":  # dQ = scale dS K: the dS chunks and K in, dQ out
+        return 2.0 * D * H * p, ds_bytes + Tk * e + Tq * e
+    if name == "bwd_dkdv":  # S, dP, dV, dK (and, on the dS-chunk path, the chunks out)
         lse = 8.0 * H * Tq if batch.act == W.SOFTMAX else 0.0
-        return 8.0 * D * H * p, 2.0 * Tq * e + 2.0 * Tk * e + 2.0 * Tk * e + lse
+        ds_out = ds_bytes if (ds and not w.block and not w.window) else 0.0
+        return 8.0 * D * H * p, 2.0 * Tq * e + 2.0 * Tk * e + 2.0 * Tk * e + lse + ds_out
     raise KeyError(name)
 
 
@@ -325,9 +345,7 @@ def run_ours(args, w, batch):
         plan_dev_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
 
-    names = KERNELS_BLOCK if w.block else [n for n in KERNELS_FULL if n != "bwd_delta" or batch.act == W.SOFTMAX]
-    if args.broadcast_q:  # the dQ pass's per-sequence rows are summed by one more kernel
-        names.insert(names.index("bwd_dq") + 1, "bwd_dq_reduce")
+    names = kernel_names(w, batch.act, args.device_plan, args.broadcast_q)
     n_fwd, n_bwd = 1, len(names) - 1
     if f32 or D == 32:
         raise SystemExit("bench: staged (fp32 / D=32) workloads are parity cases, not bench lines")
@@ -396,7 +414,7 @@ def run_ours(args, w, batch):
     # roofline of the dominant kernel (largest share of the step's kernel time)
     bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
     intensity = (f_fwd + f_bwd) / (bf + bb)
-    roof = roofline_of(w, batch, per_kernel, pk, pk_kind)
+    roof = roofline_of(w, batch, per_kernel, pk, pk_kind, ds=not args.device_plan)
 
     # the same forward and backward launches captured once as two CUDA graphs and
     # replayed (no host launch work); L2 flushed between steps as above
@@ -497,10 +515,10 @@ def run_ours(args, w, batch):
 OTHER_WORKLOADS = [(3, W.SOFTMAX), (4, W.SILU), (4, W.GELU_TANH), (5, W.SOFTMAX)]
 
 
-def roofline_of(w, batch, per_kernel, pk, pk_kind):
+def roofline_of(w, batch, per_kernel, pk, pk_kind, ds=True):
     """Roofline record of the kernel with the largest share of the step."""
     dom = max(per_kernel, key=per_kernel.get)
-    fl, by = kernel_work(w, batch, dom, pk)
+    fl, by = kernel_work(w, batch, dom, pk, ds)
     t_dom = per_kernel[dom] * 1e-3
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     if fl > 0 and fl / by >= ridge * 0.5:
@@ -534,7 +552,7 @@ def measure_other(wid, act, dev, stream, steps, flush):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
     bws = torch.empty(max(plan.bwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
-    names = KERNELS_BLOCK if w.block else [n for n in KERNELS_FULL if n != "bwd_delta" or batch.act == W.SOFTMAX]
+    names = kernel_names(w, batch.act)
 
     def step(evs=None):
         plan.update(batch.q_off, batch.kv_off, stream)

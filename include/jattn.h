@@ -172,9 +172,24 @@ jattn_status jattn_plan_update_device(jattn_plan *plan, const int32_t *q_offsets
 jattn_status jattn_plan_tiles(const jattn_plan *plan, int32_t which, const jattn_tile **tiles, int64_t *n_tiles,
                               const int32_t **cta_begin, int32_t *n_ctas);
 
-/* Device scratch the caller must pass to jattn_fwd / jattn_bwd (bytes; 0 = none needed). */
+/*
+ * Device scratch for jattn_fwd / jattn_bwd (bytes; 0 = none needed).
+ * jattn_fwd needs jattn_fwd_workspace_bytes.  jattn_bwd needs at least
+ * jattn_bwd_workspace_bytes_min and takes its fastest path when given
+ * jattn_bwd_workspace_bytes: full attention on a host plan without a sliding
+ * window or RoPE then keeps every block's dS in the workspace (bf16, 16 KB per
+ * 128 keys x 64 queries of a sequence and head; hi and lo parts in the
+ * activation modes), written once by the dK/dV pass, and computes dQ as a
+ * streaming product of it ("Training GEM at LLM scale", section "Jagged
+ * Sequence Flash Attention": dQ without atomic adds and without recomputing
+ * the scores).  With less than that (but at least the minimum) it runs a dQ
+ * pass that recomputes the scores.  Both are exact to the same tolerances;
+ * their dQ may differ in the last bits.  The sizes depend on the batch the
+ * plan was last (re)planned for.
+ */
 size_t jattn_fwd_workspace_bytes(const jattn_plan *plan);
 size_t jattn_bwd_workspace_bytes(const jattn_plan *plan);
+size_t jattn_bwd_workspace_bytes_min(const jattn_plan *plan);
 
 /* Frees the plan's host and device memory (synchronises its device). NULL is a no-op. */
 void jattn_plan_destroy(jattn_plan *plan);
@@ -196,8 +211,9 @@ jattn_status jattn_fwd(const jattn_plan *plan, const void *q, const void *k, con
  * dq, dk, dv: DEVICE outputs, fully overwritten (no accumulation, no atomics);
  * dbias: DEVICE float32 [H, NB] gradient of the bias table, overwritten when
  * non-NULL (needs a bias; full attention and sliding window only: with block
- * mode the call returns JATTN_ERR_UNSUPPORTED); workspace: DEVICE scratch of
- * jattn_bwd_workspace_bytes.
+ * mode the call returns JATTN_ERR_UNSUPPORTED); workspace: DEVICE scratch of at
+ * least jattn_bwd_workspace_bytes_min bytes (jattn_bwd_workspace_bytes for the
+ * fastest path), 16-byte aligned.
  * dq and dk include the score scale; dbias[h, n] is the plain sum of dS over
  * the pairs of head h in bucket n = min(|i - j|, NB - 1). It is summed with
  * floating-point atomic adds, so it is reproducible to rounding only (dq, dk
@@ -275,10 +291,13 @@ int64_t jattn_plan_launch_count(const jattn_plan *plan);
  * The scratch the backward needs (Delta = rowsum(dO * O), [H, Tq] floats, plus
  * bf16 staging copies for float32 or D = 32 data) lives in a fixed 16 MiB
  * device array inside the library, reserved on every GPU that loads it until
- * the process exits.  A batch whose jattn_bwd_workspace_bytes exceeds 16 MiB is
- * rejected with JATTN_ERR_WORKSPACE before anything runs (softmax, bf16: up to
- * H * Tq = 4,194,304).  Nothing is allocated: no cudaMalloc, cudaFree or
- * allocating library routine is called.
+ * the process exits.  A batch whose jattn_bwd_workspace_bytes_min exceeds
+ * 16 MiB is rejected with JATTN_ERR_WORKSPACE before anything runs (softmax,
+ * bf16: up to H * Tq = 4,194,304).  The call takes jattn_bwd's fastest path
+ * when the whole jattn_bwd_workspace_bytes fits the array, and otherwise the
+ * path that recomputes the scores for dQ; its results are then bitwise those
+ * of jattn_bwd given a workspace of the same size.  Nothing is allocated: no
+ * cudaMalloc, cudaFree or allocating library routine is called.
  *
  * The first call on a device looks up the array's device address with that
  * device current (cudaGetSymbolAddress, once per device) and keeps it for the

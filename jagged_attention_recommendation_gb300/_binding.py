@@ -25,7 +25,7 @@ EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
             "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
             "jattn_shard", "jattn_step_host", "jattn_step_host_join", "jattn_fwd_rope", "jattn_bwd_rope",
-            "jattn_plan_update_device", "jattn_test_fwd_stall")
+            "jattn_plan_update_device", "jattn_test_fwd_stall", "jattn_bwd_workspace_bytes_min")
 
 
 class JattnError(RuntimeError):
@@ -81,6 +81,8 @@ def load():
     lib.jattn_fwd_workspace_bytes.restype = sz
     lib.jattn_bwd_workspace_bytes.argtypes = [P]
     lib.jattn_bwd_workspace_bytes.restype = sz
+    lib.jattn_bwd_workspace_bytes_min.argtypes = [P]
+    lib.jattn_bwd_workspace_bytes_min.restype = sz
     lib.jattn_plan_destroy.argtypes = [P]
     lib.jattn_plan_destroy.restype = None
     lib.jattn_fwd.argtypes = [P, P, P, P, P, P, P, P, sz, P]
@@ -221,6 +223,10 @@ class Plan:
     def bwd_workspace_bytes(self) -> int:
         return int(load().jattn_bwd_workspace_bytes(self._h))
 
+    @property
+    def bwd_workspace_bytes_min(self) -> int:
+        return int(load().jattn_bwd_workspace_bytes_min(self._h))
+
     def _tdtype(self):
         return torch.float32 if self.dtype == "fp32" else torch.bfloat16
 
@@ -257,7 +263,12 @@ class Plan:
         dq = torch.empty(self.q_rows, self.H, self.D, dtype=dt, device=q.device) if dq is None else dq
         dk = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dk is None else dk
         dv = torch.empty(self.Tk, self.H, self.D, dtype=dt, device=q.device) if dv is None else dv
-        ws = self._ws(self.bwd_workspace_bytes, workspace)
+        # a given workspace of at least the minimum is passed as it is (the library
+        # takes its fastest path that fits); otherwise the full size is allocated
+        if workspace is not None and workspace.numel() * workspace.element_size() >= self.bwd_workspace_bytes_min:
+            ws = workspace
+        else:
+            ws = self._ws(self.bwd_workspace_bytes, None)
         nbytes = 0 if ws is None else ws.numel() * ws.element_size()
         if rope is not None:
             r = _rope(rope)

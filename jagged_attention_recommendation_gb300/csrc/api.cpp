@@ -47,12 +47,15 @@ struct jattn_plan {
     int32_t bcast_n = 0;  // broadcast Q: rows of the shared Q (every sequence's Lq)
     int64_t Tq = 0, Tk = 0;
     std::vector<int32_t> q_off, kv_off;
+    // backward dS chunks (host plans): first chunk of every sequence, and the total
+    std::vector<long long> ds_base;
+    int64_t ds_chunks = 0;
     std::vector<jattn_tile> tiles[2];
     std::vector<int32_t> cta[2];
     // device copies: one buffer holding both tile lists, both schedules and the offsets
     uint8_t *d_buf = nullptr;
     size_t d_cap = 0;
-    size_t off_tiles[2] = {0, 0}, off_cta[2] = {0, 0}, off_qoff = 0, off_kvoff = 0;
+    size_t off_tiles[2] = {0, 0}, off_cta[2] = {0, 0}, off_qoff = 0, off_kvoff = 0, off_dsbase = 0;
     int *d_status = nullptr;
     // pinned staging for the asynchronous upload, double-buffered
     void *h_pin[2] = {nullptr, nullptr};
@@ -225,6 +228,8 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
     off = align_up(off + p->q_off.size() * sizeof(int32_t), 16);
     p->off_kvoff = off;
     off = align_up(off + p->kv_off.size() * sizeof(int32_t), 16);
+    p->off_dsbase = off;
+    off = align_up(off + p->ds_base.size() * sizeof(long long), 16);
     const size_t bytes = off;
 
     if (bytes > p->d_cap) {
@@ -261,6 +266,7 @@ jattn_status upload(jattn_plan *p, cudaStream_t stream) {
     }
     std::memcpy(h + p->off_qoff, p->q_off.data(), p->q_off.size() * sizeof(int32_t));
     std::memcpy(h + p->off_kvoff, p->kv_off.data(), p->kv_off.size() * sizeof(int32_t));
+    std::memcpy(h + p->off_dsbase, p->ds_base.data(), p->ds_base.size() * sizeof(long long));
     CUDA_TRY(cudaMemcpyAsync(p->d_buf, h, bytes, cudaMemcpyHostToDevice, stream));
     CUDA_TRY(cudaEventRecord(p->ev[k], stream));
     p->ev_used[k] = true;
@@ -283,6 +289,16 @@ jattn_status set_batch(jattn_plan *p, const int32_t *qo, const int32_t *ko, int3
     p->Tq = qo[B];
     p->Tk = ko[B];
     build_lists(p);
+    // dS chunks of the backward: per sequence, H x (key tiles of 128) x (query blocks of 64)
+    p->ds_base.resize(static_cast<size_t>(B) + 1);
+    int64_t c = 0;
+    for (int32_t b = 0; b < B; ++b) {
+        p->ds_base[b] = c;
+        const int64_t lq = qo[b + 1] - qo[b], lk = ko[b + 1] - ko[b];
+        c += static_cast<int64_t>(p->H) * ((lk + kTileRows - 1) / kTileRows) * ((lq + 63) / 64);
+    }
+    p->ds_base[B] = c;
+    p->ds_chunks = c;
     return JATTN_OK;
 }
 
@@ -338,6 +354,24 @@ size_t bcast_ws_bytes(const jattn_plan *p) {
     return p->mode.broadcast_q ? align_up(static_cast<size_t>(p->Tq) * p->H * p->D * 4, kAlign) : 0;
 }
 
+// The backward's dS chunks (full attention, host plans, no window): the dK/dV
+// pass writes every block's dS and dQ becomes a streaming product of them.
+// Device plans (lengths unknown on the host) and sliding windows use the dQ
+// pass that recomputes the scores instead.
+size_t ds_ws_bytes(const jattn_plan *p) {
+    if (p->dev_planned || p->mode.block != 0 || p->mode.window > 0) return 0;
+    const size_t planes = p->mode.act == JATTN_SOFTMAX ? 1 : 2;
+    return align_up(static_cast<size_t>(p->ds_chunks) * planes * kDsChunkBytes, kAlign);
+}
+
+// bytes of the backward workspace without the dS chunks: Delta, staged inputs,
+// broadcast-Q dQ rows, in that order
+size_t bwd_ws_min(const jattn_plan *p) {
+    size_t n = softmax_full(p) ? align_up(static_cast<size_t>(p->H) * p->Tq * 4, kAlign) : 0;
+    if (p->staged) n += 2 * stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
+    return n + bcast_ws_bytes(p);
+}
+
 Geom make_geom(const jattn_plan *p, int which) {
     Geom g{};
     g.tiles = reinterpret_cast<const Tile *>(p->d_buf + p->off_tiles[which]);
@@ -360,6 +394,8 @@ Geom make_geom(const jattn_plan *p, int which) {
     g.bias = nullptr;
     g.status = p->d_status;
     g.wait_ns = kWaitTimeoutNs;
+    g.ds = nullptr;
+    g.ds_base = p->dev_planned ? nullptr : reinterpret_cast<const long long *>(p->d_buf + p->off_dsbase);
     return g;
 }
 
@@ -629,10 +665,10 @@ size_t jattn_fwd_workspace_bytes(const jattn_plan *p) {
 
 size_t jattn_bwd_workspace_bytes(const jattn_plan *p) {
     if (p == nullptr) return 0;
-    size_t n = softmax_full(p) ? align_up(static_cast<size_t>(p->H) * p->Tq * 4, kAlign) : 0;
-    if (p->staged) n += 2 * stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
-    return n + bcast_ws_bytes(p);
+    return bwd_ws_min(p) + ds_ws_bytes(p);
 }
+
+size_t jattn_bwd_workspace_bytes_min(const jattn_plan *p) { return p == nullptr ? 0 : bwd_ws_min(p); }
 
 void jattn_plan_destroy(jattn_plan *p) {
     if (p == nullptr) return;
@@ -741,9 +777,12 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
     if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
         !aligned16(dk) || !aligned16(dv) || !aligned16(bias) || !aligned16(lse))
         return JATTN_ERR_ALIGNMENT;
-    const size_t need = jattn_bwd_workspace_bytes(p);
+    const size_t need = bwd_ws_min(p);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return JATTN_ERR_WORKSPACE;
-    if (need > 0 && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
+    if ((need > 0 || workspace != nullptr) && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
+    // dS chunks when the workspace holds them (and the plan allows them)
+    const size_t ds_need = ds_ws_bytes(p);
+    const bool use_ds = ds_need > 0 && rope == nullptr && workspace != nullptr && workspace_bytes >= need + ds_need;
     DeviceGuard guard(p->device);
     if (!guard.ok) return note_error("jattn_bwd: cudaSetDevice failed");
     (void)cudaGetLastError();  // report only errors of this call
@@ -772,8 +811,9 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
         kk = ks;
         vv = vs;
     }
-    float *dq_rows = nullptr;  // broadcast Q: per-sequence float32 dQ rows, at the workspace's end
+    float *dq_rows = nullptr;  // broadcast Q: per-sequence float32 dQ rows, after Delta and the staging
     if (p->mode.broadcast_q) dq_rows = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + need - bcast_ws_bytes(p));
+    void *ds = use_ds ? static_cast<void *>(static_cast<uint8_t *>(workspace) + need) : nullptr;
     BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -802,18 +842,46 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
         if (e != JATTN_OK) return e;
     }
     const bool act = p->mode.act != JATTN_SOFTMAX;
+    if (dbias != nullptr) {  // the pass that sums dS adds every pair's into it
+        jattn_status e = cuda_status(
+            cudaMemsetAsync(dbias, 0, static_cast<size_t>(p->H) * p->mode.bias_buckets * sizeof(float), st),
+            "jattn_bwd: dbias zero fill");
+        if (e != JATTN_OK) return e;
+    }
+    if (use_ds) {
+        // pass 1: dK, dV over key-major tiles, writing every block's dS chunk
+        if (!make_tmap(&tm.q, qq, q_rows(p), p->H, p->Dp, 64) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 64) ||
+            !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 128) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 128))
+            return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
+        a.g = make_geom(p, JATTN_TILES_KV);
+        a.g.bias = bias;
+        a.g.ds = ds;
+        {
+            jattn_status e = cuda_status(log.done(launch_bwd_dkdv(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_KV), st)),
+                                         "jattn_bwd: dK/dV kernel launch");
+            if (e != JATTN_OK) return e;
+        }
+        // pass 2: dQ = scale dS K over query-major tiles (K in 128-row tiles, as above)
+        a.g = make_geom(p, JATTN_TILES_Q);
+        a.g.bias = bias;
+        a.g.ds = ds;
+        {
+            jattn_status e = cuda_status(log.done(launch_bwd_dq_gemm(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
+                                         "jattn_bwd: dQ product launch");
+            if (e != JATTN_OK) return e;
+        }
+        if (dq_rows != nullptr)  // the shared queries' gradient: the sum over the sequences
+            return cuda_status(
+                log.done(launch_bcast_reduce(dq_rows, p->B, p->bcast_n, static_cast<int64_t>(p->H) * p->D, dq, st)),
+                "jattn_bwd: dQ reduction launch");
+        return JATTN_OK;
+    }
     // pass 1: dQ over query-major tiles (128 query rows, keys in blocks of 64)
     if (!make_tmap(&tm.q, qq, q_rows(p), p->H, p->Dp, 128) || !make_tmap(&tm.dout, dd, p->Tq, p->H, p->Dp, 128) ||
         !make_tmap(&tm.k, kk, p->Tk, p->H, p->Dp, 64) || !make_tmap(&tm.v, vv, p->Tk, p->H, p->Dp, 64))
         return note_error("jattn_bwd: cuTensorMapEncodeTiled failed");
     a.g = make_geom(p, JATTN_TILES_Q);
     a.g.bias = bias;
-    if (dbias != nullptr) {  // the dQ pass adds every pair's dS into it
-        jattn_status e = cuda_status(
-            cudaMemsetAsync(dbias, 0, static_cast<size_t>(p->H) * p->mode.bias_buckets * sizeof(float), st),
-            "jattn_bwd: dbias zero fill");
-        if (e != JATTN_OK) return e;
-    }
     {
         jattn_status e = cuda_status(log.done(launch_bwd_dq(p->Dp, act, tm, a, n_ctas(p, JATTN_TILES_Q), st)),
                                      "jattn_bwd: dQ kernel launch");

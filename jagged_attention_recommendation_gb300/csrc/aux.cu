@@ -116,17 +116,33 @@ cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, 
     return cudaGetLastError();
 }
 
-// Broadcast Q: dq[i, c] = sum over b of ws[b * n + i, c], b in order (fp32
-// sums, one thread per element, so the result is reproducible bit for bit),
-// stored as bf16.  ws: [B * n, HD] float32; dq: [n, HD] bf16.
-__global__ void bcast_reduce_kernel(const float *__restrict__ ws, int B, int n, int64_t HD,
-                                    __nv_bfloat16 *__restrict__ dq) {
+// Broadcast Q: dq[i, c] = sum over b of ws[b * n + i, c] (fp32), stored as
+// bf16.  ws: [B * n, HD] float32; dq: [n, HD] bf16.  A block takes 32
+// consecutive elements; its warp g sums the sequences b = g, g + 8, g + 16, ...
+// in order (lane = element, so every load of a warp is one 128-byte row piece),
+// and the eight partial sums are added in the order g = 0..7.  The order is
+// fixed, so the result is reproducible bit for bit.
+constexpr int kReduceGroups = 8;
+
+__global__ void __launch_bounds__(32 * kReduceGroups)
+    bcast_reduce_kernel(const float *__restrict__ ws, int B, int n, int64_t HD, __nv_bfloat16 *__restrict__ dq) {
+    __shared__ float part[kReduceGroups][32];
     const int64_t total = static_cast<int64_t>(n) * HD;
-    for (int64_t e = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; e < total;
-         e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int lane = threadIdx.x & 31, grp = threadIdx.x >> 5;
+    for (int64_t e0 = static_cast<int64_t>(blockIdx.x) * 32; e0 < total; e0 += static_cast<int64_t>(gridDim.x) * 32) {
+        const int64_t e = e0 + lane;
         float acc = 0.0f;
-        for (int b = 0; b < B; ++b) acc += ws[static_cast<int64_t>(b) * total + e];
-        dq[e] = __float2bfloat16_rn(acc);
+        if (e < total)
+            for (int b = grp; b < B; b += kReduceGroups) acc += ws[static_cast<int64_t>(b) * total + e];
+        part[grp][lane] = acc;
+        __syncthreads();
+        if (grp == 0 && e < total) {
+            float s_ = part[0][lane];
+#pragma unroll
+            for (int k = 1; k < kReduceGroups; ++k) s_ += part[k][lane];
+            dq[e] = __float2bfloat16_rn(s_);
+        }
+        __syncthreads();
     }
 }
 
@@ -135,9 +151,9 @@ cudaError_t launch_bcast_reduce(const float *ws, int B, int n, int64_t HD, void 
     if (total <= 0 || B <= 0) return cudaSuccess;
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int64_t want = (total + 255) / 256;
+    const int64_t want = (total + 31) / 32;
     const int blocks = static_cast<int>(std::min<int64_t>(want, static_cast<int64_t>(sms) * 8));
-    bcast_reduce_kernel<<<blocks, 256, 0, stream>>>(ws, B, n, HD, static_cast<__nv_bfloat16 *>(dq));
+    bcast_reduce_kernel<<<blocks, 32 * kReduceGroups, 0, stream>>>(ws, B, n, HD, static_cast<__nv_bfloat16 *>(dq));
     return cudaGetLastError();
 }
 

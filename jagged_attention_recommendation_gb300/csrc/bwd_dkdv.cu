@@ -13,6 +13,7 @@ namespace {
 // ============================================================================
 // pass 2: dK, dV
 // ============================================================================
+
 template <int D, bool ACT, int BIAS>
 struct DkvCfg {
     static constexpr int BKV = 128, BQ = 64;
@@ -27,16 +28,18 @@ struct DkvCfg {
     static constexpr uint32_t OFF_Q = 2 * KV_BYTES;  // [NSQ][Q | dO]
     static constexpr uint32_t OFF_LD = OFF_Q + NSQ * 2 * Q_BYTES;  // [NSQ][-lse log2 e | -Delta][64] floats
     static constexpr uint32_t OFF_BAR = OFF_LD + NSQ * 2 * BQ * 4;
-    // kv_full, kv_empty, qs_full[NSQ], qs_empty[NSQ], st_full[2], p_full[2], acc_full, acc_empty,
-    // acc_done[2], drain[2]
-    static constexpr int NBAR = 2 + 2 * NSQ + 4 + 2 + 2 + 2;
+    // kv_full, kv_empty, qs_full[NSQ], qs_empty[NSQ], st_full[2], p_full[2], acc_full, dv_empty,
+    // acc_done[2], drain[2], dk_empty
+    static constexpr int NBAR = 2 + 2 * NSQ + 4 + 2 + 2 + 2 + 1;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
     // per output warp: 32 rows x 64 bf16 staging for row-contiguous stores
     static constexpr int STG_W = 64;
     static constexpr uint32_t OFF_STG = (OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0) + 127) & ~127u;
-    static constexpr uint32_t SMEM = OFF_STG + 4 * 32 * STG_W * 2;
+    // the CTA's share of the bias-table gradient [H, nb] (dS chunk mode with a bias)
+    static constexpr uint32_t OFF_DT = OFF_STG + 4 * 32 * STG_W * 2;
+    static constexpr uint32_t SMEM = OFF_DT + (BIAS != kBiasNone ? kMaxBiasFloats * 4 : 0);
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     // group g: S^T at 128 g (P^T over it), dP^T at 128 g + 64 (dS^T over it); dV, dK
@@ -46,13 +49,33 @@ struct DkvCfg {
     static_assert(OFF_Q % 1024 == 0 && Q_BYTES % 1024 == 0, "operand alignment");
     static_assert(OFF_STG % 16 == 0, "16-byte shared-memory vectors");
     static_assert(COL_DK + D <= TMEM_COLS, "TMEM budget");
+    // registers per thread after the split (launch: 512 threads x 128).  The
+    // reflected-bias compute path needs 176; the others fit in 160, which
+    // leaves the output group enough to read 64 accumulator columns per TMEM
+    // round trip instead of 32.
+    static constexpr uint32_t REG_CTRL = 56;
+    static constexpr uint32_t REG_COMPUTE = BIAS == kBiasExt ? 176 : 160;
+    static constexpr uint32_t REG_OUT = (128 * 512 - REG_CTRL * 128 - REG_COMPUTE * 256) / 128;
+    static constexpr int DRAIN_COLS = REG_OUT >= 136 ? 64 : 32;
+    static_assert(REG_CTRL * 128 + REG_COMPUTE * 256 + REG_OUT * 128 <= 128 * 512, "register split");
+    static_assert(REG_OUT % 8 == 0, "setmaxnreg granularity");
 };
 
-template <int D, bool ACT, int BIAS, bool WIN>
+// WIN: sliding window on.  DS: every block's dS (bf16; activation mode: the
+// bf16 hi and lo parts) also goes to the workspace, one 16 KB chunk per
+// (key tile, 64-query block): rows are the tile's 128 keys, each row the
+// block's 64 queries, 16-byte pieces XOR-swizzled by row (the 128-byte swizzle
+// of an MMA operand tile, so that a plain bulk copy into shared memory gives
+// the dQ product's A operand); rows past the tile's keys are zero.  DT (with
+// DS): this pass also sums the bias-table gradient.  All three are compile
+// time switches, so kernels without them carry none of their work.
+template <int D, bool ACT, int BIAS, bool WIN, bool DS, bool DT>
 __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
     using C = DkvCfg<D, ACT, BIAS>;
+    static_assert(!(DS && WIN), "dS chunks are written for full attention only");
+    static_assert(DS || !DT, "the bias gradient is summed here only with dS chunks");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -67,14 +90,16 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *st_full = qs_empty + C::NSQ;  // [2] per TMEM buffer (blocks alternate)
     uint64_t *p_full = st_full + 2;         // [2] per TMEM buffer, both compute groups arrive
     uint64_t *acc_full = p_full + 2;
-    uint64_t *acc_empty = acc_full + 1;
-    uint64_t *acc_done = acc_empty + 1;  // [2] per TMEM buffer: its block's dV / dK products finished
+    uint64_t *dv_empty = acc_full + 1;   // the output group has read dV (its columns are free)
+    uint64_t *acc_done = dv_empty + 1;   // [2] per TMEM buffer: its block's dV / dK products finished
     uint64_t *drain = acc_done + 2;      // [2] per MMA-issuing thread
+    uint64_t *dk_empty = drain + 2;      // the output group has read dK
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
     float *sext = reinterpret_cast<float *>(smem + C::OFF_BEXT);
     float *sLD = reinterpret_cast<float *>(smem + C::OFF_LD);
+    float *sdt = reinterpret_cast<float *>(smem + C::OFF_DT);
     const uint32_t sK = smem_u32(smem + C::OFF_K);
     const uint32_t sV = smem_u32(smem + C::OFF_V);
     const uint32_t sQ = smem_u32(smem + C::OFF_Q);
@@ -91,7 +116,8 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&p_full[b], 8);  // both compute groups' warps
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 4);
+        mbar_init(dv_empty, 4);
+        mbar_init(dk_empty, 4);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&acc_done[b], 1);
             mbar_init(&drain[b], 1);
@@ -105,6 +131,9 @@ __global__ void __launch_bounds__(512, 1)
     }
     if (BIAS == kBiasTable) stage_bias(g, sbias, ACT ? 1.0f : kLog2e);
     if (BIAS == kBiasExt) stage_bias_ext(g, sext, ACT ? 1.0f : kLog2e);
+    constexpr bool want_dt = DT && BIAS != kBiasNone;
+    if constexpr (want_dt)
+        for (int i = threadIdx.x; i < g.H * g.nb; i += blockDim.x) sdt[i] = 0.0f;
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
@@ -121,7 +150,7 @@ __global__ void __launch_bounds__(512, 1)
 
     const int wgi = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) >> 7, 0);
     if (wgi == 0) {
-        regs_release<kRegCtrl>();
+        regs_to<C::REG_CTRL, 128>();
         if (warp == 0) {
             // -------------------------------------------------------- Q / dO producer
             // lane 0 issues the copies; all lanes first write lse / Delta of the
@@ -237,6 +266,9 @@ __global__ void __launch_bounds__(512, 1)
             // -------------------------------------------------------- dV / dK issuer
             // dV += P^T dO and dK += dS^T Q, P^T and dS^T (bf16; activation: hi and
             // lo parts) read from TMEM; one thread, so the accumulation order is fixed.
+            // A block's dV products go first: the output group hands the dV columns
+            // back before the dK columns, so a tile's first dV products may start
+            // while the previous tile's dK is still being read.
             const uint32_t idesc_acc = idesc_bf16(128, D, false, true);
             bool ok = true;
             TileStream tsb(g, tbeg, tend);
@@ -245,8 +277,8 @@ __global__ void __launch_bounds__(512, 1)
             while (ok && tsb.next(tb)) {
                 if (!check_tile(g, tb, err, false)) continue;
                 const int nbq = cdiv(tb.q_len, C::BQ);
-                // the output group must have read dV / dK of the previous tile
-                if (!(ok = mbar_wait(acc_empty, (tb_n & 1) ^ 1, err))) break;
+                // the output group must have read dV of the previous tile
+                if (!(ok = mbar_wait(dv_empty, (tb_n & 1) ^ 1, err))) break;
                 for (int ib = 0; ib < nbq; ++ib, ++np) {
                     const uint32_t buf = np & 1;
                     if (!(ok = mbar_wait(&p_full[buf], (np >> 1) & 1, err))) break;
@@ -260,17 +292,24 @@ __global__ void __launch_bounds__(512, 1)
                     for (int k = 0; k < ksteps; ++k) {
                         const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
                         const uint64_t bdo = sdesc_add(bdo0, k * 2048);
-                        const uint64_t bq = sdesc_add(bq0, k * 2048);
                         if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
                             mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
                             mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
+                        } else {
+                            // 32-query chunk k / 2 keeps its bf16 pairs in its own first 16 columns
+                            mma_bf16_ts(tmem + C::COL_DV, aP + (k >> 1) * 32 + (k & 1) * 8, bdo, idesc_acc, acc);
+                        }
+                    }
+                    // ... and dK of the previous tile before the tile's first dK product
+                    if (ib == 0 && !(ok = mbar_wait(dk_empty, (tb_n & 1) ^ 1, err))) break;
+                    for (int k = 0; k < ksteps; ++k) {
+                        const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
+                        const uint64_t bq = sdesc_add(bq0, k * 2048);
+                        if (ACT) {
                             mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
                             mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
                         } else {
-                            // 32-query chunk k / 2 keeps its bf16 pairs in its own first 16 columns
-                            const uint32_t o = (k >> 1) * 32 + (k & 1) * 8;
-                            mma_bf16_ts(tmem + C::COL_DV, aP + o, bdo, idesc_acc, acc);
-                            mma_bf16_ts(tmem + C::COL_DK, aDS + o, bq, idesc_acc, acc);
+                            mma_bf16_ts(tmem + C::COL_DK, aDS + (k >> 1) * 32 + (k & 1) * 8, bq, idesc_acc, acc);
                         }
                     }
                     mma_commit(&qs_empty[slot]);  // last reads of the Q / dO slot
@@ -284,7 +323,7 @@ __global__ void __launch_bounds__(512, 1)
             mbar_drain(&drain[1], 0);
         }
     } else if (wgi < 3) {
-        regs_claim<kRegCompute>();
+        regs_to<C::REG_COMPUTE, 128>();
         // ------------------------------------------------------------ compute groups
         // One thread per key row (TMEM lane): P^T and dS^T of the group's query
         // blocks, 32 queries at a time, written as bf16 over the block's S^T and
@@ -306,6 +345,15 @@ __global__ void __launch_bounds__(512, 1)
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int kv_loc = t.kv_loc0 + row;
             const bool warp_live = quad * 32 < t.kv_len;
+            // dS chunks: the tile's first chunk; block i of the tile is chunk ds0 + i
+            int64_t ds0 = 0;
+            if constexpr (DS) {
+                const int lq = g.q_off[t.b + 1] - g.q_off[t.b], lk = g.kv_off[t.b + 1] - g.kv_off[t.b];
+                const int nqb = cdiv(lq, C::BQ);
+                ds0 = g.ds_base[t.b] + (static_cast<int64_t>(t.h) * cdiv(lk, C::BKV) + t.kv_loc0 / C::BKV) * nqb +
+                      t.q_loc0 / C::BQ;
+            }
+            float dt_far = 0.0f;  // this row's dS in the last bias bucket, per tile
             auto blocks = [&](auto af) {
                 constexpr int AF = decltype(af)::value;
                 // every block of the tile; this group takes its 32-query chunk c = grp
@@ -360,18 +408,71 @@ __global__ void __launch_bounds__(512, 1)
                                 window_fill32(x, wb, 0.0f);
                                 window_fill32(dp, wb, 0.0f);
                             }
+                            if constexpr (DS) {
+                                // a row past the tile's keys adds nothing to dQ (its dK row is
+                                // not stored, so zeroing it here changes no stored result)
+                                if (row >= t.kv_len) {
+#pragma unroll
+                                    for (int k = 0; k < 32; ++k) dp[k] = 0.0f;
+                                }
+                            }
+                            // bias-table gradient: dT[h, min(|i - j|, nb - 1)] += dS_ij; the far
+                            // bucket in a register, the few near ones in shared memory
+                            if constexpr (want_dt) {
+                                if (row < t.kv_len) {
+                                    const int i0 = qb + c * 32, nbm = g.nb - 1;
+                                    const int dmin = kv_loc < i0 ? i0 - kv_loc : (kv_loc > i0 + 31 ? kv_loc - i0 - 31 : 0);
+                                    if (dmin >= nbm) {
+                                        dt_far += sum32(dp);
+                                    } else {
+#pragma unroll
+                                        for (int k = 0; k < 32; ++k) {
+                                            const int d = abs(kv_loc - (i0 + k));
+                                            if (d >= nbm)
+                                                dt_far += dp[k];
+                                            else
+                                                atomicAdd(&sdt[t.h * g.nb + d], dp[k]);
+                                        }
+                                    }
+                                }
+                            }
+                            // this row's 64-byte piece of the block's dS chunk (plane p at
+                            // 16 KB p): 16-byte pieces 4 c .. 4 c + 3 of the 128-byte row,
+                            // XOR-swizzled by row
+                            auto ds_store = [&](const uint32_t *wp, int plane) {
+                                uint8_t *rowp = static_cast<uint8_t *>(g.ds) +
+                                                ((ds0 + i) * (ACT ? 2 : 1) + plane) * static_cast<int64_t>(kDsChunkBytes) +
+                                                row * 128;
+#pragma unroll
+                                for (int k = 0; k < 4; ++k)
+                                    *reinterpret_cast<uint4 *>(rowp + (((4 * c + k) ^ (row & 7)) << 4)) =
+                                        make_uint4(wp[4 * k], wp[4 * k + 1], wp[4 * k + 2], wp[4 * k + 3]);
+                            };
                             if constexpr (ACT) {
                                 uint32_t w[32];
                                 pack_hilo32(x, w);
                                 tmem_st32_u32(tS + 32 * c, w);
                                 pack_hilo32(dp, w);
                                 tmem_st32_u32(tDP + 32 * c, w);
+                                if constexpr (DS) {  // hi words: 0..7, 16..23; lo words: 8..15, 24..31
+                                    uint32_t hw[16], lw[16];
+#pragma unroll
+                                    for (int k = 0; k < 8; ++k) {
+                                        hw[k] = w[k];
+                                        hw[8 + k] = w[16 + k];
+                                        lw[k] = w[8 + k];
+                                        lw[8 + k] = w[24 + k];
+                                    }
+                                    ds_store(hw, 0);
+                                    ds_store(lw, 1);
+                                }
                             } else {
                                 uint32_t w[16];
                                 pack16(x, w);  // over the chunk's own first 16 columns
                                 tmem_st16_u32(tS + 32 * c, w);
                                 pack16(dp, w);
                                 tmem_st16_u32(tDP + 32 * c, w);
+                                if constexpr (DS) ds_store(w, 0);
                             }
                         }
                         tmem_wait_st();
@@ -386,17 +487,26 @@ __global__ void __launch_bounds__(512, 1)
             } else {
                 blocks(std::integral_constant<int, kGeluTanh>{});
             }
+            if constexpr (want_dt) {
+                {  // the tile's far-bucket sums: one shared-memory add per warp
+                    float f = dt_far;
+#pragma unroll
+                    for (int k = 16; k > 0; k >>= 1) f += __shfl_xor_sync(0xffffffffu, f, k);
+                    if (lane == 0 && f != 0.0f) atomicAdd(&sdt[t.h * g.nb + g.nb - 1], f);
+                    dt_far = 0.0f;
+                }
+            }
             if (!ok) break;
             n0 += nq;
         }
     } else {
-        regs_release<kRegOut>();
+        regs_to<C::REG_OUT, 128>();
         // ------------------------------------------------------------ output
         // One thread per key row reads dV and dK (times the score scale) from
-        // TMEM.  bf16 outputs go out row-contiguous through the warp's staging
-        // buffer: dV is staged and dK packed into registers before the
-        // accumulators are handed back, so the next tile's products wait only
-        // for the TMEM reads, not for the stores.
+        // TMEM, 64 columns per round trip.  bf16 outputs go out row-contiguous
+        // through the warp's staging buffer.  dV's columns are handed back as
+        // soon as they have been read (the next tile's dV products may start),
+        // then dK's.
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
@@ -408,6 +518,49 @@ __global__ void __launch_bounds__(512, 1)
         bool ok = true;
         TileStream ts(g, tbeg, tend);
         Tile t;
+        // one accumulator (dV or dK, times mul) W = 64 columns at a time: read
+        // (C::DRAIN_COLS per TMEM round trip), hand the columns back after the
+        // last read, stage, store
+        auto drain_acc = [&](uint32_t tacc, uint64_t *empty_bar, const OutDesc &o, float mul, bool has, int nrows,
+                             int64_t r0, int h) {
+            __nv_bfloat16 *dst0 = static_cast<__nv_bfloat16 *>(o.ptr) + r0 * o.ld + h * D;
+            constexpr int RC = C::DRAIN_COLS;
+#pragma unroll
+            for (int h0 = 0; h0 < D; h0 += W) {
+#pragma unroll
+                for (int c0 = 0; c0 < W; c0 += RC) {
+                    float v[RC];
+                    if (has) {
+                        if constexpr (RC == 64) {
+                            tmem_ld32x2(tacc + h0 + c0, tacc + h0 + c0 + 32, sub32(v, 0), sub32(v, 1));
+                        } else {
+                            tmem_ld32(tacc + h0 + c0, v);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < RC; ++i) v[i] = 0.0f;
+                    }
+                    if (h0 + c0 + RC >= D) {  // every TMEM read of this accumulator is done
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(empty_bar);
+                    }
+                    if (mul != 1.0f) {
+#pragma unroll
+                        for (int i = 0; i < RC; i += 2) mul2(v[i], v[i + 1], mul, mul);
+                    }
+#pragma unroll
+                    for (int c = 0; c < RC / 32; ++c) {
+                        uint32_t w[16];
+                        pack16(sub32(v, c), w);
+                        stage_row32_bf16<W>(stg, lane, c0 + 32 * c, w);
+                    }
+                }
+                __syncwarp();
+                store_rows_bf16<W>(stg, lane, dst0 + h0, o.ld, nrows);
+                __syncwarp();
+            }
+        };
         while (ok && ts.next(t)) {
             if (!check_tile(g, t, err, false)) continue;
             const int nq = cdiv(t.q_len, C::BQ);
@@ -415,62 +568,18 @@ __global__ void __launch_bounds__(512, 1)
             ++t_local;
             if (quad * 32 >= t.kv_len) {  // no row of this warp is stored
                 __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
+                if (lane == 0) {
+                    mbar_arrive(dv_empty);
+                    mbar_arrive(dk_empty);
+                }
                 continue;
             }
             tc_fence_after();
             if (staged) {
                 const int nrows = min(32, t.kv_len - quad * 32);
                 const int64_t r0 = static_cast<int64_t>(t.kv_start) + quad * 32;
-                __nv_bfloat16 *dv0 = static_cast<__nv_bfloat16 *>(a.dv.ptr) + r0 * a.dv.ld + t.h * D;
-                __nv_bfloat16 *dk0 = static_cast<__nv_bfloat16 *>(a.dk.ptr) + r0 * a.dk.ld + t.h * D;
-                // dV: W columns at a time through the staging buffer
-#pragma unroll
-                for (int h0 = 0; h0 < D; h0 += W) {
-#pragma unroll
-                    for (int c = 0; c < W / 32; ++c) {
-                        float v[32];
-                        uint32_t w[16];
-                        if (nq > 0) {
-                            tmem_ld32(tDV + h0 + 32 * c, v);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                        }
-                        pack16(v, w);
-                        stage_row32_bf16<W>(stg, lane, 32 * c, w);
-                    }
-                    __syncwarp();
-                    store_rows_bf16<W>(stg, lane, dv0 + h0, a.dv.ld, nrows);
-                    __syncwarp();
-                }
-                // dK (times the score scale) packed into registers
-                uint32_t kw[D / 32][16];
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    float v[32];
-                    if (nq > 0) {
-                        tmem_ld32(tDK + 32 * c, v);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; i += 2) mul2(v[i], v[i + 1], g.scale, g.scale);
-                    pack16(v, kw[c]);
-                }
-                // every TMEM read of this tile is done
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
-#pragma unroll
-                for (int h0 = 0; h0 < D; h0 += W) {
-#pragma unroll
-                    for (int c = 0; c < W / 32; ++c) stage_row32_bf16<W>(stg, lane, 32 * c, kw[h0 / 32 + c]);
-                    __syncwarp();
-                    store_rows_bf16<W>(stg, lane, dk0 + h0, a.dk.ld, nrows);
-                    __syncwarp();
-                }
+                drain_acc(tDV, dv_empty, a.dv, 1.0f, nq > 0, nrows, r0, t.h);
+                drain_acc(tDK, dk_empty, a.dk, g.scale, nq > 0, nrows, r0, t.h);
                 continue;
             }
             const bool row_ok = row < t.kv_len;
@@ -487,7 +596,10 @@ __global__ void __launch_bounds__(512, 1)
                 if (col + 32 >= D) {  // every TMEM read of this tile is done
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_empty);
+                    if (lane == 0) {
+                        mbar_arrive(dv_empty);
+                        mbar_arrive(dk_empty);
+                    }
                 }
                 if (row_ok) {
                     store_out32(a.dv, krow, t.h, col, ov, 1.0f);
@@ -499,6 +611,10 @@ __global__ void __launch_bounds__(512, 1)
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (want_dt) {  // the CTA's share of the bias-table gradient
+        for (int i = threadIdx.x; i < g.H * g.nb; i += blockDim.x)
+            if (sdt[i] != 0.0f) atomicAdd(&a.dbias[i], sdt[i]);
+    }
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, C::TMEM_COLS);
@@ -510,20 +626,28 @@ __global__ void __launch_bounds__(512, 1)
 // ============================================================================
 // launcher
 // ============================================================================
-template <int D, bool ACT, int BIAS, bool WIN>
+template <int D, bool ACT, int BIAS, bool WIN, bool DS, bool DT>
 static cudaError_t launch_dkdv_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = DkvCfg<D, ACT, BIAS>;
     static SmemOnce done;
-    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN, DS, DT>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    dkdv_kernel<D, ACT, BIAS, WIN><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    dkdv_kernel<D, ACT, BIAS, WIN, DS, DT><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 
+// the variant a launch takes: window, dS chunks (a.g.ds set), bias gradient with them
 template <int D, bool ACT, int BIAS>
 static cudaError_t launch_dkdv_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
-    return a.g.window > 0 ? launch_dkdv_w<D, ACT, BIAS, true>(tm, a, n_ctas, st)
-                          : launch_dkdv_w<D, ACT, BIAS, false>(tm, a, n_ctas, st);
+    if (a.g.ds != nullptr) {
+        if (a.g.window > 0) return cudaErrorInvalidValue;
+        if constexpr (BIAS != kBiasNone) {
+            if (a.dbias != nullptr) return launch_dkdv_w<D, ACT, BIAS, false, true, true>(tm, a, n_ctas, st);
+        }
+        return launch_dkdv_w<D, ACT, BIAS, false, true, false>(tm, a, n_ctas, st);
+    }
+    return a.g.window > 0 ? launch_dkdv_w<D, ACT, BIAS, true, false, false>(tm, a, n_ctas, st)
+                          : launch_dkdv_w<D, ACT, BIAS, false, false, false>(tm, a, n_ctas, st);
 }
 
 template <int D, bool ACT>

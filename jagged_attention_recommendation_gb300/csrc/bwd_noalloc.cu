@@ -58,10 +58,13 @@ extern "C" jattn_status jattn_bwd_noalloc(const jattn_plan *plan, const void *do
     const int dev = jattn::plan_device(plan);
     if (dev < 0) return JATTN_ERR_NO_DEVICE;
     if (dev >= kMaxDevices) return JATTN_ERR_UNSUPPORTED;
-    const size_t need = jattn_bwd_workspace_bytes(plan);
+    const size_t need = jattn_bwd_workspace_bytes_min(plan);
     if (need > kNoAllocScratchBytes) return JATTN_ERR_WORKSPACE;  // batch too large for the fixed array
+    // the array goes to jattn_bwd whenever any path could use scratch; jattn_bwd
+    // takes its dS-chunk path when the whole size fits, else the recomputing one
+    const bool give = jattn_bwd_workspace_bytes(plan) > 0;
     void *scratch = nullptr;
-    if (need > 0 && scratch_address(dev, &scratch) != cudaSuccess) return JATTN_ERR_CUDA;
-    return jattn_bwd(plan, dout, q, k, v, bias, out, lse, dq, dk, dv, dbias, need > 0 ? scratch : nullptr,
-                     need > 0 ? kNoAllocScratchBytes : 0, stream);
+    if (give && scratch_address(dev, &scratch) != cudaSuccess) return JATTN_ERR_CUDA;
+    return jattn_bwd(plan, dout, q, k, v, bias, out, lse, dq, dk, dv, dbias, give ? scratch : nullptr,
+                     give ? kNoAllocScratchBytes : 0, stream);
 }

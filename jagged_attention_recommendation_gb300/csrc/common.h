@@ -61,7 +61,15 @@ struct Geom {
     int32_t q_bcast;          // 1: every sequence's queries are the rows 0 .. Lq-1 of one shared Q
                               // (Q is read at the local row, O / dO / lse at the sequence's rows)
     unsigned long long wait_ns;  // limit of every bounded wait (kWaitTimeoutNs)
+    // backward with dS chunks (full attention): the dK/dV pass writes every block's
+    // dS to `ds` and the dQ product reads it back; chunk index of (sequence b,
+    // head h, key tile t, 64-query block i) = ds_base[b] + (h * nkt_b + t) * nqb_b + i
+    void *ds;                 // chunk workspace (16-byte aligned), or nullptr (off)
+    const long long *ds_base; // [B + 1] first chunk of every sequence (device)
 };
+
+// one dS chunk: 128 keys x 64 queries of bf16 (activation mode: two of them, hi and lo)
+constexpr int kDsChunkBytes = 128 * 64 * 2;
 
 // Where a [T, H, D] result goes: element (t, h, c) at ptr[t*ld + h*cols + c] for c < cols.
 struct OutDesc {

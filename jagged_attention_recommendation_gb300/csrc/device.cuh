@@ -184,6 +184,17 @@ __device__ __forceinline__ void regs_claim() {
     static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg range");
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
+// Set this warpgroup's budget to N from the LAUNCH registers per thread the
+// block started with: an increase above it, a decrease below it (a .dec to a
+// larger count, or an .inc to a smaller one, is not a valid instruction).
+template <uint32_t N, uint32_t LAUNCH>
+__device__ __forceinline__ void regs_to() {
+    if constexpr (N > LAUNCH) {
+        regs_claim<N>();
+    } else if constexpr (N < LAUNCH) {
+        regs_release<N>();
+    }
+}
 
 // D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulator (kind::f16).
 __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,

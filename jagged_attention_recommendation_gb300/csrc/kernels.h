@@ -52,6 +52,10 @@ cudaError_t launch_fwd_rope(int D, bool act, const TmapSet &tm, const FwdArgs &a
 cudaError_t launch_bwd_dq(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
 cudaError_t launch_bwd_dkdv(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
 
+// backward with dS chunks: dQ = scale * dS K over query-major tiles, from the
+// chunks the dK/dV pass wrote (a.g.ds, a.g.ds_base); tm.k in 128-row boxes
+cudaError_t launch_bwd_dq_gemm(int D, bool act, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
+
 // backward, BlockAttention: one fused pass over query-major tiles (with
 // rotary position embedding when a.g.rope_cos is set)
 cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t stream);
@@ -63,7 +67,7 @@ cudaError_t launch_delta(const void *out, const void *dout, int f32, int64_t Tq,
 // src [rows, D] (bf16 or fp32) -> dst [rows, Dp] bf16, zero-padded columns D..Dp-1
 cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, void *dst, cudaStream_t stream);
 
-// broadcast Q: dq [n, HD] bf16 = sum over the B samples of ws [B * n, HD] float32, in order
+// broadcast Q: dq [n, HD] bf16 = sum over the B samples of ws [B * n, HD] float32, in a fixed order
 cudaError_t launch_bcast_reduce(const float *ws, int B, int n, int64_t HD, void *dq, cudaStream_t stream);
 
 // device-side planner: tile lists and zigzag schedule from device offsets

@@ -19,9 +19,12 @@ def to_dev(t):
     return None if t is None else t.to("cuda:0").contiguous()
 
 
-def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, window=0, rope=None):
+def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, window=0, rope=None,
+                min_workspace=False):
     """Forward (+ backward) of batch dict ``bt`` on cuda:0; returns float64 numpy arrays.
-    rope = (cos, sin) host float32 tables: rotary embedding of Q and K."""
+    rope = (cos, sin) host float32 tables: rotary embedding of Q and K.
+    min_workspace: the backward gets only jattn_bwd_workspace_bytes_min (the path
+    whose dQ pass recomputes the scores) instead of the full workspace."""
     q, k, v, dout = (to_dev(bt[n]) for n in ("q", "k", "v", "dout"))
     bias = to_dev(bt["bias"].float()) if bt.get("bias") is not None else None
     rp = None if rope is None else tuple(to_dev(t.float().contiguous()) for t in rope)
@@ -33,7 +36,10 @@ def run_library(bt, act=0, block=0, dtype="bf16", backward=True, plan=None, wind
     out, lse = plan.fwd(q, k, v, bias=bias, rope=rp)
     res = {"out": out, "lse": lse}
     if backward:
-        dq, dk, dv = plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, rope=rp)
+        ws = None
+        if min_workspace:
+            ws = torch.empty(max(plan.bwd_workspace_bytes_min, 16), dtype=torch.uint8, device="cuda:0")
+        dq, dk, dv = plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, rope=rp, workspace=ws)
         res.update(dq=dq, dk=dk, dv=dv)
     torch.cuda.synchronize()
     status = plan.check_status()

@@ -152,11 +152,20 @@ def test_host_only_plan_refuses_compute(lib):
 
 def test_workspace_sizes(lib):
     qo = W.offsets(np.array([10, 20]))
+    chunk = 128 * 64 * 2  # one dS chunk: 128 keys x 64 queries of bf16
     p = J.Plan(qo, qo, 2, 128, device=-1)
     assert p.fwd_workspace_bytes == 0
-    assert p.bwd_workspace_bytes == 256  # Delta [H, Tq] fp32 = 240 B, 256-byte aligned
+    assert p.bwd_workspace_bytes_min == 256  # Delta [H, Tq] fp32 = 240 B, 256-byte aligned
+    # plus the dS chunks: 2 sequences x 2 heads x 1 key tile x 1 query block
+    assert p.bwd_workspace_bytes == 256 + 4 * chunk
     p = J.Plan(qo, qo, 2, 128, act=J.SILU, device=-1)
-    assert p.bwd_workspace_bytes == 0
+    assert p.bwd_workspace_bytes_min == 0
+    assert p.bwd_workspace_bytes == 4 * 2 * chunk  # hi and lo chunks
+    p = J.Plan(qo, qo, 2, 128, act=J.SILU, window=8, device=-1)  # no dS chunks with a window
+    assert p.bwd_workspace_bytes == p.bwd_workspace_bytes_min == 0
+    lq = np.array([300, 1, 129])  # key tiles 3, 1, 2; query blocks 5, 1, 3
+    p = J.Plan(W.offsets(lq), W.offsets(lq), 4, 64, device=-1)
+    assert p.bwd_workspace_bytes - p.bwd_workspace_bytes_min == 4 * (3 * 5 + 1 * 1 + 2 * 3) * chunk
     p = J.Plan(qo, qo, 2, 32, dtype="fp32", device=-1)
     # staging of q, k, v to bf16 [T, H, 64]
     assert p.fwd_workspace_bytes == 3 * ((30 * 2 * 64 * 2 + 255) // 256 * 256)

@@ -73,10 +73,13 @@ CASES = [
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_device_plan_results_equal_host_plan(case):
     """Every tile's result is independent of the CTA that runs it, so the device
-    schedule gives the host schedule's outputs bit for bit."""
+    schedule gives the host schedule's outputs bit for bit.  A device plan's
+    backward recomputes the scores for dQ (the host does not know the lengths
+    the dS chunks need), so the host plan runs that same path here (the
+    minimum workspace)."""
     _, lq, lk, H, D, nb, act, block, window = case
     bt = W.random_batch(71, lq, lq if lk is None else lk, H, D, bias_buckets=nb)
-    host = PT.run_library(bt, act=act, block=block, window=window)
+    host = PT.run_library(bt, act=act, block=block, window=window, min_workspace=True)
     plan = J.Plan(bt["q_off"], bt["kv_off"], H, D, act=act, block=block, bias_buckets=nb, window=window, device=0)
     # re-plan the same plan on the device (its host lists are replaced)
     plan.update_device(_dev(bt["q_off"]), _dev(bt["kv_off"]), int(bt["q_off"][-1]), int(bt["kv_off"][-1]))

@@ -141,8 +141,9 @@ DT_CASES = [
 ]
 
 
+@pytest.mark.parametrize("min_ws", [False, True], ids=["full_workspace", "min_workspace"])
 @pytest.mark.parametrize("case", DT_CASES, ids=[c[0] for c in DT_CASES])
-def test_bias_gradient(case):
+def test_bias_gradient(case, min_ws):
     """dT is a sum over up to L^2 pairs whose softmax terms cancel (each row of dS
     sums to zero), so its entries can be far smaller than the terms; the backward
     tolerance is applied per head against the head's largest entry:
@@ -156,7 +157,9 @@ def test_bias_gradient(case):
     plan = J.Plan(bt["q_off"], bt["kv_off"], H, D, act=act, bias_buckets=nb, device=0, window=win)
     out, lse = plan.fwd(q, k, v, bias=bias)
     dbias = torch.full((H, nb), float("nan"), dtype=torch.float32, device=dev)
-    plan.bwd(do, q, k, v, out, lse=lse, bias=bias, dbias=dbias)
+    # full workspace: the dK/dV pass sums dT (with the dS chunks); minimum: the dQ pass does
+    ws = torch.empty(max(plan.bwd_workspace_bytes_min, 16), dtype=torch.uint8, device=dev) if min_ws else None
+    plan.bwd(do, q, k, v, out, lse=lse, bias=bias, dbias=dbias, workspace=ws)
     torch.cuda.synchronize()
     assert plan.check_status() == 0
     _, _, _, ref = oracle.backward(bt["q_off"], bt["kv_off"], bt["q"], bt["k"], bt["v"], bt["dout"],
@@ -178,4 +181,42 @@ def test_bias_gradient_rejected_in_block_mode():
     out, lse = plan.fwd(q, k, v, bias=bias)
     with pytest.raises(J.JattnError):
         plan.bwd(do, q, k, v, out, lse=lse, bias=bias, dbias=torch.zeros(2, 4, device=dev))
+    plan.close()
+
+
+# (name, lq, lk, H, D, bias_buckets, act)
+PATH_CASES = [
+    ("paths_self_bias", [1, 127, 129, 300, 64], None, 2, 128, 16, SOFTMAX),
+    ("paths_cross", [200, 35, 511], [8, 300, 129], 2, 64, 0, SOFTMAX),
+    ("paths_silu", [32, 100, 3], [700, 129, 257], 2, 128, 0, SILU),
+    ("paths_gelu_d64", [150, 3], [90, 400], 2, 64, 8, GELU),
+]
+
+
+@pytest.mark.parametrize("case", PATH_CASES, ids=[c[0] for c in PATH_CASES])
+def test_backward_paths(case):
+    """The backward's two paths: with the full workspace the dK/dV pass writes
+    the dS chunks and dQ is a streaming product of them; with the minimum
+    workspace a dQ pass recomputes the scores.  Both match the oracle; dK and
+    dV are the same kernels' results, bit for bit."""
+    name, lq, lk, H, D, nb, act = case
+    lk = lq if lk is None else lk
+    bt = W.random_batch(zlib.crc32(name.encode()) % 10000, lq, lk, H, D, bias_buckets=nb)
+    dev = torch.device("cuda", 0)
+    q, k, v, do = (bt[n].to(dev) for n in ("q", "k", "v", "dout"))
+    bias = bt["bias"].float().to(dev) if nb else None
+    plan = J.Plan(bt["q_off"], bt["kv_off"], H, D, act=act, bias_buckets=nb, device=0)
+    assert plan.bwd_workspace_bytes > plan.bwd_workspace_bytes_min
+    out, lse = plan.fwd(q, k, v, bias=bias)
+    full = plan.bwd(do, q, k, v, out, lse=lse, bias=bias)
+    ws = torch.empty(max(plan.bwd_workspace_bytes_min, 16), dtype=torch.uint8, device=dev)
+    small = plan.bwd(do, q, k, v, out, lse=lse, bias=bias, workspace=ws)
+    torch.cuda.synchronize()
+    assert plan.check_status() == 0
+    ref = PT.run_oracle(bt, act=act)
+    for res in (full, small):
+        for t, n_, in zip(res, ("dq", "dk", "dv")):
+            PT.assert_close(t.double().cpu().numpy(), ref[n_], PT.BWD_TOL, n_)
+    for i in (1, 2):
+        assert torch.equal(full[i], small[i])
     plan.close()

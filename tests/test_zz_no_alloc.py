@@ -4,8 +4,9 @@ the C ABI against the ordinary jattn_bwd (caller-provided workspace), bit for
 bit (both run the same kernels in the same order, and dQ, dK, dV are bitwise
 reproducible), on two calls in a row, for every layout the scratch can take:
 Delta alone (bf16 softmax), Delta plus staged bf16 copies (float32 data, D = 32),
-the broadcast-Q per-sequence float32 dQ rows, and no scratch at all (an
-activation mode).  Named to run last: a failure here leaves every other test
+the broadcast-Q per-sequence float32 dQ rows, the backward's dS chunks (in all
+of these, since they fit the array), and no scratch at all (an activation mode
+with a sliding window).  Named to run last: a failure here leaves every other test
 run.
 """
 import ctypes
@@ -100,11 +101,23 @@ def test_noalloc_broadcast_q_silu():
 
 
 def test_noalloc_activation_needs_no_scratch():
-    """An activation mode on bf16 data needs no scratch: the call passes no
-    workspace at all."""
+    """An activation mode with a sliding window (no dS chunks) on bf16 data
+    needs no scratch: the call passes no workspace at all."""
     bt = _dev(W.random_batch(35, [150, 3, 64], [90, 400, 64], 2, 64))
-    plan = J.Plan(bt["q_off"], bt["kv_off"], 2, 64, act=GELU, device=0)
+    plan = J.Plan(bt["q_off"], bt["kv_off"], 2, 64, act=GELU, window=100, device=0)
     assert plan.bwd_workspace_bytes == 0
+    _both(plan, bt)
+    _both(plan, bt)
+    plan.close()
+
+
+def test_noalloc_activation_dS_chunks():
+    """An activation mode without a window: no scratch is required, but the dS
+    chunks (hi and lo parts) fit the array, so the call takes the same path as
+    jattn_bwd with the full workspace."""
+    bt = _dev(W.random_batch(36, [150, 3, 64], [90, 400, 64], 2, 64))
+    plan = J.Plan(bt["q_off"], bt["kv_off"], 2, 64, act=GELU, device=0)
+    assert plan.bwd_workspace_bytes_min == 0 and 0 < plan.bwd_workspace_bytes <= (16 << 20)
     _both(plan, bt)
     _both(plan, bt)
     plan.close()
