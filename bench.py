@@ -4,7 +4,11 @@ One step = the whole hot path over one synthetic batch: plan (tile lists +
 schedule, uploaded), forward, backward.  Inputs are resident in HBM when the
 timed region starts; L2 is flushed (a 256 MiB write) between timed steps.  The
 planner's host time is measured per step and reported as planner_host_ms; the
-device-timed step starts after the plan has been queued.
+device-timed step starts after the plan has been queued.  The forward and the
+backward are launched as two CUDA graphs captured once from the library's
+calls (the same kernels and arguments, without host launch work between
+them); the eager form's step time and the per-kernel times (events recorded by
+the library between its kernels) are reported beside it.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ID] [--impl ours|reference]
 
@@ -349,11 +353,41 @@ def run_ours(args, w, batch):
     n_fwd, n_bwd = 1, len(names) - 1
     if f32 or D == 32:
         raise SystemExit("bench: staged (fp32 / D=32) workloads are parity cases, not bench lines")
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
     phys = int(visible[local]) if local < len(visible) and visible[local].strip().isdigit() else local
+
+    # The timed step: forward and backward launched as two CUDA graphs (captured
+    # once; the same kernels and arguments as the eager calls, without the host's
+    # launch work between them), the plan update queued before each step's start
+    # event as in the eager form.  --no-graph times the eager calls instead.
+    use_graph = not args.no_graph
+    if use_graph:
+        g_f, g_b = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.graph(g_f, stream=cap):
+            plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=cap, rope=rp)
+        with torch.cuda.graph(g_b, stream=cap):
+            plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=cap,
+                     rope=rp)
+        stream.wait_stream(cap)
+
+    def timed_step():
+        if use_graph:
+            with torch.cuda.stream(stream):
+                g_f.replay()
+                g_b.replay()
+        else:
+            plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
+            plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream,
+                     rope=rp)
+
+    for _ in range(3):
+        replan()
+        timed_step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     sampler = ClockSampler(phys)
     sampler.start()
     # Load soak: the same step, back to back, for --soak seconds right before the
@@ -363,7 +397,8 @@ def run_ours(args, w, batch):
     t_soak = time.perf_counter()
     while time.perf_counter() - t_soak < args.soak:
         for _ in range(16):
-            step()
+            replan()
+            timed_step()
         soak_steps += 16
         torch.cuda.synchronize()
     if ws > 1:
@@ -377,11 +412,7 @@ def run_ours(args, w, batch):
         # on its own (planner_host_ms), not inside the device-timed step
         replan()
         starts[s].record(stream)
-        plan.set_events(kev[s][0:n_fwd + 1])
-        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
-        plan.set_events(kev[s][n_fwd:])
-        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream,
-                 rope=rp)
+        timed_step()
         ends[s].record(stream)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall0
@@ -391,20 +422,47 @@ def run_ours(args, w, batch):
     clocks = sampler.stop()
     clocks["window"] = "sampled every 50 ms over a %.1f s load soak (%d steps) and the timed steps" % (
         args.soak, soak_steps)
-    plan.set_events(None)
-    launches = plan.launch_count - launches0
+    # kernels launched in the timed region (graph replays launch the captured ones)
+    launches = args.steps * len(names) if use_graph else plan.launch_count - launches0
     st = plan.check_status()
     if st != 0:
         raise RuntimeError("device status after timed region: " + J.status_str(st))
-
     step_ms = np.array([starts[s].elapsed_time(ends[s]) for s in range(args.steps)])
     ms = float(step_ms.mean())
-    per_kernel = {n: float(np.mean([kev[s][i].elapsed_time(kev[s][i + 1]) for s in range(args.steps)]))
-                  for i, n in enumerate(names)}
     if ws > 1:
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
+
+    # per-kernel device times: the same step from eager calls, CUDA events
+    # recorded by the library between its kernels (L2 flushed as above)
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
+    es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        replan()
+        es[s].record(stream)
+        plan.set_events(kev[s][0:n_fwd + 1])
+        plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream, rope=rp)
+        plan.set_events(kev[s][n_fwd:])
+        plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream,
+                 rope=rp)
+        ee[s].record(stream)
+    torch.cuda.synchronize()
+    plan.set_events(None)
+    st = plan.check_status()
+    if st != 0:
+        raise RuntimeError("device status after the eager steps: " + J.status_str(st))
+    per_kernel = {n: float(np.mean([kev[s][i].elapsed_time(kev[s][i + 1]) for s in range(args.steps)]))
+                  for i, n in enumerate(names)}
+    eager_ms = float(np.mean([es[s].elapsed_time(ee[s]) for s in range(args.steps)]))
+    if ws > 1:
+        t = torch.tensor([eager_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        eager_ms = float(t.item())
+    if use_graph:
+        del g_f, g_b
 
     f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block, w.window)
     total_flops = args.global_flops if args.global_flops is not None else ws * (f_fwd + f_bwd)
@@ -415,48 +473,8 @@ def run_ours(args, w, batch):
     bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
     intensity = (f_fwd + f_bwd) / (bf + bb)
     roof = roofline_of(w, batch, per_kernel, pk, pk_kind, ds=not args.device_plan)
-
-    # the same forward and backward launches captured once as two CUDA graphs and
-    # replayed (no host launch work); L2 flushed between steps as above
-    graph = None
-    if not args.no_graph:
-        g_f, g_b = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        cap = torch.cuda.Stream(device=dev)
-        cap.wait_stream(stream)
-        with torch.cuda.graph(g_f, stream=cap):
-            plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=cap, rope=rp)
-        with torch.cuda.graph(g_b, stream=cap):
-            plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=cap,
-                     rope=rp)
-        stream.wait_stream(cap)
-        gev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                g_f.replay()
-                g_b.replay()
-            for s_ in range(args.steps):
-                flush.fill_(s_ & 0xFF)
-                gev[s_][0].record(stream)
-                g_f.replay()
-                gev[s_][1].record(stream)
-                g_b.replay()
-                gev[s_][2].record(stream)
-        torch.cuda.synchronize()
-        st = plan.check_status()
-        if st != 0:
-            raise RuntimeError("device status after graph replays: " + J.status_str(st))
-        gf = float(np.mean([gev[s_][0].elapsed_time(gev[s_][1]) for s_ in range(args.steps)]))
-        gb = float(np.mean([gev[s_][1].elapsed_time(gev[s_][2]) for s_ in range(args.steps)]))
-        if ws > 1:
-            t = torch.tensor([gf + gb], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            gsum = float(t.item())
-        else:
-            gsum = gf + gb
-        graph = {"fwd_ms": gf, "bwd_ms": gb, "ms_per_step": gsum,
-                 "value": total_flops / (gsum * 1e-3) / 1e12, "unit": UNIT,
-                 "note": "fwd and bwd launches replayed from CUDA graphs; plan update not included"}
-        del g_f, g_b
+    eager = {"ms_per_step": eager_ms, "value": total_flops / (eager_ms * 1e-3) / 1e12, "unit": UNIT,
+             "note": "the same step from eager calls (host launch work between kernels)"}
 
     # end to end through the public API with host buffers (the host-buffer step
     # has no rotary-embedding form)
@@ -469,6 +487,7 @@ def run_ours(args, w, batch):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "launch": "CUDA graphs (forward, backward) replayed per step" if use_graph else "eager calls",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": dict(workload_config(w, batch.act, batch.B, True, ws, args.global_B), **variant_keys(args, w)),
             "pct_of_bf16_peak": 100.0 * value / ws / pk["bf16_tflops"],
@@ -482,8 +501,7 @@ def run_ours(args, w, batch):
             "planner_stream_ms": float(np.median(plan_dev_ms)),
             "planner": "device (jattn_plan_update_device)" if args.device_plan else "host (jattn_plan_update)",
             "timed_wall_s": t_wall}
-    if graph is not None:
-        line["graph"] = graph
+    line["eager"] = eager
     if e2e is not None:
         line["e2e"] = {k2: e2e[k2] for k2 in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
         line["e2e"]["ms_per_step"] = e2e["ms_per_step"]
@@ -647,7 +665,8 @@ def main():
     ap.add_argument("--cpu-frac", type=float, default=1.0, help="share of the batch's pairs the CPU baseline runs")
     ap.add_argument("--ref-frac", type=float, default=1.0 / 32, help="share of the batch per reference-arm step")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-graph", action="store_true", help="skip the CUDA-graph replay timing")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager calls instead of CUDA-graph replays of the forward and backward")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--broadcast-q", action="store_true",
                     help="pooled-attention workload: one shared Q read by every sequence, dQ summed (--workload 4)")
