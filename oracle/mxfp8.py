@@ -29,10 +29,17 @@ The readings of the pages taken here:
     Blocks start at the sequence's first row; the last block of a sequence is
     partial.
   * P: quantised per query row in groups of 32 keys (the K dimension of the
-    P V product), after exp(s - m) with the row max m.
+    P V product).  "Online" in the softmax warps means against a running row
+    max; read here as a max kept as an integer M in log2 units (an integer no
+    smaller than any score of the row in log2 units): P = 2^(s log2 e - M).
+    Every rescale of an online softmax is then a power of two, and a
+    power-of-two factor moves the block exponent and leaves the quantised
+    mantissas as they are, so the result does not depend on the order of the
+    key blocks or on when the max was raised; M = ceil(max_j s_ij log2 e)
+    gives it in one step here.
   * The row sum l is accumulated from the unquantised P, as the softmax warps
     hold it in float32 before the conversion.
-  * O = (P_q V_q) / l, with lse = m + ln l.
+  * O = (P_q V_q) / l; lse = ln sum_j exp(s_ij) (the max cancels).
   * Backward: dO is quantised like Q (32 x 32 blocks).  P and dS each feed
     two products with different K dimensions (P: dV = P^T dO; dS: dQ = dS K
     and dK = dS^T Q), so in the backward they are quantised in 32 x 32 blocks,
@@ -113,6 +120,39 @@ def qdq_rows_cols(x: np.ndarray, rb: int, cb: int) -> np.ndarray:
     return out
 
 
+def qdq_allowance(x: np.ndarray, rb: int, cb: int, err: np.ndarray) -> np.ndarray:
+    """Per element, how far the quantised value of x could move if x itself
+    moved by up to err (elementwise, >= 0): one grid step where x lies within
+    err of a rounding midpoint of its block's grid, and a quarter of |x| plus a
+    step of the next coarser grid for every element of a block whose largest
+    magnitude lies within err of a power of two (its exponent could differ).
+    Zero elsewhere: there the rounding decision cannot change.  This bounds the
+    effect of computing x in another floating-point precision (float32 instead
+    of float64) on the quantised result."""
+    x = np.asarray(x, dtype=np.float64)
+    err = np.broadcast_to(np.asarray(err, dtype=np.float64), x.shape)
+    out = np.zeros_like(x)
+    R, Cn = x.shape
+    for r in range(0, R, rb):
+        for c in range(0, Cn, cb):
+            xb, eb = np.abs(x[r:r + rb, c:c + cb]), err[r:r + rb, c:c + cb]
+            amax = xb.max() if xb.size else 0.0
+            e = block_exponent(amax)
+            sc = 2.0 ** e
+            ea = eb.max() if eb.size else 0.0
+            lo_e = block_exponent(max(amax - ea, 0.0))
+            hi_e = block_exponent(amax + ea)
+            if lo_e != e or hi_e != e:
+                out[r:r + rb, c:c + cb] = 0.25 * xb + 2.0 ** (max(e, hi_e) + 1 - 9)
+                continue
+            v = np.minimum(xb / sc, E4M3_MAX)
+            i = np.clip(np.searchsorted(_POS, v, side="left"), 1, len(_POS) - 1)
+            lo, hi = _POS[i - 1], _POS[i]
+            near = np.abs(v - 0.5 * (lo + hi)) <= eb / sc
+            out[r:r + rb, c:c + cb] = np.where(near, (hi - lo) * sc, 0.0)
+    return out
+
+
 def qdq_jagged(x, offsets) -> np.ndarray:
     """[T, H, D]: per sequence and head, 32 local rows x 32 features per block."""
     x = np.asarray(x, dtype=np.float64)
@@ -125,13 +165,24 @@ def qdq_jagged(x, offsets) -> np.ndarray:
     return out
 
 
-def forward(q_off, kv_off, q, k, v, scale=None):
-    """MXFP8 softmax attention forward: returns (out [Tq,H,D], lse [H,Tq]) in float64."""
+LOG2E = 1.0 / np.log(2.0)
+# relative size of the float32 rounding of an unquantised P or dS value that
+# flip allowances assume (generous: the kernels' float32 scores and exponentials
+# are far closer)
+FP32_REL = 1e-4
+
+
+def forward(q_off, kv_off, q, k, v, scale=None, with_allowance=False):
+    """MXFP8 softmax attention forward: returns (out [Tq,H,D], lse [H,Tq]) in
+    float64, and with with_allowance also allow [Tq,H,D]: how far out could move
+    if P were computed in float32 (qdq_allowance of P with a relative error of
+    FP32_REL, carried through P V / l)."""
     q, k, v = (np.asarray(t, dtype=np.float64) for t in (q, k, v))
     Tq, H, D = q.shape
     scale = 1.0 / np.sqrt(D) if scale is None else scale
     qq, kq, vq = qdq_jagged(q, q_off), qdq_jagged(k, kv_off), qdq_jagged(v, kv_off)
     out = np.zeros((Tq, H, D))
+    allow = np.zeros((Tq, H, D))
     lse = np.full((H, Tq), -np.inf)
     qo = np.asarray(q_off, dtype=np.int64)
     ko = np.asarray(kv_off, dtype=np.int64)
@@ -141,24 +192,38 @@ def forward(q_off, kv_off, q, k, v, scale=None):
             continue
         for h in range(H):
             s = scale * qq[q0:q1, h] @ kq[k0:k1, h].T
-            m = s.max(axis=1, keepdims=True)
-            p = np.exp(s - m)
+            t = s * LOG2E
+            M = np.ceil(t.max(axis=1, keepdims=True))  # integer max, log2 units
+            p = 2.0 ** (t - M)
             l = p.sum(axis=1, keepdims=True)
             pq = qdq_rows_cols(p, 1, 32)
             out[q0:q1, h] = (pq @ vq[k0:k1, h]) / l
-            lse[h, q0:q1] = (m + np.log(l))[:, 0]
+            m = s.max(axis=1, keepdims=True)
+            lse[h, q0:q1] = (m + np.log(np.exp(s - m).sum(axis=1, keepdims=True)))[:, 0]
+            if with_allowance:
+                a = qdq_allowance(p, 1, 32, FP32_REL * p)
+                allow[q0:q1, h] = (a @ np.abs(vq[k0:k1, h])) / l
+    if with_allowance:
+        return out, lse, allow
     return out, lse
 
 
-def backward(q_off, kv_off, q, k, v, dout, scale=None):
-    """MXFP8 softmax attention backward: returns (dq, dk, dv) in float64."""
+def backward(q_off, kv_off, q, k, v, dout, scale=None, with_allowance=False):
+    """MXFP8 softmax attention backward: returns (dq, dk, dv) in float64, and
+    with with_allowance also (allow_dq, allow_dk, allow_dv): how far they could
+    move through flipped quantisation decisions of P and dS if those were
+    computed in float32 from a forward output rounded to bf16 and a forward
+    that is itself within its own allowance (qdq_allowance with a relative
+    error of FP32_REL on P; on dS the same on P and dP plus 2^-8 sum_d |dO O|
+    and sum_d |dO| times the forward allowance for Delta)."""
     q, k, v, dout = (np.asarray(t, dtype=np.float64) for t in (q, k, v, dout))
     Tq, H, D = q.shape
     scale = 1.0 / np.sqrt(D) if scale is None else scale
-    out, lse = forward(q_off, kv_off, q, k, v, scale)
+    out, lse, fallow = forward(q_off, kv_off, q, k, v, scale, with_allowance=True)
     qq, kq, vq = qdq_jagged(q, q_off), qdq_jagged(k, kv_off), qdq_jagged(v, kv_off)
     dq_ = qdq_jagged(dout, q_off)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    adq, adk, adv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
     qo = np.asarray(q_off, dtype=np.int64)
     ko = np.asarray(kv_off, dtype=np.int64)
     for b in range(len(qo) - 1):
@@ -175,4 +240,16 @@ def backward(q_off, kv_off, q, k, v, dout, scale=None):
             dv[k0:k1, h] = pq.T @ dq_[q0:q1, h]
             dq[q0:q1, h] = scale * dsq @ kq[k0:k1, h]
             dk[k0:k1, h] = scale * dsq.T @ qq[q0:q1, h]
+            if with_allowance:
+                do_h, o_h = dout[q0:q1, h], out[q0:q1, h]
+                d_err = 2.0 ** -8 * np.sum(np.abs(do_h * o_h), axis=1, keepdims=True) + \
+                    np.abs(do_h) @ np.ones((D, 1)) * fallow[q0:q1, h].max(axis=1, keepdims=True)
+                ap = qdq_allowance(p, 32, 32, FP32_REL * p)
+                e_ds = FP32_REL * np.abs(ds) + p * (FP32_REL * (np.abs(dp) + np.abs(delta)) + d_err)
+                ads = qdq_allowance(ds, 32, 32, e_ds)
+                adv[k0:k1, h] = ap.T @ np.abs(dq_[q0:q1, h])
+                adq[q0:q1, h] = scale * ads @ np.abs(kq[k0:k1, h])
+                adk[k0:k1, h] = scale * ads.T @ np.abs(qq[q0:q1, h])
+    if with_allowance:
+        return dq, dk, dv, adq, adk, adv
     return dq, dk, dv
