@@ -152,6 +152,9 @@ def variant_keys(args, w: W.Workload) -> dict:
         out["rope"] = "Q and K rotated in the kernels, standard table (base 10000)"
     if args.broadcast_q:
         out["broadcast_q"] = "%d shared query rows, dQ summed over the sequences" % w.q_rows_shared
+    if getattr(args, "mxfp8", False):
+        out["mxfp8"] = ("Q, K, V, dO quantised to E4M3 with E8M0 scales per 32 x 32 block, P and dS quantised "
+                        "online; products on the bf16 tensor cores (the quantised values are exact in bf16)")
     return out
 
 
@@ -161,7 +164,7 @@ def rope_tables(batch: W.Batch, w: W.Workload):
     return W.rope_table(longest, w.D, "standard")
 
 
-def time_oracle(batch: W.Batch, frac: float, seed: int = 0, rope=None):
+def time_oracle(batch: W.Batch, frac: float, seed: int = 0, rope=None, mxfp8=False):
     from oracle import oracle
     w = batch.w
     seqs = sample_sequences(batch.q_off, batch.kv_off, frac, seed)
@@ -169,10 +172,17 @@ def time_oracle(batch: W.Batch, frac: float, seed: int = 0, rope=None):
                                                        tensors_kv=(batch.k, batch.v))
     nthreads = oracle.default_threads()
     t0 = time.perf_counter()
-    oracle.forward(qo, ko, q, k, v, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
-                   nthreads=nthreads, window=w.window, rope=rope)
-    oracle.backward(qo, ko, q, k, v, dout, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
-                    nthreads=nthreads, window=w.window, rope=rope)
+    if mxfp8:  # the MXFP8 oracle (numpy, one thread)
+        from oracle import mxfp8 as MX
+        nthreads = 1
+        qd, kd, vd, dd = (t.double().numpy() for t in (q, k, v, dout))
+        MX.forward(qo, ko, qd, kd, vd, scale=batch.scale)
+        MX.backward(qo, ko, qd, kd, vd, dd, scale=batch.scale)
+    else:
+        oracle.forward(qo, ko, q, k, v, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
+                       nthreads=nthreads, window=w.window, rope=rope)
+        oracle.backward(qo, ko, q, k, v, dout, bias=batch.bias, scale=batch.scale, act=batch.act, block=w.block,
+                        nthreads=nthreads, window=w.window, rope=rope)
     dt = time.perf_counter() - t0
     f, b = W.flops(qo, ko, w.H, w.D, w.block, w.window)
     desc = "%d of %d sequences (seeded), %.1f%% of the valid pairs" % (
@@ -187,10 +197,10 @@ def run_reference(args, w, batch):
     if rank != 0:
         return
     for _ in range(args.warmup):
-        time_oracle(batch, args.ref_frac, seed=1, rope=rope)
+        time_oracle(batch, args.ref_frac, seed=1, rope=rope, mxfp8=args.mxfp8)
     vals, times = [], []
     for s in range(args.steps):
-        v, dt, cores, desc = time_oracle(batch, args.ref_frac, seed=2 + s, rope=rope)
+        v, dt, cores, desc = time_oracle(batch, args.ref_frac, seed=2 + s, rope=rope, mxfp8=args.mxfp8)
         vals.append(v)
         times.append(dt)
     value = float(np.mean(vals))
@@ -239,16 +249,21 @@ KERNELS_FULL_DS = ["fwd", "bwd_delta", "bwd_dkdv", "bwd_dq_gemm"]  # backward wi
 KERNELS_BLOCK = ["fwd", "bwd_block"]
 
 
-def kernel_names(w, act, device_plan=False, broadcast_q=False):
+def kernel_names(w, act, device_plan=False, broadcast_q=False, mxfp8=False):
     """The kernels one step launches, in order (the library takes the dS-chunk
     backward for full attention on a host plan without a window, given the full
-    workspace as the bench does)."""
+    workspace as the bench does).  MXFP8: the forward first quantises Q, K, V,
+    the backward Q, dO, K, V."""
     if w.block:
         return list(KERNELS_BLOCK)
     ds = not w.window and not device_plan
     names = [n for n in (KERNELS_FULL_DS if ds else KERNELS_FULL) if n != "bwd_delta" or act == W.SOFTMAX]
     if broadcast_q:  # the per-sequence dQ rows are summed by one more kernel
         names.insert(names.index("bwd_dq_gemm" if ds else "bwd_dq") + 1, "bwd_dq_reduce")
+    if mxfp8:
+        names = ["mx_quant_q", "mx_quant_k", "mx_quant_v"] + names
+        names[names.index("fwd") + 1:names.index("fwd") + 1] = ["bwd_mx_quant_q", "bwd_mx_quant_dout",
+                                                               "bwd_mx_quant_k", "bwd_mx_quant_v"]
     return names
 
 
@@ -265,6 +280,9 @@ def kernel_work(w, batch, name, pk, ds=True):
         return 10.0 * D * H * p, W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)[1]
     if name == "bwd_delta":
         return 0.0, 2.0 * Tq * e + 4.0 * H * Tq
+    if name.startswith("mx_quant_") or name.startswith("bwd_mx_quant_"):  # bf16 rows in, their MXFP8 values out
+        rows = Tk if name.endswith(("_k", "_v")) else Tq
+        return 0.0, 2.0 * rows * e
     if name == "bwd_dq_reduce":  # fp32 per-sequence dQ rows in, the shared rows' bf16 sum out
         return 0.0, 4.0 * Tq * H * D + 2.0 * w.q_rows_shared * H * D
     # the dS chunks (bf16 per valid pair and head; activation modes: hi and lo)
@@ -300,7 +318,7 @@ def run_ours(args, w, batch):
     bias = batch.bias.to(dev) if batch.bias is not None else None
     plan = J.Plan(batch.q_off, batch.kv_off, H, D, act=batch.act, block=w.block, bias_buckets=w.bias_buckets,
                   window=w.window,
-                  dtype="fp32" if f32 else "bf16", device=local, broadcast_q=args.broadcast_q)
+                  dtype="fp32" if f32 else "bf16", device=local, broadcast_q=args.broadcast_q, mxfp8=args.mxfp8)
     if args.broadcast_q:  # the shared query rows once, not one copy per sequence
         q = q[:w.q_rows_shared].contiguous()
     out = torch.empty(batch.Tq, H, D, dtype=tdt, device=dev)
@@ -349,8 +367,9 @@ def run_ours(args, w, batch):
         plan_dev_ms.append(e0.elapsed_time(e1))
     torch.cuda.synchronize()
 
-    names = kernel_names(w, batch.act, args.device_plan, args.broadcast_q)
-    n_fwd, n_bwd = 1, len(names) - 1
+    names = kernel_names(w, batch.act, args.device_plan, args.broadcast_q, args.mxfp8)
+    n_fwd = names.index("fwd") + 1
+    n_bwd = len(names) - n_fwd
     if f32 or D == 32:
         raise SystemExit("bench: staged (fp32 / D=32) workloads are parity cases, not bench lines")
     visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
@@ -505,7 +524,8 @@ def run_ours(args, w, batch):
     if e2e is not None:
         line["e2e"] = {k2: e2e[k2] for k2 in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step")}
         line["e2e"]["ms_per_step"] = e2e["ms_per_step"]
-    plain = not (args.rope or args.broadcast_q or args.window or args.device_plan or args.act is not None)
+    plain = not (args.rope or args.broadcast_q or args.window or args.device_plan or args.act is not None or
+                 args.mxfp8)
     if rank == 0 and ws == 1 and w.wid == 2 and plain and not args.no_others:
         # the other workloads' step throughput and dominant-kernel roofline
         # fractions, measured in this run beside the self-attention line
@@ -516,9 +536,15 @@ def run_ours(args, w, batch):
             key = "%d_%s" % (wid, W.ACT_NAMES[act])
             others[key] = measure_other(wid, act, dev, stream, max(10, min(args.steps, 30)), flush)
             torch.cuda.empty_cache()
+        # MXFP8 attention on the self-attention batch (without its bias)
+        others["2_mxfp8"] = measure_other(2, W.SOFTMAX, dev, stream, max(10, min(args.steps, 30)), flush,
+                                          mxfp8=True)
+        torch.cuda.empty_cache()
         line["others"] = others
     if rank == 0 and ws == 1 and not args.no_cpu:
-        v_cpu, dt, cores, desc = time_oracle(batch, args.cpu_frac, seed=0, rope=rope)
+        # the MXFP8 oracle is numpy on one thread: a smaller seeded share of the batch
+        v_cpu, dt, cores, desc = time_oracle(batch, min(args.cpu_frac, 0.02) if args.mxfp8 else args.cpu_frac,
+                                             seed=0, rope=rope, mxfp8=args.mxfp8)
         line["cpu_baseline"] = {"value": v_cpu, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
     if ws > 1:
@@ -553,32 +579,36 @@ def roofline_of(w, batch, per_kernel, pk, pk_kind, ds=True):
     return roof
 
 
-def measure_other(wid, act, dev, stream, steps, flush):
+def measure_other(wid, act, dev, stream, steps, flush, mxfp8=False):
     """One other workload at full size: device-timed steps (plan update queued
     first, L2 flushed between steps), per-kernel times from the library's event
     hook, valid-token TFLOP/s and the dominant kernel's roofline fraction."""
     import jagged_attention_recommendation_gb300 as J
     batch = W.make_batch(wid, act=act)
+    if mxfp8:  # MXFP8 takes no bias
+        batch.w = dataclasses.replace(batch.w, bias_buckets=0)
+        batch.bias = None
     w = batch.w
     H, D = w.H, w.D
     q, k, v, dout = (t.to(dev) for t in (batch.q, batch.k, batch.v, batch.dout))
     bias = batch.bias.to(dev) if batch.bias is not None else None
     plan = J.Plan(batch.q_off, batch.kv_off, H, D, act=batch.act, block=w.block, bias_buckets=w.bias_buckets,
-                  device=dev.index)
+                  device=dev.index, mxfp8=mxfp8)
     out = torch.empty(batch.Tq, H, D, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(H, batch.Tq, dtype=torch.float32, device=dev) if batch.act == W.SOFTMAX else None
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     fws = torch.empty(max(plan.fwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
     bws = torch.empty(max(plan.bwd_workspace_bytes, 1), dtype=torch.uint8, device=dev)
-    names = kernel_names(w, batch.act)
+    names = kernel_names(w, batch.act, mxfp8=mxfp8)
+    nf = names.index("fwd") + 1
 
     def step(evs=None):
         plan.update(batch.q_off, batch.kv_off, stream)
         if evs is not None:
-            plan.set_events(evs[0:2])
+            plan.set_events(evs[0:nf + 1])
         plan.fwd(q, k, v, bias=bias, out=out, lse=lse, workspace=fws, stream=stream)
         if evs is not None:
-            plan.set_events(evs[1:])
+            plan.set_events(evs[nf:])
         plan.bwd(dout, q, k, v, out, lse=lse, bias=bias, dq=dq, dk=dk, dv=dv, workspace=bws, stream=stream)
 
     for _ in range(3):
@@ -601,7 +631,8 @@ def measure_other(wid, act, dev, stream, steps, flush):
     pk, pk_kind = peaks()
     roof = roofline_of(w, batch, per_kernel, pk, pk_kind)
     plan.close()
-    return {"workload": workload_config(w, batch.act, batch.B, True)["workload"], "steps": steps,
+    return {"workload": workload_config(w, batch.act, batch.B, True)["workload"] + (", MXFP8" if mxfp8 else ""),
+            "steps": steps,
             "value": (f_fwd + f_bwd) / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
             "per_kernel_ms": per_kernel,
             "step_hbm_frac": (bf + bb) / (ms * 1e-3) / 1e9 / pk["hbm_gbs"],
@@ -676,6 +707,8 @@ def main():
                     help="rotary position embedding of Q and K (standard frequency table; block workload only)")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window W (keys with |i - j| < W) on the chosen workload; 0 = off")
+    ap.add_argument("--mxfp8", action="store_true",
+                    help="MXFP8 attention (jattn_mode.mxfp8) on the chosen softmax workload, without its bias")
     ap.add_argument("--soak", type=float, default=1.5,
                     help="seconds of back-to-back steps right before the timed region (clocks under load)")
     ap.add_argument("--no-others", action="store_true",
@@ -709,6 +742,11 @@ def main():
         if batch.w.block:
             ap.error("--window does not combine with the block workload")
         batch.w = dataclasses.replace(batch.w, window=args.window)
+    if args.mxfp8:
+        if batch.w.block or args.window or args.broadcast_q or batch.act != W.SOFTMAX or batch.w.dtype != "bf16":
+            ap.error("--mxfp8 runs softmax full attention on bf16 data (workloads 2, 3)")
+        batch.w = dataclasses.replace(batch.w, bias_buckets=0)  # MXFP8 takes no bias
+        batch.bias = None
     if args.impl == "reference":
         run_reference(args, batch.w, batch)
     else:

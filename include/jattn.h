@@ -91,6 +91,21 @@ typedef struct {
                              reduced in a fixed order (bitwise reproducible).  Needs full
                              attention (no block), bf16 data and D in {64, 128}; jattn_step_host
                              does not take it.  0 = off. */
+    int32_t mxfp8;        /* 1: MXFP8 attention ("Training GEM at LLM scale", section "Low
+                             Precision Flash Attention"): Q, K, V (and dO in the backward) are
+                             quantised to the microscaling format, FP8 E4M3 elements with one
+                             power-of-two E8M0 scale per 32 local rows x 32 features of a
+                             sequence and head (exponent floor(log2 amax) - 8, elements rounded
+                             to nearest even and saturated at 448); P is quantised online per
+                             query row in 32-key groups against an integer running max in log2
+                             units (the row sum from the unquantised P); the backward
+                             quantises P and dS in 32 x 32 blocks.  The quantised values are
+                             exactly representable in bf16 and the products run on the bf16
+                             tensor cores with fp32 accumulation, which gives the products of a
+                             block-scaled MMA exactly.  Needs softmax, full attention, bf16 data,
+                             D in {64, 128}, no bias, window or broadcast Q, and a host plan at
+                             fwd / bwd time; the backward needs jattn_bwd_workspace_bytes.
+                             0 = off. */
 } jattn_mode;
 
 /* One unit of work: rows [q_start, q_start+q_len) of Q against rows
@@ -356,6 +371,19 @@ jattn_status jattn_step_host(jattn_plan *plan, const int32_t *q_offsets, const i
  * no call was issued, JATTN_ERR_CUDA when the wait cannot be enqueued.
  */
 jattn_status jattn_step_host_join(jattn_plan *plan, void *stream);
+
+/*
+ * MXFP8 quantisation of one input tensor, as the mxfp8 mode applies it to Q, K,
+ * V and dO: blocks of 32 local rows (the sequence's rows under the plan's
+ * query offsets, which = JATTN_TILES_Q, or key offsets, JATTN_TILES_KV) x 32
+ * features of one head, one E8M0 exponent per block (floor(log2 amax) - 8,
+ * clamped to [-127, 127]), E4M3 elements (nearest, ties to even, saturated at
+ * +-448).  xq receives the values the blocks stand for, element times scale,
+ * as bf16 (exact).  x, xq: DEVICE bf16 [T, H, D], 16-byte aligned; the plan
+ * must be an mxfp8 plan (else JATTN_ERR_UNSUPPORTED) made or updated on the
+ * host.  Stream-ordered.
+ */
+jattn_status jattn_mxfp8_quantize(const jattn_plan *plan, const void *x, int32_t which, void *xq, void *stream);
 
 /*
  * Test hook: the error path of a bounded wait on a real launch.  The paper has

@@ -25,7 +25,8 @@ EXPORTED = ("jattn_plan_create", "jattn_plan_update", "jattn_plan_tiles", "jattn
             "jattn_bwd_workspace_bytes", "jattn_plan_destroy", "jattn_fwd", "jattn_bwd",
             "jattn_check_device_status", "jattn_status_str", "jattn_plan_set_events", "jattn_plan_launch_count", "jattn_last_cuda_error", "jattn_bwd_noalloc",
             "jattn_shard", "jattn_step_host", "jattn_step_host_join", "jattn_fwd_rope", "jattn_bwd_rope",
-            "jattn_plan_update_device", "jattn_test_fwd_stall", "jattn_bwd_workspace_bytes_min")
+            "jattn_plan_update_device", "jattn_test_fwd_stall", "jattn_bwd_workspace_bytes_min",
+            "jattn_mxfp8_quantize")
 
 
 class JattnError(RuntimeError):
@@ -40,7 +41,7 @@ class JattnError(RuntimeError):
 class Mode(ctypes.Structure):
     _fields_ = [("act", ctypes.c_int32), ("block", ctypes.c_int32), ("scale", ctypes.c_float),
                 ("bias_buckets", ctypes.c_int32), ("dtype", ctypes.c_int32), ("window", ctypes.c_int32),
-                ("broadcast_q", ctypes.c_int32)]
+                ("broadcast_q", ctypes.c_int32), ("mxfp8", ctypes.c_int32)]
 
 
 class Rope(ctypes.Structure):
@@ -95,6 +96,8 @@ def load():
     lib.jattn_bwd_rope.restype = i32
     lib.jattn_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.jattn_bwd_noalloc.restype = i32
+    lib.jattn_mxfp8_quantize.argtypes = [P, P, i32, P, P]
+    lib.jattn_mxfp8_quantize.restype = i32
     lib.jattn_test_fwd_stall.argtypes = [P, P, P, P, P, P, ctypes.c_uint64, P]
     lib.jattn_test_fwd_stall.restype = i32
     lib.jattn_step_host.argtypes = [P, P, P, i32, P, P, P, P, P, P, P, P, P, P, P]
@@ -159,10 +162,10 @@ class Plan:
 
     def __init__(self, q_off, kv_off, H: int, D: int, act: int = SOFTMAX, block: int = 0, scale: float = 0.0,
                  bias_buckets: int = 0, dtype: str = "bf16", device: int = 0, window: int = 0,
-                 broadcast_q: bool = False):
+                 broadcast_q: bool = False, mxfp8: bool = False):
         """broadcast_q: every sequence's queries are the rows of one shared Q
         [n, H, D] (n = each sequence's Lq); bwd then returns dq [n, H, D], the
-        sum over the sequences."""
+        sum over the sequences.  mxfp8: MXFP8 attention (jattn_mode.mxfp8)."""
         lib = load()
         qo, ko = _i32(q_off), _i32(kv_off)
         self.H, self.D, self.act, self.block, self.bias_buckets = H, D, act, block, bias_buckets
@@ -170,8 +173,9 @@ class Plan:
         self.dtype = dtype
         self.device = device
         self.broadcast_q = bool(broadcast_q)
+        self.mxfp8 = bool(mxfp8)
         self.mode = Mode(act, block, float(scale), bias_buckets, FP32 if dtype == "fp32" else BF16, window,
-                         1 if broadcast_q else 0)
+                         1 if broadcast_q else 0, 1 if mxfp8 else 0)
         self._h = ctypes.c_void_p()
         _check(lib.jattn_plan_create(qo.ctypes.data_as(ctypes.c_void_p), ko.ctypes.data_as(ctypes.c_void_p),
                                      len(qo) - 1, H, D, ctypes.byref(self.mode), device, ctypes.byref(self._h)),
@@ -280,6 +284,15 @@ class Plan:
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dbias), _ptr(ws), nbytes, _stream(stream)),
                "jattn_bwd")
         return dq, dk, dv
+
+    def mxfp8_quantize(self, x, which: int = TILES_Q, out=None, stream=None):
+        """x [T, H, D] bf16 (device) -> the values of its MXFP8 quantisation, as
+        bf16 [T, H, D] (jattn_mxfp8_quantize; which: TILES_Q = query offsets,
+        TILES_KV = key offsets)."""
+        out = torch.empty_like(x) if out is None else out
+        _check(load().jattn_mxfp8_quantize(self._h, _ptr(x), which, _ptr(out), _stream(stream)),
+               "jattn_mxfp8_quantize")
+        return out
 
     def bwd_noalloc(self, dout, q, k, v, out, lse=None, bias=None, dq=None, dk=None, dv=None, dbias=None,
                     stream=None):

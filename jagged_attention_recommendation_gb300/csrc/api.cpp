@@ -364,12 +364,27 @@ size_t ds_ws_bytes(const jattn_plan *p) {
     return align_up(static_cast<size_t>(p->ds_chunks) * planes * kDsChunkBytes, kAlign);
 }
 
-// bytes of the backward workspace without the dS chunks: Delta, staged inputs,
-// broadcast-Q dQ rows, in that order
-size_t bwd_ws_min(const jattn_plan *p) {
+// the backward workspace's first part: Delta, staged inputs, broadcast-Q dQ
+// rows, in that order
+size_t bwd_ws_base(const jattn_plan *p) {
     size_t n = softmax_full(p) ? align_up(static_cast<size_t>(p->H) * p->Tq * 4, kAlign) : 0;
     if (p->staged) n += 2 * stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
     return n + bcast_ws_bytes(p);
+}
+
+// MXFP8: the quantised copies (bf16 [T, H, D]) of q, k, v (forward) and of q,
+// dout, k, v (backward, in that order after the base part)
+size_t mx_copy_bytes(const jattn_plan *p, int64_t rows) {
+    return align_up(static_cast<size_t>(rows) * p->H * p->D * 2, kAlign);
+}
+size_t mx_bwd_bytes(const jattn_plan *p) {
+    return p->mode.mxfp8 ? 2 * mx_copy_bytes(p, p->Tq) + 2 * mx_copy_bytes(p, p->Tk) : 0;
+}
+
+// bytes the backward cannot run without: the base part, the MXFP8 copies and,
+// for MXFP8 (whose dQ comes only from the dS chunks), the chunks
+size_t bwd_ws_min(const jattn_plan *p) {
+    return bwd_ws_base(p) + mx_bwd_bytes(p) + (p->mode.mxfp8 ? ds_ws_bytes(p) : 0);
 }
 
 Geom make_geom(const jattn_plan *p, int which) {
@@ -396,6 +411,7 @@ Geom make_geom(const jattn_plan *p, int which) {
     g.wait_ns = kWaitTimeoutNs;
     g.ds = nullptr;
     g.ds_base = p->dev_planned ? nullptr : reinterpret_cast<const long long *>(p->d_buf + p->off_dsbase);
+    g.mxfp8 = p->mode.mxfp8;
     return g;
 }
 
@@ -486,6 +502,11 @@ jattn_status jattn_plan_create(const int32_t *q_offsets, const int32_t *kv_offse
     // rows keep that rounding inside the tolerances; unnormalised activation
     // sums over many keys do not, so float32 is offered with softmax only.
     if (mode->dtype == JATTN_FP32 && mode->act != JATTN_SOFTMAX) return JATTN_ERR_UNSUPPORTED;
+    // MXFP8 attention: softmax, full attention, bf16, D in {64, 128}, no bias, window or broadcast Q
+    if (mode->mxfp8 != 0 && mode->mxfp8 != 1) return JATTN_ERR_INVALID_ARG;
+    if (mode->mxfp8 && (mode->act != JATTN_SOFTMAX || mode->block != 0 || mode->window != 0 ||
+                        mode->dtype != JATTN_BF16 || mode->broadcast_q || mode->bias_buckets > 0 || D < 64))
+        return JATTN_ERR_UNSUPPORTED;
     if (mode->bias_buckets < 0) return JATTN_ERR_INVALID_ARG;
     if (mode->bias_buckets > 0 && H * mode->bias_buckets > kMaxBiasFloats) return JATTN_ERR_UNSUPPORTED;
     if (!(mode->scale >= 0.0f) || std::isinf(mode->scale)) return JATTN_ERR_INVALID_ARG;
@@ -659,13 +680,15 @@ jattn_status jattn_plan_tiles(const jattn_plan *plan, int32_t which, const jattn
 }
 
 size_t jattn_fwd_workspace_bytes(const jattn_plan *p) {
-    if (p == nullptr || !p->staged) return 0;
+    if (p == nullptr) return 0;
+    if (p->mode.mxfp8) return mx_copy_bytes(p, p->Tq) + 2 * mx_copy_bytes(p, p->Tk);
+    if (!p->staged) return 0;
     return stage_bytes(p, p->Tq) + 2 * stage_bytes(p, p->Tk);
 }
 
 size_t jattn_bwd_workspace_bytes(const jattn_plan *p) {
     if (p == nullptr) return 0;
-    return bwd_ws_min(p) + ds_ws_bytes(p);
+    return bwd_ws_base(p) + mx_bwd_bytes(p) + ds_ws_bytes(p);
 }
 
 size_t jattn_bwd_workspace_bytes_min(const jattn_plan *p) { return p == nullptr ? 0 : bwd_ws_min(p); }
@@ -724,7 +747,20 @@ jattn_status jattn_fwd_rope(const jattn_plan *p, const void *q, const void *k, c
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int f32 = p->mode.dtype == JATTN_FP32;
     const void *qq = q, *kk = k, *vv = v;
+    if (p->mode.mxfp8 && p->dev_planned) return JATTN_ERR_UNSUPPORTED;  // the quantisation reads host-planned offsets
     LaunchLog log(p, st);
+    if (p->mode.mxfp8) {  // Q, K, V replaced by the values of their MXFP8 quantisation
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        void *qs = ws, *ks = ws + mx_copy_bytes(p, p->Tq), *vs = ws + mx_copy_bytes(p, p->Tq) + mx_copy_bytes(p, p->Tk);
+        const int32_t *dqo = reinterpret_cast<const int32_t *>(p->d_buf + p->off_qoff);
+        const int32_t *dko = reinterpret_cast<const int32_t *>(p->d_buf + p->off_kvoff);
+        CUDA_TRY(log.done(launch_mx_quant(q, dqo, p->B, p->H, p->D, qs, st)));
+        CUDA_TRY(log.done(launch_mx_quant(k, dko, p->B, p->H, p->D, ks, st)));
+        CUDA_TRY(log.done(launch_mx_quant(v, dko, p->B, p->H, p->D, vs, st)));
+        qq = qs;
+        kk = ks;
+        vv = vs;
+    }
     if (p->staged) {
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         void *qs = ws, *ks = ws + stage_bytes(p, p->Tq), *vs = ws + stage_bytes(p, p->Tq) + stage_bytes(p, p->Tk);
@@ -777,12 +813,16 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
     if (!aligned16(dout) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dq) ||
         !aligned16(dk) || !aligned16(dv) || !aligned16(bias) || !aligned16(lse))
         return JATTN_ERR_ALIGNMENT;
+    if (p->mode.mxfp8 && p->dev_planned) return JATTN_ERR_UNSUPPORTED;  // the quantisation reads host-planned offsets
     const size_t need = bwd_ws_min(p);
     if (need > 0 && (workspace == nullptr || workspace_bytes < need)) return JATTN_ERR_WORKSPACE;
     if ((need > 0 || workspace != nullptr) && !aligned16(workspace)) return JATTN_ERR_ALIGNMENT;
-    // dS chunks when the workspace holds them (and the plan allows them)
+    // dS chunks when the workspace holds them (and the plan allows them); MXFP8 always
+    const size_t base = bwd_ws_base(p), mxb = mx_bwd_bytes(p);
     const size_t ds_need = ds_ws_bytes(p);
-    const bool use_ds = ds_need > 0 && rope == nullptr && workspace != nullptr && workspace_bytes >= need + ds_need;
+    const bool use_ds =
+        ds_need > 0 && rope == nullptr && workspace != nullptr && workspace_bytes >= base + mxb + ds_need;
+    if (p->mode.mxfp8 && !use_ds) return JATTN_ERR_WORKSPACE;
     DeviceGuard guard(p->device);
     if (!guard.ok) return note_error("jattn_bwd: cudaSetDevice failed");
     (void)cudaGetLastError();  // report only errors of this call
@@ -812,8 +852,24 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
         vv = vs;
     }
     float *dq_rows = nullptr;  // broadcast Q: per-sequence float32 dQ rows, after Delta and the staging
-    if (p->mode.broadcast_q) dq_rows = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + need - bcast_ws_bytes(p));
-    void *ds = use_ds ? static_cast<void *>(static_cast<uint8_t *>(workspace) + need) : nullptr;
+    if (p->mode.broadcast_q) dq_rows = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + base - bcast_ws_bytes(p));
+    void *ds = use_ds ? static_cast<void *>(static_cast<uint8_t *>(workspace) + base + mxb) : nullptr;
+    if (p->mode.mxfp8) {  // Q, dO, K, V replaced by the values of their MXFP8 quantisation
+        uint8_t *mx = static_cast<uint8_t *>(workspace) + base;
+        void *qs = mx, *ds_ = mx + mx_copy_bytes(p, p->Tq), *ks = mx + 2 * mx_copy_bytes(p, p->Tq);
+        void *vs = mx + 2 * mx_copy_bytes(p, p->Tq) + mx_copy_bytes(p, p->Tk);
+        const int32_t *dqo = reinterpret_cast<const int32_t *>(p->d_buf + p->off_qoff);
+        const int32_t *dko = reinterpret_cast<const int32_t *>(p->d_buf + p->off_kvoff);
+        if (log.done(launch_mx_quant(q, dqo, p->B, p->H, p->D, qs, st)) != cudaSuccess ||
+            log.done(launch_mx_quant(dout, dqo, p->B, p->H, p->D, ds_, st)) != cudaSuccess ||
+            log.done(launch_mx_quant(k, dko, p->B, p->H, p->D, ks, st)) != cudaSuccess ||
+            log.done(launch_mx_quant(v, dko, p->B, p->H, p->D, vs, st)) != cudaSuccess)
+            return note_error("jattn_bwd: MXFP8 quantisation launch");
+        qq = qs;
+        dd = ds_;
+        kk = ks;
+        vv = vs;
+    }
     BwdArgs a;
     a.lse = lse;
     a.delta = delta;
@@ -1020,6 +1076,23 @@ jattn_status jattn_plan_set_events(jattn_plan *p, void *const *events, int32_t n
 }
 
 int64_t jattn_plan_launch_count(const jattn_plan *p) { return p == nullptr ? 0 : p->launches; }
+
+jattn_status jattn_mxfp8_quantize(const jattn_plan *p, const void *x, int32_t which, void *xq, void *stream) {
+    if (p == nullptr || x == nullptr || xq == nullptr) return JATTN_ERR_INVALID_ARG;
+    if (which != JATTN_TILES_Q && which != JATTN_TILES_KV) return JATTN_ERR_INVALID_ARG;
+    if (p->device < 0) return JATTN_ERR_NO_DEVICE;
+    if (!p->mode.mxfp8 || p->dev_planned) return JATTN_ERR_UNSUPPORTED;
+    if (!aligned16(x) || !aligned16(xq)) return JATTN_ERR_ALIGNMENT;
+    DeviceGuard guard(p->device);
+    if (!guard.ok) return note_error("jattn_mxfp8_quantize: cudaSetDevice failed");
+    (void)cudaGetLastError();
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int32_t *off =
+        reinterpret_cast<const int32_t *>(p->d_buf + (which == JATTN_TILES_Q ? p->off_qoff : p->off_kvoff));
+    LaunchLog log(p, st);
+    return cuda_status(log.done(launch_mx_quant(x, off, p->B, p->H, p->D, xq, st)),
+                       "jattn_mxfp8_quantize: kernel launch");
+}
 
 jattn_status jattn_test_fwd_stall(const jattn_plan *p, const void *q, const void *k, const void *v, void *out,
                                   float *lse, uint64_t wait_ns, void *stream) {

@@ -3,6 +3,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <math.h>
 
 #include "common.h"
@@ -395,6 +397,49 @@ __device__ __forceinline__ float sum32(const float (&v)[32]) {
     }
     add2(a0, a1, b0, b1);
     return a0 + a1;
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 ("Training GEM at LLM scale", section "Low Precision Flash Attention"):
+// FP8 E4M3 elements with one power-of-two (E8M0) scale per block.  The scale
+// exponent of a block with largest magnitude amax is floor(log2 amax) - 8 (8 =
+// the exponent of E4M3's largest normal, 448), clamped to [-127, 127], read
+// from the float's exponent bits; an element x becomes E4M3(x 2^-e) 2^e, the
+// E4M3 rounding to nearest even and saturating at +-448.
+// ---------------------------------------------------------------------------
+// 2^k as a float, k in [-149, 127]
+__device__ __forceinline__ float pow2i(int k) {
+    return k >= -126 ? __int_as_float((k + 127) << 23) : __int_as_float(1 << (k + 149));
+}
+// block exponent of a non-negative amax
+__device__ __forceinline__ int mx_exponent(float amax) {
+    const int e = ((__float_as_int(amax) >> 23) & 0xFF) - 127 - 8;  // zero / subnormal: below -127
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+// the values of 32 elements' MXFP8 quantisation with block exponent e, in place
+__device__ __forceinline__ void mx_qdq32(float (&x)[32], int e) {
+    const float down = pow2i(-e), up = pow2i(e);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+        const __nv_fp8x2_storage_t q =
+            __nv_cvt_float2_to_fp8x2(make_float2(x[i] * down, x[i + 1] * down), __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+        x[i] = f.x * up;
+        x[i + 1] = f.y * up;
+    }
+}
+// largest magnitude of 32 values
+__device__ __forceinline__ float amax32(const float (&x)[32]) {
+    float a = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) a = fmaxf(a, fabsf(x[i]));
+    return a;
+}
+// largest of a non-negative value over the warp (non-negative floats order as
+// their bit patterns)
+__device__ __forceinline__ float warp_max_nonneg(float a) {
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(a)));
 }
 
 // ---------------------------------------------------------------------------

@@ -4,6 +4,7 @@
 #include <algorithm>
 #include <cuda_runtime.h>
 
+#include "attn.cuh"
 #include "kernels.h"
 
 namespace jattn {
@@ -68,6 +69,63 @@ __global__ void delta_kernel(const T *__restrict__ out, const T *__restrict__ do
             delta[static_cast<int64_t>(h) * Tq + t] = acc;
         }
     }
+}
+
+// MXFP8 quantisation of x [T, H, D] (bf16) per sequence and head, in blocks of
+// 32 local rows x 32 features: xq receives the values the quantised blocks
+// stand for (bf16, exact).  A CTA takes one (sequence, head) at a time; each
+// warp takes one block: lane = row, the block's largest magnitude by a warp
+// reduction.
+__global__ void mx_quant_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ off, int B, int H,
+                                int D, __nv_bfloat16 *__restrict__ xq) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int fbs = D / 32;
+    for (int64_t bh = blockIdx.x; bh < static_cast<int64_t>(B) * H; bh += gridDim.x) {
+        const int b = static_cast<int>(bh / H), h = static_cast<int>(bh - static_cast<int64_t>(b) * H);
+        const int r0 = off[b], L = off[b + 1] - r0;
+        const int ntask = ((L + 31) / 32) * fbs;
+        for (int task = warp; task < ntask; task += nw) {
+            const int rb = task / fbs, fb = task - rb * fbs;
+            const int row = rb * 32 + lane;
+            const bool ok = row < L;
+            const int64_t base = (static_cast<int64_t>(r0 + row) * H + h) * D + fb * 32;
+            float v[32];
+            if (ok) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(x + base) + k);
+                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        v[8 * k + 2 * j] = __uint_as_float(ws[j] << 16);
+                        v[8 * k + 2 * j + 1] = __uint_as_float(ws[j] & 0xffff0000u);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            }
+            const int e = dev::mx_exponent(dev::warp_max_nonneg(dev::amax32(v)));
+            dev::mx_qdq32(v, e);
+            if (ok) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    reinterpret_cast<uint4 *>(xq + base)[k] =
+                        make_uint4(dev::pack_bf16x2(v[8 * k], v[8 * k + 1]), dev::pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                                   dev::pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                                   dev::pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+            }
+        }
+    }
+}
+
+cudaError_t launch_mx_quant(const void *x, const int32_t *off, int B, int H, int D, void *xq, cudaStream_t stream) {
+    if (B <= 0 || D % 32 != 0) return B <= 0 ? cudaSuccess : cudaErrorInvalidValue;
+    const int64_t want = static_cast<int64_t>(B) * H;
+    const int blocks = static_cast<int>(std::min<int64_t>(want, 152 * 8));
+    mx_quant_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), off, B, H, D,
+                                                static_cast<__nv_bfloat16 *>(xq));
+    return cudaGetLastError();
 }
 
 // src [rows, D] -> dst [rows, Dp] bf16 (columns D..Dp-1 zero).

@@ -69,13 +69,20 @@ struct DkvCfg {
 // the dQ product's A operand); rows past the tile's keys are zero.  DT (with
 // DS): this pass also sums the bias-table gradient.  All three are compile
 // time switches, so kernels without them carry none of their work.
-template <int D, bool ACT, int BIAS, bool WIN, bool DS, bool DT>
+// MX (with DS): MXFP8 attention ("Training GEM at LLM scale", section "Low
+// Precision Flash Attention"): Q, K, V, dO arrive quantised, and P and dS are
+// quantised in 32 x 32 blocks before the products that take them (dV, and dK
+// with the dS chunks for dQ).  A compute warp's chunk of a block, 32 keys (its
+// lanes) x 32 queries, is exactly one such block of the sequence's local
+// positions; its scale comes from a warp-wide maximum.
+template <int D, bool ACT, int BIAS, bool WIN, bool DS, bool DT, bool MX = false>
 __global__ void __launch_bounds__(512, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                 const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO, const BwdArgs a) {
     using C = DkvCfg<D, ACT, BIAS>;
     static_assert(!(DS && WIN), "dS chunks are written for full attention only");
     static_assert(DS || !DT, "the bias gradient is summed here only with dS chunks");
+    static_assert(!MX || (DS && !ACT && BIAS == kBiasNone && !DT), "MXFP8: softmax, dS chunks, no bias");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -413,8 +420,12 @@ __global__ void __launch_bounds__(512, 1)
                                 // not stored, so zeroing it here changes no stored result)
                                 if (row >= t.kv_len) {
 #pragma unroll
-                                    for (int k = 0; k < 32; ++k) dp[k] = 0.0f;
+                                    for (int k = 0; k < 32; ++k) dp[k] = MX ? (x[k] = 0.0f) : 0.0f;
                                 }
+                            }
+                            if constexpr (MX) {  // this warp's 32 x 32 block of P and of dS
+                                mx_qdq32(x, mx_exponent(warp_max_nonneg(amax32(x))));
+                                mx_qdq32(dp, mx_exponent(warp_max_nonneg(amax32(dp))));
                             }
                             // bias-table gradient: dT[h, min(|i - j|, nb - 1)] += dS_ij; the far
                             // bucket in a register, the few near ones in shared memory
@@ -626,19 +637,27 @@ __global__ void __launch_bounds__(512, 1)
 // ============================================================================
 // launcher
 // ============================================================================
-template <int D, bool ACT, int BIAS, bool WIN, bool DS, bool DT>
+template <int D, bool ACT, int BIAS, bool WIN, bool DS, bool DT, bool MX = false>
 static cudaError_t launch_dkdv_w(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = DkvCfg<D, ACT, BIAS>;
     static SmemOnce done;
-    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN, DS, DT>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(dkdv_kernel<D, ACT, BIAS, WIN, DS, DT, MX>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    dkdv_kernel<D, ACT, BIAS, WIN, DS, DT><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    dkdv_kernel<D, ACT, BIAS, WIN, DS, DT, MX><<<n_ctas, 512, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 
-// the variant a launch takes: window, dS chunks (a.g.ds set), bias gradient with them
+// the variant a launch takes: window, dS chunks (a.g.ds set), bias gradient with
+// them, MXFP8 (softmax, dS chunks, no bias)
 template <int D, bool ACT, int BIAS>
 static cudaError_t launch_dkdv_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
+    if (a.g.mxfp8) {
+        if constexpr (!ACT && BIAS == kBiasNone) {
+            if (a.g.ds == nullptr || a.g.window > 0 || a.dbias != nullptr) return cudaErrorInvalidValue;
+            return launch_dkdv_w<D, false, kBiasNone, false, true, false, true>(tm, a, n_ctas, st);
+        }
+        return cudaErrorInvalidValue;
+    }
     if (a.g.ds != nullptr) {
         if (a.g.window > 0) return cudaErrorInvalidValue;
         if constexpr (BIAS != kBiasNone) {

@@ -66,6 +66,7 @@ struct Geom {
     // head h, key tile t, 64-query block i) = ds_base[b] + (h * nkt_b + t) * nqb_b + i
     void *ds;                 // chunk workspace (16-byte aligned), or nullptr (off)
     const long long *ds_base; // [B + 1] first chunk of every sequence (device)
+    int32_t mxfp8;            // 1: MXFP8 attention (P, and in the backward dS, quantised online)
 };
 
 // one dS chunk: 128 keys x 64 queries of bf16 (activation mode: two of them, hi and lo)

@@ -15,8 +15,24 @@ static cudaError_t launch_fwd_w(const TmapSet &tm, const FwdArgs &a, int n_ctas,
     return cudaGetLastError();
 }
 
+// MXFP8: softmax, no bias, no window
+template <int D>
+static cudaError_t launch_fwd_mx(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
+    using C = FwdCfg<D, false, kBiasNone>;
+    auto kern = fwd_kernel<D, false, kBiasNone, false, false, false, true>;
+    static SmemOnce done;
+    cudaError_t e = ensure_smem(kern, C::SMEM_ALLOC, done);
+    if (e != cudaSuccess || n_ctas <= 0) return e;
+    kern<<<n_ctas, C::THREADS, C::SMEM_ALLOC, stream>>>(tm.q, tm.k, tm.v, a);
+    return cudaGetLastError();
+}
+
 template <int D, bool ACT, int BIAS>
 static cudaError_t launch_fwd_t(const TmapSet &tm, const FwdArgs &a, int n_ctas, cudaStream_t stream) {
+    if constexpr (!ACT && BIAS == kBiasNone) {
+        if (a.g.mxfp8) return a.g.window > 0 ? cudaErrorInvalidValue : launch_fwd_mx<D>(tm, a, n_ctas, stream);
+    }
+    if (a.g.mxfp8) return cudaErrorInvalidValue;
     return a.g.window > 0 ? launch_fwd_w<D, ACT, BIAS, true>(tm, a, n_ctas, stream)
                           : launch_fwd_w<D, ACT, BIAS, false>(tm, a, n_ctas, stream);
 }

@@ -116,11 +116,19 @@ struct FwdCfg {
 // the S issuer waits on a barrier that nothing completes at that point, so
 // the bounded wait runs out and the kernel takes its error path (status word,
 // abort flag, drained copies, TMEM freed) on a real launch.
-template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false, bool STALL = false>
+// MX: MXFP8 attention ("Training GEM at LLM scale", section "Low Precision
+// Flash Attention"; softmax without bias, window or RoPE): Q, K, V arrive
+// already quantised (their MXFP8 values, bf16), the running row max is kept
+// as an integer in log2 units, so every rescale is an exact power of two,
+// and each row's P is quantised online in its 32-key chunks (one E8M0 scale
+// per chunk from the chunk's largest value) after the row sum has taken the
+// unquantised values.
+template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false, bool STALL = false, bool MX = false>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
     using C = FwdCfg<D, ACT, BIAS, ROPE>;
+    static_assert(!MX || (!ACT && BIAS == kBiasNone && !WIN && !ROPE), "MXFP8: softmax without bias, window, RoPE");
     const int win = WIN ? a.g.window : 0;  // |i - j| < win, 0 = no window
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
@@ -482,7 +490,8 @@ __global__ void __launch_bounds__(512, 1)
                     }
                     if constexpr (scaled) tmem_wait_st();
                     if (!scaled) mloc *= sc;
-                    const float m_new = fmaxf(m, mloc);
+                    // MXFP8: the max is an integer (log2 units), so alpha is a power of two
+                    const float m_new = MX ? ceilf(fmaxf(m, mloc)) : fmaxf(m, mloc);
                     // lazy rescale: keep the old max while it is within the threshold
                     float alpha = 1.0f;
                     bool resc = false;
@@ -491,7 +500,12 @@ __global__ void __launch_bounds__(512, 1)
                     } else if (__any_sync(0xffffffffu, m_new > m + kRescaleThreshold)) {
                         // the test is warp-wide: a row of the warp that has seen no
                         // key yet (m = m_new = -inf) keeps its zero l and O as they are
-                        alpha = m_new == -INFINITY ? 1.0f : ex2_approx(m - m_new);
+                        if constexpr (MX) {
+                            alpha = m_new == -INFINITY ? 1.0f
+                                    : (m == -INFINITY ? 0.0f : (m - m_new < -126.0f ? 0.0f : pow2i(static_cast<int>(m - m_new))));
+                        } else {
+                            alpha = m_new == -INFINITY ? 1.0f : ex2_approx(m - m_new);
+                        }
                         resc = true;
                         l *= alpha;
                         m = m_new;
@@ -525,6 +539,9 @@ __global__ void __launch_bounds__(512, 1)
                             }
                             if constexpr (WIN && !scaled) window_fill32(xc, window_bits32(win, q_loc, kvb + c * 32), 0.0f);
                             rs += sum32(xc);
+                            // MXFP8: the chunk's 32 keys of this row are one quantisation
+                            // group (the row sum above took the unquantised values)
+                            if constexpr (MX) mx_qdq32(xc, mx_exponent(amax32(xc)));
 #pragma unroll
                             for (int i = 0; i < 16; ++i) pw[i] = pack_bf16x2(xc[2 * i], xc[2 * i + 1]);
                         }

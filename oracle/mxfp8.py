@@ -139,9 +139,9 @@ def qdq_allowance(x: np.ndarray, rb: int, cb: int, err: np.ndarray) -> np.ndarra
             amax = xb.max() if xb.size else 0.0
             e = block_exponent(amax)
             sc = 2.0 ** e
-            ea = eb.max() if eb.size else 0.0
-            lo_e = block_exponent(max(amax - ea, 0.0))
-            hi_e = block_exponent(amax + ea)
+            # the block's largest magnitude lies in [max(|x| - err), max(|x| + err)]
+            lo_e = block_exponent(max((xb - eb).max(), 0.0) if xb.size else 0.0)
+            hi_e = block_exponent((xb + eb).max() if xb.size else 0.0)
             if lo_e != e or hi_e != e:
                 out[r:r + rb, c:c + cb] = 0.25 * xb + 2.0 ** (max(e, hi_e) + 1 - 9)
                 continue
@@ -214,8 +214,9 @@ def backward(q_off, kv_off, q, k, v, dout, scale=None, with_allowance=False):
     move through flipped quantisation decisions of P and dS if those were
     computed in float32 from a forward output rounded to bf16 and a forward
     that is itself within its own allowance (qdq_allowance with a relative
-    error of FP32_REL on P; on dS the same on P and dP plus 2^-8 sum_d |dO O|
-    and sum_d |dO| times the forward allowance for Delta)."""
+    error of FP32_REL on P; on dS the same on P and dP, plus, for Delta, the
+    bf16 rounding of O, 2^-9 sum_d |dO O|, and sum_d |dO| times the forward
+    allowance)."""
     q, k, v, dout = (np.asarray(t, dtype=np.float64) for t in (q, k, v, dout))
     Tq, H, D = q.shape
     scale = 1.0 / np.sqrt(D) if scale is None else scale
@@ -242,7 +243,7 @@ def backward(q_off, kv_off, q, k, v, dout, scale=None, with_allowance=False):
             dk[k0:k1, h] = scale * dsq.T @ qq[q0:q1, h]
             if with_allowance:
                 do_h, o_h = dout[q0:q1, h], out[q0:q1, h]
-                d_err = 2.0 ** -8 * np.sum(np.abs(do_h * o_h), axis=1, keepdims=True) + \
+                d_err = 2.0 ** -9 * np.sum(np.abs(do_h * o_h), axis=1, keepdims=True) + \
                     np.abs(do_h) @ np.ones((D, 1)) * fallow[q0:q1, h].max(axis=1, keepdims=True)
                 ap = qdq_allowance(p, 32, 32, FP32_REL * p)
                 e_ds = FP32_REL * np.abs(ds) + p * (FP32_REL * (np.abs(dp) + np.abs(delta)) + d_err)
