@@ -217,14 +217,43 @@ def run_reference(args, w, batch):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-# DRAM bytes (read + write) per launch from one ncu capture, keyed by (workload,
-# kernel), with the hash of the kernel sources the counters were taken on; a
-# record whose sources have changed since is reported as null.
+# DRAM bytes (read + write) per launch from one ncu capture (the launch list of
+# the bench command, profiles/launches_*.md), keyed by (workload, activation,
+# MXFP8, kernel), with the hash of the kernel sources the counters were taken
+# on; a record whose sources have changed since is reported as null.
+KERNEL_FILES = {"fwd": ("fwd.cu", "fwd_kernel.cuh"), "bwd_dkdv": ("bwd_dkdv.cu", "bwd_common.cuh"),
+                "bwd_dq_gemm": ("bwd_dqg.cu",), "bwd_dq": ("bwd.cu", "bwd_common.cuh"), "bwd_delta": ("aux.cu",),
+                "bwd_block": ("bwd_block.cu",)}
+KERNEL_FILES.update({n: ("aux.cu",) for n in ("mx_quant_q", "mx_quant_k", "mx_quant_v", "bwd_mx_quant_q",
+                                               "bwd_mx_quant_dout", "bwd_mx_quant_k", "bwd_mx_quant_v")})
 NCU_TRAFFIC = {
-    (2, "fwd"): (268.75e6, ("fwd.cu", "fwd_kernel.cuh"), "829d30b172bed1f8"),
-    (2, "bwd_dq"): (348.20e6, ("bwd.cu", "bwd_common.cuh"), "2d3cd5efca0bcb3c"),
-    (2, "bwd_dkdv"): (409.81e6, ("bwd_dkdv.cu", "bwd_common.cuh"), "30566429cd452b1c"),
-    (2, "bwd_delta"): (137.69e6, ("aux.cu",), "b68c404579d00663"),
+    (2, "softmax", False, "fwd"): (2.688e+08, "fe45e6159f08f846"),
+    (2, "softmax", False, "bwd_delta"): (1.378e+08, "5b3017196ed2c0ae"),
+    (2, "softmax", False, "bwd_dkdv"): (6.52e+08, "cc6ed5d8f9b2111b"),
+    (2, "softmax", False, "bwd_dq_gemm"): (3.671e+08, "dda20c5457a31c91"),
+    (3, "softmax", False, "fwd"): (5.439e+08, "fe45e6159f08f846"),
+    (3, "softmax", False, "bwd_delta"): (4.766e+08, "5b3017196ed2c0ae"),
+    (3, "softmax", False, "bwd_dkdv"): (7.053e+08, "cc6ed5d8f9b2111b"),
+    (3, "softmax", False, "bwd_dq_gemm"): (2.936e+08, "dda20c5457a31c91"),
+    (4, "silu", False, "fwd"): (9.36e+08, "fe45e6159f08f846"),
+    (4, "silu", False, "bwd_dkdv"): (1.965e+09, "cc6ed5d8f9b2111b"),
+    (4, "silu", False, "bwd_dq_gemm"): (9.018e+08, "dda20c5457a31c91"),
+    (4, "gelu_tanh", False, "fwd"): (9.361e+08, "fe45e6159f08f846"),
+    (4, "gelu_tanh", False, "bwd_dkdv"): (1.965e+09, "cc6ed5d8f9b2111b"),
+    (4, "gelu_tanh", False, "bwd_dq_gemm"): (9.018e+08, "dda20c5457a31c91"),
+    (5, "softmax", False, "fwd"): (1.12e+09, "fe45e6159f08f846"),
+    (5, "softmax", False, "bwd_block"): (1.955e+09, "8c61ef6780f5d20d"),
+    (2, "softmax", True, "mx_quant_q"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "mx_quant_k"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "mx_quant_v"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "bwd_mx_quant_q"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "bwd_mx_quant_dout"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "bwd_mx_quant_k"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "bwd_mx_quant_v"): (8.421e+07, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "fwd"): (2.693e+08, "fe45e6159f08f846"),
+    (2, "softmax", True, "bwd_delta"): (1.379e+08, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "bwd_dkdv"): (6.519e+08, "cc6ed5d8f9b2111b"),
+    (2, "softmax", True, "bwd_dq_gemm"): (3.672e+08, "dda20c5457a31c91"),
 }
 
 
@@ -237,9 +266,9 @@ def kernel_source_hash(files) -> str:
     return m.hexdigest()[:16]
 
 
-def measured_traffic(wid: int, kernel: str):
-    rec = NCU_TRAFFIC.get((wid, kernel))
-    if rec is None or kernel_source_hash(rec[1]) != rec[2]:
+def measured_traffic(wid: int, act: int, mxfp8: bool, kernel: str):
+    rec = NCU_TRAFFIC.get((wid, W.ACT_NAMES[act], bool(mxfp8), kernel))
+    if rec is None or kernel not in KERNEL_FILES or kernel_source_hash(KERNEL_FILES[kernel]) != rec[1]:
         return None
     return rec[0]
 
@@ -491,7 +520,7 @@ def run_ours(args, w, batch):
     # roofline of the dominant kernel (largest share of the step's kernel time)
     bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
     intensity = (f_fwd + f_bwd) / (bf + bb)
-    roof = roofline_of(w, batch, per_kernel, pk, pk_kind, ds=not args.device_plan)
+    roof = roofline_of(w, batch, per_kernel, pk, pk_kind, ds=not args.device_plan, mxfp8=args.mxfp8)
     eager = {"ms_per_step": eager_ms, "value": total_flops / (eager_ms * 1e-3) / 1e12, "unit": UNIT,
              "note": "the same step from eager calls (host launch work between kernels)"}
 
@@ -559,7 +588,7 @@ def run_ours(args, w, batch):
 OTHER_WORKLOADS = [(3, W.SOFTMAX), (4, W.SILU), (4, W.GELU_TANH), (5, W.SOFTMAX)]
 
 
-def roofline_of(w, batch, per_kernel, pk, pk_kind, ds=True):
+def roofline_of(w, batch, per_kernel, pk, pk_kind, ds=True, mxfp8=False):
     """Roofline record of the kernel with the largest share of the step."""
     dom = max(per_kernel, key=per_kernel.get)
     fl, by = kernel_work(w, batch, dom, pk, ds)
@@ -570,7 +599,7 @@ def roofline_of(w, batch, per_kernel, pk, pk_kind, ds=True):
     else:
         roof = {"bound": "hbm", "achieved": by / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = measured_traffic(w.wid, dom)
+    roof["traffic"] = measured_traffic(w.wid, batch.act, mxfp8, dom)
     roof["traffic_unit"] = "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)"
     roof["kernel"] = dom
     roof["peak_source"] = pk_kind + " (burst)"
@@ -629,7 +658,7 @@ def measure_other(wid, act, dev, stream, steps, flush, mxfp8=False):
     f_fwd, f_bwd = W.flops(batch.q_off, batch.kv_off, H, D, w.block, w.window)
     bf, bb = W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)
     pk, pk_kind = peaks()
-    roof = roofline_of(w, batch, per_kernel, pk, pk_kind)
+    roof = roofline_of(w, batch, per_kernel, pk, pk_kind, mxfp8=mxfp8)
     plan.close()
     return {"workload": workload_config(w, batch.act, batch.B, True)["workload"] + (", MXFP8" if mxfp8 else ""),
             "steps": steps,

@@ -60,8 +60,19 @@ def test_work_accounting():
 
 def test_traffic_record_is_keyed_to_the_sources():
     """A recorded ncu traffic figure is reported only while its kernel's sources
-    hash to the recorded value."""
-    for (wid, kernel), (value, files, digest) in bench.NCU_TRAFFIC.items():
-        expect = value if bench.kernel_source_hash(files) == digest else None
-        assert bench.measured_traffic(wid, kernel) == expect
-    assert bench.measured_traffic(99, "fwd") is None
+    hash to the recorded value; a changed source (a different digest) or an
+    unknown key gives null."""
+    acts = {v: k for k, v in W.ACT_NAMES.items()}
+    for (wid, act, mx, kernel), (value, digest) in bench.NCU_TRAFFIC.items():
+        expect = value if bench.kernel_source_hash(bench.KERNEL_FILES[kernel]) == digest else None
+        assert bench.measured_traffic(wid, acts[act], mx, kernel) == expect
+    assert bench.measured_traffic(99, W.SOFTMAX, False, "fwd") is None
+    saved = dict(bench.NCU_TRAFFIC)
+    try:
+        bench.NCU_TRAFFIC[(2, "softmax", False, "fwd")] = (1.0, "0" * 16)
+        assert bench.measured_traffic(2, W.SOFTMAX, False, "fwd") is None
+        bench.NCU_TRAFFIC[(2, "softmax", False, "fwd")] = (1.0, bench.kernel_source_hash(bench.KERNEL_FILES["fwd"]))
+        assert bench.measured_traffic(2, W.SOFTMAX, False, "fwd") == 1.0
+    finally:
+        bench.NCU_TRAFFIC.clear()
+        bench.NCU_TRAFFIC.update(saved)
