@@ -224,8 +224,7 @@ def run_reference(args, w, batch):
 KERNEL_FILES = {"fwd": ("fwd.cu", "fwd_kernel.cuh"), "bwd_dkdv": ("bwd_dkdv.cu", "bwd_common.cuh"),
                 "bwd_dq_gemm": ("bwd_dqg.cu",), "bwd_dq": ("bwd.cu", "bwd_common.cuh"), "bwd_delta": ("aux.cu",),
                 "bwd_block": ("bwd_block.cu",)}
-KERNEL_FILES.update({n: ("aux.cu",) for n in ("mx_quant_q", "mx_quant_k", "mx_quant_v", "bwd_mx_quant_q",
-                                               "bwd_mx_quant_dout", "bwd_mx_quant_k", "bwd_mx_quant_v")})
+KERNEL_FILES.update({n: ("aux.cu",) for n in ("mx_quant", "bwd_mx_quant")})
 NCU_TRAFFIC = {
     (2, "softmax", False, "fwd"): (2.688e+08, "fe45e6159f08f846"),
     (2, "softmax", False, "bwd_delta"): (1.378e+08, "5b3017196ed2c0ae"),
@@ -243,13 +242,6 @@ NCU_TRAFFIC = {
     (4, "gelu_tanh", False, "bwd_dq_gemm"): (9.018e+08, "dda20c5457a31c91"),
     (5, "softmax", False, "fwd"): (1.12e+09, "fe45e6159f08f846"),
     (5, "softmax", False, "bwd_block"): (1.955e+09, "8c61ef6780f5d20d"),
-    (2, "softmax", True, "mx_quant_q"): (8.421e+07, "5b3017196ed2c0ae"),
-    (2, "softmax", True, "mx_quant_k"): (8.421e+07, "5b3017196ed2c0ae"),
-    (2, "softmax", True, "mx_quant_v"): (8.421e+07, "5b3017196ed2c0ae"),
-    (2, "softmax", True, "bwd_mx_quant_q"): (8.421e+07, "5b3017196ed2c0ae"),
-    (2, "softmax", True, "bwd_mx_quant_dout"): (8.421e+07, "5b3017196ed2c0ae"),
-    (2, "softmax", True, "bwd_mx_quant_k"): (8.421e+07, "5b3017196ed2c0ae"),
-    (2, "softmax", True, "bwd_mx_quant_v"): (8.421e+07, "5b3017196ed2c0ae"),
     (2, "softmax", True, "fwd"): (2.693e+08, "fe45e6159f08f846"),
     (2, "softmax", True, "bwd_delta"): (1.379e+08, "5b3017196ed2c0ae"),
     (2, "softmax", True, "bwd_dkdv"): (6.519e+08, "cc6ed5d8f9b2111b"),
@@ -282,7 +274,7 @@ def kernel_names(w, act, device_plan=False, broadcast_q=False, mxfp8=False):
     """The kernels one step launches, in order (the library takes the dS-chunk
     backward for full attention on a host plan without a window, given the full
     workspace as the bench does).  MXFP8: the forward first quantises Q, K, V,
-    the backward Q, dO, K, V."""
+    the backward Q, dO, K, V (one launch each)."""
     if w.block:
         return list(KERNELS_BLOCK)
     ds = not w.window and not device_plan
@@ -290,9 +282,8 @@ def kernel_names(w, act, device_plan=False, broadcast_q=False, mxfp8=False):
     if broadcast_q:  # the per-sequence dQ rows are summed by one more kernel
         names.insert(names.index("bwd_dq_gemm" if ds else "bwd_dq") + 1, "bwd_dq_reduce")
     if mxfp8:
-        names = ["mx_quant_q", "mx_quant_k", "mx_quant_v"] + names
-        names[names.index("fwd") + 1:names.index("fwd") + 1] = ["bwd_mx_quant_q", "bwd_mx_quant_dout",
-                                                               "bwd_mx_quant_k", "bwd_mx_quant_v"]
+        names = ["mx_quant"] + names
+        names.insert(names.index("fwd") + 1, "bwd_mx_quant")
     return names
 
 
@@ -309,9 +300,10 @@ def kernel_work(w, batch, name, pk, ds=True):
         return 10.0 * D * H * p, W.hbm_bytes(batch.q_off, batch.kv_off, H, D, batch.act, w.block)[1]
     if name == "bwd_delta":
         return 0.0, 2.0 * Tq * e + 4.0 * H * Tq
-    if name.startswith("mx_quant_") or name.startswith("bwd_mx_quant_"):  # bf16 rows in, their MXFP8 values out
-        rows = Tk if name.endswith(("_k", "_v")) else Tq
-        return 0.0, 2.0 * rows * e
+    if name == "mx_quant":  # Q, K, V bf16 rows in, their MXFP8 values out (bf16)
+        return 0.0, 2.0 * (Tq + 2 * Tk) * e
+    if name == "bwd_mx_quant":  # Q, dO, K, V
+        return 0.0, 2.0 * (2 * Tq + 2 * Tk) * e
     if name == "bwd_dq_reduce":  # fp32 per-sequence dQ rows in, the shared rows' bf16 sum out
         return 0.0, 4.0 * Tq * H * D + 2.0 * w.q_rows_shared * H * D
     # the dS chunks (bf16 per valid pair and head; activation modes: hi and lo)

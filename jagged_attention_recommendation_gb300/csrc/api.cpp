@@ -208,6 +208,16 @@ jattn_status cuda_status(cudaError_t e, const char *where = "") {
         if (e_ != cudaSuccess) return cuda_status(e_, #expr); \
     } while (0)
 
+// MXFP8 quantisation job over one side's tile list (host-planned plans only)
+void add_mx_job(MxJobs &jobs, const jattn_plan *p, int which, const void *x, void *xq) {
+    const int j = jobs.n++;
+    jobs.x[j] = x;
+    jobs.xq[j] = xq;
+    jobs.tiles[j] = reinterpret_cast<const Tile *>(p->d_buf + p->off_tiles[which]);
+    jobs.ntiles[j] = static_cast<int32_t>(p->tiles[which].size());
+    jobs.kv_side[j] = which == JATTN_TILES_KV;
+}
+
 jattn_status note_error(const char *where) {
     std::snprintf(g_last_cuda_error, sizeof(g_last_cuda_error), "%s", where);
     return JATTN_ERR_CUDA;
@@ -752,11 +762,11 @@ jattn_status jattn_fwd_rope(const jattn_plan *p, const void *q, const void *k, c
     if (p->mode.mxfp8) {  // Q, K, V replaced by the values of their MXFP8 quantisation
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         void *qs = ws, *ks = ws + mx_copy_bytes(p, p->Tq), *vs = ws + mx_copy_bytes(p, p->Tq) + mx_copy_bytes(p, p->Tk);
-        const int32_t *dqo = reinterpret_cast<const int32_t *>(p->d_buf + p->off_qoff);
-        const int32_t *dko = reinterpret_cast<const int32_t *>(p->d_buf + p->off_kvoff);
-        CUDA_TRY(log.done(launch_mx_quant(q, dqo, p->B, p->H, p->D, qs, st)));
-        CUDA_TRY(log.done(launch_mx_quant(k, dko, p->B, p->H, p->D, ks, st)));
-        CUDA_TRY(log.done(launch_mx_quant(v, dko, p->B, p->H, p->D, vs, st)));
+        MxJobs jobs{};
+        add_mx_job(jobs, p, JATTN_TILES_Q, q, qs);
+        add_mx_job(jobs, p, JATTN_TILES_KV, k, ks);
+        add_mx_job(jobs, p, JATTN_TILES_KV, v, vs);
+        CUDA_TRY(log.done(launch_mx_quant(jobs, p->H, p->D, st)));
         qq = qs;
         kk = ks;
         vv = vs;
@@ -858,12 +868,12 @@ jattn_status jattn_bwd_rope(const jattn_plan *p, const void *dout, const void *q
         uint8_t *mx = static_cast<uint8_t *>(workspace) + base;
         void *qs = mx, *ds_ = mx + mx_copy_bytes(p, p->Tq), *ks = mx + 2 * mx_copy_bytes(p, p->Tq);
         void *vs = mx + 2 * mx_copy_bytes(p, p->Tq) + mx_copy_bytes(p, p->Tk);
-        const int32_t *dqo = reinterpret_cast<const int32_t *>(p->d_buf + p->off_qoff);
-        const int32_t *dko = reinterpret_cast<const int32_t *>(p->d_buf + p->off_kvoff);
-        if (log.done(launch_mx_quant(q, dqo, p->B, p->H, p->D, qs, st)) != cudaSuccess ||
-            log.done(launch_mx_quant(dout, dqo, p->B, p->H, p->D, ds_, st)) != cudaSuccess ||
-            log.done(launch_mx_quant(k, dko, p->B, p->H, p->D, ks, st)) != cudaSuccess ||
-            log.done(launch_mx_quant(v, dko, p->B, p->H, p->D, vs, st)) != cudaSuccess)
+        MxJobs jobs{};
+        add_mx_job(jobs, p, JATTN_TILES_Q, q, qs);
+        add_mx_job(jobs, p, JATTN_TILES_Q, dout, ds_);
+        add_mx_job(jobs, p, JATTN_TILES_KV, k, ks);
+        add_mx_job(jobs, p, JATTN_TILES_KV, v, vs);
+        if (log.done(launch_mx_quant(jobs, p->H, p->D, st)) != cudaSuccess)
             return note_error("jattn_bwd: MXFP8 quantisation launch");
         qq = qs;
         dd = ds_;
@@ -1087,10 +1097,10 @@ jattn_status jattn_mxfp8_quantize(const jattn_plan *p, const void *x, int32_t wh
     if (!guard.ok) return note_error("jattn_mxfp8_quantize: cudaSetDevice failed");
     (void)cudaGetLastError();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int32_t *off =
-        reinterpret_cast<const int32_t *>(p->d_buf + (which == JATTN_TILES_Q ? p->off_qoff : p->off_kvoff));
+    MxJobs jobs{};
+    add_mx_job(jobs, p, which, x, xq);
     LaunchLog log(p, st);
-    return cuda_status(log.done(launch_mx_quant(x, off, p->B, p->H, p->D, xq, st)),
+    return cuda_status(log.done(launch_mx_quant(jobs, p->H, p->D, st)),
                        "jattn_mxfp8_quantize: kernel launch");
 }
 

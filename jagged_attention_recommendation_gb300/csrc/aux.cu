@@ -71,60 +71,88 @@ __global__ void delta_kernel(const T *__restrict__ out, const T *__restrict__ do
     }
 }
 
-// MXFP8 quantisation of x [T, H, D] (bf16) per sequence and head, in blocks of
-// 32 local rows x 32 features: xq receives the values the quantised blocks
-// stand for (bf16, exact).  A CTA takes one (sequence, head) at a time; each
-// warp takes one block: lane = row, the block's largest magnitude by a warp
-// reduction.
-__global__ void mx_quant_kernel(const __nv_bfloat16 *__restrict__ x, const int32_t *__restrict__ off, int B, int H,
-                                int D, __nv_bfloat16 *__restrict__ xq) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int fbs = D / 32;
-    for (int64_t bh = blockIdx.x; bh < static_cast<int64_t>(B) * H; bh += gridDim.x) {
-        const int b = static_cast<int>(bh / H), h = static_cast<int>(bh - static_cast<int64_t>(b) * H);
-        const int r0 = off[b], L = off[b + 1] - r0;
-        const int ntask = ((L + 31) / 32) * fbs;
-        for (int task = warp; task < ntask; task += nw) {
-            const int rb = task / fbs, fb = task - rb * fbs;
-            const int row = rb * 32 + lane;
-            const bool ok = row < L;
-            const int64_t base = (static_cast<int64_t>(r0 + row) * H + h) * D + fb * 32;
-            float v[32];
-            if (ok) {
+// MXFP8 quantisation of up to four tensors x [T, H, D] (bf16) per sequence and
+// head, in blocks of 32 local rows x 32 features: xq receives the values the
+// quantised blocks stand for (bf16, exact).  The work items are the plan's
+// 128-row tiles of each tensor's side (every tile is one sequence and head,
+// and starts at a multiple of 128 local rows, so its 32-row slices are the
+// blocks' rows).  A CTA takes one tile, each of its four warps one 32-row
+// slice, all D features: a warp instruction reads whole rows' D features (16
+// bytes a lane, D / 8 lanes a row), so every load and store is row-contiguous.
+// A block's largest magnitude comes from the four lanes of its 32 features
+// over the slice's rows, by butterfly shuffles.  Each lane holds its 32 rows'
+// loads at once (D = 128: 64 registers), so the launch bound keeps three CTAs
+// on an SM without spilling.
+__device__ __forceinline__ uint32_t mx_qdq_bf16x2(uint32_t w, float down, float up) {
+    const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+    const __nv_fp8x2_storage_t q = __nv_cvt_float2_to_fp8x2(make_float2(lo * down, hi * down), __NV_SATFINITE, __NV_E4M3);
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+    return dev::pack_bf16x2(f.x * up, f.y * up);
+}
+
+__device__ __forceinline__ float amax_bf16x2(float a, uint32_t w) {
+    return fmaxf(a, fmaxf(fabsf(__uint_as_float(w << 16)), fabsf(__uint_as_float(w & 0xffff0000u))));
+}
+
+template <int D>
+__global__ void __launch_bounds__(128, 3) mx_quant_kernel(const __grid_constant__ MxJobs jobs, int H) {
+    constexpr int LPR = D / 8;     // lanes per row, 16 bytes each
+    constexpr int RPI = 32 / LPR;  // rows per warp instruction
+    constexpr int NI = 32 / RPI;   // instructions per 32-row slice
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sub = lane / LPR, c = lane % LPR;
+    int total = 0;
+    for (int j = 0; j < jobs.n; ++j) total += jobs.ntiles[j];
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+        int j = 0, i = t;
+        while (j + 1 < jobs.n && i >= jobs.ntiles[j]) i -= jobs.ntiles[j++];
+        const Tile tile = jobs.tiles[j][i];
+        const int start = jobs.kv_side[j] ? tile.kv_start : tile.q_start;
+        const int n = min(32, (jobs.kv_side[j] ? tile.kv_len : tile.q_len) - 32 * warp);
+        if (n <= 0) continue;
+        const int64_t rs = static_cast<int64_t>(H) * D;
+        const int64_t base = (static_cast<int64_t>(start + 32 * warp) * H + tile.h) * D + c * 8;
+        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(jobs.x[j]) + base;
+        uint4 w[NI];
+        float a = 0.0f;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 w = __ldg(reinterpret_cast<const uint4 *>(x + base) + k);
-                    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        for (int k = 0; k < NI; ++k) {
+            const int row = k * RPI + sub;
+            w[k] = row < n ? __ldg(reinterpret_cast<const uint4 *>(src + row * rs)) : make_uint4(0u, 0u, 0u, 0u);
+        }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        v[8 * k + 2 * j] = __uint_as_float(ws[j] << 16);
-                        v[8 * k + 2 * j + 1] = __uint_as_float(ws[j] & 0xffff0000u);
-                    }
-                }
-            } else {
+        for (int k = 0; k < NI; ++k) a = amax_bf16x2(amax_bf16x2(amax_bf16x2(amax_bf16x2(a, w[k].x), w[k].y), w[k].z), w[k].w);
+        // the block's lanes: the four of its features (lane bits 0, 1) on every row group
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = 0.0f;
-            }
-            const int e = dev::mx_exponent(dev::warp_max_nonneg(dev::amax32(v)));
-            dev::mx_qdq32(v, e);
-            if (ok) {
+        for (int m = LPR; m < 32; m <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, m));
+        const int e = dev::mx_exponent(a);
+        const float down = dev::pow2i(-e), up = dev::pow2i(e);
+        __nv_bfloat16 *dst = static_cast<__nv_bfloat16 *>(jobs.xq[j]) + base;
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    reinterpret_cast<uint4 *>(xq + base)[k] =
-                        make_uint4(dev::pack_bf16x2(v[8 * k], v[8 * k + 1]), dev::pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                                   dev::pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
-                                   dev::pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
-            }
+        for (int k = 0; k < NI; ++k) {
+            const int row = k * RPI + sub;
+            if (row < n)
+                *reinterpret_cast<uint4 *>(dst + row * rs) =
+                    make_uint4(mx_qdq_bf16x2(w[k].x, down, up), mx_qdq_bf16x2(w[k].y, down, up),
+                               mx_qdq_bf16x2(w[k].z, down, up), mx_qdq_bf16x2(w[k].w, down, up));
         }
     }
 }
 
-cudaError_t launch_mx_quant(const void *x, const int32_t *off, int B, int H, int D, void *xq, cudaStream_t stream) {
-    if (B <= 0 || D % 32 != 0) return B <= 0 ? cudaSuccess : cudaErrorInvalidValue;
-    const int64_t want = static_cast<int64_t>(B) * H;
-    const int blocks = static_cast<int>(std::min<int64_t>(want, 152 * 8));
-    mx_quant_kernel<<<blocks, 256, 0, stream>>>(static_cast<const __nv_bfloat16 *>(x), off, B, H, D,
-                                                static_cast<__nv_bfloat16 *>(xq));
+cudaError_t launch_mx_quant(const MxJobs &jobs, int H, int D, cudaStream_t stream) {
+    int64_t total = 0;
+    for (int j = 0; j < jobs.n; ++j) total += jobs.ntiles[j];
+    if (total == 0) return cudaSuccess;
+    if (jobs.n < 1 || jobs.n > 4 || (D != 64 && D != 128)) return cudaErrorInvalidValue;
+    // about one tile per CTA: the hardware hands tiles to SMs as CTAs finish
+    const int blocks = static_cast<int>(std::min<int64_t>(total, 152 * 64));
+    if (D == 128)
+        mx_quant_kernel<128><<<blocks, 128, 0, stream>>>(jobs, H);
+    else
+        mx_quant_kernel<64><<<blocks, 128, 0, stream>>>(jobs, H);
     return cudaGetLastError();
 }
 

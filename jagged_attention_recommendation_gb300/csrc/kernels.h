@@ -64,9 +64,19 @@ cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_c
 cudaError_t launch_delta(const void *out, const void *dout, int f32, int64_t Tq, int H, int D, float *delta,
                          cudaStream_t stream);
 
-// MXFP8 quantisation (32 local rows x 32 features per block) of x [T, H, D] bf16
-// under the device offsets off [B + 1]: xq = the quantised values, bf16
-cudaError_t launch_mx_quant(const void *x, const int32_t *off, int B, int H, int D, void *xq, cudaStream_t stream);
+// MXFP8 quantisation (32 local rows x 32 features per block) of up to four
+// tensors x [T, H, D] bf16: job j quantises x[j] into xq[j] over the plan's
+// device tile list tiles[j] (ntiles[j] tiles of 128 rows; kv_side[j]: the
+// tiles' key rows, else their query rows).  D is 64 or 128.
+struct MxJobs {
+    const void *x[4];  // bf16
+    void *xq[4];       // bf16
+    const Tile *tiles[4];
+    int32_t ntiles[4];
+    int32_t kv_side[4];
+    int32_t n;
+};
+cudaError_t launch_mx_quant(const MxJobs &jobs, int H, int D, cudaStream_t stream);
 
 // src [rows, D] (bf16 or fp32) -> dst [rows, Dp] bf16, zero-padded columns D..Dp-1
 cudaError_t launch_stage(const void *src, int f32, int64_t rows, int D, int Dp, void *dst, cudaStream_t stream);
