@@ -227,11 +227,11 @@ KERNEL_FILES = {"fwd": ("fwd.cu", "fwd_kernel.cuh"), "bwd_dkdv": ("bwd_dkdv.cu",
 KERNEL_FILES.update({n: ("aux.cu",) for n in ("mx_quant", "bwd_mx_quant")})
 NCU_TRAFFIC = {
     (2, "softmax", False, "fwd"): (2.688e+08, "fe45e6159f08f846"),
-    (2, "softmax", False, "bwd_delta"): (1.378e+08, "5b3017196ed2c0ae"),
+    (2, "softmax", False, "bwd_delta"): (1.377e+08, "73313212df416eda"),
     (2, "softmax", False, "bwd_dkdv"): (6.52e+08, "cc6ed5d8f9b2111b"),
     (2, "softmax", False, "bwd_dq_gemm"): (3.671e+08, "dda20c5457a31c91"),
     (3, "softmax", False, "fwd"): (5.439e+08, "fe45e6159f08f846"),
-    (3, "softmax", False, "bwd_delta"): (4.766e+08, "5b3017196ed2c0ae"),
+    (3, "softmax", False, "bwd_delta"): (4.766e+08, "73313212df416eda"),
     (3, "softmax", False, "bwd_dkdv"): (7.053e+08, "cc6ed5d8f9b2111b"),
     (3, "softmax", False, "bwd_dq_gemm"): (2.936e+08, "dda20c5457a31c91"),
     (4, "silu", False, "fwd"): (9.36e+08, "fe45e6159f08f846"),
@@ -243,7 +243,9 @@ NCU_TRAFFIC = {
     (5, "softmax", False, "fwd"): (1.12e+09, "fe45e6159f08f846"),
     (5, "softmax", False, "bwd_block"): (1.955e+09, "8c61ef6780f5d20d"),
     (2, "softmax", True, "fwd"): (2.693e+08, "fe45e6159f08f846"),
-    (2, "softmax", True, "bwd_delta"): (1.379e+08, "5b3017196ed2c0ae"),
+    (2, "softmax", True, "mx_quant"): (3.613e+08, "73313212df416eda"),
+    (2, "softmax", True, "bwd_mx_quant"): (4.996e+08, "73313212df416eda"),
+    (2, "softmax", True, "bwd_delta"): (1.379e+08, "73313212df416eda"),
     (2, "softmax", True, "bwd_dkdv"): (6.519e+08, "cc6ed5d8f9b2111b"),
     (2, "softmax", True, "bwd_dq_gemm"): (3.672e+08, "dda20c5457a31c91"),
 }
