@@ -290,19 +290,25 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t buf = np & 1;
                     if (!(ok = mbar_wait(&ds_full[buf], (np >> 1) & 1, err))) break;
                     tc_fence_after();
-                    const int ksteps = round_up16(min(C::BN, tb.kv_len - jb * C::BN)) / 16;
+                    const int ksteps = (min(C::BN, tb.kv_len - jb * C::BN) + 15) >> 4;
                     const uint32_t ks = np % C::NSK;
                     const uint64_t bd0 = sdesc_sw128(sK + ks * C::KV_BYTES, C::SUB_KV, 1024);
                     const uint32_t aS = tmem + buf * 128;
-                    for (int k = 0; k < ksteps; ++k) {
-                        const uint64_t bd = sdesc_add(bd0, k * 2048);
-                        const uint32_t acc = (jb > 0 || k > 0) ? 1u : 0u;
-                        if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
-                            mma_bf16_ts(dq, aS + k * 16, bd, idesc_dq, acc);
-                            mma_bf16_ts(dq, aS + k * 16 + 8, bd, idesc_dq, 1u);
-                        } else {
-                            // 32-key chunk k / 2 keeps its bf16 pairs in its own first 16 columns
-                            mma_bf16_ts(dq, aS + (k >> 1) * 32 + (k & 1) * 8, bd, idesc_dq, acc);
+                    const uint32_t acc0 = jb > 0 ? 1u : 0u;
+                    // fully unrolled with a guard per step (constant operand offsets), so
+                    // the products issue as fast as the tensor pipe takes them
+#pragma unroll
+                    for (int k = 0; k < C::BN / 16; ++k) {
+                        if (k < ksteps) {
+                            const uint64_t bd = sdesc_add(bd0, k * 2048);
+                            const uint32_t acc = k > 0 ? 1u : acc0;
+                            if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                                mma_bf16_ts(dq, aS + k * 16, bd, idesc_dq, acc);
+                                mma_bf16_ts(dq, aS + k * 16 + 8, bd, idesc_dq, 1u);
+                            } else {
+                                // 32-key chunk k / 2 keeps its bf16 pairs in its own first 16 columns
+                                mma_bf16_ts(dq, aS + (k >> 1) * 32 + (k & 1) * 8, bd, idesc_dq, acc);
+                            }
                         }
                     }
                     mma_commit(&k_empty[ks]);     // S and dQ were the K slot's readers

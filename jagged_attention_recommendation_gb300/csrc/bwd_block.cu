@@ -177,42 +177,54 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                 const uint32_t base = sIn + buf * C::IN_BYTES;
                 const int n16 = round_up16(t.q_len);
                 const uint32_t idesc_s = idesc_bf16(128, n16, false, false);
+                // Descriptors are built once per tile and the product runs are fully
+                // unrolled (a guard per step where the count varies): constant offsets
+                // and nothing else between two products, so this one thread issues them
+                // as fast as the tensor pipe takes them.
+                const uint64_t kQ = sdesc_sw128(base + C::IQ, 16, 1024), kK = sdesc_sw128(base + C::IK, 16, 1024);
+                const uint64_t kDO = sdesc_sw128(base + C::IDO, 16, 1024), kV = sdesc_sw128(base + C::IV, 16, 1024);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
                     const uint32_t o = (ks >> 2) * C::SUB + (ks & 3) * 32;
-                    mma_bf16_ss(tmem + C::COL_S, sdesc_sw128(base + C::IQ + o, 16, 1024),
-                                sdesc_sw128(base + C::IK + o, 16, 1024), idesc_s, ks > 0);
-                    mma_bf16_ss(tmem + C::COL_DP, sdesc_sw128(base + C::IDO + o, 16, 1024),
-                                sdesc_sw128(base + C::IV + o, 16, 1024), idesc_s, ks > 0);
+                    mma_bf16_ss(tmem + C::COL_S, sdesc_add(kQ, o), sdesc_add(kK, o), idesc_s, ks > 0);
+                    mma_bf16_ss(tmem + C::COL_DP, sdesc_add(kDO, o), sdesc_add(kV, o), idesc_s, ks > 0);
                 }
                 mma_commit(s_full);
                 if (!(ok = mbar_wait(pd_full, t_local & 1, err))) break;
                 tc_fence_after();
                 const int ksteps = n16 / 16;
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    // dV += P^T dO and dK += dS^T Q: reduction over query rows ks*16..+15
-                    const uint32_t acc = ks > 0 ? 1u : 0u;
-                    mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sP + ks * 2048, C::SUB, 1024),
-                                sdesc_sw128(base + C::IDO + ks * 2048, C::SUB, 1024), idesc_mn, acc);
-                    if (ACT)  // unnormalised P: its bf16 remainder, in the lo plane for now
-                        mma_bf16_ss(tmem + C::COL_DV, sdesc_sw128(sDSlo + ks * 2048, C::SUB, 1024),
-                                    sdesc_sw128(base + C::IDO + ks * 2048, C::SUB, 1024), idesc_mn, 1u);
-                    mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDS + ks * 2048, C::SUB, 1024),
-                                sdesc_sw128(base + C::IQ + ks * 2048, C::SUB, 1024), idesc_mn, acc);
-                    // dQ += dS K: reduction over key rows ks*16..+15
-                    mma_bf16_ss(tmem + C::COL_S, sdesc_sw128(sDS + (ks >> 2) * C::SUB + (ks & 3) * 32, 16, 1024),
-                                sdesc_sw128(base + C::IK + ks * 2048, C::SUB, 1024), idesc_kmn, acc);
+                const uint64_t mP = sdesc_sw128(sP, C::SUB, 1024), mDS = sdesc_sw128(sDS, C::SUB, 1024);
+                const uint64_t mDSlo = sdesc_sw128(sDSlo, C::SUB, 1024), kDS = sdesc_sw128(sDS, 16, 1024);
+                const uint64_t kDSlo = sdesc_sw128(sDSlo, 16, 1024);
+                const uint64_t mDO = sdesc_sw128(base + C::IDO, C::SUB, 1024), mQ = sdesc_sw128(base + C::IQ, C::SUB, 1024);
+                const uint64_t mK = sdesc_sw128(base + C::IK, C::SUB, 1024);
+#pragma unroll
+                for (int ks = 0; ks < C::BM / 16; ++ks) {
+                    if (ks < ksteps) {
+                        // dV += P^T dO and dK += dS^T Q: reduction over query rows ks*16..+15
+                        const uint32_t acc = ks > 0 ? 1u : 0u;
+                        mma_bf16_ss(tmem + C::COL_DV, sdesc_add(mP, ks * 2048), sdesc_add(mDO, ks * 2048), idesc_mn, acc);
+                        if (ACT)  // unnormalised P: its bf16 remainder, in the lo plane for now
+                            mma_bf16_ss(tmem + C::COL_DV, sdesc_add(mDSlo, ks * 2048), sdesc_add(mDO, ks * 2048),
+                                        idesc_mn, 1u);
+                        mma_bf16_ss(tmem + C::COL_DK, sdesc_add(mDS, ks * 2048), sdesc_add(mQ, ks * 2048), idesc_mn, acc);
+                        // dQ += dS K: reduction over key rows ks*16..+15
+                        mma_bf16_ss(tmem + C::COL_S, sdesc_add(kDS, (ks >> 2) * C::SUB + (ks & 3) * 32),
+                                    sdesc_add(mK, ks * 2048), idesc_kmn, acc);
+                    }
                 }
                 if (ACT) {  // unnormalised dS: add its bf16 remainder to dK and dQ
                     mma_commit(lo_free);
                     if (!(ok = mbar_wait(dslo_full, t_local & 1, err))) break;
                     tc_fence_after();
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        mma_bf16_ss(tmem + C::COL_DK, sdesc_sw128(sDSlo + ks * 2048, C::SUB, 1024),
-                                    sdesc_sw128(base + C::IQ + ks * 2048, C::SUB, 1024), idesc_mn, 1u);
-                        mma_bf16_ss(tmem + C::COL_S,
-                                    sdesc_sw128(sDSlo + (ks >> 2) * C::SUB + (ks & 3) * 32, 16, 1024),
-                                    sdesc_sw128(base + C::IK + ks * 2048, C::SUB, 1024), idesc_kmn, 1u);
+#pragma unroll
+                    for (int ks = 0; ks < C::BM / 16; ++ks) {
+                        if (ks < ksteps) {
+                            mma_bf16_ss(tmem + C::COL_DK, sdesc_add(mDSlo, ks * 2048), sdesc_add(mQ, ks * 2048),
+                                        idesc_mn, 1u);
+                            mma_bf16_ss(tmem + C::COL_S, sdesc_add(kDSlo, (ks >> 2) * C::SUB + (ks & 3) * 32),
+                                        sdesc_add(mK, ks * 2048), idesc_kmn, 1u);
+                        }
                     }
                 }
                 mma_commit(&in_empty[buf]);

@@ -290,33 +290,43 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t buf = np & 1;
                     if (!(ok = mbar_wait(&p_full[buf], (np >> 1) & 1, err))) break;
                     tc_fence_after();
-                    const int ksteps = round_up16(min(C::BQ, tb.q_len - ib * C::BQ)) / 16;
+                    const int ksteps = (min(C::BQ, tb.q_len - ib * C::BQ) + 15) >> 4;
                     const uint32_t slot = np % C::NSQ;
                     const uint32_t qb = sQ + slot * 2 * C::Q_BYTES;
                     const uint64_t bq0 = sdesc_sw128(qb, C::SUB_Q, 1024);
                     const uint64_t bdo0 = sdesc_sw128(qb + C::Q_BYTES, C::SUB_Q, 1024);
                     const uint32_t aP = tmem + buf * 128, aDS = aP + 64;
-                    for (int k = 0; k < ksteps; ++k) {
-                        const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
-                        const uint64_t bdo = sdesc_add(bdo0, k * 2048);
-                        if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
-                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
-                            mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
-                        } else {
-                            // 32-query chunk k / 2 keeps its bf16 pairs in its own first 16 columns
-                            mma_bf16_ts(tmem + C::COL_DV, aP + (k >> 1) * 32 + (k & 1) * 8, bdo, idesc_acc, acc);
+                    const uint32_t acc0 = ib > 0 ? 1u : 0u;
+                    // Both product runs are fully unrolled with a guard per step: constant
+                    // operand offsets and nothing else between two products, so this one
+                    // thread issues them as fast as the tensor pipe takes them.
+#pragma unroll
+                    for (int k = 0; k < C::BQ / 16; ++k) {
+                        if (k < ksteps) {
+                            const uint32_t acc = k > 0 ? 1u : acc0;
+                            const uint64_t bdo = sdesc_add(bdo0, k * 2048);
+                            if (ACT) {  // hi at columns 16 k .. +7, lo at 16 k + 8 .. +15
+                                mma_bf16_ts(tmem + C::COL_DV, aP + k * 16, bdo, idesc_acc, acc);
+                                mma_bf16_ts(tmem + C::COL_DV, aP + k * 16 + 8, bdo, idesc_acc, 1u);
+                            } else {
+                                // 32-query chunk k / 2 keeps its bf16 pairs in its own first 16 columns
+                                mma_bf16_ts(tmem + C::COL_DV, aP + (k >> 1) * 32 + (k & 1) * 8, bdo, idesc_acc, acc);
+                            }
                         }
                     }
                     // ... and dK of the previous tile before the tile's first dK product
                     if (ib == 0 && !(ok = mbar_wait(dk_empty, (tb_n & 1) ^ 1, err))) break;
-                    for (int k = 0; k < ksteps; ++k) {
-                        const uint32_t acc = (ib > 0 || k > 0) ? 1u : 0u;
-                        const uint64_t bq = sdesc_add(bq0, k * 2048);
-                        if (ACT) {
-                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
-                            mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
-                        } else {
-                            mma_bf16_ts(tmem + C::COL_DK, aDS + (k >> 1) * 32 + (k & 1) * 8, bq, idesc_acc, acc);
+#pragma unroll
+                    for (int k = 0; k < C::BQ / 16; ++k) {
+                        if (k < ksteps) {
+                            const uint32_t acc = k > 0 ? 1u : acc0;
+                            const uint64_t bq = sdesc_add(bq0, k * 2048);
+                            if (ACT) {
+                                mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16, bq, idesc_acc, acc);
+                                mma_bf16_ts(tmem + C::COL_DK, aDS + k * 16 + 8, bq, idesc_acc, 1u);
+                            } else {
+                                mma_bf16_ts(tmem + C::COL_DK, aDS + (k >> 1) * 32 + (k & 1) * 8, bq, idesc_acc, acc);
+                            }
                         }
                     }
                     mma_commit(&qs_empty[slot]);  // last reads of the Q / dO slot

@@ -171,14 +171,19 @@ __global__ void __launch_bounds__(256, 1)
                     tc_fence_after();
                     const uint32_t st = sbase + slot * C::STAGE;
                     const uint64_t bd0 = sdesc_sw128(st + C::A_BYTES, C::SUB_K, 1024);
-                    const int ksteps = round_up16(min(C::BK, lk - kt * C::BK)) / 16;
-                    for (int k = 0; k < ksteps; ++k) {
-                        const uint32_t acc = (kt > 0 || k > 0) ? 1u : 0u;
-                        const uint64_t bd = sdesc_add(bd0, k * 2048);
+                    const int ksteps = (min(C::BK, lk - kt * C::BK) + 15) >> 4;
+                    const uint32_t acc0 = kt > 0 ? 1u : 0u;
+                    const uint64_t ad0 = sdesc_sw128(st, kDsChunkBytes, 1024);
+                    // fully unrolled with a guard per step (constant operand offsets), so
+                    // the products issue as fast as the tensor pipe takes them
 #pragma unroll
-                        for (int p = 0; p < PLANES; ++p) {
-                            const uint64_t ad = sdesc_sw128(st + p * 2 * kDsChunkBytes + k * 2048, kDsChunkBytes, 1024);
-                            mma_bf16_ss(dq, ad, bd, idesc, p > 0 ? 1u : acc);
+                    for (int k = 0; k < C::BK / 16; ++k) {
+                        if (k < ksteps) {
+                            const uint32_t acc = k > 0 ? 1u : acc0;
+                            const uint64_t bd = sdesc_add(bd0, k * 2048);
+#pragma unroll
+                            for (int p = 0; p < PLANES; ++p)
+                                mma_bf16_ss(dq, sdesc_add(ad0, p * 2 * kDsChunkBytes + k * 2048), bd, idesc, p > 0 ? 1u : acc);
                         }
                     }
                     mma_commit(&empty[slot]);

@@ -366,22 +366,29 @@ __global__ void __launch_bounds__(512, 1)
                     const int nvalid = min(C::BN, tb.kv_len - jb * C::BN);
                     const uint64_t bd0 = sdesc_sw128(sV + slot * C::KV_BYTES, C::SUB_KV, 1024);
                     const uint32_t aP = tmem + C::COL_S + buf * C::BN;
+                    // Fully unrolled with a guard per step: every operand offset is a
+                    // constant and nothing but the guard runs between two products, so
+                    // one thread issues them as fast as the tensor pipe takes them (a
+                    // loop with a run-time trip count throttles it to about half).
+                    const uint32_t acc0 = jb > 0 ? 1u : 0u;  // the tile's first block starts O_grp
 #pragma unroll
                     for (int grp = 0; grp < 2; ++grp) {
                         // group grp's keys 64 grp .. of the block; its 16-key step ks is
                         // block step 4 grp + ks, whose P sits in 32-key chunk (4 grp + ks) / 2
-                        const int keys = min(64, nvalid - 64 * grp);
-                        const int ksteps = keys > 0 ? round_up16(keys) / 16 : 0;
+                        const int ksteps = (min(64, nvalid - 64 * grp) + 15) >> 4;  // <= 0: none
                         const uint32_t dO = tmem + C::COL_O + grp * D;
-                        for (int ks = 0; ks < ksteps; ++ks) {
-                            const int st = 4 * grp + ks;
-                            const uint64_t bd = sdesc_add(bd0, st * 2048);
-                            const uint32_t acc = (jb > 0 || ks > 0) ? 1u : 0u;  // the tile's first block starts O_grp
-                            if (ACT) {  // hi at columns 16 st .. +7, lo at 16 st + 8 .. +15
-                                mma_bf16_ts(dO, aP + st * 16, bd, idesc_pv, acc);
-                                mma_bf16_ts(dO, aP + st * 16 + 8, bd, idesc_pv, 1u);
-                            } else {
-                                mma_bf16_ts(dO, aP + (st >> 1) * 32 + (st & 1) * 8, bd, idesc_pv, acc);
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            if (ks < ksteps) {
+                                const int st = 4 * grp + ks;
+                                const uint64_t bd = sdesc_add(bd0, st * 2048);
+                                const uint32_t acc = ks > 0 ? 1u : acc0;
+                                if (ACT) {  // hi at columns 16 st .. +7, lo at 16 st + 8 .. +15
+                                    mma_bf16_ts(dO, aP + st * 16, bd, idesc_pv, acc);
+                                    mma_bf16_ts(dO, aP + st * 16 + 8, bd, idesc_pv, 1u);
+                                } else {
+                                    mma_bf16_ts(dO, aP + (st >> 1) * 32 + (st & 1) * 8, bd, idesc_pv, acc);
+                                }
                             }
                         }
                     }
