@@ -40,7 +40,10 @@ struct DqgCfg {
     // full[NS], empty[NS], acc_full[2], acc_empty[2], drain
     static constexpr int NBAR = 2 * NS + 5;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-    static constexpr uint32_t SMEM = OFF_MISC + 16;
+    // per output warp: 32 rows x 64 bf16 staging for row-contiguous stores
+    static constexpr int STG_W = 64;
+    static constexpr uint32_t OFF_STG = (OFF_MISC + 16 + 127) & ~127u;
+    static constexpr uint32_t SMEM = OFF_STG + 4 * 32 * STG_W * 2;
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 2 * D < 32 ? 32 : 2 * D;  // dQ[2]
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -201,6 +204,8 @@ __global__ void __launch_bounds__(256, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+        const uint32_t stg = sbase + C::OFF_STG + static_cast<uint32_t>(quad) * (32 * C::STG_W * 2);
+        const bool staged = !a.dq.f32 && a.dq.cols == D;
         uint32_t tn = 0;
         bool ok = true;
         TileStream ts(g, tbeg, tend);
@@ -220,6 +225,41 @@ __global__ void __launch_bounds__(256, 1)
             const bool row_ok = row < t.q_len;
             const int64_t qrow = static_cast<int64_t>(t.q_start) + row;
             const uint32_t tq = tmem + lane_base + b * D;
+            if (staged) {
+                // 32 columns per TMEM round trip, packed to bf16 into the warp's staging
+                // rows; each 64-column half then goes out as whole 128-byte row pieces
+                constexpr int W = C::STG_W;
+                const int nrows = min(32, t.q_len - quad * 32);
+                __nv_bfloat16 *dst0 = static_cast<__nv_bfloat16 *>(a.dq.ptr) +
+                                      (static_cast<int64_t>(t.q_start) + quad * 32) * a.dq.ld + static_cast<int64_t>(t.h) * D;
+#pragma unroll
+                for (int col = 0; col < D; col += 32) {
+                    float o[32];
+                    if (has_keys) {
+                        tmem_ld32(tq + col, o);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+                    }
+                    if (col + 32 >= D) {  // every TMEM read of this tile is done
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&acc_empty[b]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], g.scale, g.scale);
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+                    stage_row32_bf16<W>(stg, lane, col % W, w);
+                    if ((col + 32) % W == 0) {
+                        __syncwarp();
+                        store_rows_bf16<W>(stg, lane, dst0 + (col + 32 - W), a.dq.ld, nrows);
+                        __syncwarp();
+                    }
+                }
+                continue;
+            }
 #pragma unroll 1
             for (int col = 0; col < D; col += 32) {
                 float o[32];

@@ -92,14 +92,23 @@ struct FwdCfg {
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;  // [H, nb] table (kBiasTable)
     static constexpr uint32_t OFF_BEXT = OFF_BIAS + (BIAS == kBiasTable ? kMaxBiasFloats * 4 : 0);
     static constexpr uint32_t OFF_ROWS = OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0);
-    static constexpr uint32_t SMEM = OFF_ROWS + (ACT ? 0 : 2 * 4 * 128 * 4);  // [2][m0 l0 m1 l1][128]
+    // D = 128: per output warp 32 rows x 64 bf16 of staging for row-contiguous
+    // stores (D = 64 and RoPE keep per-row stores: their output registers do not
+    // fit both)
+    static constexpr bool STAGE_OUT = D == 128 && !ROPE;
+    static constexpr int STG_W = 64;
+    static constexpr uint32_t OFF_STG = (OFF_ROWS + (ACT ? 0 : 2 * 4 * 128 * 4) + 127) & ~127u;  // after [2][m0 l0 m1 l1][128]
+    static constexpr uint32_t SMEM = OFF_STG + (STAGE_OUT ? 4 * 32 * STG_W * 2 : 0);
     static constexpr int THREADS = 512;
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;  // slack to align the base to 1024
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;    // S_g / P_g: BN columns per group
     static constexpr uint32_t COL_O = 256;  // O_g: D columns per group
     // registers per thread after the split (launch: 512 threads x 128)
-    static constexpr uint32_t REG_CTRL = 56, REG_SOFTMAX = 176, REG_OUT = 104;
+    // (the staged D = 128 softmax output without a bias needs 120 in the output
+    // group; its softmax fits in 168)
+    static constexpr bool WIDE_OUT = STAGE_OUT && !ACT && BIAS == kBiasNone;
+    static constexpr uint32_t REG_CTRL = 56, REG_SOFTMAX = WIDE_OUT ? 168 : 176, REG_OUT = WIDE_OUT ? 120 : 104;
     static_assert(REG_CTRL * 128 + REG_SOFTMAX * 256 + REG_OUT * 128 <= 128 * 512, "register split");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "operand alignment");
@@ -639,6 +648,8 @@ __global__ void __launch_bounds__(512, 1)
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tO0 = tmem + lane_base + C::COL_O, tO1 = tO0 + D;
+        const uint32_t stg = smem_u32(smem + C::OFF_STG) + static_cast<uint32_t>(quad) * (32 * C::STG_W * 2);
+        const bool staged = C::STAGE_OUT && !a.out.f32 && a.out.cols == D;
         uint32_t t_local = 0, n0 = 0;
         bool ok = true;
         // RoPE: this warpgroup rotates Q and K two tiles ahead of the one whose
@@ -716,6 +727,55 @@ __global__ void __launch_bounds__(512, 1)
             if (quad * 32 >= t.q_len) {  // no row of this warp is stored
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&o_empty[sl]);
+                n0 += nkv;
+                ++t_local;
+                continue;
+            }
+            if (C::STAGE_OUT && staged) {
+                // each 64-column half of the warp's 32 rows goes out through the staging
+                // rows as whole 128-byte row pieces (not 32 rows' 16-byte pieces per store)
+                constexpr int W = C::STG_W;
+                const int nrows = min(32, t.q_len - quad * 32);
+                __nv_bfloat16 *dst0 = static_cast<__nv_bfloat16 *>(a.out.ptr) +
+                                      (static_cast<int64_t>(t.q_start) + quad * 32) * a.out.ld +
+                                      static_cast<int64_t>(t.h) * D;
+#pragma unroll 1
+                for (int col = 0; col < D; col += 32) {
+                    float o[32];
+                    if (has0) {
+                        tmem_ld32(tO0 + col, o);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], c0, c0);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = 0.0f;
+                    }
+                    if (has1) {
+                        float o1[32];
+                        tmem_ld32(tO1 + col, o1);
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2) {  // o += c1 * o1
+                            fma2(o1[i], o1[i + 1], c1, c1, o[i], o[i + 1]);
+                            o[i] = o1[i];
+                            o[i + 1] = o1[i + 1];
+                        }
+                    }
+                    if (col + 32 >= D) {  // every TMEM read of this tile is done: O_0 / O_1 are free
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&o_empty[sl]);
+                    }
+                    uint32_t w[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(o[2 * i], o[2 * i + 1]);
+                    stage_row32_bf16<W>(stg, lane, col % W, w);
+                    if ((col + 32) % W == 0) {
+                        __syncwarp();
+                        store_rows_bf16<W>(stg, lane, dst0 + (col + 32 - W), a.out.ld, nrows);
+                        __syncwarp();
+                    }
+                }
+                if (!ACT && a.lse != nullptr && row_ok) a.lse[static_cast<int64_t>(t.h) * g.Tq + orow] = lse;
                 n0 += nkv;
                 ++t_local;
                 continue;
