@@ -23,6 +23,18 @@
 // and the epilogue applies the transposed rotation to dQ and dK in float32,
 // before the bf16 store, so the gradients leave for the unrotated inputs and
 // no separate rotary kernel reads or writes them.
+// OVL (D = 64, softmax, bf16 results, no RoPE): the compute warps write a
+// chunk's results one chunk late, after they have handed the next chunk's P
+// and dS to the products, so the epilogue overlaps the products of the next
+// chunk.  dQ then has its own TMEM columns (the S columns take the next
+// chunk's scores at once); the MMA thread waits only for the compute warps to
+// have read S and dP (sp_free) before the next scores, and for the previous
+// chunk's results to be read out (acc_empty) before the next chunk's dV / dK /
+// dQ products; the compute warps wait for the previous chunk's products to be
+// done with the P / dS tiles (pd_free) before they overwrite them, and stage
+// the results in the lo plane, which softmax leaves unused.  (A separate
+// output warpgroup would overlap the epilogue with the softmax as well, but
+// the compute warps' 255 registers leave no room for its registers.)
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -47,8 +59,8 @@ struct BlkCfg {
     static constexpr uint32_t OFF_DSLO = OFF_DS + M_BYTES;  // bf16 remainder of dS (activation mode)
     static constexpr uint32_t OFF_BAR = OFF_DSLO + M_BYTES;
     // in_full[NBUF], in_empty[NBUF], s_full, pd_full, acc_full, acc_empty, drain, rot_full[NBUF],
-    // lo_free, dslo_full
-    static constexpr int NBAR = 3 * NBUF + 7;
+    // lo_free, dslo_full, sp_free, pd_free
+    static constexpr int NBAR = 3 * NBUF + 9;
     static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
     static constexpr uint32_t OFF_BIAS = OFF_MISC + 16;
     static constexpr uint32_t SMEM = OFF_BIAS + kMaxBiasFloats * 4;
@@ -58,6 +70,7 @@ struct BlkCfg {
     static constexpr uint32_t COL_DP = 128;
     static constexpr uint32_t COL_DK = 256;
     static constexpr uint32_t COL_DV = 256 + D;
+    static constexpr uint32_t COL_DQ_OVL = 256 + 2 * D;  // OVL: dQ's own columns (D = 64)
     // RoPE, D = 64: the epilogue's cos / sin row per lane (columns past dV)
     static constexpr uint32_t COL_TAB = D == 64 ? 256 + 2 * D : 0;
     // operand offsets inside one input buffer
@@ -65,12 +78,13 @@ struct BlkCfg {
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
 };
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool OVL>
 __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     bwd_block_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const BwdArgs a) {
     using C = BlkCfg<D>;
+    static_assert(!OVL || (D == 64 && !ROPE), "the overlapped epilogue: D = 64 without RoPE");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
     const Geom &g = a.g;
@@ -88,6 +102,8 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     uint64_t *rot_full = drain + 1;  // [NBUF] RoPE: the buffer's Q and K rows are rotated
     uint64_t *lo_free = rot_full + C::NBUF;  // activation: the dV products are done with P's lo plane
     uint64_t *dslo_full = lo_free + 1;       // activation: dS's lo plane is written
+    uint64_t *sp_free = dslo_full + 1;       // OVL: the compute warps have read S and dP
+    uint64_t *pd_free = sp_free + 1;         // OVL: the chunk's products are done with the P / dS tiles
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
     float *sbias = reinterpret_cast<float *>(smem + C::OFF_BIAS);
@@ -110,6 +126,8 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
         for (int b = 0; b < C::NBUF; ++b) mbar_init(&rot_full[b], 2);  // the two rotation warps
         mbar_init(lo_free, 1);
         mbar_init(dslo_full, 4);
+        mbar_init(sp_free, 4);
+        mbar_init(pd_free, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -132,6 +150,34 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     const int tbeg = g.cta_begin[blockIdx.x];
     const int tend = g.cta_begin[blockIdx.x + 1];
 
+    // OVL: chunk n's dV, dQ, dK from TMEM through this warp's rows of the
+    // staging tile (the lo plane) to whole 128-byte result rows; TMEM goes
+    // back after the last read, before the last stores
+    auto drain_ovl = [&](const Tile &pt, uint32_t n, int row, int quad, uint32_t lane_base) -> bool {
+        if (!mbar_wait_warp(acc_full, n & 1, err)) return false;
+        tc_fence_after();
+#pragma unroll 1
+        for (int pass = 0; pass < 3; ++pass) {  // dV, dQ, dK
+            const uint32_t col = pass == 0 ? C::COL_DV : (pass == 1 ? C::COL_DQ_OVL : C::COL_DK);
+            const float mul = pass == 0 ? 1.0f : g.scale;
+            float oa[64];
+            tmem_ld64(tmem + lane_base + col, oa);
+            if (pass == 2) {  // every TMEM read of the chunk is done
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
+#pragma unroll
+            for (int i = 0; i < 64; i += 2) mul2(oa[i], oa[i + 1], mul, mul);
+            st_row32_bf16(sDSlo, C::SUB, row, 0, sub32(oa, 0));
+            st_row32_bf16(sDSlo, C::SUB, row, 32, sub32(oa, 1));
+            __syncwarp();
+            copy_rows_out<D>(sDSlo, C::SUB, quad * 32, pt.q_len, pass == 0 ? a.dv : (pass == 1 ? a.dq : a.dk),
+                             pass == 1 ? pt.q_start : pt.kv_start, pt.h, lane);
+            __syncwarp();
+        }
+        return true;
+    };
     if (warp == 0) {
         if (lane == 0) {
             uint32_t t_local = 0;
@@ -161,7 +207,74 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
+        if (lane == 0 && OVL) {
+            // one chunk ahead: the next chunk's S and dP are issued as soon as the
+            // compute warps have read this chunk's, before this chunk's dV / dK / dQ
+            const uint32_t idesc_mn = idesc_bf16(128, D, true, true);   // dV, dK
+            const uint32_t idesc_kmn = idesc_bf16(128, D, false, true); // dQ
+            TileStream ts(g, tbeg, tend);
+            auto next_valid = [&](Tile &x) -> bool {
+                while (ts.next(x))
+                    if (check_tile(g, x, err, false)) return true;
+                return false;
+            };
+            auto issue_s = [&](const Tile &x, uint32_t n) -> bool {  // chunk n's S and dP
+                const uint32_t buf = n % C::NBUF, use = n / C::NBUF;
+                if (!mbar_wait(&in_full[buf], use & 1, err)) return false;
+                if (n > 0 && !mbar_wait(sp_free, (n - 1) & 1, err)) return false;  // chunk n - 1's read out
+                tc_fence_after();
+                const uint32_t base = sIn + buf * C::IN_BYTES;
+                const uint32_t idesc_s = idesc_bf16(128, round_up16(x.q_len), false, false);
+                const uint64_t kQ = sdesc_sw128(base + C::IQ, 16, 1024), kK = sdesc_sw128(base + C::IK, 16, 1024);
+                const uint64_t kDO = sdesc_sw128(base + C::IDO, 16, 1024), kV = sdesc_sw128(base + C::IV, 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t o = (ks >> 2) * C::SUB + (ks & 3) * 32;
+                    mma_bf16_ss(tmem + C::COL_S, sdesc_add(kQ, o), sdesc_add(kK, o), idesc_s, ks > 0);
+                    mma_bf16_ss(tmem + C::COL_DP, sdesc_add(kDO, o), sdesc_add(kV, o), idesc_s, ks > 0);
+                }
+                mma_commit(s_full);
+                return true;
+            };
+            auto issue_acc = [&](const Tile &x, uint32_t n) -> bool {  // chunk n's dV, dK, dQ
+                const uint32_t buf = n % C::NBUF;
+                if (!mbar_wait(pd_full, n & 1, err)) return false;
+                if (!mbar_wait(acc_empty, (n & 1) ^ 1, err)) return false;  // chunk n - 1's results read out
+                tc_fence_after();
+                const uint32_t base = sIn + buf * C::IN_BYTES;
+                const int ksteps = round_up16(x.q_len) / 16;
+                const uint64_t mP = sdesc_sw128(sP, C::SUB, 1024), mDS = sdesc_sw128(sDS, C::SUB, 1024);
+                const uint64_t kDS = sdesc_sw128(sDS, 16, 1024);
+                const uint64_t mDO = sdesc_sw128(base + C::IDO, C::SUB, 1024), mQ = sdesc_sw128(base + C::IQ, C::SUB, 1024);
+                const uint64_t mK = sdesc_sw128(base + C::IK, C::SUB, 1024);
+#pragma unroll
+                for (int ks = 0; ks < C::BM / 16; ++ks) {
+                    if (ks < ksteps) {
+                        const uint32_t acc = ks > 0 ? 1u : 0u;
+                        mma_bf16_ss(tmem + C::COL_DV, sdesc_add(mP, ks * 2048), sdesc_add(mDO, ks * 2048), idesc_mn, acc);
+                        mma_bf16_ss(tmem + C::COL_DK, sdesc_add(mDS, ks * 2048), sdesc_add(mQ, ks * 2048), idesc_mn, acc);
+                        mma_bf16_ss(tmem + C::COL_DQ_OVL, sdesc_add(kDS, (ks >> 2) * C::SUB + (ks & 3) * 32),
+                                    sdesc_add(mK, ks * 2048), idesc_kmn, acc);
+                    }
+                }
+                mma_commit(&in_empty[buf]);
+                mma_commit(pd_free);
+                mma_commit(acc_full);
+                return true;
+            };
+            Tile cur, nxt;
+            bool have = next_valid(cur), ok = true;
+            if (have) ok = issue_s(cur, 0);
+            for (uint32_t n = 0; ok && have; ++n) {
+                const bool have_next = next_valid(nxt);
+                if (have_next && !(ok = issue_s(nxt, n + 1))) break;
+                if (!(ok = issue_acc(cur, n))) break;
+                cur = nxt;
+                have = have_next;
+            }
+            mma_commit(drain);
+            mbar_drain(drain, 0);
+        } else if (lane == 0) {
             uint32_t t_local = 0;
             const uint32_t idesc_mn = idesc_bf16(128, D, true, true);   // dV, dK
             const uint32_t idesc_kmn = idesc_bf16(128, D, false, true); // dQ
@@ -172,7 +285,9 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                 if (!check_tile(g, t, err, false)) continue;
                 const uint32_t buf = t_local % C::NBUF, use = t_local / C::NBUF;
                 if (!(ok = mbar_wait(ROPE ? &rot_full[buf] : &in_full[buf], use & 1, err))) break;
-                if (!(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
+                // the S / dP columns: read out by the compute warps (OVL), or the whole
+                // previous chunk written out (dQ reuses them otherwise)
+                if (!(ok = mbar_wait(OVL ? sp_free : acc_empty, (t_local & 1) ^ 1, err))) break;
                 tc_fence_after();
                 const uint32_t base = sIn + buf * C::IN_BYTES;
                 const int n16 = round_up16(t.q_len);
@@ -191,6 +306,9 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                 }
                 mma_commit(s_full);
                 if (!(ok = mbar_wait(pd_full, t_local & 1, err))) break;
+                // OVL: the previous chunk's dV, dK, dQ have been read out before these
+                // products start over in their columns
+                if (OVL && !(ok = mbar_wait(acc_empty, (t_local & 1) ^ 1, err))) break;
                 tc_fence_after();
                 const int ksteps = n16 / 16;
                 const uint64_t mP = sdesc_sw128(sP, C::SUB, 1024), mDS = sdesc_sw128(sDS, C::SUB, 1024);
@@ -209,8 +327,9 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                                         idesc_mn, 1u);
                         mma_bf16_ss(tmem + C::COL_DK, sdesc_add(mDS, ks * 2048), sdesc_add(mQ, ks * 2048), idesc_mn, acc);
                         // dQ += dS K: reduction over key rows ks*16..+15
-                        mma_bf16_ss(tmem + C::COL_S, sdesc_add(kDS, (ks >> 2) * C::SUB + (ks & 3) * 32),
-                                    sdesc_add(mK, ks * 2048), idesc_kmn, acc);
+                        mma_bf16_ss(tmem + (OVL ? C::COL_DQ_OVL : C::COL_S),
+                                    sdesc_add(kDS, (ks >> 2) * C::SUB + (ks & 3) * 32), sdesc_add(mK, ks * 2048),
+                                    idesc_kmn, acc);
                     }
                 }
                 if (ACT) {  // unnormalised dS: add its bf16 remainder to dK and dQ
@@ -228,6 +347,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                     }
                 }
                 mma_commit(&in_empty[buf]);
+                if (OVL) mma_commit(pd_free);
                 mma_commit(acc_full);
                 ++t_local;
             }
@@ -266,6 +386,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
         const float sc = ACT ? g.scale : g.scale * kLog2e;
         uint32_t t_local = 0;
         bool ok = true;
+        Tile prev{};  // OVL: the chunk whose results are written next
         TileStream ts(g, tbeg, tend);
         Tile t;
         while (ok && ts.next(t)) {
@@ -285,6 +406,11 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
             for (int c = 0; c < 2; ++c) live[c] = c * 32 < nvalid;  // uniform: one warp lies in one block
             if (nvalid > 0)
                 tmem_ld64x2(tmem + lane_base + C::COL_S + half * 64, tmem + lane_base + C::COL_DP + half * 64, s, dp);
+            if constexpr (OVL) {  // S and dP are in registers: the next chunk's scores may start
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sp_free);
+            }
 #pragma unroll
             for (int c = 0; c < 2; ++c) {
                 if (!live[c]) continue;
@@ -353,6 +479,8 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                         }
                     }
             }
+            // OVL: the previous chunk's products have read the P / dS tiles
+            if (OVL && !(ok = mbar_wait_warp(pd_free, (t_local & 1) ^ 1, err))) break;
             // P and dS rows: this row's block gets values, the other block zeros
             // (activation: the lo plane takes P's remainder first)
 #pragma unroll
@@ -378,6 +506,12 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(pd_full);
+            if constexpr (OVL) {  // the previous chunk's results, now that this chunk's products may run
+                if (t_local > 0 && !(ok = drain_ovl(prev, t_local - 1, row, quad, lane_base))) break;
+                prev = t;
+                ++t_local;
+                continue;
+            }
             if (ACT) {
                 // once the dV products are done with P's remainder, the lo plane
                 // takes dS's (hi was rounded from the same values above); the rest
@@ -521,6 +655,7 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
             if (lane == 0) mbar_arrive(acc_empty);
             ++t_local;
         }
+        if (OVL && ok && t_local > 0) drain_ovl(prev, t_local - 1, row, quad, lane_base);  // the last chunk
     }
 
     tc_fence_before();
@@ -531,13 +666,13 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
     }
 }
 
-template <int D, bool ROPE>
+template <int D, bool ROPE, bool OVL = false>
 static cudaError_t launch_block_t(const TmapSet &tm, const BwdArgs &a, int n_ctas, cudaStream_t st) {
     using C = BlkCfg<D>;
     static SmemOnce done;
-    cudaError_t e = ensure_smem(bwd_block_kernel<D, ROPE>, C::SMEM_ALLOC, done);
+    cudaError_t e = ensure_smem(bwd_block_kernel<D, ROPE, OVL>, C::SMEM_ALLOC, done);
     if (e != cudaSuccess || n_ctas <= 0) return e;
-    bwd_block_kernel<D, ROPE><<<n_ctas, ROPE ? 256 : 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
+    bwd_block_kernel<D, ROPE, OVL><<<n_ctas, ROPE ? 256 : 192, C::SMEM_ALLOC, st>>>(tm.q, tm.k, tm.v, tm.dout, a);
     return cudaGetLastError();
 }
 
@@ -546,7 +681,13 @@ cudaError_t launch_bwd_block(int D, const TmapSet &tm, const BwdArgs &a, int n_c
     // the rotation is offered with softmax only (checked by the host first)
     if (rope && (a.g.rope_sin == nullptr || a.g.act != kSoftmax)) return cudaErrorInvalidValue;
     if (D == 128) return rope ? launch_block_t<128, true>(tm, a, n_ctas, st) : launch_block_t<128, false>(tm, a, n_ctas, st);
-    if (D == 64) return rope ? launch_block_t<64, true>(tm, a, n_ctas, st) : launch_block_t<64, false>(tm, a, n_ctas, st);
+    if (D == 64) {
+        if (rope) return launch_block_t<64, true>(tm, a, n_ctas, st);
+        // softmax with bf16 results of width D: the epilogue runs on its own warps
+        const bool rows = !a.dq.f32 && !a.dk.f32 && !a.dv.f32 && a.dq.cols == D && a.dk.cols == D && a.dv.cols == D;
+        if (a.g.act == kSoftmax && rows) return launch_block_t<64, false, true>(tm, a, n_ctas, st);
+        return launch_block_t<64, false>(tm, a, n_ctas, st);
+    }
     return cudaErrorInvalidValue;
 }
 
