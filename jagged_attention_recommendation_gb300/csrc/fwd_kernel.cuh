@@ -80,9 +80,9 @@ struct FwdCfg {
     static constexpr uint32_t Q_BYTES = BM * D * 2;
     static constexpr uint32_t KV_BYTES = BN * D * 2;
     // q_full[2], q_empty[2], k_full[NST], k_empty[NST], v_full[NST], v_empty[NST],
-    // s_full[2], p_full[2], o_full, o_empty[2], l_full[2], pv_done[2], drain[2]
+    // s_full[2], p_full[2], o_full[2], o_empty[2], l_full[2], pv_done[2], drain[2]
     // (RoPE: q_rot[2], k_rot[NST])
-    static constexpr int NBAR = 4 + 4 * NST + 2 + 2 + 1 + 2 + 2 + 2 + 2 + (ROPE ? 2 + NST : 0);
+    static constexpr int NBAR = 4 + 4 * NST + 2 + 2 + 2 + 2 + 2 + 2 + 2 + (ROPE ? 2 + NST : 0);
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + 2 * Q_BYTES;
     static constexpr uint32_t OFF_V = OFF_K + NST * KV_BYTES;
@@ -104,6 +104,9 @@ struct FwdCfg {
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;    // S_g / P_g: BN columns per group
     static constexpr uint32_t COL_O = 256;  // O_g: D columns per group
+    // D = 64: two sets of O_0 / O_1 by tile parity, so the next tile's P V
+    // products need not wait for the output group to read this tile's
+    static constexpr int OB = (D == 64) ? 2 : 1;
     // registers per thread after the split (launch: 512 threads x 128)
     // (the staged D = 128 softmax output without a bias needs 120 in the output
     // group; its softmax fits in 168)
@@ -112,7 +115,7 @@ struct FwdCfg {
     static_assert(REG_CTRL * 128 + REG_SOFTMAX * 256 + REG_OUT * 128 <= 128 * 512, "register split");
     static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
     static_assert(OFF_K % 1024 == 0 && OFF_V % 1024 == 0, "operand alignment");
-    static_assert(COL_O + 2 * D <= TMEM_COLS, "TMEM budget");
+    static_assert(COL_O + OB * 2 * D <= TMEM_COLS, "TMEM budget");
 };
 
 // WIN: sliding window on (a compile-time switch, so that kernels without one
@@ -154,8 +157,8 @@ __global__ void __launch_bounds__(512, 1)
     uint64_t *v_empty = v_full + C::NST;
     uint64_t *s_full = v_empty + C::NST;  // [2] per score buffer (blocks alternate)
     uint64_t *p_full = s_full + 2;        // [2] per score buffer, both softmax groups arrive
-    uint64_t *o_full = p_full + 2;
-    uint64_t *o_empty = o_full + 1;  // [2] per tile parity
+    uint64_t *o_full = p_full + 2;   // [2] per tile parity: the tile's last P V is done
+    uint64_t *o_empty = o_full + 2;  // [2] per tile parity
     uint64_t *l_full = o_empty + 2;  // [2] per tile parity
     uint64_t *pv_done = l_full + 2;  // [2] per score buffer: its block's P V finished
     uint64_t *drain = pv_done + 2;   // [2] per MMA-issuing thread
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(512, 1)
             for (int s = 0; s < 2; ++s) mbar_init(&q_rot[s], 4);
             for (int s = 0; s < C::NST; ++s) mbar_init(&k_rot[s], 4);
         }
-        mbar_init(o_full, 1);
+        for (int s = 0; s < 2; ++s) mbar_init(&o_full[s], 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -365,7 +368,10 @@ __global__ void __launch_bounds__(512, 1)
                 const int nbk = cdiv(tb.kv_len, C::BN);
                 // the output group must have read tile tb_n - 1 before O_0 / O_1 are
                 // reused (a tile without keys hands over all-zero rows in order)
-                if (tb_n > 0 && !(ok = mbar_wait(&o_empty[(tb_n - 1) & 1], ((tb_n - 1) >> 1) & 1, err))) break;
+                // (D = 64: two O sets, so the tile before the previous one)
+                if (tb_n >= static_cast<uint32_t>(C::OB) &&
+                    !(ok = mbar_wait(&o_empty[(tb_n - C::OB) & 1], ((tb_n - C::OB) >> 1) & 1, err)))
+                    break;
                 for (int jb = 0; jb < nbk; ++jb, ++np) {
                     const uint32_t buf = np & 1;
                     if (!(ok = mbar_wait(&p_full[buf], (np >> 1) & 1, err))) break;
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(512, 1)
                         // group grp's keys 64 grp .. of the block; its 16-key step ks is
                         // block step 4 grp + ks, whose P sits in 32-key chunk (4 grp + ks) / 2
                         const int ksteps = (min(64, nvalid - 64 * grp) + 15) >> 4;  // <= 0: none
-                        const uint32_t dO = tmem + C::COL_O + grp * D;
+                        const uint32_t dO = tmem + C::COL_O + (tb_n % C::OB) * 2 * D + grp * D;
 #pragma unroll
                         for (int ks = 0; ks < 4; ++ks) {
                             if (ks < ksteps) {
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(512, 1)
                     mma_commit(&pv_done[buf]);  // the buffer may take block np + 2; O_0 / O_1 hold block np
                 }
                 if (!ok) break;
-                mma_commit(o_full);
+                mma_commit(&o_full[tb_n & 1]);
                 ++tb_n;
             }
             mma_commit(&drain[1]);
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__(512, 1)
         const int row = quad * 32 + lane;          // query row within the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
         const uint32_t tS0 = tmem + lane_base + C::COL_S;  // buffer b of block n = n % 2 at b BN
-        const uint32_t tO = tmem + lane_base + C::COL_O + grp * D;
+        const uint32_t tO_base = tmem + lane_base + C::COL_O + grp * D;
         const float sc = ACT ? g.scale : g.scale * kLog2e;
         constexpr bool scaled = ACT || BIAS != kBiasNone;  // else the scale is folded into the exponent
         uint32_t t_local = 0, n0 = 0;  // n0: global number of the tile's first block
@@ -574,10 +580,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll 1
                         for (int c = 0; c < D / 32; ++c) {
                             float o[32];
-                            tmem_ld32(tO + c * 32, o);
+                            tmem_ld32(tO_base + (t_local % C::OB) * 2 * D + c * 32, o);
 #pragma unroll
                             for (int i = 0; i < 32; i += 2) mul2(o[i], o[i + 1], alpha, alpha);
-                            tmem_st32(tO + c * 32, o);
+                            tmem_st32(tO_base + (t_local % C::OB) * 2 * D + c * 32, o);
                         }
                     }
                 } else {
@@ -647,7 +653,7 @@ __global__ void __launch_bounds__(512, 1)
         const int quad = warp & 3;
         const int row = quad * 32 + lane;
         const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-        const uint32_t tO0 = tmem + lane_base + C::COL_O, tO1 = tO0 + D;
+        const uint32_t tO_base = tmem + lane_base + C::COL_O;  // + (tile % OB) 2 D: this tile's O set
         const uint32_t stg = smem_u32(smem + C::OFF_STG) + static_cast<uint32_t>(quad) * (32 * C::STG_W * 2);
         const bool staged = C::STAGE_OUT && !a.out.f32 && a.out.cols == D;
         uint32_t t_local = 0, n0 = 0;
@@ -706,7 +712,8 @@ __global__ void __launch_bounds__(512, 1)
             const bool has0 = t.kv_len > 0;
             const bool has1 = t.kv_len > 64;
             const uint32_t sl = t_local & 1;
-            if (!(ok = mbar_wait_warp(o_full, t_local & 1, err))) break;
+            if (!(ok = mbar_wait_warp(&o_full[t_local & 1], (t_local >> 1) & 1, err))) break;
+            const uint32_t tO0 = tO_base + (t_local % C::OB) * 2 * D, tO1 = tO0 + D;
             float c0 = has0 ? 1.0f : 0.0f, c1 = has1 ? 1.0f : 0.0f, lse = -INFINITY;
             if constexpr (!ACT) {
                 if (!(ok = mbar_wait_warp(&l_full[sl], (t_local >> 1) & 1, err))) break;
