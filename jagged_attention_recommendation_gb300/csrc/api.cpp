@@ -50,6 +50,7 @@ struct jattn_plan {
     // backward dS chunks (host plans): first chunk of every sequence, and the total
     std::vector<long long> ds_base;
     int64_t ds_chunks = 0;
+    int32_t max_tile_kv = 0;  // largest key range of a query tile (host plans)
     std::vector<jattn_tile> tiles[2];
     std::vector<int32_t> cta[2];
     // device copies: one buffer holding both tile lists, both schedules and the offsets
@@ -152,6 +153,7 @@ void build_lists(jattn_plan *p) {
     std::vector<jattn_tile> &tq = p->tiles[JATTN_TILES_Q];
     std::vector<jattn_tile> &tk = p->tiles[JATTN_TILES_KV];
     tq.clear();
+    p->max_tile_kv = 0;
     tk.clear();
     for (int32_t b = 0; b < p->B; ++b) {
         const int32_t q0 = p->q_off[b], Lq = p->q_off[b + 1] - q0;
@@ -170,6 +172,7 @@ void build_lists(jattn_plan *p) {
                 if (hi < lo) hi = lo;  // no key in reach: an empty range inside the sequence
             }
             for (int32_t h = 0; h < p->H; ++h) tq.push_back({b, h, q0 + s, ql, k0 + lo, hi - lo});
+            p->max_tile_kv = std::max(p->max_tile_kv, hi - lo);
         }
     }
     if (!block) {
@@ -422,6 +425,8 @@ Geom make_geom(const jattn_plan *p, int which) {
     g.ds = nullptr;
     g.ds_base = p->dev_planned ? nullptr : reinterpret_cast<const long long *>(p->d_buf + p->off_dsbase);
     g.mxfp8 = p->mode.mxfp8;
+    g.tile_parallel = which == JATTN_TILES_Q && !p->dev_planned && p->mode.window == 0 && !p->mode.mxfp8 &&
+                      p->max_tile_kv <= kTileRows;
     return g;
 }
 

@@ -67,6 +67,8 @@ struct Geom {
     void *ds;                 // chunk workspace (16-byte aligned), or nullptr (off)
     const long long *ds_base; // [B + 1] first chunk of every sequence (device)
     int32_t mxfp8;            // 1: MXFP8 attention (P, and in the backward dS, quantised online)
+    int32_t tile_parallel;    // 1: every query tile meets at most one 128-key block (host plans
+                              // without a window); the forward may give whole tiles to its groups
 };
 
 // one dS chunk: 128 keys x 64 queries of bf16 (activation mode: two of them, hi and lo)

@@ -135,12 +135,23 @@ struct FwdCfg {
 // and each row's P is quantised online in its 32-key chunks (one E8M0 scale
 // per chunk from the chunk's largest value) after the row sum has taken the
 // unquantised values.
-template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false, bool STALL = false, bool MX = false>
+// TP: tile-parallel, for batches whose every query tile meets at most one
+// 128-key block (short key sequences; BlockAttention): softmax group g takes
+// the whole block of the CTA's tiles of parity g, into its own O_g, so the two
+// groups run two tiles at once instead of splitting every block's keys (half
+// of which are masked in such tiles), and a tile's P V never waits for the
+// previous tile's output (the other group's O).  Every tile counts as one
+// block, also a tile without keys, so that block and tile numbers agree.
+template <int D, bool ACT, int BIAS, bool WIN, bool ROPE = false, bool STALL = false, bool MX = false,
+          bool TP = false>
 __global__ void __launch_bounds__(512, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const FwdArgs a) {
     using C = FwdCfg<D, ACT, BIAS, ROPE>;
     static_assert(!MX || (!ACT && BIAS == kBiasNone && !WIN && !ROPE), "MXFP8: softmax without bias, window, RoPE");
+    static_assert(!TP || (!ACT && !WIN && !ROPE && !MX && !STALL), "tile-parallel: plain softmax");
+    // block count of a tile (tile-parallel: exactly one)
+    auto nblocks = [](const Tile &x) { return TP ? 1 : cdiv(x.kv_len, C::BN); };
     const int win = WIN ? a.g.window : 0;  // |i - j| < win, 0 = no window
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = align1024(smem_raw);
@@ -179,9 +190,9 @@ __global__ void __launch_bounds__(512, 1)
             mbar_init(&q_full[s], 1);
             mbar_init(&q_empty[s], 1);
             mbar_init(&s_full[s], 1);
-            mbar_init(&p_full[s], 8);  // both softmax groups' warps
+            mbar_init(&p_full[s], TP ? 4 : 8);  // both softmax groups' warps (TP: the tile's group)
             mbar_init(&o_empty[s], 4);
-            mbar_init(&l_full[s], 8);
+            mbar_init(&l_full[s], TP ? 4 : 8);
             mbar_init(&pv_done[s], 1);
             mbar_init(&drain[s], 1);
         }
@@ -247,7 +258,7 @@ __global__ void __launch_bounds__(512, 1)
             Tile t;
             while (ok && ts.next(t)) {
                 if (!check_tile(g, t, err, true)) continue;
-                const int nkv = cdiv(t.kv_len, C::BN);
+                const int nkv = nblocks(t);
                 for (int j = 0; j < nkv; ++j) {
                     const uint32_t slot = k_it % C::NST, use = k_it / C::NST;
                     if (!(ok = mbar_wait(&k_empty[slot], (use & 1) ^ 1, err))) break;
@@ -325,7 +336,7 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t ta_n = 0, ns = 0;
             while (ok && tsa.next(ta)) {
                 if (!check_tile(g, ta, err, false)) continue;
-                const int na = cdiv(ta.kv_len, C::BN);
+                const int na = nblocks(ta);
                 const uint32_t qs = ta_n & 1;
                 if (!(ok = mbar_wait(ROPE ? &q_rot[qs] : &q_full[qs], (ta_n >> 1) & 1, err))) break;
                 const uint64_t ad0 = sdesc_sw128(sQ + qs * C::Q_BYTES, 16, 1024);
@@ -335,7 +346,7 @@ __global__ void __launch_bounds__(512, 1)
                     const uint32_t slot = ns % C::NST, use = ns / C::NST;
                     if (!(ok = mbar_wait(ROPE ? &k_rot[slot] : &k_full[slot], use & 1, err))) break;
                     tc_fence_after();
-                    const int ncols = round_up16(min(C::BN, ta.kv_len - ja * C::BN));
+                    const int ncols = round_up16(max(1, min(C::BN, ta.kv_len - ja * C::BN)));  // >= 16
                     const uint32_t idesc = idesc_bf16(128, ncols, false, false);
                     const uint64_t bd0 = sdesc_sw128(sK + slot * C::KV_BYTES, 16, 1024);
                     const uint32_t dS = tmem + C::COL_S + buf * C::BN;
@@ -365,12 +376,12 @@ __global__ void __launch_bounds__(512, 1)
             uint32_t tb_n = 0, np = 0;
             while (ok && tsb.next(tb)) {
                 if (!check_tile(g, tb, err, false)) continue;
-                const int nbk = cdiv(tb.kv_len, C::BN);
+                const int nbk = nblocks(tb);
                 // the output group must have read tile tb_n - 1 before O_0 / O_1 are
                 // reused (a tile without keys hands over all-zero rows in order)
-                // (D = 64: two O sets, so the tile before the previous one)
-                if (tb_n >= static_cast<uint32_t>(C::OB) &&
-                    !(ok = mbar_wait(&o_empty[(tb_n - C::OB) & 1], ((tb_n - C::OB) >> 1) & 1, err)))
+                // (D = 64, or tile-parallel: two O sets, so the tile before the previous one)
+                constexpr uint32_t OBX = TP ? 2 : C::OB;
+                if (tb_n >= OBX && !(ok = mbar_wait(&o_empty[(tb_n - OBX) & 1], ((tb_n - OBX) >> 1) & 1, err)))
                     break;
                 for (int jb = 0; jb < nbk; ++jb, ++np) {
                     const uint32_t buf = np & 1;
@@ -386,23 +397,35 @@ __global__ void __launch_bounds__(512, 1)
                     // one thread issues them as fast as the tensor pipe takes them (a
                     // loop with a run-time trip count throttles it to about half).
                     const uint32_t acc0 = jb > 0 ? 1u : 0u;  // the tile's first block starts O_grp
+                    if constexpr (TP) {
+                        // the tile's group has all of the block's keys, into its own O
+                        const uint32_t dO = tmem + C::COL_O + (tb_n & 1) * D;
+                        const int ksteps = (nvalid + 15) >> 4;
 #pragma unroll
-                    for (int grp = 0; grp < 2; ++grp) {
-                        // group grp's keys 64 grp .. of the block; its 16-key step ks is
-                        // block step 4 grp + ks, whose P sits in 32-key chunk (4 grp + ks) / 2
-                        const int ksteps = (min(64, nvalid - 64 * grp) + 15) >> 4;  // <= 0: none
-                        const uint32_t dO = tmem + C::COL_O + (tb_n % C::OB) * 2 * D + grp * D;
+                        for (int st = 0; st < 8; ++st) {
+                            if (st < ksteps)
+                                mma_bf16_ts(dO, aP + (st >> 1) * 32 + (st & 1) * 8, sdesc_add(bd0, st * 2048), idesc_pv,
+                                            st > 0 ? 1u : acc0);
+                        }
+                    } else {
 #pragma unroll
-                        for (int ks = 0; ks < 4; ++ks) {
-                            if (ks < ksteps) {
-                                const int st = 4 * grp + ks;
-                                const uint64_t bd = sdesc_add(bd0, st * 2048);
-                                const uint32_t acc = ks > 0 ? 1u : acc0;
-                                if (ACT) {  // hi at columns 16 st .. +7, lo at 16 st + 8 .. +15
-                                    mma_bf16_ts(dO, aP + st * 16, bd, idesc_pv, acc);
-                                    mma_bf16_ts(dO, aP + st * 16 + 8, bd, idesc_pv, 1u);
-                                } else {
-                                    mma_bf16_ts(dO, aP + (st >> 1) * 32 + (st & 1) * 8, bd, idesc_pv, acc);
+                        for (int grp = 0; grp < 2; ++grp) {
+                            // group grp's keys 64 grp .. of the block; its 16-key step ks is
+                            // block step 4 grp + ks, whose P sits in 32-key chunk (4 grp + ks) / 2
+                            const int ksteps = (min(64, nvalid - 64 * grp) + 15) >> 4;  // <= 0: none
+                            const uint32_t dO = tmem + C::COL_O + (tb_n % C::OB) * 2 * D + grp * D;
+#pragma unroll
+                            for (int ks = 0; ks < 4; ++ks) {
+                                if (ks < ksteps) {
+                                    const int st = 4 * grp + ks;
+                                    const uint64_t bd = sdesc_add(bd0, st * 2048);
+                                    const uint32_t acc = ks > 0 ? 1u : acc0;
+                                    if (ACT) {  // hi at columns 16 st .. +7, lo at 16 st + 8 .. +15
+                                        mma_bf16_ts(dO, aP + st * 16, bd, idesc_pv, acc);
+                                        mma_bf16_ts(dO, aP + st * 16 + 8, bd, idesc_pv, 1u);
+                                    } else {
+                                        mma_bf16_ts(dO, aP + (st >> 1) * 32 + (st & 1) * 8, bd, idesc_pv, acc);
+                                    }
                                 }
                             }
                         }
@@ -439,7 +462,12 @@ __global__ void __launch_bounds__(512, 1)
         Tile t;
         while (ok && ts.next(t)) {
             if (!check_tile(g, t, err, false)) continue;
-            const int nkv = cdiv(t.kv_len, C::BN);
+            const int nkv = nblocks(t);
+            if (TP && (t_local & 1) != static_cast<uint32_t>(grp)) {  // the other group's tile
+                n0 += nkv;
+                ++t_local;
+                continue;
+            }
             const float *bt = sbias + t.h * g.nb;
             const float *ext_h = sext + t.h * ext_len(g.nb);
             const int q_loc = t.q_loc0 + row;
@@ -497,7 +525,7 @@ __global__ void __launch_bounds__(512, 1)
                     // pass 1: row max of the block (biased scores written back in place)
                     float mloc = -INFINITY;
 #pragma unroll 1
-                    for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
+                    for (int c = TP ? 0 : 2 * grp; c < (TP ? 4 : 2 * grp + 2); ++c) {
                         if (!live(c)) continue;
                         float xc[32];
                         tmem_ld32(tS + 32 * c, xc);
@@ -537,7 +565,7 @@ __global__ void __launch_bounds__(512, 1)
                     // columns 32c..32c+15, scores already consumed
                     float rs = 0.0f;
 #pragma unroll 1
-                    for (int c = 2 * grp; c < 2 * grp + 2; ++c) {
+                    for (int c = TP ? 0 : 2 * grp; c < (TP ? 4 : 2 * grp + 2); ++c) {
                         uint32_t pw[16];
                         if (!live(c)) {
 #pragma unroll
@@ -707,18 +735,22 @@ __global__ void __launch_bounds__(512, 1)
         while (ok && ts.next(t)) {
             if (!check_tile(g, t, err, false)) continue;
             if (ROPE && !(ok = rotate_next())) break;
-            const int nkv = cdiv(t.kv_len, C::BN);
+            const int nkv = nblocks(t);
             // group g has keys in this tile when the tile has more than 64 g keys
+            // (tile-parallel: the tile's group, read as group 0, has them all)
             const bool has0 = t.kv_len > 0;
-            const bool has1 = t.kv_len > 64;
+            const bool has1 = !TP && t.kv_len > 64;
             const uint32_t sl = t_local & 1;
             if (!(ok = mbar_wait_warp(&o_full[t_local & 1], (t_local >> 1) & 1, err))) break;
-            const uint32_t tO0 = tO_base + (t_local % C::OB) * 2 * D, tO1 = tO0 + D;
+            const uint32_t tO0 = TP ? tO_base + (t_local & 1) * D : tO_base + (t_local % C::OB) * 2 * D, tO1 = tO0 + D;
             float c0 = has0 ? 1.0f : 0.0f, c1 = has1 ? 1.0f : 0.0f, lse = -INFINITY;
             if constexpr (!ACT) {
                 if (!(ok = mbar_wait_warp(&l_full[sl], (t_local >> 1) & 1, err))) break;
-                const float m0 = srows[(sl * 4 + 0) * 128 + row], l0 = srows[(sl * 4 + 1) * 128 + row];
-                const float m1 = srows[(sl * 4 + 2) * 128 + row], l1 = srows[(sl * 4 + 3) * 128 + row];
+                // (tile-parallel: only the tile's group, g = sl, wrote its statistics)
+                const float m0 = srows[(sl * 4 + (TP ? 2 * sl : 0)) * 128 + row];
+                const float l0 = srows[(sl * 4 + (TP ? 2 * sl : 0) + 1) * 128 + row];
+                const float m1 = TP ? -INFINITY : srows[(sl * 4 + 2) * 128 + row];
+                const float l1 = TP ? 0.0f : srows[(sl * 4 + 3) * 128 + row];
                 const float mm = fmaxf(m0, m1);
                 const float w0 = l0 > 0.0f ? ex2_approx(m0 - mm) : 0.0f;
                 const float w1 = l1 > 0.0f ? ex2_approx(m1 - mm) : 0.0f;

@@ -34,6 +34,12 @@ CASES = [
     ("bf16_d32", [5, 140, 64], [9, 130, 1], 2, 32, 0, SOFTMAX, 0, torch.bfloat16),
     ("fp32_d128_bias", [40, 130, 257], [300, 20, 129], 2, 128, 16, SOFTMAX, 0, torch.float32),
     ("fp32_d64_block", [70, 130], None, 2, 64, 0, SOFTMAX, 64, torch.float32),
+    # every query tile meets at most one 128-key block: the forward's groups take
+    # whole tiles (reflected bias table, bias table, empty key sets, exactly 128 keys)
+    ("tiles_d128_bias", [1, 64, 100, 128, 77, 260], [1, 64, 100, 128, 77, 100], 4, 128, 64, SOFTMAX, 0,
+     torch.bfloat16),
+    ("tiles_d64_table", [3, 128, 65, 90], None, 16, 64, 16, SOFTMAX, 0, torch.bfloat16),
+    ("tiles_d64_empty", [300, 0, 17, 129], [128, 3, 0, 64], 2, 64, 0, SOFTMAX, 0, torch.bfloat16),
 ]
 
 
