@@ -630,10 +630,13 @@ __global__ void __launch_bounds__(512, 1)
                                 float xc[32];
                                 tmem_ld32(tS + 32 * c, xc);
                                 scores(c, xc);
+                                // keys past the sequence's end are 0 after scores(), and act(0) = 0:
+                                // no per-element test (one around a larger activation would become
+                                // a branch per element)
 #pragma unroll
                                 for (int i = 0; i < 32; i += 2) {
-                                    const float a0 = c * 32 + i < nvalid ? act_fwd_t<AF>(xc[i]) : 0.0f;
-                                    const float a1 = c * 32 + i + 1 < nvalid ? act_fwd_t<AF>(xc[i + 1]) : 0.0f;
+                                    const float a0 = act_fwd_t<AF>(xc[i]);
+                                    const float a1 = act_fwd_t<AF>(xc[i + 1]);
                                     __nv_bfloat162 h2 = __floats2bfloat162_rn(a0, a1);
                                     const int k = i >> 4, e = (i & 15) >> 1;  // MMA step within the chunk, pair
                                     w[16 * k + e] = *reinterpret_cast<uint32_t *>(&h2);
