@@ -38,6 +38,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "attn.cuh"
 #include "kernels.h"
 
@@ -465,19 +467,28 @@ __global__ void __launch_bounds__(ROPE ? 256 : 192, 1)
                         for (int i = 0; i < 32; ++i) dp[c * 32 + i] = s[c * 32 + i] * (dp[c * 32 + i] - delta);
                     }
             } else {
+                // the activation fixed per loop (a run-time choice per element
+                // would put a branch around every element)
+                auto act_rows = [&](auto af) {
+                    constexpr int AF = decltype(af)::value;
 #pragma unroll
-                for (int c = 0; c < 2; ++c)
-                    if (live[c]) {
+                    for (int c = 0; c < 2; ++c)
+                        if (live[c]) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const int cc = c * 32 + i;
-                            float av;
-                            const float dv = act_bwd(g.act, s[cc], av) * dp[cc];
-                            const bool in = row_valid && cc < nvalid;
-                            s[cc] = in ? av : 0.0f;
-                            dp[cc] = in ? dv : 0.0f;
+                            for (int i = 0; i < 32; ++i) {
+                                const int cc = c * 32 + i;
+                                float av;
+                                const float dv = act_bwd_t<AF>(s[cc], av) * dp[cc];
+                                const bool in = row_valid && cc < nvalid;
+                                s[cc] = in ? av : 0.0f;
+                                dp[cc] = in ? dv : 0.0f;
+                            }
                         }
-                    }
+                };
+                if (g.act == kSilu)
+                    act_rows(std::integral_constant<int, kSilu>{});
+                else
+                    act_rows(std::integral_constant<int, kGeluTanh>{});
             }
             // OVL: the previous chunk's products have read the P / dS tiles
             if (OVL && !(ok = mbar_wait_warp(pd_free, (t_local & 1) ^ 1, err))) break;

@@ -30,6 +30,7 @@ CASES = [
     ("block64_d64", [1, 63, 64, 65, 200, 513], None, 4, 64, 0, SOFTMAX, 64, torch.bfloat16),
     ("block64_d128_bias", [130, 64, 7, 300], None, 2, 128, 64, SOFTMAX, 64, torch.bfloat16),
     ("block64_silu", [100, 257], None, 2, 64, 0, SILU, 64, torch.bfloat16),
+    ("block64_gelu_d128", [100, 257, 64], None, 2, 128, 0, GELU, 64, torch.bfloat16),
     ("fp32_d32", [31, 33, 49, 61], None, 2, 32, 0, SOFTMAX, 0, torch.float32),
     ("bf16_d32", [5, 140, 64], [9, 130, 1], 2, 32, 0, SOFTMAX, 0, torch.bfloat16),
     ("fp32_d128_bias", [40, 130, 257], [300, 20, 129], 2, 128, 16, SOFTMAX, 0, torch.float32),
