@@ -227,26 +227,26 @@ KERNEL_FILES = {"fwd": ("fwd.cu", "fwd_kernel.cuh"), "bwd_dkdv": ("bwd_dkdv.cu",
 KERNEL_FILES.update({n: ("aux.cu",) for n in ("mx_quant", "bwd_mx_quant")})
 NCU_TRAFFIC = {
     (2, "softmax", False, "fwd"): (2.71e+08, "688683d13ce05447"),
-    (2, "softmax", False, "bwd_delta"): (1.378e+08, "9d5551d5e8e5569d"),
-    (2, "softmax", False, "bwd_dkdv"): (6.524e+08, "1913e41f7a8d5021"),
+    (2, "softmax", False, "bwd_delta"): (1.378e+08, "a8f3db73114ce982"),
+    (2, "softmax", False, "bwd_dkdv"): (6.552e+08, "0b28b2c0fd36c3d4"),
     (2, "softmax", False, "bwd_dq_gemm"): (3.689e+08, "d415a547fd8f09fa"),
-    (3, "softmax", False, "fwd"): (5.455e+08, "688683d13ce05447"),
-    (3, "softmax", False, "bwd_delta"): (4.766e+08, "9d5551d5e8e5569d"),
-    (3, "softmax", False, "bwd_dkdv"): (7.06e+08, "1913e41f7a8d5021"),
-    (3, "softmax", False, "bwd_dq_gemm"): (2.962e+08, "d415a547fd8f09fa"),
-    (4, "silu", False, "fwd"): (9.359e+08, "688683d13ce05447"),
-    (4, "silu", False, "bwd_dkdv"): (1.965e+09, "1913e41f7a8d5021"),
+    (3, "softmax", False, "fwd"): (5.452e+08, "688683d13ce05447"),
+    (3, "softmax", False, "bwd_delta"): (4.765e+08, "a8f3db73114ce982"),
+    (3, "softmax", False, "bwd_dkdv"): (7.057e+08, "0b28b2c0fd36c3d4"),
+    (3, "softmax", False, "bwd_dq_gemm"): (2.959e+08, "d415a547fd8f09fa"),
+    (4, "silu", False, "fwd"): (9.357e+08, "688683d13ce05447"),
+    (4, "silu", False, "bwd_dkdv"): (1.965e+09, "0b28b2c0fd36c3d4"),
     (4, "silu", False, "bwd_dq_gemm"): (9.018e+08, "d415a547fd8f09fa"),
-    (4, "gelu_tanh", False, "fwd"): (9.36e+08, "688683d13ce05447"),
-    (4, "gelu_tanh", False, "bwd_dkdv"): (1.965e+09, "1913e41f7a8d5021"),
-    (4, "gelu_tanh", False, "bwd_dq_gemm"): (9.018e+08, "d415a547fd8f09fa"),
+    (4, "gelu_tanh", False, "fwd"): (9.357e+08, "688683d13ce05447"),
+    (4, "gelu_tanh", False, "bwd_dkdv"): (1.966e+09, "0b28b2c0fd36c3d4"),
+    (4, "gelu_tanh", False, "bwd_dq_gemm"): (9.019e+08, "d415a547fd8f09fa"),
     (5, "softmax", False, "fwd"): (1.12e+09, "688683d13ce05447"),
     (5, "softmax", False, "bwd_block"): (1.953e+09, "2733bc711320aacd"),
-    (2, "softmax", True, "mx_quant"): (3.612e+08, "9d5551d5e8e5569d"),
-    (2, "softmax", True, "fwd"): (2.716e+08, "688683d13ce05447"),
-    (2, "softmax", True, "bwd_mx_quant"): (4.996e+08, "9d5551d5e8e5569d"),
-    (2, "softmax", True, "bwd_delta"): (1.379e+08, "9d5551d5e8e5569d"),
-    (2, "softmax", True, "bwd_dkdv"): (6.52e+08, "1913e41f7a8d5021"),
+    (2, "softmax", True, "mx_quant"): (3.612e+08, "a8f3db73114ce982"),
+    (2, "softmax", True, "fwd"): (2.715e+08, "688683d13ce05447"),
+    (2, "softmax", True, "bwd_mx_quant"): (4.996e+08, "a8f3db73114ce982"),
+    (2, "softmax", True, "bwd_delta"): (1.379e+08, "a8f3db73114ce982"),
+    (2, "softmax", True, "bwd_dkdv"): (6.519e+08, "0b28b2c0fd36c3d4"),
     (2, "softmax", True, "bwd_dq_gemm"): (3.692e+08, "d415a547fd8f09fa"),
 }
 

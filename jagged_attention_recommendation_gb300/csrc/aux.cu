@@ -53,20 +53,32 @@ __global__ void delta_kernel(const T *__restrict__ out, const T *__restrict__ do
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int sub = threadIdx.x & (tpr - 1);
-    // whole warps stay in the loop together so the shuffles see every lane
-    for (int64_t base = (gtid / tpr) - ((threadIdx.x & 31) / tpr); base < nrows; base += nthreads / tpr) {
-        const int64_t r = base + (threadIdx.x & 31) / tpr;
-        float acc = 0.0f;
-        if (r < nrows) {
-            const uint4 *o = reinterpret_cast<const uint4 *>(out + r * D);
-            const uint4 *d = reinterpret_cast<const uint4 *>(dout + r * D);
-            acc = dot16<T>(__ldg(o + sub), __ldg(d + sub));
+    // Two rows per lane group and pass, both rows' loads issued before either
+    // sum.  Whole warps stay in the loop together so the shuffles see every lane.
+    const int64_t rstep = nthreads / tpr;
+    for (int64_t base = (gtid / tpr) - ((threadIdx.x & 31) / tpr); base < nrows; base += 2 * rstep) {
+        const int64_t r[2] = {base + (threadIdx.x & 31) / tpr, base + (threadIdx.x & 31) / tpr + rstep};
+        uint4 o[2], d[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            o[j] = d[j] = make_uint4(0u, 0u, 0u, 0u);
+            if (r[j] < nrows) {
+                o[j] = __ldg(reinterpret_cast<const uint4 *>(out + r[j] * D) + sub);
+                d[j] = __ldg(reinterpret_cast<const uint4 *>(dout + r[j] * D) + sub);
+            }
         }
-        for (int k = tpr >> 1; k > 0; k >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, k);
-        if (sub == 0 && r < nrows) {
-            const int64_t t = r / H;
-            const int h = static_cast<int>(r - t * H);
-            delta[static_cast<int64_t>(h) * Tq + t] = acc;
+        float acc[2] = {dot16<T>(o[0], d[0]), dot16<T>(o[1], d[1])};
+        for (int k = tpr >> 1; k > 0; k >>= 1) {
+            acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], k);
+            acc[1] += __shfl_xor_sync(0xffffffffu, acc[1], k);
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (sub == 0 && r[j] < nrows) {
+                const int64_t t = r[j] / H;
+                const int h = static_cast<int>(r[j] - t * H);
+                delta[static_cast<int64_t>(h) * Tq + t] = acc[j];
+            }
         }
     }
 }

@@ -39,7 +39,11 @@ struct DkvCfg {
     static constexpr uint32_t OFF_STG = (OFF_BEXT + (BIAS == kBiasExt ? kMaxBiasExtFloats * 4 : 0) + 127) & ~127u;
     // the CTA's share of the bias-table gradient [H, nb] (dS chunk mode with a bias)
     static constexpr uint32_t OFF_DT = OFF_STG + 4 * 32 * STG_W * 2;
-    static constexpr uint32_t SMEM = OFF_DT + (BIAS != kBiasNone ? kMaxBiasFloats * 4 : 0);
+    // per compute warp: 16 rows x 64 bytes of its dS piece, for row-grouped
+    // stores (softmax with a bias, where the compute warps bound the block rate)
+    static constexpr bool DS_STAGED = !ACT && BIAS != kBiasNone;
+    static constexpr uint32_t OFF_DSS = OFF_DT + (BIAS != kBiasNone ? kMaxBiasFloats * 4 : 0);
+    static constexpr uint32_t SMEM = OFF_DSS + (DS_STAGED ? 8 * 1024 : 0);
     static constexpr uint32_t SMEM_ALLOC = SMEM + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     // group g: S^T at 128 g (P^T over it), dP^T at 128 g + 64 (dS^T over it); dV, dK
@@ -459,15 +463,45 @@ __global__ void __launch_bounds__(512, 1)
                             }
                             // this row's 64-byte piece of the block's dS chunk (plane p at
                             // 16 KB p): 16-byte pieces 4 c .. 4 c + 3 of the 128-byte row,
-                            // XOR-swizzled by row
+                            // XOR-swizzled by row.  Stored straight from the lanes, each
+                            // 16-byte warp store touches 32 rows; staged (16 rows at a time
+                            // through the warp's 1 KB of shared memory, pieces rotated by
+                            // row pair so that neither side has bank conflicts), four lanes
+                            // write one row's 64 contiguous bytes and a store touches 8 rows.
                             auto ds_store = [&](const uint32_t *wp, int plane) {
-                                uint8_t *rowp = static_cast<uint8_t *>(g.ds) +
-                                                ((ds0 + i) * (ACT ? 2 : 1) + plane) * static_cast<int64_t>(kDsChunkBytes) +
-                                                row * 128;
+                                uint8_t *chunk = static_cast<uint8_t *>(g.ds) +
+                                                 ((ds0 + i) * (ACT ? 2 : 1) + plane) * static_cast<int64_t>(kDsChunkBytes);
+                                if constexpr (C::DS_STAGED) {
+                                    const uint32_t sb = smem_u32(smem + C::OFF_DSS) +
+                                                        static_cast<uint32_t>((grp * 4 + quad) * 1024);
+                                    const int pc = lane & 3, jr = lane >> 2;  // piece, row within 8
 #pragma unroll
-                                for (int k = 0; k < 4; ++k)
-                                    *reinterpret_cast<uint4 *>(rowp + (((4 * c + k) ^ (row & 7)) << 4)) =
-                                        make_uint4(wp[4 * k], wp[4 * k + 1], wp[4 * k + 2], wp[4 * k + 3]);
+                                    for (int r = 0; r < 2; ++r) {
+                                        if ((lane >> 4) == r) {
+                                            const int lr = lane & 15;
+#pragma unroll
+                                            for (int k = 0; k < 4; ++k)
+                                                st_shared_v4(sb + lr * 64 + ((k ^ ((lr >> 1) & 3)) << 4), wp[4 * k],
+                                                             wp[4 * k + 1], wp[4 * k + 2], wp[4 * k + 3]);
+                                        }
+                                        __syncwarp();
+#pragma unroll
+                                        for (int i2 = 0; i2 < 2; ++i2) {
+                                            const int lr = 8 * i2 + jr;
+                                            const uint4 v = ld_shared_v4(sb + lr * 64 + ((pc ^ ((lr >> 1) & 3)) << 4));
+                                            const int grow = quad * 32 + 16 * r + lr;
+                                            *reinterpret_cast<uint4 *>(chunk + grow * 128 +
+                                                                       (((4 * c + pc) ^ (grow & 7)) << 4)) = v;
+                                        }
+                                        __syncwarp();  // the buffer is rewritten next
+                                    }
+                                } else {
+                                    uint8_t *rowp = chunk + row * 128;
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k)
+                                        *reinterpret_cast<uint4 *>(rowp + (((4 * c + k) ^ (row & 7)) << 4)) =
+                                            make_uint4(wp[4 * k], wp[4 * k + 1], wp[4 * k + 2], wp[4 * k + 3]);
+                                }
                             };
                             if constexpr (ACT) {
                                 uint32_t w[32];
